@@ -1,0 +1,153 @@
+"""fp64 CPU oracle for paged-attention decode.
+
+TEST INFRASTRUCTURE ONLY.  Only ``tests/``, ``__graft_entry__.smoke()`` and the
+CPU-baseline / reference legs of ``bench.py`` may import this package.  The
+product path (``paged_kv_attention_08_gb300``) never imports it and shares no
+code with it; the two meet only in the seeded input generator, which holds none
+of the method's arithmetic.
+
+The arithmetic lives in ``pa_oracle.c`` (plain C, fp64, one block-table lookup
+per token; see that file's header for the passages it follows and the readings
+it takes).  This module compiles it with gcc on first use and marshals torch /
+numpy arrays into it.
+
+Parity status of each function (pins live in ``tests/test_oracle_pins.py``):
+  decode, decode_rows  -- pinned: closed forms (single token, equal keys, one
+                          dominant score, a hand-worked two-token case), dense
+                          brute force, torch SDPA special case, pool-permutation
+                          invariance, masking semantics.
+  resolve_blocks       -- pinned: brute force over an independent per-page rule
+                          and hand-written cases.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import subprocess
+import threading
+
+import numpy as np
+import torch
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+_SRC = os.path.join(_HERE, "pa_oracle.c")
+_BUILD_DIR = os.path.join(_HERE, "_build")
+_LIB_PATH = os.path.join(_BUILD_DIR, "libpa_oracle.so")
+
+_lock = threading.Lock()
+_lib = None
+
+F16, BF16 = 0, 1
+
+
+def build(force: bool = False) -> str:
+    """Compile ``pa_oracle.c`` into ``oracle/_build/libpa_oracle.so`` with gcc."""
+    os.makedirs(_BUILD_DIR, exist_ok=True)
+    if force or not os.path.exists(_LIB_PATH) or os.path.getmtime(_LIB_PATH) < os.path.getmtime(_SRC):
+        tmp = _LIB_PATH + f".{os.getpid()}.tmp"
+        subprocess.run(
+            ["gcc", "-O2", "-std=c99", "-fPIC", "-shared", "-o", tmp, _SRC, "-lm"],
+            check=True,
+        )
+        os.replace(tmp, _LIB_PATH)
+    return _LIB_PATH
+
+
+def _load():
+    global _lib
+    with _lock:
+        if _lib is None:
+            # PA_ORACLE_LIB lets the mutation test load a deliberately broken
+            # copy of the oracle to prove that the pins catch it.
+            lib = ctypes.CDLL(os.environ.get("PA_ORACLE_LIB") or build())
+            P = ctypes.c_void_p
+            i32, i64, f64 = ctypes.c_int32, ctypes.c_int64, ctypes.c_double
+            lib.pao_decode.argtypes = [P, P, P, P, P, P, i32, i32, i32, i32, i32, i32, i64, i32, f64]
+            lib.pao_decode.restype = ctypes.c_int
+            lib.pao_decode_rows.argtypes = [P, P, P, P, P, P, i32, i32, i32, i32, i32, i32, i64,
+                                            i32, f64, P, i32]
+            lib.pao_decode_rows.restype = ctypes.c_int
+            lib.pao_resolve_blocks.argtypes = [P, P, P, i32, i32, i32, i64]
+            lib.pao_resolve_blocks.restype = ctypes.c_int
+            _lib = lib
+    return _lib
+
+
+def _u16(t: torch.Tensor) -> np.ndarray:
+    """Raw 16-bit patterns of an fp16/bf16 tensor, on the host, contiguous."""
+    if t.dtype not in (torch.float16, torch.bfloat16):
+        raise TypeError(f"oracle takes fp16/bf16 inputs, got {t.dtype}")
+    return np.ascontiguousarray(t.detach().cpu().contiguous().view(torch.int16).numpy().view(np.uint16))
+
+
+def _i32(t) -> np.ndarray:
+    if isinstance(t, torch.Tensor):
+        t = t.detach().cpu().numpy()
+    return np.ascontiguousarray(np.asarray(t, dtype=np.int32))
+
+
+def _dtype_code(t: torch.Tensor) -> int:
+    return BF16 if t.dtype == torch.bfloat16 else F16
+
+
+def _ptr(a: np.ndarray):
+    return a.ctypes.data_as(ctypes.c_void_p)
+
+
+def _common(q, k_cache, v_cache, block_tables, context_lens):
+    if q.dtype != k_cache.dtype or k_cache.dtype != v_cache.dtype:
+        raise TypeError("q, k_cache and v_cache must share one dtype")
+    B, H, D = q.shape
+    NB, bs, Hkv, D2 = k_cache.shape
+    if D2 != D or tuple(v_cache.shape) != tuple(k_cache.shape):
+        raise ValueError("cache shape does not match q")
+    bt = _i32(block_tables)
+    if bt.ndim != 2 or bt.shape[0] != B:
+        raise ValueError("block_tables must be [batch, max_blocks]")
+    lens = _i32(context_lens)
+    if lens.shape != (B,):
+        raise ValueError("context_lens must be [batch]")
+    return (B, H, Hkv, D, bs, bt.shape[1], NB), bt, lens
+
+
+def decode(q, k_cache, v_cache, block_tables, context_lens, scale: float) -> np.ndarray:
+    """out[b, h, :] in float64 for every sequence and query head.
+
+    ``scale`` is rounded to fp32 first: the decode library takes it as a C
+    float, so that fp32 value is the input both sides compute with.
+    """
+    (B, H, Hkv, D, bs, mb, NB), bt, lens = _common(q, k_cache, v_cache, block_tables, context_lens)
+    qa, ka, va = _u16(q), _u16(k_cache), _u16(v_cache)
+    out = np.zeros((B, H, D), dtype=np.float64)
+    rc = _load().pao_decode(_ptr(out), _ptr(qa), _ptr(ka), _ptr(va), _ptr(bt), _ptr(lens),
+                            B, H, Hkv, D, bs, mb, NB, _dtype_code(q), float(np.float32(scale)))
+    if rc != 0:
+        raise RuntimeError("oracle decode rejected its arguments")
+    return out
+
+
+def decode_rows(q, k_cache, v_cache, block_tables, context_lens, scale: float, rows) -> np.ndarray:
+    """out for selected (b, h) pairs only: ``rows`` is an [n, 2] int array."""
+    (B, H, Hkv, D, bs, mb, NB), bt, lens = _common(q, k_cache, v_cache, block_tables, context_lens)
+    rows = _i32(rows).reshape(-1, 2)
+    qa, ka, va = _u16(q), _u16(k_cache), _u16(v_cache)
+    out = np.zeros((rows.shape[0], D), dtype=np.float64)
+    rc = _load().pao_decode_rows(_ptr(out), _ptr(qa), _ptr(ka), _ptr(va), _ptr(bt), _ptr(lens),
+                                 B, H, Hkv, D, bs, mb, NB, _dtype_code(q),
+                                 float(np.float32(scale)), _ptr(rows), rows.shape[0])
+    if rc != 0:
+        raise RuntimeError("oracle decode_rows rejected its arguments")
+    return out
+
+
+def resolve_blocks(block_tables, context_lens, block_size: int, num_blocks: int) -> np.ndarray:
+    """[batch, max_blocks] int32: the physical block read for each logical page,
+    -1 where the page holds no attended token."""
+    bt = _i32(block_tables)
+    lens = _i32(context_lens)
+    B, mb = bt.shape
+    out = np.full((B, mb), -1, dtype=np.int32)
+    rc = _load().pao_resolve_blocks(_ptr(out), _ptr(bt), _ptr(lens), B, block_size, mb, num_blocks)
+    if rc != 0:
+        raise RuntimeError("oracle resolve_blocks rejected its arguments")
+    return out
