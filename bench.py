@@ -1,0 +1,488 @@
+"""Benchmark of paged-attention decode on GB300.
+
+One step = one decode call for each workload of the chosen group (default:
+the pages' sweep, (batch, ctx) in {(1,512), (16,256), (4,2048)}, 32 query /
+8 kv heads, head_dim 128, block_size 16, fp16), each through
+``pa_decode_splitkv`` with the automatic partition choice (which runs the
+single pass when one partition suffices).  Inputs rotate among enough
+independent seeded sets that every step reads from HBM, not L2.  The step is
+captured once per input set as a CUDA graph and replayed, so host launch
+overhead does not pace the GPU.
+
+Prints one JSON line (rank 0).  ``--impl reference`` times the fp64 CPU oracle
+on the same workload instead.  Under torchrun each rank runs an independent
+replica on its own GPU (the decode step has no cross-GPU exchange).
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import tempfile
+import time
+
+import numpy as np
+import torch
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+from paged_kv_attention_08_gb300 import workloads  # noqa: E402
+
+METRIC = "paged decode µs/step and achieved HBM GB/s (fraction of GB300 roofline)"
+FALLBACK_HBM_GBS = 6800.0
+DTYPE_NAME = {torch.float16: "f16", torch.bfloat16: "bf16", torch.float32: "f32"}
+
+
+# ---------------------------------------------------------------------------
+# bytes
+# ---------------------------------------------------------------------------
+def algorithmic_bytes(x: workloads.Inputs, out_elem: int = 4) -> int:
+    """Bytes one decode call must move at least once: K and V of every attended
+    token for each kv head, q, the output, the block table and the lengths."""
+    B, H, D = x.q.shape
+    _, bs, Hkv, _ = x.k_cache.shape
+    e = x.q.element_size()
+    mb = x.block_tables.shape[1]
+    tokens = sum(min(max(t, 0), mb * bs) for t in x.lens_host)
+    return (tokens * Hkv * D * 2 * e + B * H * D * e + B * H * D * out_elem
+            + B * mb * 4 + B * 4)
+
+
+def input_bytes(x: workloads.Inputs) -> int:
+    return sum(t.numel() * t.element_size()
+               for t in (x.q, x.k_cache, x.v_cache, x.block_tables, x.context_lens))
+
+
+# ---------------------------------------------------------------------------
+# distributed helpers (replicas: no data-path collective)
+# ---------------------------------------------------------------------------
+def dist_env():
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return world, rank, local
+
+
+def reduce_max(value: float, device) -> float:
+    """Max over ranks (identity for one process)."""
+    import torch.distributed as dist
+    if not (dist.is_available() and dist.is_initialized()):
+        return value
+    t = torch.tensor([value], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def reduce_sum(value: float, device) -> float:
+    import torch.distributed as dist
+    if not (dist.is_available() and dist.is_initialized()):
+        return value
+    t = torch.tensor([value], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.SUM)
+    return float(t.item())
+
+
+def barrier():
+    import torch.distributed as dist
+    if dist.is_available() and dist.is_initialized():
+        dist.barrier()
+
+
+# ---------------------------------------------------------------------------
+# clocks
+# ---------------------------------------------------------------------------
+class ClockSampler:
+    """nvidia-smi clock / throttle samples every 200 ms while active."""
+
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.gpu = gpu_index
+        self.proc = None
+        self.path = None
+
+    def __enter__(self):
+        fd, self.path = tempfile.mkstemp(prefix="pa_clocks_", suffix=".csv")
+        os.close(fd)
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--id={self.gpu}", f"--query-gpu={self.FIELDS}",
+                 "--format=csv,noheader,nounits", "-lms", "200"],
+                stdout=open(self.path, "w"), stderr=subprocess.DEVNULL)
+        except OSError:
+            self.proc = None
+        time.sleep(0.3)
+        return self
+
+    def __exit__(self, *a):
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+
+    def summary(self):
+        if self.proc is None or not self.path or not os.path.exists(self.path):
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        rows = []
+        for line in open(self.path):
+            parts = [p.strip() for p in line.split(",")]
+            if len(parts) < 9:
+                continue
+            try:
+                rows.append((float(parts[1]), float(parts[2]), float(parts[3]), parts[4:9]))
+            except ValueError:
+                continue
+        os.unlink(self.path)
+        if not rows:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["no samples"]}
+        names = ["active_mask", "hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown",
+                 "sw_power_cap"]
+        reasons = set()
+        for r in rows:
+            for n, v in zip(names[1:], r[3][1:]):
+                if v.lower().startswith("active"):
+                    reasons.add(n)
+        return {"sm_mhz": statistics.median(r[0] for r in rows),
+                "sm_max_mhz": max(r[1] for r in rows),
+                "power_w_max": max(r[2] for r in rows),
+                "samples": len(rows), "reasons": sorted(reasons)}
+
+
+# ---------------------------------------------------------------------------
+# peaks
+# ---------------------------------------------------------------------------
+def hbm_peak():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        v = float(json.load(open(path))["hbm_gbs"])
+        return v, "measured"
+    except (OSError, KeyError, ValueError):
+        return FALLBACK_HBM_GBS, "fallback"
+
+
+def ncu_traffic(kernel: str, workload: str):
+    """DRAM bytes per launch recorded from an ncu capture (profiles/), or None."""
+    path = os.path.join(ROOT, "profiles", f"{kernel}_{workload}.txt")
+    try:
+        for line in open(path):
+            if line.startswith("dram_bytes_per_launch_full_size:"):
+                return int(float(line.split(":", 1)[1]))
+    except OSError:
+        pass
+    return None
+
+
+# ---------------------------------------------------------------------------
+# CPU oracle arm
+# ---------------------------------------------------------------------------
+def oracle_step(sets_host):
+    import oracle
+    for x in sets_host:
+        oracle.decode(x.q, x.k_cache, x.v_cache, x.block_tables, x.context_lens, x.scale)
+
+
+def time_oracle(sets_host, min_s=10.0, max_steps=None):
+    """Whole oracle steps on one host thread until ``min_s`` elapse; seconds/step."""
+    n, t0 = 0, time.perf_counter()
+    while True:
+        oracle_step(sets_host)
+        n += 1
+        el = time.perf_counter() - t0
+        if el >= min_s or (max_steps and n >= max_steps):
+            return el / n, n
+
+
+# ---------------------------------------------------------------------------
+# main
+# ---------------------------------------------------------------------------
+def describe(group):
+    specs = [workloads.SPECS[n] for n in workloads.GROUPS[group]]
+    s0 = specs[0]
+    return (f"{group}: (batch, ctx) in {{{', '.join(f'({s.batch},{s.lens})' for s in specs)}}}, "
+            f"H{s0.num_heads}/Hkv{s0.num_kv_heads}, D{s0.head_dim}, bs{s0.block_size}, "
+            f"{DTYPE_NAME[s0.dtype]} K/V, fp32 out")
+
+
+def run_reference(args):
+    world, rank, _ = dist_env()
+    if rank != 0:
+        return 0
+    import oracle
+    oracle.build()
+    names = workloads.GROUPS[args.workload]
+    sets = [workloads.make(n, seed=0, device="cpu") for n in names]
+    step_bytes = sum(algorithmic_bytes(x) for x in sets)
+    for _ in range(args.warmup):
+        oracle_step(sets)
+    t0 = time.perf_counter()
+    for _ in range(args.steps):
+        oracle_step(sets)
+    sec = (time.perf_counter() - t0) / max(1, args.steps)
+    gbs = step_bytes / sec / 1e9
+    sample = f"{args.steps} whole steps of the {args.workload} group (every sequence, every head)"
+    line = {"impl": "reference", "metric": METRIC, "value": gbs, "unit": "GB/s", "n_gpus": 1,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": sec * 1e3,
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+            "data": "synthetic", "config": {"workload": describe(args.workload),
+                                            "kind": "fp64 CPU oracle, single thread"},
+            "cpu_baseline": {"value": gbs, "unit": "GB/s", "cores": 1, "kind": "oracle",
+                             "sample": sample},
+            "e2e": {"value": gbs, "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+    print(json.dumps(line), flush=True)
+    return 0
+
+
+def main(argv=None):
+    ap = argparse.ArgumentParser(description=__doc__.split("\n")[0])
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=2000)
+    ap.add_argument("--warmup", type=int, default=50)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--workload", choices=sorted(workloads.GROUPS), default="sweep")
+    ap.add_argument("--partition-tokens", type=int, default=-1,
+                    help="split-KV partition size; -1 = each workload's own (0/auto unless stated)")
+    ap.add_argument("--no-graph", action="store_true", help="launch eagerly instead of graph replay")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-e2e", action="store_true")
+    args = ap.parse_args(argv)
+    args.warmup = max(args.warmup, 3)
+
+    if args.impl == "reference":
+        return run_reference(args)
+
+    import paged_kv_attention_08_gb300 as pa
+    world, rank, local = dist_env()
+    if not torch.cuda.is_available():
+        print(json.dumps({"metric": METRIC, "error": "no CUDA device"}))
+        return 1
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl", device_id=dev)
+
+    names = workloads.GROUPS[args.workload]
+    specs = [workloads.SPECS[n] for n in names]
+    props = torch.cuda.get_device_properties(dev)
+    l2 = int(getattr(props, "L2_cache_size", 128 << 20))
+    set0 = [workloads.make(n, seed=0, device=dev) for n in names]
+    set_bytes = sum(input_bytes(x) for x in set0)
+    nsets = max(1, min(64, math.ceil(3 * l2 / set_bytes) + 1))
+    sets = [set0] + [[workloads.make(n, seed=100 * r + rank, device=dev) for n in names]
+                     for r in range(1, nsets)]
+    pts = [s.partition_tokens if args.partition_tokens < 0 else args.partition_tokens for s in specs]
+
+    outs = [[torch.empty(x.q.shape, dtype=torch.float32, device=dev) for x in st] for st in sets]
+    ws = []
+    for i, x in enumerate(set0):
+        need = pa.workspace_size(x.q, x.k_cache, x.block_tables, torch.float32,
+                                 x.max_context_len, pts[i])
+        ws.append(torch.empty(max(need, 16), dtype=torch.uint8, device=dev))
+    splits = [ws[i].numel() > 16 for i in range(len(set0))]
+    launches_per_step = sum(2 if s else 1 for s in splits)
+
+    stream = torch.cuda.Stream(device=dev)
+
+    def call(si, i, st):
+        x = sets[si][i]
+        pa.decode_splitkv(outs[si][i], x.q, x.k_cache, x.v_cache, x.block_tables, x.context_lens,
+                          x.scale, x.max_context_len, pts[i], workspace=ws[i], stream=st)
+
+    # ---- parity before timing (sampled rows against the fp64 oracle) ----
+    import oracle
+    with torch.cuda.stream(stream):
+        for i in range(len(set0)):
+            call(0, i, stream)
+    stream.synchronize()
+    max_err = 0.0
+    if rank == 0:
+        for i, x in enumerate(set0):
+            g = np.random.default_rng(i)
+            B, H = x.q.shape[:2]
+            rows = np.stack([g.integers(0, B, 16), g.integers(0, H, 16)], 1).astype(np.int32)
+            h = x.to("cpu")
+            want = oracle.decode_rows(h.q, h.k_cache, h.v_cache, h.block_tables, h.context_lens,
+                                      h.scale, rows)
+            got = outs[0][i][rows[:, 0], rows[:, 1]].double().cpu().numpy()
+            max_err = max(max_err, float(np.abs(got - want).max()))
+        if not max_err <= 2e-3:
+            print(json.dumps({"metric": METRIC, "error": f"parity failed: max_err {max_err}"}))
+            return 1
+
+    # ---- graphs: one per input set ----
+    graphs = []
+    if not args.no_graph:
+        with torch.cuda.stream(stream):
+            for si in range(nsets):               # warm every set once before capture
+                for i in range(len(set0)):
+                    call(si, i, stream)
+        stream.synchronize()
+        for si in range(nsets):
+            g = torch.cuda.CUDAGraph()
+            with torch.cuda.graph(g, stream=stream):
+                for i in range(len(set0)):
+                    call(si, i, torch.cuda.current_stream())
+            graphs.append(g)
+    torch.cuda.synchronize()
+
+    def step(k, st):
+        si = k % nsets
+        if graphs:
+            graphs[si].replay()
+        else:
+            for i in range(len(set0)):
+                call(si, i, st)
+
+    # per-call events for the per-kernel roofline: a second timed pass, eager,
+    # one event pair around each call
+    ev_pairs = []
+
+    step_bytes = sum(algorithmic_bytes(x) for x in set0)
+    with ClockSampler(local) as clocks:
+        with torch.cuda.stream(stream):
+            t_warm = time.perf_counter()
+            k = 0
+            while k < args.warmup or time.perf_counter() - t_warm < 1.0:
+                step(k, stream)
+                k += 1
+                if k % 256 == 0:
+                    stream.synchronize()
+            stream.synchronize()
+            barrier()
+            torch.cuda.synchronize()
+            e0 = torch.cuda.Event(enable_timing=True)
+            e1 = torch.cuda.Event(enable_timing=True)
+            e0.record(stream)
+            for k in range(args.steps):
+                step(k, stream)
+            e1.record(stream)
+            e1.synchronize()
+            torch.cuda.synchronize()
+            barrier()
+            ms_total = e0.elapsed_time(e1)
+
+            # per-call timing pass (same calls, each bracketed by events)
+            per_call = [[] for _ in set0]
+            reps = max(1, min(args.steps, 400))
+            pairs = []
+            for k in range(reps):
+                si = k % nsets
+                for i in range(len(set0)):
+                    a = torch.cuda.Event(enable_timing=True)
+                    b = torch.cuda.Event(enable_timing=True)
+                    a.record(stream)
+                    call(si, i, stream)
+                    b.record(stream)
+                    pairs.append((i, a, b))
+            stream.synchronize()
+            for i, a, b in pairs:
+                per_call[i].append(a.elapsed_time(b))
+    clk = clocks.summary() if rank == 0 else None
+
+    ms_step = reduce_max(ms_total, dev) / args.steps
+    total_bytes = reduce_sum(float(step_bytes), dev)
+    value = total_bytes / (ms_step * 1e-3) / 1e9
+    peak, peak_kind = hbm_peak()
+
+    # dominant call: largest share of time; its achieved bytes / its own duration
+    call_us = [statistics.median(v) * 1e3 for v in per_call]
+    dom = int(np.argmax(call_us))
+    dom_bytes = algorithmic_bytes(set0[dom])
+    dom_gbs = dom_bytes / (call_us[dom] * 1e-6) / 1e9
+    dom_name = names[dom]
+
+    # ---- end to end: host buffers, copies inside the timed region ----
+    e2e = None
+    if not args.no_e2e:
+        host = [x.to("cpu") for x in set0]
+        pinned = []
+        for h in host:
+            pinned.append([t.pin_memory() for t in (h.q, h.k_cache, h.v_cache, h.block_tables,
+                                                     h.context_lens)])
+        dev_bufs = [[torch.empty_like(t, device=dev) for t in p] for p in pinned]
+        out_host = [torch.empty(x.q.shape, dtype=torch.float32).pin_memory() for x in set0]
+        h2d = sum(t.numel() * t.element_size() for p in pinned for t in p)
+        d2h = sum(t.numel() * t.element_size() for t in out_host)
+        e2e_steps = max(3, min(args.steps, 50))
+        with torch.cuda.stream(stream):
+            def e2e_step():
+                for i, x in enumerate(set0):
+                    for dst, src in zip(dev_bufs[i], pinned[i]):
+                        dst.copy_(src, non_blocking=True)
+                    q, k_, v_, bt, ln = dev_bufs[i]
+                    pa.decode_splitkv(outs[0][i], q, k_, v_, bt, ln, x.scale, x.max_context_len,
+                                      pts[i], workspace=ws[i], stream=stream)
+                    out_host[i].copy_(outs[0][i], non_blocking=True)
+            for _ in range(3):
+                e2e_step()
+            stream.synchronize()
+            barrier()
+            a = torch.cuda.Event(enable_timing=True)
+            b = torch.cuda.Event(enable_timing=True)
+            a.record(stream)
+            for _ in range(e2e_steps):
+                e2e_step()
+            b.record(stream)
+            b.synchronize()
+        ms_e2e = reduce_max(a.elapsed_time(b), dev) / e2e_steps
+        e2e = {"value": total_bytes / (ms_e2e * 1e-3) / 1e9, "unit": "GB/s",
+               "ms_per_step": ms_e2e, "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
+               "steps": e2e_steps}
+
+    cpu = None
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        host = [x.to("cpu") for x in set0]
+        sec, n = time_oracle(host, min_s=10.0)
+        cpu = {"value": step_bytes / sec / 1e9, "unit": "GB/s", "cores": 1, "kind": "oracle",
+               "sample": f"{n} whole steps of the {args.workload} group (input set 0), "
+                         f"fp64 oracle on one host thread, {sec * 1e3:.1f} ms/step"}
+
+    if rank == 0:
+        line = {
+            "metric": METRIC, "value": value, "unit": "GB/s", "n_gpus": world,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms_step,
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f32",
+            "data": "synthetic",
+            "config": {
+                "workload": describe(args.workload),
+                "us_per_step": ms_step * 1e3,
+                "per_call_us": {n: round(u, 3) for n, u in zip(names, call_us)},
+                "algorithmic_bytes_per_step": step_bytes,
+                "partition_tokens": {n: (p if p else "auto") for n, p in zip(names, pts)},
+                "split": {n: s for n, s in zip(names, splits)},
+                "l2": f"rotating {nsets} input sets of {set_bytes / 1e6:.1f} MB "
+                      f"({nsets * set_bytes / 1e6:.0f} MB > 3x L2 {l2 / 1e6:.0f} MB)",
+                "launch": "CUDA graph replay per step" if graphs else "eager",
+                "parallelism": f"replicas x{world}",
+                "parity_max_abs_err": max_err,
+            },
+            "e2e": e2e,
+            "gpu_launches": launches_per_step * args.steps,
+            "roofline": {"bound": "hbm", "achieved": dom_gbs, "peak": peak, "unit": "GB/s",
+                         "frac": dom_gbs / peak, "peak_kind": peak_kind,
+                         "kernel": f"decode call on {dom_name} "
+                                   f"({'partial+combine' if splits[dom] else 'single pass'})",
+                         "traffic": ncu_traffic("pa_attn", dom_name),
+                         "step_frac": value / world / peak},
+            "cpu_baseline": cpu,
+            "clocks": clk,
+        }
+        print(json.dumps(line), flush=True)
+    if world > 1:
+        import torch.distributed as dist
+        dist.destroy_process_group()
+    return 0
+
+
+if __name__ == "__main__":
+    sys.exit(main())

@@ -1,0 +1,168 @@
+/*
+ * pa_decode.h -- C ABI of the GB300 (sm_103a) paged-attention decode library
+ * (libpa_decode.so).
+ *
+ * The operation.  One decode step: every sequence b of a batch has one query
+ * token q[b, h, :] per query head h; it attends over the keys and values of
+ * its context_lens[b] cached tokens, which live in a pool of fixed-size
+ * physical blocks reached through a per-sequence block table:
+ *
+ *   out[b, h, :] = sum_t softmax_t(scale * q[b, h, :] . K_t) * V_t
+ *   K_t = k_cache[block_tables[b][t / block_size], t % block_size, kvh, :]
+ *   kvh = h / (num_heads / num_kv_heads)       (grouped-query heads)
+ *
+ * Sources: MiniVLLM docs "Decoding Benchmark" (sections "What paged attention
+ * decode does" and "Block table lookup mechanics"); "benchmark_decoding.py"
+ * (reference_output: the float32 definition; setup_test_data: the layouts;
+ * the Triton (new) kernel: head grouping and masking of -1 entries);
+ * flash-decoding-bench "design.md" (Flash-Decoding: split the KV sequence into
+ * chunks processed in parallel, each producing a local max, sum and weighted
+ * value sum, then reduce the partials into the output).
+ *
+ * Layouts (all row-major, contiguous, device memory owned by the caller):
+ *   q            [batch, num_heads, head_dim]                      kv_dtype
+ *   k_cache      [num_blocks, block_size, num_kv_heads, head_dim]  kv_dtype
+ *   v_cache      same shape and dtype as k_cache
+ *   block_tables [batch, max_blocks_per_seq]                       int32, -1 = unallocated
+ *   context_lens [batch]                                           int32
+ *   out          [batch, num_heads, head_dim]                      out_dtype
+ *
+ * Semantics at the edges (the pages are silent or disagree; this library and
+ * its tests take these readings):
+ *   - tokens t >= max_blocks_per_seq * block_size are unreachable and ignored;
+ *     a negative context length counts as 0;
+ *   - a table entry inside the used range that is -1 or outside
+ *     [0, num_blocks) excludes its tokens from the softmax (never read);
+ *   - a sequence with no attended token gets an all-zero output row.
+ *
+ * Arithmetic: scores, the online softmax (running max m and normaliser l) and
+ * the value accumulation are fp32; K/V/q are fp16 or bf16.
+ *
+ * Calls.  All entry points validate on the host and either launch work on
+ * `stream` (a cudaStream_t; NULL = the legacy default stream) and return
+ * PA_OK immediately, or return an error status and launch nothing.  A
+ * PA_ERR_CUDA status means the launch itself failed.  The library allocates no
+ * device memory.  Entry points may be called from several host threads; the
+ * only shared state is a per-device cache of the SM count and of the device
+ * error word's address.
+ *
+ * Supported shapes: head_dim in {64, 128, 256}; block_size in {16, 32};
+ * num_heads / num_kv_heads in {1, 2, 4, 8, 16}; kv_dtype fp16 or bf16; out_dtype
+ * fp32 or equal to kv_dtype; every pointer 16-byte aligned.  Anything else
+ * returns PA_ERR_UNSUPPORTED (or PA_ERR_INVALID_ARG for inconsistent values).
+ */
+#ifndef PA_DECODE_H
+#define PA_DECODE_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum pa_status {
+    PA_OK = 0,
+    PA_ERR_INVALID_ARG = 1, /* null pointer, inconsistent or negative sizes */
+    PA_ERR_UNSUPPORTED = 2, /* a shape or dtype this library has no kernel for */
+    PA_ERR_WORKSPACE = 3,   /* split-KV workspace missing, misaligned or too small */
+    PA_ERR_CUDA = 4,        /* a CUDA runtime call or kernel launch failed */
+    PA_ERR_TIMEOUT = 5      /* a kernel gave up waiting on its own copy pipeline */
+} pa_status;
+
+typedef enum pa_dtype { PA_F16 = 0, PA_BF16 = 1, PA_F32 = 2 } pa_dtype;
+
+typedef struct pa_shape {
+    int32_t batch;              /* B >= 0 (B = 0 launches nothing) */
+    int32_t num_heads;          /* H, query heads */
+    int32_t num_kv_heads;       /* Hkv, H % Hkv == 0 */
+    int32_t head_dim;           /* D */
+    int32_t block_size;         /* tokens per physical block */
+    int32_t max_blocks_per_seq; /* columns of block_tables */
+    int64_t num_blocks;         /* physical blocks in the pool, < 2^31 */
+    int32_t kv_dtype;           /* pa_dtype of q, k_cache, v_cache: PA_F16 or PA_BF16 */
+    int32_t out_dtype;          /* pa_dtype of out: PA_F32 or kv_dtype */
+} pa_shape;
+
+/*
+ * Single-pass decode ("benchmark_decoding.py", reference_output and the
+ * Triton (new) kernel; MiniVLLM docs "Decoding Benchmark", "Why CUDA chunk
+ * processing matters"): one CTA per (sequence, kv head) walks all of that
+ * sequence's pages, one block-table read per page, with an fp32 online
+ * softmax, and writes out[b, h, :] for the head group.
+ * Arguments: device pointers as laid out above; `scale` multiplies q.K
+ * (1/sqrt(head_dim) in the pages' set-up); `stream` is a cudaStream_t.
+ */
+pa_status pa_decode(void* out, const void* q, const void* k_cache, const void* v_cache,
+                    const int32_t* block_tables, const int32_t* context_lens,
+                    const pa_shape* shape, float scale, void* stream);
+
+/*
+ * Bytes of device workspace pa_decode_splitkv needs for this shape, longest
+ * context `max_context_len` and partition size `partition_tokens` (tokens per
+ * split, a multiple of block_size; 0 = choose automatically for the current
+ * device).  Returns 0 for invalid arguments or when no split is needed.
+ */
+size_t pa_workspace_size(const pa_shape* shape, int32_t max_context_len,
+                         int32_t partition_tokens);
+
+/*
+ * Partition size (tokens) the automatic choice picks for `num_sms`
+ * multiprocessors: 0 < result, a multiple of block_size; a result >=
+ * max_context_len means "no split".  Host-only, no device access (a pure
+ * function, exported so that its choice can be checked without a GPU).
+ * This heuristic is this library's own: the flash-decoding-bench design notes
+ * only say that the chunk size is picked from the KV length.
+ */
+int32_t pa_choose_partition_tokens(const pa_shape* shape, int32_t max_context_len,
+                                   int32_t num_sms);
+
+/*
+ * Flash-Decoding split-KV decode (flash-decoding-bench "design.md": the KV
+ * cache is split into chunks, one thread block each, each computing its local
+ * max, sum and weighted value sum, followed by a reduction of the partials).
+ * Kernel 1 writes, per (sequence, kv head, partition of `partition_tokens`
+ * tokens), fp32 partials (m, l, acc[head_dim]) for each query head of the
+ * group into `workspace`; kernel 2 combines them with a log-sum-exp reduction
+ * into out.  `max_context_len` must be >= every context_lens[b] that should be
+ * attended in full (tokens beyond it are dropped; no device->host read is
+ * made); `partition_tokens` = 0 chooses automatically, and a choice of one
+ * partition runs the single pass without touching the workspace.
+ * `workspace` (device, 16-byte aligned) must hold at least
+ * pa_workspace_size(shape, max_context_len, partition_tokens) bytes; it is
+ * scratch owned by the caller and may be reused once the stream has passed
+ * this call.
+ */
+pa_status pa_decode_splitkv(void* out, const void* q, const void* k_cache, const void* v_cache,
+                            const int32_t* block_tables, const int32_t* context_lens,
+                            const pa_shape* shape, float scale, int32_t max_context_len,
+                            int32_t partition_tokens, void* workspace, size_t workspace_bytes,
+                            void* stream);
+
+/*
+ * Test export of the page walk (MiniVLLM docs "Decoding Benchmark", "Block
+ * table lookup mechanics"): out_phys[b][j] (device, int32, [batch,
+ * max_blocks_per_seq]) = the physical block the decode kernels read for
+ * logical page j of sequence b, or -1 where that page holds no attended token
+ * (beyond the context, or a masked entry).  Uses the kernels' own page-walk
+ * code.
+ */
+pa_status pa_resolve_blocks(int32_t* out_phys, const int32_t* block_tables,
+                            const int32_t* context_lens, const pa_shape* shape, void* stream);
+
+/*
+ * Reads and clears the current device's error word, which a kernel sets when
+ * a bounded wait on its own copy pipeline runs out (it then abandons the
+ * work and returns instead of hanging).  Synchronises `stream`.  *code is 0
+ * or the pa_status the kernel recorded.
+ */
+pa_status pa_device_error(int32_t* code, void* stream);
+
+/* Static, human-readable name of a status. */
+const char* pa_status_string(pa_status status);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* PA_DECODE_H */

@@ -1,1 +1,202 @@
-"""Paged-attention decode for GB300 (sm_103a)."""
+"""Paged-attention decode for GB300 (sm_103a): thin Python binding.
+
+Every call marshals torch tensors into the C ABI of ``libpa_decode.so``
+(declared in ``include/pa_decode.h``) and launches on the current torch CUDA
+stream.  Torch supplies device memory and streams only; all arithmetic runs in
+the library's CUDA kernels.  There is no fallback: if the library is not built
+or a call is rejected, an exception is raised.
+
+    decode(out, q, k_cache, v_cache, block_tables, context_lens, scale)
+    decode_splitkv(out, q, k_cache, v_cache, block_tables, context_lens, scale,
+                   max_context_len, partition_tokens=0, workspace=None)
+    workspace_size(q, k_cache, block_tables, out_dtype, max_context_len, partition_tokens=0)
+    choose_partition_tokens(q, k_cache, block_tables, max_context_len, num_sms)
+    resolve_blocks(out_phys, block_tables, context_lens, block_size, num_blocks)
+    device_error()
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import threading
+
+import torch
+
+__all__ = ["PaError", "decode", "decode_splitkv", "workspace_size", "choose_partition_tokens",
+           "resolve_blocks", "device_error", "library_path", "F16", "BF16", "F32"]
+
+F16, BF16, F32 = 0, 1, 2
+_STATUS = {0: "PA_OK", 1: "PA_ERR_INVALID_ARG", 2: "PA_ERR_UNSUPPORTED", 3: "PA_ERR_WORKSPACE",
+           4: "PA_ERR_CUDA", 5: "PA_ERR_TIMEOUT"}
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+_LIB_PATH = os.path.join(_HERE, "libpa_decode.so")
+_lock = threading.Lock()
+_lib = None
+
+
+class PaError(RuntimeError):
+    """A non-OK pa_status returned by the library."""
+
+    def __init__(self, code: int, what: str):
+        self.code = code
+        super().__init__(f"{what}: {_STATUS.get(code, code)}")
+
+
+class _Shape(ctypes.Structure):
+    _fields_ = [("batch", ctypes.c_int32), ("num_heads", ctypes.c_int32),
+                ("num_kv_heads", ctypes.c_int32), ("head_dim", ctypes.c_int32),
+                ("block_size", ctypes.c_int32), ("max_blocks_per_seq", ctypes.c_int32),
+                ("num_blocks", ctypes.c_int64), ("kv_dtype", ctypes.c_int32),
+                ("out_dtype", ctypes.c_int32)]
+
+
+def library_path() -> str:
+    return _LIB_PATH
+
+
+def _load():
+    global _lib
+    with _lock:
+        if _lib is None:
+            if not os.path.exists(_LIB_PATH):
+                raise RuntimeError(
+                    f"{_LIB_PATH} is missing: build it with "
+                    "`python -m paged_kv_attention_08_gb300.build` (there is no fallback path)")
+            lib = ctypes.CDLL(_LIB_PATH)
+            P, S = ctypes.c_void_p, ctypes.POINTER(_Shape)
+            i32, f32, sz = ctypes.c_int32, ctypes.c_float, ctypes.c_size_t
+            lib.pa_decode.argtypes = [P, P, P, P, P, P, S, f32, P]
+            lib.pa_decode.restype = ctypes.c_int
+            lib.pa_decode_splitkv.argtypes = [P, P, P, P, P, P, S, f32, i32, i32, P, sz, P]
+            lib.pa_decode_splitkv.restype = ctypes.c_int
+            lib.pa_workspace_size.argtypes = [S, i32, i32]
+            lib.pa_workspace_size.restype = sz
+            lib.pa_choose_partition_tokens.argtypes = [S, i32, i32]
+            lib.pa_choose_partition_tokens.restype = i32
+            lib.pa_resolve_blocks.argtypes = [P, P, P, S, P]
+            lib.pa_resolve_blocks.restype = ctypes.c_int
+            lib.pa_device_error.argtypes = [ctypes.POINTER(i32), P]
+            lib.pa_device_error.restype = ctypes.c_int
+            lib.pa_status_string.argtypes = [ctypes.c_int]
+            lib.pa_status_string.restype = ctypes.c_char_p
+            _lib = lib
+    return _lib
+
+
+def _dtype_code(dt: torch.dtype) -> int:
+    if dt == torch.float16:
+        return F16
+    if dt == torch.bfloat16:
+        return BF16
+    if dt == torch.float32:
+        return F32
+    raise TypeError(f"unsupported dtype {dt}")
+
+
+def make_shape(q: torch.Tensor, k_cache: torch.Tensor, block_tables: torch.Tensor,
+               out_dtype: torch.dtype | None = None) -> _Shape:
+    """pa_shape from tensor shapes: q [B,H,D], k_cache [NB,bs,Hkv,D], block_tables [B,max_blocks]."""
+    if q.dim() != 3 or k_cache.dim() != 4 or block_tables.dim() != 2:
+        raise ValueError("expected q [B,H,D], k_cache [NB,bs,Hkv,D], block_tables [B,max_blocks]")
+    B, H, D = q.shape
+    NB, bs, Hkv, _ = k_cache.shape
+    return _Shape(B, H, Hkv, D, bs, block_tables.shape[1], NB, _dtype_code(k_cache.dtype),
+                  _dtype_code(out_dtype if out_dtype is not None else q.dtype))
+
+
+def _stream_ptr(stream) -> int:
+    s = stream if stream is not None else torch.cuda.current_stream()
+    return s.cuda_stream
+
+
+def _check(code: int, what: str):
+    if code != 0:
+        raise PaError(code, what)
+
+
+def _dev_tensors(*ts):
+    dev = None
+    for t in ts:
+        if not t.is_cuda:
+            raise ValueError("all tensors must be CUDA tensors")
+        if not t.is_contiguous():
+            raise ValueError("all tensors must be contiguous")
+        if dev is None:
+            dev = t.device
+        elif t.device != dev:
+            raise ValueError("all tensors must be on one device")
+
+
+def _ints(block_tables, context_lens):
+    if block_tables.dtype != torch.int32 or context_lens.dtype != torch.int32:
+        raise TypeError("block_tables and context_lens must be int32")
+
+
+def decode(out, q, k_cache, v_cache, block_tables, context_lens, scale: float, stream=None):
+    """Single-pass paged decode into ``out`` ([B,H,D], fp32 or q's dtype)."""
+    _dev_tensors(out, q, k_cache, v_cache, block_tables, context_lens)
+    _ints(block_tables, context_lens)
+    shape = make_shape(q, k_cache, block_tables, out.dtype)
+    _check(_load().pa_decode(out.data_ptr(), q.data_ptr(), k_cache.data_ptr(), v_cache.data_ptr(),
+                             block_tables.data_ptr(), context_lens.data_ptr(),
+                             ctypes.byref(shape), float(scale), _stream_ptr(stream)), "pa_decode")
+    return out
+
+
+def workspace_size(q, k_cache, block_tables, out_dtype, max_context_len: int,
+                   partition_tokens: int = 0) -> int:
+    shape = make_shape(q, k_cache, block_tables, out_dtype)
+    return int(_load().pa_workspace_size(ctypes.byref(shape), int(max_context_len),
+                                         int(partition_tokens)))
+
+
+def choose_partition_tokens(q, k_cache, block_tables, max_context_len: int, num_sms: int) -> int:
+    shape = make_shape(q, k_cache, block_tables, None)
+    return int(_load().pa_choose_partition_tokens(ctypes.byref(shape), int(max_context_len),
+                                                  int(num_sms)))
+
+
+def decode_splitkv(out, q, k_cache, v_cache, block_tables, context_lens, scale: float,
+                   max_context_len: int, partition_tokens: int = 0, workspace=None, stream=None):
+    """Flash-Decoding split-KV decode.  ``workspace`` is a CUDA byte tensor of at
+    least ``workspace_size(...)`` bytes; when omitted one is taken from torch's
+    allocator for this call."""
+    _dev_tensors(out, q, k_cache, v_cache, block_tables, context_lens)
+    _ints(block_tables, context_lens)
+    shape = make_shape(q, k_cache, block_tables, out.dtype)
+    lib = _load()
+    if workspace is None:
+        need = lib.pa_workspace_size(ctypes.byref(shape), int(max_context_len), int(partition_tokens))
+        workspace = torch.empty(max(int(need), 16), dtype=torch.uint8, device=q.device)
+    else:
+        _dev_tensors(workspace)
+    _check(lib.pa_decode_splitkv(out.data_ptr(), q.data_ptr(), k_cache.data_ptr(),
+                                 v_cache.data_ptr(), block_tables.data_ptr(),
+                                 context_lens.data_ptr(), ctypes.byref(shape), float(scale),
+                                 int(max_context_len), int(partition_tokens),
+                                 workspace.data_ptr(), workspace.numel() * workspace.element_size(),
+                                 _stream_ptr(stream)), "pa_decode_splitkv")
+    return out
+
+
+def resolve_blocks(out_phys, block_tables, context_lens, block_size: int, num_blocks: int,
+                   stream=None):
+    """Physical block the kernels read for each (sequence, logical page); -1 if none."""
+    _dev_tensors(out_phys, block_tables, context_lens)
+    _ints(block_tables, context_lens)
+    if out_phys.dtype != torch.int32 or out_phys.shape != block_tables.shape:
+        raise ValueError("out_phys must be int32 shaped like block_tables")
+    B, mb = block_tables.shape
+    shape = _Shape(B, 1, 1, 64, int(block_size), mb, int(num_blocks), F16, F32)
+    _check(_load().pa_resolve_blocks(out_phys.data_ptr(), block_tables.data_ptr(),
+                                     context_lens.data_ptr(), ctypes.byref(shape),
+                                     _stream_ptr(stream)), "pa_resolve_blocks")
+    return out_phys
+
+
+def device_error(stream=None) -> int:
+    """Read and clear the device error word (synchronises the stream)."""
+    code = ctypes.c_int32(0)
+    _check(_load().pa_device_error(ctypes.byref(code), _stream_ptr(stream)), "pa_device_error")
+    return int(code.value)

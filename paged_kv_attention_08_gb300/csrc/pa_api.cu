@@ -1,0 +1,401 @@
+// Host side of the C ABI in include/pa_decode.h: validation, the split-KV
+// plan, TMA descriptors, and the launches.
+#include <cudaTypedefs.h>
+
+#include <atomic>
+#include <cstdlib>
+#include <cstring>
+#include <mutex>
+
+#include "pa_internal.h"
+
+// One error word per device; kernels set it when a bounded wait runs out.
+__device__ int32_t pa_device_error_word;
+
+namespace pa {
+namespace {
+
+constexpr int kMaxDevices = 64;
+constexpr uint64_t kDefaultTimeoutNs = 2000000000ull;  // 2 s per wait
+std::atomic<int> g_sm_count[kMaxDevices];
+std::atomic<int32_t*> g_err_word[kMaxDevices];
+
+std::once_flag g_encode_once;
+PFN_cuTensorMapEncodeTiled_v12000 g_encode = nullptr;
+
+int elem_size(int dtype) { return dtype == PA_F32 ? 4 : 2; }
+
+bool aligned(const void* ptr, size_t a) { return reinterpret_cast<uintptr_t>(ptr) % a == 0; }
+
+bool pow2_group_ok(int g) { return g == 1 || g == 2 || g == 4 || g == 8 || g == 16; }
+
+pa_status check_shape(const pa_shape* s) {
+    if (!s) return PA_ERR_INVALID_ARG;
+    if (s->batch < 0 || s->num_heads <= 0 || s->num_kv_heads <= 0 || s->head_dim <= 0 ||
+        s->block_size <= 0 || s->max_blocks_per_seq <= 0 || s->num_blocks <= 0)
+        return PA_ERR_INVALID_ARG;
+    if (s->num_heads % s->num_kv_heads != 0) return PA_ERR_INVALID_ARG;
+    if (s->kv_dtype != PA_F16 && s->kv_dtype != PA_BF16) return PA_ERR_UNSUPPORTED;
+    if (s->out_dtype != PA_F32 && s->out_dtype != s->kv_dtype) return PA_ERR_UNSUPPORTED;
+    if (!pow2_group_ok(s->num_heads / s->num_kv_heads)) return PA_ERR_UNSUPPORTED;
+    if (s->head_dim != 64 && s->head_dim != 128 && s->head_dim != 256) return PA_ERR_UNSUPPORTED;
+    if (s->block_size != 16 && s->block_size != 32) return PA_ERR_UNSUPPORTED;
+    if (s->batch > 65535 || s->num_kv_heads > 65535) return PA_ERR_UNSUPPORTED;
+    if (s->num_blocks >= (int64_t(1) << 31)) return PA_ERR_UNSUPPORTED;
+    if ((int64_t)s->max_blocks_per_seq * s->block_size >= (int64_t(1) << 31))
+        return PA_ERR_UNSUPPORTED;
+    return PA_OK;
+}
+
+pa_status check_ptrs(const void* out, const void* q, const void* k, const void* v,
+                     const int32_t* bt, const int32_t* lens) {
+    if (!out || !q || !k || !v || !bt || !lens) return PA_ERR_INVALID_ARG;
+    if (!aligned(out, 16) || !aligned(q, 16) || !aligned(k, 16) || !aligned(v, 16))
+        return PA_ERR_INVALID_ARG;
+    if (!aligned(bt, 4) || !aligned(lens, 4)) return PA_ERR_INVALID_ARG;
+    return PA_OK;
+}
+
+// SM count and error-word address of the current device (cached).
+pa_status device_state(int* sms, int32_t** err) {
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) return PA_ERR_CUDA;
+    if (dev < 0 || dev >= kMaxDevices) return PA_ERR_UNSUPPORTED;
+    int n = g_sm_count[dev].load(std::memory_order_relaxed);
+    if (n == 0) {
+        if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || n <= 0)
+            return PA_ERR_CUDA;
+        g_sm_count[dev].store(n, std::memory_order_relaxed);
+    }
+    int32_t* e = g_err_word[dev].load(std::memory_order_acquire);
+    if (!e) {
+        void* ptr = nullptr;
+        if (cudaGetSymbolAddress(&ptr, pa_device_error_word) != cudaSuccess || !ptr)
+            return PA_ERR_CUDA;
+        e = static_cast<int32_t*>(ptr);
+        g_err_word[dev].store(e, std::memory_order_release);
+    }
+    if (sms) *sms = n;
+    if (err) *err = e;
+    return PA_OK;
+}
+
+// Launch shape of the attention kernel for one problem: warps per stream
+// (head-group slices), streams per CTA and stages per stream.
+struct Tune {
+    int gw, nh, nt, ns;
+};
+
+int env_int(const char* name, int fallback) {
+    const char* s = std::getenv(name);
+    if (!s || !*s) return fallback;
+    const int v = std::atoi(s);
+    return v > 0 ? v : fallback;
+}
+
+Tune pick_tune(const pa_shape* s) {
+    Tune t;
+    const int G = s->num_heads / s->num_kv_heads;
+    t.gw = G < kHeadsPerWarpMax ? G : kHeadsPerWarpMax;
+    t.nh = G / t.gw;
+    const int stage = 2 * s->block_size * s->head_dim * elem_size(s->kv_dtype);
+    t.nt = t.nh >= 4 ? 2 : (t.nh == 2 ? 2 : 4);
+    // Stages per stream: about 96 KB of pages in flight per CTA, at least two.
+    int ns = (96 * 1024) / (t.nt * stage);
+    t.ns = ns < 2 ? 2 : (ns > 8 ? 8 : ns);
+    static const int env_nt = env_int("PA_TUNE_STREAMS", 0);
+    static const int env_ns = env_int("PA_TUNE_STAGES", 0);
+    if (env_nt > 0 && env_nt * t.nh <= 8) t.nt = env_nt;
+    if (env_ns > 0 && env_ns <= 16) t.ns = env_ns;
+    return t;
+}
+
+AttnSmem tune_smem(const pa_shape* s, const Tune& t) {
+    const int LPT = s->head_dim / 8, TPS = 32 / LPT;
+    const int STEPS = (8 * TPS <= s->block_size) ? 8 : s->block_size / TPS;
+    return attn_smem_layout(s->head_dim, s->block_size, elem_size(s->kv_dtype), t.gw, TPS, STEPS,
+                            t.nt, t.nh, t.ns);
+}
+
+int pages_for(const pa_shape* s, int32_t max_context_len) {
+    int64_t t = max_context_len < 1 ? 1 : max_context_len;
+    const int64_t cap = (int64_t)s->max_blocks_per_seq * s->block_size;
+    if (t > cap) t = cap;
+    return (int)((t + s->block_size - 1) / s->block_size);
+}
+
+// Automatic partition size.  Cost model, in units of one page's time at a
+// fair share of bandwidth: a wave of resident CTAs costs (pages per CTA + a
+// fixed start-up of kCtaStartPages); splitting adds the combine pass
+// (kCombinePages).  The sequence length assumed is the longest one.
+int32_t choose_partition_tokens(const pa_shape* s, int32_t max_context_len, int num_sms) {
+    constexpr double kCtaStartPages = 4.0;
+    constexpr double kCombinePages = 8.0;
+    const Tune t = pick_tune(s);
+    const AttnSmem L = tune_smem(s, t);
+    int ctas_per_sm = (int)((227u * 1024u) / (L.total + kSmemAlignSlack));
+    if (ctas_per_sm < 1) ctas_per_sm = 1;
+    if (ctas_per_sm > 8) ctas_per_sm = 8;
+    const int64_t slots = (int64_t)num_sms * ctas_per_sm;
+    const int pages = pages_for(s, max_context_len);
+    const int64_t units = (int64_t)s->batch * s->num_kv_heads;
+    int best_pp = pages;
+    double best = 1e300;
+    int last_parts = 0;
+    for (int pp = pages; pp >= 1; --pp) {
+        const int parts = (pages + pp - 1) / pp;
+        if (parts == last_parts) continue;
+        last_parts = parts;
+        const int use_pp = (pages + parts - 1) / parts;  // smallest pp giving this count
+        const int64_t ctas = units * parts;
+        const int64_t waves = (ctas + slots - 1) / slots;
+        const double cost = (double)waves * (use_pp + kCtaStartPages) + (parts > 1 ? kCombinePages : 0.0);
+        if (cost < best - 1e-9) {
+            best = cost;
+            best_pp = use_pp;
+        }
+    }
+    return best_pp * s->block_size;
+}
+
+struct Plan {
+    int part_pages, num_parts;
+};
+
+Plan make_plan(const pa_shape* s, int32_t max_context_len, int32_t partition_tokens) {
+    const int pages = pages_for(s, max_context_len);
+    const int pp = partition_tokens / s->block_size;
+    Plan p;
+    p.num_parts = (pages + pp - 1) / pp;
+    p.part_pages = p.num_parts <= 1 ? s->max_blocks_per_seq : pp;
+    if (p.num_parts < 1) p.num_parts = 1;
+    return p;
+}
+
+// Workspace: part_acc [B, Hkv, P, G, D] fp32, then part_ml [B, Hkv, P, G, 2] fp32.
+size_t workspace_bytes_for(const pa_shape* s, int num_parts, size_t* ml_offset) {
+    if (num_parts <= 1) return 0;
+    const size_t rows = (size_t)s->batch * s->num_heads * num_parts;  // B*Hkv*P*G
+    const size_t acc = rows * s->head_dim * sizeof(float);
+    const size_t off = (acc + 255) / 256 * 256;
+    if (ml_offset) *ml_offset = off;
+    return off + rows * 2 * sizeof(float);
+}
+
+pa_status encode_maps(const pa_shape* s, const void* k, const void* v, CUtensorMap* mk,
+                      CUtensorMap* mv) {
+    std::call_once(g_encode_once, [] {
+        void* fn = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &fn, 12000,
+                                             cudaEnableDefault, &q) == cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            g_encode = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(fn);
+    });
+    if (!g_encode) return PA_ERR_CUDA;
+    const cuuint64_t e = elem_size(s->kv_dtype);
+    // dims innermost first: head_dim, kv head, slot in block, block
+    const cuuint64_t dims[4] = {(cuuint64_t)s->head_dim, (cuuint64_t)s->num_kv_heads,
+                                (cuuint64_t)s->block_size, (cuuint64_t)s->num_blocks};
+    const cuuint64_t strides[3] = {e * s->head_dim, e * s->head_dim * s->num_kv_heads,
+                                   e * s->head_dim * s->num_kv_heads * s->block_size};
+    const cuuint32_t box[4] = {(cuuint32_t)s->head_dim, 1u, (cuuint32_t)s->block_size, 1u};
+    const cuuint32_t estr[4] = {1u, 1u, 1u, 1u};
+    const CUtensorMapDataType dt =
+        s->kv_dtype == PA_BF16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16;
+    for (int which = 0; which < 2; ++which) {
+        CUresult r = g_encode(which ? mv : mk, dt, 4, const_cast<void*>(which ? v : k), dims,
+                              strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                              CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                              CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+        if (r != CUDA_SUCCESS) return PA_ERR_CUDA;
+    }
+    return PA_OK;
+}
+
+pa_status launch_attention(void* out, const void* q, const void* k, const void* v,
+                           const int32_t* bt, const int32_t* lens, const pa_shape* s, float scale,
+                           const Plan& plan, float* part_acc, float* part_ml, int32_t* err,
+                           cudaStream_t stream) {
+    AttnLaunch L;
+    std::memset(&L, 0, sizeof L);
+    pa_status st = encode_maps(s, k, v, &L.tmap_k, &L.tmap_v);
+    if (st != PA_OK) return st;
+    const Tune t = pick_tune(s);
+    const AttnSmem sm = tune_smem(s, t);
+    AttnParams& p = L.p;
+    p.q = q;
+    p.out = out;
+    p.block_tables = bt;
+    p.context_lens = lens;
+    p.part_acc = part_acc;
+    p.part_ml = part_ml;
+    p.err = err;
+    p.batch = s->batch;
+    p.num_heads = s->num_heads;
+    p.num_kv_heads = s->num_kv_heads;
+    p.group = s->num_heads / s->num_kv_heads;
+    p.max_blocks = s->max_blocks_per_seq;
+    p.num_blocks = s->num_blocks;
+    p.qscale = scale * 1.4426950408889634f;  // log2(e)
+    p.part_pages = plan.part_pages;
+    p.num_parts = plan.num_parts;
+    p.nt = t.nt;
+    p.nh = t.nh;
+    p.ns = t.ns;
+    p.out_dtype = s->out_dtype;
+    p.final_out = plan.num_parts <= 1 ? 1 : 0;
+    p.timeout_ns = kDefaultTimeoutNs;
+    L.head_dim = s->head_dim;
+    L.block_size = s->block_size;
+    L.kv_dtype = s->kv_dtype;
+    L.heads_per_warp = t.gw;
+    L.grid = dim3((unsigned)plan.num_parts, (unsigned)s->num_kv_heads, (unsigned)s->batch);
+    L.threads = 32 * t.nt * t.nh;
+    L.smem_bytes = sm.total + kSmemAlignSlack;
+    cudaError_t e;
+    switch (s->head_dim) {
+        case 64: e = launch_attn_d64(L, stream); break;
+        case 128: e = launch_attn_d128(L, stream); break;
+        default: e = launch_attn_d256(L, stream); break;
+    }
+    return e == cudaSuccess ? PA_OK : PA_ERR_CUDA;
+}
+
+}  // namespace
+}  // namespace pa
+
+using namespace pa;
+
+extern "C" {
+
+const char* pa_status_string(pa_status status) {
+    switch (status) {
+        case PA_OK: return "ok";
+        case PA_ERR_INVALID_ARG: return "invalid argument";
+        case PA_ERR_UNSUPPORTED: return "unsupported shape or dtype";
+        case PA_ERR_WORKSPACE: return "workspace missing, misaligned or too small";
+        case PA_ERR_CUDA: return "CUDA error";
+        case PA_ERR_TIMEOUT: return "kernel wait timed out";
+    }
+    return "unknown status";
+}
+
+int32_t pa_choose_partition_tokens(const pa_shape* shape, int32_t max_context_len,
+                                   int32_t num_sms) {
+    if (check_shape(shape) != PA_OK || max_context_len < 0 || num_sms <= 0) return 0;
+    return choose_partition_tokens(shape, max_context_len, num_sms);
+}
+
+size_t pa_workspace_size(const pa_shape* shape, int32_t max_context_len,
+                         int32_t partition_tokens) {
+    if (check_shape(shape) != PA_OK || max_context_len < 0 || partition_tokens < 0) return 0;
+    if (partition_tokens % shape->block_size != 0) return 0;
+    if (partition_tokens == 0) {
+        int sms = 0;
+        if (device_state(&sms, nullptr) != PA_OK) return 0;
+        partition_tokens = choose_partition_tokens(shape, max_context_len, sms);
+    }
+    const Plan plan = make_plan(shape, max_context_len, partition_tokens);
+    return workspace_bytes_for(shape, plan.num_parts, nullptr);
+}
+
+pa_status pa_decode(void* out, const void* q, const void* k_cache, const void* v_cache,
+                    const int32_t* block_tables, const int32_t* context_lens,
+                    const pa_shape* shape, float scale, void* stream) {
+    pa_status st = check_shape(shape);
+    if (st != PA_OK) return st;
+    if (shape->batch == 0) return PA_OK;
+    st = check_ptrs(out, q, k_cache, v_cache, block_tables, context_lens);
+    if (st != PA_OK) return st;
+    int32_t* err = nullptr;
+    st = device_state(nullptr, &err);
+    if (st != PA_OK) return st;
+    Plan plan{shape->max_blocks_per_seq, 1};
+    return launch_attention(out, q, k_cache, v_cache, block_tables, context_lens, shape, scale,
+                            plan, nullptr, nullptr, err, static_cast<cudaStream_t>(stream));
+}
+
+pa_status pa_decode_splitkv(void* out, const void* q, const void* k_cache, const void* v_cache,
+                            const int32_t* block_tables, const int32_t* context_lens,
+                            const pa_shape* shape, float scale, int32_t max_context_len,
+                            int32_t partition_tokens, void* workspace, size_t workspace_bytes,
+                            void* stream) {
+    pa_status st = check_shape(shape);
+    if (st != PA_OK) return st;
+    if (max_context_len < 0 || partition_tokens < 0 || partition_tokens % shape->block_size != 0)
+        return PA_ERR_INVALID_ARG;
+    if (shape->batch == 0) return PA_OK;
+    st = check_ptrs(out, q, k_cache, v_cache, block_tables, context_lens);
+    if (st != PA_OK) return st;
+    int sms = 0;
+    int32_t* err = nullptr;
+    st = device_state(&sms, &err);
+    if (st != PA_OK) return st;
+    if (partition_tokens == 0) partition_tokens = choose_partition_tokens(shape, max_context_len, sms);
+    const Plan plan = make_plan(shape, max_context_len, partition_tokens);
+    cudaStream_t cs = static_cast<cudaStream_t>(stream);
+    if (plan.num_parts <= 1)
+        return launch_attention(out, q, k_cache, v_cache, block_tables, context_lens, shape, scale,
+                                plan, nullptr, nullptr, err, cs);
+
+    size_t ml_off = 0;
+    const size_t need = workspace_bytes_for(shape, plan.num_parts, &ml_off);
+    if (!workspace || !aligned(workspace, 16) || workspace_bytes < need) return PA_ERR_WORKSPACE;
+    const uint32_t combine_smem = (uint32_t)plan.num_parts * sizeof(float);
+    if (combine_smem > 200u * 1024u) return PA_ERR_UNSUPPORTED;
+    float* part_acc = static_cast<float*>(workspace);
+    float* part_ml = reinterpret_cast<float*>(static_cast<char*>(workspace) + ml_off);
+    st = launch_attention(out, q, k_cache, v_cache, block_tables, context_lens, shape, scale, plan,
+                          part_acc, part_ml, err, cs);
+    if (st != PA_OK) return st;
+    CombineParams c;
+    c.out = out;
+    c.context_lens = context_lens;
+    c.part_acc = part_acc;
+    c.part_ml = part_ml;
+    c.batch = shape->batch;
+    c.num_heads = shape->num_heads;
+    c.num_kv_heads = shape->num_kv_heads;
+    c.group = shape->num_heads / shape->num_kv_heads;
+    c.max_blocks = shape->max_blocks_per_seq;
+    c.block_size = shape->block_size;
+    c.part_pages = plan.part_pages;
+    c.num_parts = plan.num_parts;
+    c.out_dtype = shape->out_dtype;
+    const cudaError_t e = launch_combine(c, shape->head_dim,
+                                         dim3((unsigned)shape->num_heads, (unsigned)shape->batch),
+                                         shape->head_dim, combine_smem, cs);
+    return e == cudaSuccess ? PA_OK : PA_ERR_CUDA;
+}
+
+pa_status pa_resolve_blocks(int32_t* out_phys, const int32_t* block_tables,
+                            const int32_t* context_lens, const pa_shape* shape, void* stream) {
+    pa_status st = check_shape(shape);
+    if (st != PA_OK) return st;
+    if (shape->batch == 0) return PA_OK;
+    if (!out_phys || !block_tables || !context_lens || !aligned(out_phys, 4) ||
+        !aligned(block_tables, 4) || !aligned(context_lens, 4))
+        return PA_ERR_INVALID_ARG;
+    const cudaError_t e = launch_resolve(out_phys, block_tables, context_lens, shape->batch,
+                                         shape->max_blocks_per_seq, shape->block_size,
+                                         shape->num_blocks, static_cast<cudaStream_t>(stream));
+    return e == cudaSuccess ? PA_OK : PA_ERR_CUDA;
+}
+
+pa_status pa_device_error(int32_t* code, void* stream) {
+    if (!code) return PA_ERR_INVALID_ARG;
+    int32_t* err = nullptr;
+    pa_status st = device_state(nullptr, &err);
+    if (st != PA_OK) return st;
+    cudaStream_t cs = static_cast<cudaStream_t>(stream);
+    int32_t v = 0;
+    if (cudaMemcpyAsync(&v, err, sizeof v, cudaMemcpyDeviceToHost, cs) != cudaSuccess)
+        return PA_ERR_CUDA;
+    if (cudaMemsetAsync(err, 0, sizeof(int32_t), cs) != cudaSuccess) return PA_ERR_CUDA;
+    if (cudaStreamSynchronize(cs) != cudaSuccess) return PA_ERR_CUDA;
+    *code = v;
+    return PA_OK;
+}
+
+}  // extern "C"

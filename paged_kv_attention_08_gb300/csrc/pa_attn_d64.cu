@@ -1,0 +1,9 @@
+// Instantiations of the decode kernel for head_dim 64 (kept in their own
+// translation unit so that the library builds in parallel).
+#include "pa_attn.cuh"
+
+namespace pa {
+cudaError_t launch_attn_d64(const AttnLaunch& L, cudaStream_t stream) {
+    return launch_attn_for_d<64>(L, stream);
+}
+}  // namespace pa

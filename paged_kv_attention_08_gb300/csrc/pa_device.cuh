@@ -1,0 +1,169 @@
+// Device helpers of the decode library: the page walk, mbarrier / TMA inline
+// PTX with bounded waits, and 16-byte vector conversions.
+#pragma once
+
+#include <cuda.h>
+#include <cuda_bf16.h>
+#include <cuda_fp16.h>
+#include <cuda_runtime.h>
+#include <math.h>
+#include <stdint.h>
+
+#include "pa_internal.h"
+
+namespace pa {
+
+constexpr unsigned kFullMask = 0xffffffffu;
+
+// ---------------------------------------------------------------------------
+// Page walk (MiniVLLM docs "Decoding Benchmark", "Block table lookup
+// mechanics"): logical page j of a sequence lives in physical block
+// block_tables[b][j].  A page holds attended tokens only if j < npages; an
+// entry that is -1 or outside [0, num_blocks) is masked and never read.
+// ---------------------------------------------------------------------------
+__device__ __forceinline__ int reachable_tokens(const int32_t* context_lens, int b, int max_blocks,
+                                                int block_size) {
+    int t = __ldg(context_lens + b);
+    const int cap = max_blocks * block_size;
+    t = t < 0 ? 0 : t;
+    return t > cap ? cap : t;
+}
+
+__device__ __forceinline__ int page_phys(const int32_t* table_row, int j, int npages,
+                                         int64_t num_blocks) {
+    if (j >= npages) return -1;
+    const int e = __ldg(table_row + j);
+    return (e >= 0 && (int64_t)e < num_blocks) ? e : -1;
+}
+
+// ---------------------------------------------------------------------------
+// mbarrier / TMA
+// ---------------------------------------------------------------------------
+__device__ __forceinline__ uint32_t smem_u32(const void* p) {
+    return static_cast<uint32_t>(__cvta_generic_to_shared(p));
+}
+
+__device__ __forceinline__ void mbar_init(uint32_t bar, uint32_t count) {
+    asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(bar), "r"(count) : "memory");
+}
+
+__device__ __forceinline__ void mbar_init_fence() {
+    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+}
+
+__device__ __forceinline__ void mbar_arrive(uint32_t bar) {
+    asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(bar) : "memory");
+}
+
+__device__ __forceinline__ void mbar_arrive_expect_tx(uint32_t bar, uint32_t bytes) {
+    asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(bar), "r"(bytes)
+                 : "memory");
+}
+
+__device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
+    uint32_t ok;
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+        "selp.u32 %0, 1, 0, p;\n\t}"
+        : "=r"(ok)
+        : "r"(bar), "r"(parity)
+        : "memory");
+    return ok != 0;
+}
+
+__device__ __forceinline__ uint64_t global_timer_ns() {
+    uint64_t t;
+    asm volatile("mov.u64 %0, %globaltimer;" : "=l"(t));
+    return t;
+}
+
+// Wait for phase `parity` of an mbarrier, giving up after `timeout_ns`.
+// Returns false on timeout; the caller records the error and abandons work.
+__device__ __forceinline__ bool mbar_wait_bounded(uint32_t bar, uint32_t parity,
+                                                  uint64_t timeout_ns) {
+    if (mbar_try_wait(bar, parity)) return true;
+    const uint64_t start = global_timer_ns();
+    for (uint32_t it = 1;; ++it) {
+        if (mbar_try_wait(bar, parity)) return true;
+        if ((it & 63u) == 0 && global_timer_ns() - start > timeout_ns) return false;
+    }
+}
+
+// Order this thread's earlier generic-proxy shared-memory accesses before
+// later async-proxy (TMA) writes to the same buffers.
+__device__ __forceinline__ void fence_proxy_async_smem() {
+    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+}
+
+// 4-D tiled TMA load into shared memory; completion is signalled on `bar`
+// as transaction bytes.  Coordinates are innermost first.
+__device__ __forceinline__ void tma_load_4d(uint32_t dst, const CUtensorMap* map, int c0, int c1,
+                                            int c2, int c3, uint32_t bar, uint64_t policy) {
+    asm volatile(
+        "cp.async.bulk.tensor.4d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
+        ".L2::cache_hint [%0], [%1, {%2, %3, %4, %5}], [%6], %7;" ::"r"(dst),
+        "l"(reinterpret_cast<uint64_t>(map)), "r"(c0), "r"(c1), "r"(c2), "r"(c3), "r"(bar),
+        "l"(policy)
+        : "memory");
+}
+
+// L2 policy for data read exactly once per step: evict it first.
+__device__ __forceinline__ uint64_t l2_policy_evict_first() {
+    uint64_t pol;
+    asm volatile("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;" : "=l"(pol));
+    return pol;
+}
+
+__device__ __forceinline__ void prefetch_tensormap(const CUtensorMap* map) {
+    asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(map)) : "memory");
+}
+
+__device__ __forceinline__ void record_error(int32_t* err, int32_t code) {
+    if (err) atomicCAS(err, 0, code);
+}
+
+// ---------------------------------------------------------------------------
+// 16-byte vectors of eight fp16 / bf16 values -> fp32
+// ---------------------------------------------------------------------------
+template <typename KV>
+struct Vec8;
+
+template <>
+struct Vec8<__half> {
+    static __device__ __forceinline__ void to_float(const uint4& r, float (&f)[8]) {
+        const __half2* h = reinterpret_cast<const __half2*>(&r);
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+            const float2 x = __half22float2(h[i]);
+            f[2 * i] = x.x;
+            f[2 * i + 1] = x.y;
+        }
+    }
+};
+
+template <>
+struct Vec8<__nv_bfloat16> {
+    static __device__ __forceinline__ void to_float(const uint4& r, float (&f)[8]) {
+        const __nv_bfloat162* h = reinterpret_cast<const __nv_bfloat162*>(&r);
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+            const float2 x = __bfloat1622float2(h[i]);
+            f[2 * i] = x.x;
+            f[2 * i + 1] = x.y;
+        }
+    }
+};
+
+// Store one fp32 value as the output dtype.
+__device__ __forceinline__ void store_out(void* out, size_t idx, float v, int out_dtype) {
+    if (out_dtype == PA_F32) {
+        static_cast<float*>(out)[idx] = v;
+    } else if (out_dtype == PA_F16) {
+        static_cast<__half*>(out)[idx] = __float2half_rn(v);
+    } else {
+        static_cast<__nv_bfloat16*>(out)[idx] = __float2bfloat16_rn(v);
+    }
+}
+
+}  // namespace pa

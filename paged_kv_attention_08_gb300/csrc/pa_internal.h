@@ -1,0 +1,110 @@
+// Internal host/device declarations shared by the decode library's translation
+// units: the kernel parameter block, the shared-memory layout of the attention
+// kernel, and the per-head_dim launchers.
+#pragma once
+
+#include <cuda.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "../../include/pa_decode.h"
+
+namespace pa {
+
+// Up to this many query heads share one kv head (num_heads / num_kv_heads).
+constexpr int kMaxGroup = 16;
+// Query heads one warp carries through a page (its share of the group).
+constexpr int kHeadsPerWarpMax = 4;
+
+struct AttnParams {
+    const void* q;            // [B, H, D] kv dtype
+    void* out;                // [B, H, D] out dtype (final mode)
+    const int32_t* block_tables;
+    const int32_t* context_lens;
+    float* part_acc;          // [B, Hkv, P, G, D] fp32 (split mode)
+    float* part_ml;           // [B, Hkv, P, G, 2] fp32 (split mode): running max (log2 units), normaliser
+    int32_t* err;             // device error word
+    int32_t batch, num_heads, num_kv_heads, group, max_blocks;
+    int64_t num_blocks;
+    float qscale;             // scale * log2(e): scores are kept in base-2 units
+    int32_t part_pages;       // pages per partition
+    int32_t num_parts;        // partitions per (sequence, kv head) = gridDim.x
+    int32_t nt;               // token streams (independent page rings) per CTA
+    int32_t nh;               // warps per stream, each holding a slice of the head group
+    int32_t ns;               // pipeline stages per stream
+    int32_t out_dtype;        // pa_dtype
+    int32_t final_out;        // 1: write out; 0: write partials
+    uint64_t timeout_ns;      // bound on every wait of the copy pipeline
+};
+
+struct CombineParams {
+    void* out;
+    const int32_t* context_lens;
+    const float* part_acc;
+    const float* part_ml;
+    int32_t batch, num_heads, num_kv_heads, group, max_blocks, block_size;
+    int32_t part_pages, num_parts, out_dtype;
+};
+
+// Shared-memory layout of the attention kernel, identical on host and device.
+struct AttnSmem {
+    uint32_t stage_bytes;   // one stage: K tile then V tile, each block_size x head_dim
+    uint32_t stages_off;    // [nt][ns] stages
+    uint32_t full_off;      // [nt][ns] uint64 mbarriers: page landed
+    uint32_t empty_off;     // [nt][ns] uint64 mbarriers: page consumed
+    uint32_t phys_off;      // [nt][ns] int32 physical block of the staged page (-1 = masked)
+    uint32_t pbuf_off;      // per warp: probabilities of one chunk
+    uint32_t mrg_off;       // per warp: acc [GW][D] then m [GW], l [GW] for the final merge
+    uint32_t total;         // bytes, excluding the alignment slack
+};
+
+__host__ __device__ inline uint32_t pa_align_up(uint32_t x, uint32_t a) { return (x + a - 1) / a * a; }
+
+__host__ __device__ inline AttnSmem attn_smem_layout(int D, int BS, int esize, int GW, int TPS,
+                                                     int STEPS, int nt, int nh, int ns) {
+    AttnSmem L;
+    const int nw = nt * nh;
+    L.stage_bytes = 2u * BS * D * esize;
+    L.stages_off = 0;
+    uint32_t o = L.stage_bytes * nt * ns;
+    L.full_off = o;
+    o += 8u * nt * ns;
+    L.empty_off = o;
+    o += 8u * nt * ns;
+    L.phys_off = o;
+    o = pa_align_up(o + 4u * nt * ns, 16);
+    L.pbuf_off = o;
+    o += 4u * nw * TPS * STEPS * GW;
+    o = pa_align_up(o, 16);
+    L.mrg_off = o;
+    o += 4u * nw * GW * (D + 2);
+    L.total = pa_align_up(o, 16);
+    return L;
+}
+
+// Slack added to the dynamic shared-memory request so that the kernel can
+// align its base to 1024 bytes (TMA destinations).
+constexpr uint32_t kSmemAlignSlack = 1024;
+
+struct AttnLaunch {
+    AttnParams p;
+    CUtensorMap tmap_k;
+    CUtensorMap tmap_v;
+    int head_dim, block_size, kv_dtype, heads_per_warp;
+    dim3 grid;
+    int threads;
+    uint32_t smem_bytes;
+};
+
+// Per-head_dim launchers (one translation unit each, compiled in parallel).
+cudaError_t launch_attn_d64(const AttnLaunch& L, cudaStream_t stream);
+cudaError_t launch_attn_d128(const AttnLaunch& L, cudaStream_t stream);
+cudaError_t launch_attn_d256(const AttnLaunch& L, cudaStream_t stream);
+
+cudaError_t launch_combine(const CombineParams& p, int head_dim, dim3 grid, int threads,
+                           uint32_t smem_bytes, cudaStream_t stream);
+cudaError_t launch_resolve(int32_t* out_phys, const int32_t* block_tables,
+                           const int32_t* context_lens, int32_t batch, int32_t max_blocks,
+                           int32_t block_size, int64_t num_blocks, cudaStream_t stream);
+
+}  // namespace pa

@@ -1,0 +1,141 @@
+"""CPU-side checks of the C ABI: the library loads, exports every entry point
+that include/*.h declares, and its host logic (status strings, validation,
+partition choice, workspace sizing) behaves as documented.  No call here
+reaches a kernel launch: every decode call is built to fail validation first.
+"""
+import ctypes
+import glob
+import os
+import re
+
+import pytest
+import torch
+
+import paged_kv_attention_08_gb300 as pa
+from paged_kv_attention_08_gb300 import build as pa_build
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+def declared_entry_points():
+    names = set()
+    for h in glob.glob(os.path.join(ROOT, "include", "*.h")):
+        text = re.sub(r"/\*.*?\*/", "", open(h).read(), flags=re.S)
+        names.update(re.findall(r"\b(pa_[a-z_0-9]+)\s*\(", text))
+    return sorted(names)
+
+
+@pytest.fixture(scope="module")
+def lib():
+    pa_build.build()
+    pa._load()
+    return pa._lib
+
+
+def test_library_exports_every_declared_symbol(lib):
+    names = declared_entry_points()
+    assert {"pa_decode", "pa_decode_splitkv", "pa_workspace_size", "pa_resolve_blocks",
+            "pa_status_string", "pa_choose_partition_tokens", "pa_device_error"} <= set(names)
+    for n in names:
+        assert hasattr(lib, n), f"{n} declared in include/ but not exported"
+
+
+def test_status_strings(lib):
+    for code in range(6):
+        assert lib.pa_status_string(code)
+    assert lib.pa_status_string(99) == b"unknown status"
+
+
+def shape(**kw):
+    base = dict(batch=4, num_heads=32, num_kv_heads=8, head_dim=128, block_size=16,
+                max_blocks_per_seq=128, num_blocks=512, kv_dtype=pa.F16, out_dtype=pa.F32)
+    base.update(kw)
+    return pa._Shape(**base)
+
+
+FAKE = 0x10000  # 16-byte aligned, never dereferenced: validation fails before any launch
+
+
+@pytest.mark.parametrize("kw,code", [
+    (dict(num_heads=30), 1),                 # H % Hkv != 0
+    (dict(batch=-1), 1),
+    (dict(max_blocks_per_seq=0), 1),
+    (dict(num_blocks=0), 1),
+    (dict(head_dim=96), 2),
+    (dict(block_size=8), 2),
+    (dict(num_heads=24, num_kv_heads=8), 2),  # group 3
+    (dict(kv_dtype=pa.F32), 2),
+    (dict(out_dtype=pa.BF16), 2),             # neither fp32 nor the kv dtype
+    (dict(num_blocks=1 << 31), 2),
+])
+def test_shape_validation(lib, kw, code):
+    s = shape(**kw)
+    rc = lib.pa_decode(FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, ctypes.byref(s), 0.1, None)
+    assert rc == code
+    rc = lib.pa_decode_splitkv(FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, ctypes.byref(s), 0.1, 100, 0,
+                               FAKE, 1 << 20, None)
+    assert rc == code
+
+
+def test_pointer_validation(lib):
+    s = shape()
+    assert lib.pa_decode(None, FAKE, FAKE, FAKE, FAKE, FAKE, ctypes.byref(s), 0.1, None) == 1
+    assert lib.pa_decode(FAKE + 8, FAKE, FAKE, FAKE, FAKE, FAKE, ctypes.byref(s), 0.1, None) == 1
+    assert lib.pa_decode(FAKE, FAKE, FAKE, FAKE, FAKE + 2, FAKE, ctypes.byref(s), 0.1, None) == 1
+    assert lib.pa_decode(FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, None, 0.1, None) == 1
+    # split-only arguments
+    assert lib.pa_decode_splitkv(FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, ctypes.byref(s), 0.1, -1, 0,
+                                 FAKE, 1 << 20, None) == 1
+    assert lib.pa_decode_splitkv(FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, ctypes.byref(s), 0.1, 100, 24,
+                                 FAKE, 1 << 20, None) == 1
+    # an empty batch is a no-op, whatever the pointers
+    e = shape(batch=0)
+    assert lib.pa_decode(None, None, None, None, None, None, ctypes.byref(e), 0.1, None) == 0
+    assert lib.pa_resolve_blocks(None, FAKE, FAKE, ctypes.byref(s), None) == 1
+
+
+def test_workspace_size_explicit_partition(lib):
+    s = shape(batch=4, max_blocks_per_seq=8192)
+    # 131072 tokens in partitions of 512: 256 partitions; acc then (m, l) rows
+    n = lib.pa_workspace_size(ctypes.byref(s), 131072, 512)
+    rows = 4 * 32 * 256
+    acc = rows * 128 * 4
+    assert n == (acc + 255) // 256 * 256 + rows * 2 * 4
+    assert lib.pa_workspace_size(ctypes.byref(s), 131072, 131072) == 0      # one partition
+    assert lib.pa_workspace_size(ctypes.byref(s), 131072, 100) == 0        # not a multiple of 16
+    assert lib.pa_workspace_size(ctypes.byref(s), 0, 512) == 0
+    # tokens past the table row are not planned for
+    s2 = shape(batch=1, max_blocks_per_seq=4)
+    assert lib.pa_workspace_size(ctypes.byref(s2), 10_000, 16) == \
+        (1 * 32 * 4 * 128 * 4 + 255) // 256 * 256 + 1 * 32 * 4 * 2 * 4
+
+
+@pytest.mark.parametrize("B,T,Hkv", [(1, 512, 8), (16, 256, 8), (4, 2048, 8), (64, 4096, 8),
+                                     (1, 131072, 8), (4, 131072, 8), (32, 16384, 1), (2, 60, 8)])
+def test_partition_choice_properties(lib, B, T, Hkv):
+    H = 32 if Hkv == 8 else 16
+    D, bs = (128, 16) if Hkv == 8 else (256, 32)
+    s = shape(batch=B, num_heads=H, num_kv_heads=Hkv, head_dim=D, block_size=bs,
+              max_blocks_per_seq=(T + bs - 1) // bs)
+    for sms in (1, 8, 148, 152):
+        pt = lib.pa_choose_partition_tokens(ctypes.byref(s), T, sms)
+        assert pt > 0 and pt % bs == 0
+        assert pt <= ((T + bs - 1) // bs) * bs
+    # many (sequence, kv head) pairs per SM need no split
+    assert lib.pa_choose_partition_tokens(ctypes.byref(s), T, 1) >= T
+    assert lib.pa_choose_partition_tokens(ctypes.byref(s), T, 0) == 0     # invalid SM count
+
+
+def test_single_sequence_long_context_is_split(lib):
+    s = shape(batch=1, max_blocks_per_seq=8192, kv_dtype=pa.BF16)
+    pt = lib.pa_choose_partition_tokens(ctypes.byref(s), 131072, 152)
+    parts = -(-131072 // pt)
+    assert parts * 8 >= 152           # at least one CTA per SM
+
+
+def test_binding_refuses_cpu_tensors():
+    x = torch.zeros(2, 32, 128, dtype=torch.float16)
+    with pytest.raises(ValueError):
+        pa.decode(torch.zeros(2, 32, 128), x, torch.zeros(8, 16, 8, 128, dtype=torch.float16),
+                  torch.zeros(8, 16, 8, 128, dtype=torch.float16),
+                  torch.zeros(2, 4, dtype=torch.int32), torch.zeros(2, dtype=torch.int32), 0.1)

@@ -1,0 +1,265 @@
+"""GPU parity: the CUDA path (through the C ABI) against the fp64 oracle.
+
+Bar: max |gpu - oracle| <= 2e-3 on fp32 output (fp16/bf16 K/V, fp32
+accumulate); q-dtype output within 2e-3 plus one ulp of the oracle rounded to
+that dtype; bit-exact page indices; bit-identical output under pool
+permutation and poison in unreferenced memory.
+"""
+import math
+
+import numpy as np
+import pytest
+import torch
+
+import oracle
+import paged_kv_attention_08_gb300 as pa
+from paged_kv_attention_08_gb300 import workloads
+
+pytestmark = pytest.mark.gpu
+
+TOL = 2e-3
+DEV = "cuda:0"
+
+
+def run(x, mode="single", out_dtype=torch.float32, partition_tokens=0):
+    out = torch.full(x.q.shape, float("nan"), dtype=out_dtype, device=x.q.device)
+    if mode == "single":
+        pa.decode(out, x.q, x.k_cache, x.v_cache, x.block_tables, x.context_lens, x.scale)
+    else:
+        pa.decode_splitkv(out, x.q, x.k_cache, x.v_cache, x.block_tables, x.context_lens, x.scale,
+                          x.max_context_len, partition_tokens)
+    torch.cuda.synchronize()
+    return out
+
+
+def assert_close_fp32(got, want, tol=TOL):
+    g = got.double().cpu().numpy()
+    assert np.isfinite(g).all(), "non-finite output"
+    err = np.abs(g - want).max()
+    assert err <= tol, f"max abs err {err:.3e} > {tol}"
+    return err
+
+
+def sample_rows(x, n, seed=0):
+    """(b, h) pairs: corners, the longest and shortest sequences, random others."""
+    B, H = x.q.shape[0], x.q.shape[1]
+    lens = x.lens_host
+    rows = {(0, 0), (B - 1, H - 1), (int(np.argmax(lens)), H // 2), (int(np.argmin(lens)), 1 % H)}
+    g = np.random.default_rng(seed)
+    while len(rows) < min(n, B * H):
+        rows.add((int(g.integers(B)), int(g.integers(H))))
+    return np.array(sorted(rows), dtype=np.int32)
+
+
+# ---------------------------------------------------------------------------
+# workloads small enough for the whole oracle
+# ---------------------------------------------------------------------------
+@pytest.mark.parametrize("name", ["tiny", "sweep_b1_t512", "sweep_b16_t256", "sweep_b4_t2048"])
+@pytest.mark.parametrize("mode,pt", [("single", 0), ("split", 0), ("split", 16), ("split", 64)])
+def test_small_workloads_vs_oracle(name, mode, pt):
+    x = workloads.make(name, seed=0, device=DEV)
+    want = oracle.decode(x.q, x.k_cache, x.v_cache, x.block_tables, x.context_lens, x.scale)
+    assert_close_fp32(run(x, mode, partition_tokens=pt), want)
+
+
+@pytest.mark.parametrize("name", ["tiny", "sweep_b4_t2048"])
+@pytest.mark.parametrize("mode", ["single", "split"])
+def test_qdtype_output(name, mode):
+    x = workloads.make(name, seed=1, device=DEV)
+    want = oracle.decode(x.q, x.k_cache, x.v_cache, x.block_tables, x.context_lens, x.scale)
+    got = run(x, mode, out_dtype=x.q.dtype).double().cpu().numpy()
+    want_r = torch.from_numpy(want).to(x.q.dtype).double().numpy()   # RNE to the output dtype
+    mant = 7 if x.q.dtype == torch.bfloat16 else 10
+    a = np.abs(want_r)
+    ulp = np.where(a > 0, 2.0 ** (np.floor(np.log2(np.where(a > 0, a, 1.0))) - mant), 2.0 ** -24)
+    assert np.isfinite(got).all()
+    assert (np.abs(got - want_r) <= TOL + ulp).all()
+
+
+# ---------------------------------------------------------------------------
+# full-size workloads: sampled rows through the oracle
+# ---------------------------------------------------------------------------
+@pytest.mark.parametrize("name,mode,pt", [
+    ("ragged_b64", "single", 0), ("ragged_b64", "split", 0), ("ragged_b64", "split", 512),
+    ("long_b1_t8192", "split", 512), ("long_b1_t32768", "split", 512),
+    ("long_b1_t131072", "split", 512), ("long_b4_t8192", "split", 512),
+    ("long_b4_t32768", "split", 512), ("long_b4_t131072", "split", 512),
+    ("long_b1_t131072", "split", 0), ("long_b4_t32768", "single", 0),
+    ("mqa_b32_t16384", "split", 0), ("mqa_b32_t16384", "single", 0),
+])
+def test_full_size_sampled(name, mode, pt):
+    x = workloads.make(name, seed=0, device=DEV)
+    got = run(x, mode, partition_tokens=pt)
+    assert torch.isfinite(got).all()
+    rows = sample_rows(x, 24)
+    host = x.to("cpu")
+    want = oracle.decode_rows(host.q, host.k_cache, host.v_cache, host.block_tables,
+                              host.context_lens, host.scale, rows)
+    assert_close_fp32(got[rows[:, 0], rows[:, 1]], want)
+
+
+# ---------------------------------------------------------------------------
+# other instantiations: head_dim 64/256, groups 1/2/8/16, block 16/32
+# ---------------------------------------------------------------------------
+def random_case(seed, B, H, Hkv, D, bs, lens, dtype, spare=5, mb_extra=1):
+    g = torch.Generator().manual_seed(seed)
+    pages = [(t + bs - 1) // bs for t in lens]
+    mb = max(1, max(pages)) + mb_extra
+    pool = sum(pages) + spare
+    perm = torch.randperm(pool, generator=g)
+    bt = torch.full((B, mb), -1, dtype=torch.int32)
+    c = 0
+    for b, n in enumerate(pages):
+        bt[b, :n] = perm[c:c + n].to(torch.int32)
+        c += n
+    spec = workloads.Spec("case", B, H, Hkv, D, bs, dtype, "list:" + ",".join(map(str, lens)))
+    x = workloads.Inputs(spec, torch.randn(B, H, D, generator=g).to(dtype),
+                         torch.randn(pool, bs, Hkv, D, generator=g).to(dtype),
+                         torch.randn(pool, bs, Hkv, D, generator=g).to(dtype),
+                         bt, torch.tensor(lens, dtype=torch.int32), 1.0 / math.sqrt(D),
+                         max(lens), list(lens))
+    return x
+
+
+SHAPES = [
+    dict(B=3, H=8, Hkv=8, D=64, bs=16, lens=[1, 37, 200]),
+    dict(B=2, H=8, Hkv=4, D=64, bs=32, lens=[64, 333]),
+    dict(B=2, H=16, Hkv=2, D=128, bs=16, lens=[129, 7]),
+    dict(B=2, H=32, Hkv=8, D=128, bs=32, lens=[500, 31]),
+    dict(B=2, H=16, Hkv=1, D=256, bs=32, lens=[1000, 33]),
+    dict(B=3, H=4, Hkv=4, D=256, bs=16, lens=[17, 256, 2]),
+    dict(B=2, H=8, Hkv=4, D=256, bs=16, lens=[100, 401]),
+    dict(B=1, H=16, Hkv=2, D=64, bs=16, lens=[777]),
+]
+
+
+@pytest.mark.parametrize("dtype", [torch.float16, torch.bfloat16])
+@pytest.mark.parametrize("shape", SHAPES, ids=lambda s: f"H{s['H']}kv{s['Hkv']}D{s['D']}bs{s['bs']}")
+def test_other_shapes(shape, dtype):
+    x = random_case(3, dtype=dtype, **shape)
+    want = oracle.decode(x.q, x.k_cache, x.v_cache, x.block_tables, x.context_lens, x.scale)
+    xd = x.to(DEV)
+    for mode, pt in [("single", 0), ("split", 0), ("split", shape["bs"] * 2)]:
+        assert_close_fp32(run(xd, mode, partition_tokens=pt), want)
+
+
+# ---------------------------------------------------------------------------
+# edge cases and invariances
+# ---------------------------------------------------------------------------
+def test_edge_lengths_and_masking():
+    x = random_case(5, B=6, H=8, Hkv=2, D=128, bs=16, lens=[0, 1, 15, 16, 17, 95], dtype=torch.bfloat16,
+                    mb_extra=0)
+    NB = x.k_cache.shape[0]
+    bt = x.block_tables.clone()
+    bt[5, 2] = -1            # unallocated entry inside the context
+    bt[4, 1] = NB + 7        # id outside the pool
+    x.block_tables = bt
+    lens = torch.tensor([0, 1, 15, 16, 17, 10_000], dtype=torch.int32)   # last: clamped to the row
+    x.context_lens = lens
+    x.lens_host = lens.tolist()
+    want = oracle.decode(x.q, x.k_cache, x.v_cache, bt, lens, x.scale)
+    xd = x.to(DEV)
+    xd.max_context_len = 10_000
+    for mode, pt in [("single", 0), ("split", 16), ("split", 32), ("split", 0)]:
+        got = run(xd, mode, partition_tokens=pt)
+        assert_close_fp32(got, want)
+        assert torch.all(got[0] == 0)        # empty context -> zeros
+
+
+def test_all_masked_and_empty_batch():
+    x = random_case(6, B=2, H=4, Hkv=4, D=128, bs=16, lens=[40, 20], dtype=torch.float16)
+    x.block_tables = torch.full_like(x.block_tables, -1)
+    xd = x.to(DEV)
+    for mode, pt in [("single", 0), ("split", 16)]:
+        assert torch.all(run(xd, mode, partition_tokens=pt) == 0)
+    e = workloads.make("tiny", device=DEV)
+    out = torch.empty(0, 32, 128, device=DEV)
+    pa.decode(out, e.q[:0], e.k_cache, e.v_cache, e.block_tables[:0], e.context_lens[:0], e.scale)
+
+
+@pytest.mark.parametrize("mode,pt", [("single", 0), ("split", 32)])
+def test_poison_does_not_leak(mode, pt):
+    x = workloads.make("sweep_b16_t256", seed=2, device=DEV)
+    lens = torch.randint(1, 257, (16,), generator=torch.Generator().manual_seed(3)).to(torch.int32)
+    x.context_lens = lens.to(DEV)
+    clean = run(x, mode, partition_tokens=pt)
+    k, v = x.k_cache.clone(), x.v_cache.clone()
+    bt = x.block_tables.cpu()
+    for b in range(16):
+        t = int(lens[b])
+        last = int(bt[b, (t - 1) // 16])
+        k[last, (t - 1) % 16 + 1:] = float("nan")
+        v[last, (t - 1) % 16 + 1:] = float("nan")
+        for j in range((t + 15) // 16, bt.shape[1]):        # pages past the context
+            k[int(bt[b, j])] = float("nan")
+            v[int(bt[b, j])] = float("nan")
+    x.k_cache, x.v_cache = k, v
+    poisoned = run(x, mode, partition_tokens=pt)
+    assert torch.equal(poisoned, clean)
+
+
+@pytest.mark.parametrize("mode,pt", [("single", 0), ("split", 64)])
+def test_pool_permutation_bit_identical(mode, pt):
+    x = workloads.make("ragged_b64", seed=4, device=DEV)
+    base = run(x, mode, partition_tokens=pt)
+    NB = x.k_cache.shape[0]
+    perm = torch.randperm(NB, generator=torch.Generator().manual_seed(9)).to(DEV)
+    k2, v2 = torch.empty_like(x.k_cache), torch.empty_like(x.v_cache)
+    k2[perm], v2[perm] = x.k_cache, x.v_cache
+    bt = x.block_tables
+    x.block_tables = torch.where(bt >= 0, perm[bt.clamp(min=0).long()].to(torch.int32), bt)
+    x.k_cache, x.v_cache = k2, v2
+    assert torch.equal(run(x, mode, partition_tokens=pt), base)
+
+
+def test_split_count_invariance():
+    x = workloads.make("long_b1_t32768", seed=5, device=DEV)
+    rows = sample_rows(x, 8)
+    host = x.to("cpu")
+    want = oracle.decode_rows(host.q, host.k_cache, host.v_cache, host.block_tables,
+                              host.context_lens, host.scale, rows)
+    outs = []
+    for mode, pt in [("single", 0), ("split", 16), ("split", 256), ("split", 512), ("split", 4096),
+                     ("split", 0)]:
+        got = run(x, mode, partition_tokens=pt)
+        assert_close_fp32(got[rows[:, 0], rows[:, 1]], want)
+        outs.append(got)
+    for o in outs[1:]:
+        assert (o - outs[0]).abs().max().item() <= 1e-5
+
+
+@pytest.mark.parametrize("name", ["tiny", "ragged_b64", "mqa_b32_t16384"])
+def test_resolve_blocks_bit_exact(name):
+    x = workloads.make(name, seed=0, device=DEV)
+    got = torch.empty_like(x.block_tables)
+    pa.resolve_blocks(got, x.block_tables, x.context_lens, x.k_cache.shape[1], x.k_cache.shape[0])
+    torch.cuda.synchronize()
+    want = oracle.resolve_blocks(x.block_tables, x.context_lens, x.k_cache.shape[1], x.k_cache.shape[0])
+    np.testing.assert_array_equal(got.cpu().numpy(), want)
+
+
+def test_resolve_blocks_garbage_tables():
+    g = np.random.default_rng(12)
+    B, mb, bs, NB = 33, 17, 16, 50
+    bt = torch.from_numpy(g.integers(-5, NB + 5, size=(B, mb)).astype(np.int32))
+    lens = torch.from_numpy(g.integers(-3, mb * bs + 40, size=B).astype(np.int32))
+    got = torch.empty(B, mb, dtype=torch.int32, device=DEV)
+    pa.resolve_blocks(got, bt.to(DEV), lens.to(DEV), bs, NB)
+    torch.cuda.synchronize()
+    np.testing.assert_array_equal(got.cpu().numpy(), oracle.resolve_blocks(bt, lens, bs, NB))
+
+
+def test_workspace_errors_and_no_device_error():
+    x = workloads.make("long_b1_t8192", device=DEV)
+    out = torch.empty(x.q.shape, dtype=torch.float32, device=DEV)
+    need = pa.workspace_size(x.q, x.k_cache, x.block_tables, torch.float32, x.max_context_len, 512)
+    assert need > 0
+    small = torch.empty(need - 16, dtype=torch.uint8, device=DEV)
+    with pytest.raises(pa.PaError) as ei:
+        pa.decode_splitkv(out, x.q, x.k_cache, x.v_cache, x.block_tables, x.context_lens, x.scale,
+                          x.max_context_len, 512, workspace=small)
+    assert ei.value.code == 3
+    with pytest.raises(pa.PaError):
+        pa.decode_splitkv(out, x.q, x.k_cache, x.v_cache, x.block_tables, x.context_lens, x.scale,
+                          x.max_context_len, 100)        # not a multiple of block_size
+    assert pa.device_error() == 0
