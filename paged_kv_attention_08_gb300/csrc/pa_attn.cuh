@@ -339,7 +339,8 @@ __global__ void __launch_bounds__(256, 1)
 #pragma unroll
     for (int mask = LPT; mask < 32; mask <<= 1) l_own += __shfl_xor_sync(kFullMask, l_own, mask);
 
-    float* wm = mrg + (size_t)warp * GW * (D + 2);  // acc [GW][D], then m [GW], l [GW]
+    const uint32_t MS = merge_stride(D, GW);
+    float* wm = mrg + (size_t)warp * MS;  // acc [GW][D], then m [GW], l [GW]
 #pragma unroll
     for (int g = 0; g < GW; ++g) {
         const float lg = __shfl_sync(kFullMask, l_own, g * HL);
@@ -361,11 +362,11 @@ __global__ void __launch_bounds__(256, 1)
         const int hgx = gfull / GW, gi = gfull % GW;
         float M = NEG_INF;
         for (int s2 = 0; s2 < p.nt; ++s2)
-            M = fmaxf(M, mrg[(size_t)(s2 * p.nh + hgx) * GW * (D + 2) + GW * D + gi]);
+            M = fmaxf(M, mrg[(size_t)(s2 * p.nh + hgx) * MS + GW * D + gi]);
         float A = 0.f, Ls = 0.f;
         if (M != NEG_INF) {
             for (int s2 = 0; s2 < p.nt; ++s2) {
-                const float* w2 = mrg + (size_t)(s2 * p.nh + hgx) * GW * (D + 2);
+                const float* w2 = mrg + (size_t)(s2 * p.nh + hgx) * MS;
                 const float ms = w2[GW * D + gi];
                 if (ms != NEG_INF) {
                     const float f = exp2f(ms - M);

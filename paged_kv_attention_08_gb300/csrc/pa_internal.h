@@ -60,6 +60,12 @@ struct AttnSmem {
 
 __host__ __device__ inline uint32_t pa_align_up(uint32_t x, uint32_t a) { return (x + a - 1) / a * a; }
 
+// Floats of one warp's merge block (acc [GW][D], m [GW], l [GW]), padded to a
+// multiple of four so that every block starts on a 16-byte boundary.
+__host__ __device__ inline uint32_t merge_stride(int D, int GW) {
+    return pa_align_up((uint32_t)(GW * (D + 2)), 4u);
+}
+
 __host__ __device__ inline AttnSmem attn_smem_layout(int D, int BS, int esize, int GW, int TPS,
                                                      int STEPS, int nt, int nh, int ns) {
     AttnSmem L;
@@ -77,7 +83,7 @@ __host__ __device__ inline AttnSmem attn_smem_layout(int D, int BS, int esize, i
     o += 4u * nw * TPS * STEPS * GW;
     o = pa_align_up(o, 16);
     L.mrg_off = o;
-    o += 4u * nw * GW * (D + 2);
+    o += 4u * nw * merge_stride(D, GW);
     L.total = pa_align_up(o, 16);
     return L;
 }
