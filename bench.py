@@ -254,6 +254,8 @@ def main(argv=None):
     ap.add_argument("--no-graph", action="store_true", help="launch eagerly instead of graph replay")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--min-warmup-s", type=float, default=1.0,
+                    help="keep warming up (graph replays) at least this long")
     args = ap.parse_args(argv)
     args.warmup = max(args.warmup, 3)
 
@@ -343,16 +345,12 @@ def main(argv=None):
             for i in range(len(set0)):
                 call(si, i, st)
 
-    # per-call events for the per-kernel roofline: a second timed pass, eager,
-    # one event pair around each call
-    ev_pairs = []
-
     step_bytes = sum(algorithmic_bytes(x) for x in set0)
     with ClockSampler(local) as clocks:
         with torch.cuda.stream(stream):
             t_warm = time.perf_counter()
             k = 0
-            while k < args.warmup or time.perf_counter() - t_warm < 1.0:
+            while k < args.warmup or time.perf_counter() - t_warm < args.min_warmup_s:
                 step(k, stream)
                 k += 1
                 if k % 256 == 0:
@@ -371,22 +369,27 @@ def main(argv=None):
             barrier()
             ms_total = e0.elapsed_time(e1)
 
-            # per-call timing pass (same calls, each bracketed by events)
+            # per-call durations: one graph per workload that runs its call once on
+            # every input set (L2-cold, back to back); replay time / sets = the
+            # call's device time (attention kernel plus, when it splits, combine)
             per_call = [[] for _ in set0]
-            reps = max(1, min(args.steps, 400))
-            pairs = []
-            for k in range(reps):
-                si = k % nsets
-                for i in range(len(set0)):
+            call_graphs = []
+            for i in range(len(set0)):
+                g = torch.cuda.CUDAGraph()
+                with torch.cuda.graph(g, stream=stream):
+                    for si in range(nsets):
+                        call(si, i, torch.cuda.current_stream())
+                call_graphs.append(g)
+            reps = max(3, min(args.steps // 10, 50))
+            for _ in range(reps):
+                for i, g in enumerate(call_graphs):
                     a = torch.cuda.Event(enable_timing=True)
                     b = torch.cuda.Event(enable_timing=True)
                     a.record(stream)
-                    call(si, i, stream)
+                    g.replay()
                     b.record(stream)
-                    pairs.append((i, a, b))
-            stream.synchronize()
-            for i, a, b in pairs:
-                per_call[i].append(a.elapsed_time(b))
+                    b.synchronize()
+                    per_call[i].append(a.elapsed_time(b) / nsets)
     clk = clocks.summary() if rank == 0 else None
 
     ms_step = reduce_max(ms_total, dev) / args.steps
