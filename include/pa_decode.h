@@ -158,6 +158,34 @@ pa_status pa_resolve_blocks(int32_t* out_phys, const int32_t* block_tables,
  */
 pa_status pa_device_error(int32_t* code, void* stream);
 
+/*
+ * pa_decode_splitkv without a caller-supplied workspace, for callers that
+ * cannot allocate device memory: for instance code that runs inside a host
+ * application which hands it only fixed input/output buffers and forbids
+ * further allocation, or a latency-critical loop that must not pay for
+ * cudaMalloc's device-wide synchronisation.  (The pages have no counterpart;
+ * this is a convenience of this library.)
+ *
+ * The split-KV partials go to a fixed scratch array inside the library, 16 MiB
+ * of device memory on every GPU that loads it, held until the process exits.
+ * A call whose partials need more than that -- batch * num_heads * partitions
+ * * (head_dim + 2) * 4 bytes, plus alignment -- returns PA_ERR_WORKSPACE and
+ * launches nothing; use pa_decode_splitkv with your own workspace then.  The
+ * call allocates nothing and needs no clearing of the scratch.
+ *
+ * The first call on a device looks up that device's scratch address
+ * (cudaGetSymbolAddress); make that first call before any stream capture.
+ * All calls on a device share the one array, which keeps the last call's
+ * contents: two calls that can run at the same time on the GPU (different
+ * streams without ordering between them) race on it and both results are then
+ * undefined.  Other arguments and behaviour are those of pa_decode_splitkv.
+ */
+pa_status pa_decode_splitkv_noalloc(void* out, const void* q, const void* k_cache,
+                                    const void* v_cache, const int32_t* block_tables,
+                                    const int32_t* context_lens, const pa_shape* shape,
+                                    float scale, int32_t max_context_len,
+                                    int32_t partition_tokens, void* stream);
+
 /* Static, human-readable name of a status. */
 const char* pa_status_string(pa_status status);
 

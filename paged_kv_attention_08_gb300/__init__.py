@@ -22,7 +22,7 @@ import threading
 
 import torch
 
-__all__ = ["PaError", "decode", "decode_splitkv", "workspace_size", "choose_partition_tokens",
+__all__ = ["PaError", "decode", "decode_splitkv", "decode_splitkv_noalloc", "workspace_size", "choose_partition_tokens",
            "resolve_blocks", "device_error", "library_path", "F16", "BF16", "F32"]
 
 F16, BF16, F32 = 0, 1, 2
@@ -70,6 +70,8 @@ def _load():
             lib.pa_decode.restype = ctypes.c_int
             lib.pa_decode_splitkv.argtypes = [P, P, P, P, P, P, S, f32, i32, i32, P, sz, P]
             lib.pa_decode_splitkv.restype = ctypes.c_int
+            lib.pa_decode_splitkv_noalloc.argtypes = [P, P, P, P, P, P, S, f32, i32, i32, P]
+            lib.pa_decode_splitkv_noalloc.restype = ctypes.c_int
             lib.pa_workspace_size.argtypes = [S, i32, i32]
             lib.pa_workspace_size.restype = sz
             lib.pa_choose_partition_tokens.argtypes = [S, i32, i32]
@@ -177,6 +179,24 @@ def decode_splitkv(out, q, k_cache, v_cache, block_tables, context_lens, scale: 
                                  int(max_context_len), int(partition_tokens),
                                  workspace.data_ptr(), workspace.numel() * workspace.element_size(),
                                  _stream_ptr(stream)), "pa_decode_splitkv")
+    return out
+
+
+def decode_splitkv_noalloc(out, q, k_cache, v_cache, block_tables, context_lens, scale: float,
+                           max_context_len: int, partition_tokens: int = 0, stream=None):
+    """Split-KV decode whose partials live in the library's fixed 16 MiB
+    scratch instead of a caller workspace, for callers that cannot allocate
+    device memory.  Calls that may overlap on the GPU race on that scratch;
+    the first call on a device should come before any stream capture.
+    Raises PaError (PA_ERR_WORKSPACE) when the partials would not fit."""
+    _dev_tensors(out, q, k_cache, v_cache, block_tables, context_lens)
+    _ints(block_tables, context_lens)
+    shape = make_shape(q, k_cache, block_tables, out.dtype)
+    _check(_load().pa_decode_splitkv_noalloc(
+        out.data_ptr(), q.data_ptr(), k_cache.data_ptr(), v_cache.data_ptr(),
+        block_tables.data_ptr(), context_lens.data_ptr(), ctypes.byref(shape), float(scale),
+        int(max_context_len), int(partition_tokens), _stream_ptr(stream)),
+        "pa_decode_splitkv_noalloc")
     return out
 
 

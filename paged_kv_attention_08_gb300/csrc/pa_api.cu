@@ -12,6 +12,13 @@
 // One error word per device; kernels set it when a bounded wait runs out.
 __device__ int32_t pa_device_error_word;
 
+// Fixed split-KV scratch for pa_decode_splitkv_noalloc: 16 MiB of fp32 per
+// device that loads this library, held until the process exits.  In host code
+// this name is only a stand-in for the symbol, never a device address: the
+// address is looked up per device with cudaGetSymbolAddress.
+constexpr size_t kNoAllocScratchBytes = size_t(16) << 20;
+static __device__ __align__(256) float pa_noalloc_scratch[kNoAllocScratchBytes / sizeof(float)];
+
 namespace pa {
 namespace {
 
@@ -19,6 +26,8 @@ constexpr int kMaxDevices = 64;
 constexpr uint64_t kDefaultTimeoutNs = 2000000000ull;  // 2 s per wait
 std::atomic<int> g_sm_count[kMaxDevices];
 std::atomic<int32_t*> g_err_word[kMaxDevices];
+
+std::atomic<void*> g_noalloc_scratch[kMaxDevices];
 
 std::once_flag g_encode_once;
 PFN_cuTensorMapEncodeTiled_v12000 g_encode = nullptr;
@@ -396,6 +405,46 @@ pa_status pa_device_error(int32_t* code, void* stream) {
     if (cudaStreamSynchronize(cs) != cudaSuccess) return PA_ERR_CUDA;
     *code = v;
     return PA_OK;
+}
+
+pa_status pa_decode_splitkv_noalloc(void* out, const void* q, const void* k_cache,
+                                    const void* v_cache, const int32_t* block_tables,
+                                    const int32_t* context_lens, const pa_shape* shape,
+                                    float scale, int32_t max_context_len,
+                                    int32_t partition_tokens, void* stream) {
+    pa_status st = check_shape(shape);
+    if (st != PA_OK) return st;
+    if (max_context_len < 0 || partition_tokens < 0 || partition_tokens % shape->block_size != 0)
+        return PA_ERR_INVALID_ARG;
+    if (shape->batch == 0) return PA_OK;
+    st = check_ptrs(out, q, k_cache, v_cache, block_tables, context_lens);
+    if (st != PA_OK) return st;
+    int sms = 0;
+    st = device_state(&sms, nullptr);
+    if (st != PA_OK) return st;
+    if (partition_tokens == 0) partition_tokens = choose_partition_tokens(shape, max_context_len, sms);
+    const Plan plan = make_plan(shape, max_context_len, partition_tokens);
+    if (workspace_bytes_for(shape, plan.num_parts, nullptr) > kNoAllocScratchBytes)
+        return PA_ERR_WORKSPACE;  // more partials than the fixed scratch holds
+
+    // Device address of this device's copy of the scratch array, looked up
+    // once per device with that device current (the caller's current device).
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) return PA_ERR_CUDA;
+    void* scratch = g_noalloc_scratch[dev].load(std::memory_order_acquire);
+    if (!scratch) {
+        void* ptr = nullptr;
+        if (cudaGetSymbolAddress(&ptr, pa_noalloc_scratch) != cudaSuccess || !ptr)
+            return PA_ERR_CUDA;
+        g_noalloc_scratch[dev].store(ptr, std::memory_order_release);
+        scratch = ptr;
+    }
+    // The partials need no clearing: every partition inside a sequence's
+    // context writes its (m, l, acc) before the combine reads it, and the
+    // combine never reads partitions past the context.
+    return pa_decode_splitkv(out, q, k_cache, v_cache, block_tables, context_lens, shape, scale,
+                             max_context_len, partition_tokens, scratch, kNoAllocScratchBytes,
+                             stream);
 }
 
 }  // extern "C"
