@@ -90,9 +90,10 @@ pa_status device_state(int* sms, int32_t** err) {
 }
 
 // Launch shape of the attention kernel for one problem: warps per stream
-// (head-group slices), streams per CTA and stages per stream.
+// (head_dim 256 splits a page's output columns over two warps), streams per
+// CTA and stages per stream.
 struct Tune {
-    int gw, nh, nt, ns;
+    int nh, nt, ns;
 };
 
 int env_int(const char* name, int fallback) {
@@ -104,13 +105,11 @@ int env_int(const char* name, int fallback) {
 
 Tune pick_tune(const pa_shape* s) {
     Tune t;
-    const int G = s->num_heads / s->num_kv_heads;
-    t.gw = G < kHeadsPerWarpMax ? G : kHeadsPerWarpMax;
-    t.nh = G / t.gw;
-    const int stage = 2 * s->block_size * s->head_dim * elem_size(s->kv_dtype);
-    t.nt = t.nh >= 4 ? 2 : (t.nh == 2 ? 2 : 4);
+    t.nh = s->head_dim == 256 ? 2 : 1;
+    const int stage = 2 * s->block_size * s->head_dim * 2;
+    t.nt = t.nh == 2 ? 2 : 4;
     // Stages per stream: about 96 KB of pages in flight per CTA, at least two.
-    int ns = (96 * 1024) / (t.nt * stage);
+    const int ns = (96 * 1024) / (t.nt * stage);
     t.ns = ns < 2 ? 2 : (ns > 8 ? 8 : ns);
     static const int env_nt = env_int("PA_TUNE_STREAMS", 0);
     static const int env_ns = env_int("PA_TUNE_STAGES", 0);
@@ -119,11 +118,15 @@ Tune pick_tune(const pa_shape* s) {
     return t;
 }
 
+// Programmatic dependent launch lets each kernel's launch overlap the tail
+// of the previous one in the stream; PA_NO_PDL=1 launches plainly instead.
+bool use_pdl() {
+    static const bool off = std::getenv("PA_NO_PDL") && std::atoi(std::getenv("PA_NO_PDL")) > 0;
+    return !off;
+}
+
 AttnSmem tune_smem(const pa_shape* s, const Tune& t) {
-    const int LPT = s->head_dim / 8, TPS = 32 / LPT;
-    const int STEPS = (8 * TPS <= s->block_size) ? 8 : s->block_size / TPS;
-    return attn_smem_layout(s->head_dim, s->block_size, elem_size(s->kv_dtype), t.gw, TPS, STEPS,
-                            t.nt, t.nh, t.ns);
+    return attn_smem_layout(s->head_dim, s->block_size, t.nt, t.ns);
 }
 
 int pages_for(const pa_shape* s, int32_t max_context_len) {
@@ -208,14 +211,16 @@ pa_status encode_maps(const pa_shape* s, const void* k, const void* v, CUtensorM
                                 (cuuint64_t)s->block_size, (cuuint64_t)s->num_blocks};
     const cuuint64_t strides[3] = {e * s->head_dim, e * s->head_dim * s->num_kv_heads,
                                    e * s->head_dim * s->num_kv_heads * s->block_size};
-    const cuuint32_t box[4] = {(cuuint32_t)s->head_dim, 1u, (cuuint32_t)s->block_size, 1u};
+    // one 64-column block (128 bytes) of one kv head's block_size rows, written
+    // to shared memory with the 128-byte swizzle that ldmatrix reads conflict-free
+    const cuuint32_t box[4] = {64u, 1u, (cuuint32_t)s->block_size, 1u};
     const cuuint32_t estr[4] = {1u, 1u, 1u, 1u};
     const CUtensorMapDataType dt =
         s->kv_dtype == PA_BF16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16;
     for (int which = 0; which < 2; ++which) {
         CUresult r = g_encode(which ? mv : mk, dt, 4, const_cast<void*>(which ? v : k), dims,
                               strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
-                              CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                              CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
                               CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
         if (r != CUDA_SUCCESS) return PA_ERR_CUDA;
     }
@@ -232,6 +237,9 @@ pa_status launch_attention(void* out, const void* q, const void* k, const void* 
     if (st != PA_OK) return st;
     const Tune t = pick_tune(s);
     const AttnSmem sm = tune_smem(s, t);
+    const int G = s->num_heads / s->num_kv_heads;
+    if (4u * merge_floats(t.nt * t.nh, G, s->head_dim / t.nh) > sm.stage_bytes * t.nt * t.ns)
+        return PA_ERR_UNSUPPORTED;  // the final merge must fit in the stage area
     AttnParams& p = L.p;
     p.q = q;
     p.out = out;
@@ -258,7 +266,7 @@ pa_status launch_attention(void* out, const void* q, const void* k, const void* 
     L.head_dim = s->head_dim;
     L.block_size = s->block_size;
     L.kv_dtype = s->kv_dtype;
-    L.heads_per_warp = t.gw;
+    L.pdl = use_pdl();
     L.grid = dim3((unsigned)plan.num_parts, (unsigned)s->num_kv_heads, (unsigned)s->batch);
     L.threads = 32 * t.nt * t.nh;
     L.smem_bytes = sm.total + kSmemAlignSlack;
@@ -351,8 +359,7 @@ pa_status pa_decode_splitkv(void* out, const void* q, const void* k_cache, const
     size_t ml_off = 0;
     const size_t need = workspace_bytes_for(shape, plan.num_parts, &ml_off);
     if (!workspace || !aligned(workspace, 16) || workspace_bytes < need) return PA_ERR_WORKSPACE;
-    const uint32_t combine_smem = (uint32_t)plan.num_parts * sizeof(float);
-    if (combine_smem > 200u * 1024u) return PA_ERR_UNSUPPORTED;
+    if ((size_t)plan.num_parts * 2 * sizeof(float) > 200u * 1024u) return PA_ERR_UNSUPPORTED;
     float* part_acc = static_cast<float*>(workspace);
     float* part_ml = reinterpret_cast<float*>(static_cast<char*>(workspace) + ml_off);
     st = launch_attention(out, q, k_cache, v_cache, block_tables, context_lens, shape, scale, plan,
@@ -374,7 +381,7 @@ pa_status pa_decode_splitkv(void* out, const void* q, const void* k_cache, const
     c.out_dtype = shape->out_dtype;
     const cudaError_t e = launch_combine(c, shape->head_dim,
                                          dim3((unsigned)shape->num_heads, (unsigned)shape->batch),
-                                         shape->head_dim, combine_smem, cs);
+                                         use_pdl(), cs);
     return e == cudaSuccess ? PA_OK : PA_ERR_CUDA;
 }
 

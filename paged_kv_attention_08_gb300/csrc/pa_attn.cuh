@@ -12,104 +12,115 @@
 // values), and a second kernel combines the partitions.
 //
 // How it maps to GB300:
-//   - K/V are read once per (sequence, kv head): every query head of the GQA
-//     group is served from the same staged page, so the group does not re-read
-//     it (the Triton kernel launches one program per query head instead).
+//   - K/V are read from HBM once per (sequence, kv head): the whole GQA group
+//     (up to 16 query heads) is served from the same staged page.
 //   - The CTA's warps form `nt` independent token streams.  Each stream owns a
-//     ring of `ns` shared-memory stages; one lane issues a 4-D TMA copy per K
-//     and V page (a single block-table read per page, not per token) and an
-//     mbarrier signals its arrival.  A stream's `nh` warps split the head group
-//     (at most 4 heads each) and release a stage through a second mbarrier.
-//   - Inside a warp, LPT = head_dim/8 lanes cover one token row with 16-byte
-//     vectors (8 elements each) and 32/LPT rows are processed side by side.
-//     Partial q.K dot products of a chunk (8 row steps x up to 4 heads) are
-//     summed across the LPT lanes with a transposing butterfly: each level
-//     halves the values a lane carries, so a chunk costs ~STEPS*GW shuffles
-//     instead of STEPS*GW*log2(LPT).
-//   - Scores are kept in base-2 units (q is pre-multiplied by
-//     scale*log2(e)); softmax uses exp2.  All arithmetic is fp32.
-//   - Tokens past the context (and pages whose table entry is masked) are
-//     excluded by select, never by multiplying by zero, so poison in unused
-//     slots cannot leak into the result.
+//     ring of `ns` shared-memory stages; one lane reads one block-table entry
+//     per page and issues 4-D TMA copies of the page's K and V tiles (column
+//     blocks of 64 elements, 128-byte swizzle), and an mbarrier signals their
+//     arrival.  The stream's warps release a stage through a second mbarrier.
+//   - The two contractions of a page run on the tensor cores as warp-level
+//     m16n8k16 MMAs with fp32 accumulation: the group's query heads are the 16
+//     rows (padded with zero rows when the group is smaller), tokens and head
+//     dims the other two dimensions.  S = Q K^T takes K fragments straight
+//     from the swizzled tile with ldmatrix; O += P V takes V fragments with
+//     ldmatrix.trans and P from the S accumulators, split into a high and a
+//     low 16-bit part (two MMAs) so that P keeps ~16 significant bits.  This
+//     replaces ~2*G*D multiply-adds per token on the CUDA cores, which at the
+//     GB300's bandwidth-to-FP32 ratio would consume the SM's whole issue budget.
+//   - Online softmax in base-2 units with conditional rescaling: the running
+//     max of a head only moves (and acc, l are rescaled) when a page's max
+//     exceeds it by more than 2^8; the result acc/l is the same for any such
+//     reference value.
+//   - Tokens past the context are excluded by select; the V rows of a partial
+//     last page are zeroed in shared memory before the MMA (0 * NaN would
+//     otherwise leak poison), masked pages are never read.
 //   - Every mbarrier wait is bounded; on timeout the kernel records
 //     PA_ERR_TIMEOUT in the device error word and abandons its work.
-// No tensor cores: with one query token per sequence the contraction is a
-// matrix-vector product, bound by HBM bandwidth, not by math throughput.
 #pragma once
 
 #include "pa_device.cuh"
 
 namespace pa {
 
-template <int D, int BS, int GW>
+template <int D, int BS>
 struct AttnCfg {
-    static constexpr int LPT = D / 8;                               // lanes per token row
-    static constexpr int TPS = 32 / LPT;                            // rows per warp step
-    static constexpr int STEPS = (8 * TPS <= BS) ? 8 : BS / TPS;    // row steps per chunk
-    static constexpr int CHUNK = STEPS * TPS;                       // tokens per chunk
-    static constexpr int NVAL = STEPS * GW;                         // partial dots per lane
-    static constexpr int NOUT = NVAL >= LPT ? NVAL / LPT : 1;       // reduced dots per lane
-    static constexpr int DUP = NVAL >= LPT ? 1 : LPT / NVAL;        // lanes holding one dot
-    static constexpr int HL = LPT / GW;                             // lanes per head in a row group
+    static constexpr int DS = (D == 256) ? 2 : 1;  // warps that split one page's output columns
+    static constexpr int DW = D / DS;              // output columns per warp
+    static constexpr int KSTEPS = D / 16;          // k-steps of S = Q K^T
+    static constexpr int NT = BS / 8;              // token n-tiles of S per page
+    static constexpr int PKS = BS / 16;            // k-steps of O += P V per page
+    static constexpr int ONT = DW / 8;             // output n-tiles per warp
+    static constexpr int DBLK = D / 64;            // 128-byte column blocks per tile
     static_assert(D == 64 || D == 128 || D == 256, "head_dim");
-    static_assert(BS % CHUNK == 0, "a chunk must not straddle a page");
-    static_assert(STEPS % NOUT == 0, "a lane's reduced dots belong to one head");
+    static_assert(BS == 16 || BS == 32, "block_size");
 };
 
-// Sum each of N per-lane values over the LPT lanes of a row group (xor masks
-// LPT/2 .. 1).  While a lane carries two or more values, each level keeps half
-// of them and trades the other half with its partner, so after log2(N) levels
-// a lane holds the full sums of its own values; remaining levels (N < LPT)
-// are plain butterflies that leave duplicates.  On return vals[0..NOUT) hold
-// the sums of original indices [lig*NOUT, lig*NOUT + NOUT) when N >= LPT, or
-// of index lig / (LPT/N) otherwise (lig = lane % LPT).
-template <int N, int LPT>
-__device__ __forceinline__ void transpose_reduce(float (&vals)[N], int lane) {
-    int n = N;
-#pragma unroll
-    for (int mask = LPT / 2; mask >= 1; mask >>= 1) {
-        if (n >= 2) {
-            const int half = n / 2;
-            const bool upper = (lane & mask) != 0;
-#pragma unroll
-            for (int i = 0; i < N / 2; ++i) {
-                if (i < half) {
-                    const float lo = vals[i], hi = vals[i + half];
-                    const float send = upper ? lo : hi;
-                    const float keep = upper ? hi : lo;
-                    vals[i] = keep + __shfl_xor_sync(kFullMask, send, mask);
-                }
-            }
-            n = half;
-        } else {
-            vals[0] += __shfl_xor_sync(kFullMask, vals[0], mask);
-        }
-    }
+// Byte offset of (row t, 16-byte chunk c) in a tile written by TMA with the
+// 128-byte swizzle: chunk c & 7 of a 128-byte row lands at (c & 7) ^ (t & 7).
+template <int BS>
+__device__ __forceinline__ uint32_t swz(int t, int c) {
+    return (uint32_t)((c >> 3) * BS * 128 + t * 128 + (((c & 7) ^ (t & 7)) << 4));
 }
 
-template <int D, int BS, typename KV, int GW>
+constexpr float kRescaleSlack = 8.0f;  // log2 units: p may reach 2^8 before a rescale
+
+template <int D, int BS, typename KV>
 __global__ void __launch_bounds__(256, 1)
     attn_kernel(const __grid_constant__ CUtensorMap tmap_k,
                 const __grid_constant__ CUtensorMap tmap_v, const AttnParams p) {
-    using C = AttnCfg<D, BS, GW>;
-    constexpr int LPT = C::LPT, TPS = C::TPS, STEPS = C::STEPS, CHUNK = C::CHUNK;
-    constexpr int NVAL = C::NVAL, NOUT = C::NOUT, DUP = C::DUP, HL = C::HL;
+    using C = AttnCfg<D, BS>;
+    constexpr int DS = C::DS, DW = C::DW, KSTEPS = C::KSTEPS, NT = C::NT, PKS = C::PKS;
+    constexpr int ONT = C::ONT, DBLK = C::DBLK;
     constexpr float NEG_INF = -INFINITY;
 
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = reinterpret_cast<uint8_t*>(
         (reinterpret_cast<uintptr_t>(smem_raw) + (kSmemAlignSlack - 1)) &
         ~uintptr_t(kSmemAlignSlack - 1));
-    const AttnSmem L = attn_smem_layout(D, BS, (int)sizeof(KV), GW, TPS, STEPS, p.nt, p.nh, p.ns);
+    const AttnSmem L = attn_smem_layout(D, BS, p.nt, p.ns);
 
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-    const int stream = warp / p.nh, hg = warp % p.nh;
+    const int stream = warp / DS, ds = warp % DS;
     const int part = blockIdx.x, kvh = blockIdx.y, b = blockIdx.z;
     const int G = p.group;
 
+    uint64_t* full = reinterpret_cast<uint64_t*>(smem + L.full_off);
+    uint64_t* empty = reinterpret_cast<uint64_t*>(smem + L.empty_off);
+    int32_t* phys_of = reinterpret_cast<int32_t*>(smem + L.phys_off);
+    if (tid == 0) {
+        for (int i = 0; i < p.nt * p.ns; ++i) {
+            mbar_init(smem_u32(full + i), 1);
+            mbar_init(smem_u32(empty + i), DS);
+        }
+        mbar_init_fence();
+        prefetch_tensormap(&tmap_k);
+        prefetch_tensormap(&tmap_v);
+    }
+    // Inputs may come from the previous kernel in the stream.
+    grid_dependency_wait();
+    grid_launch_dependents();
+
+    // This stream's pages are pb + stream + i*nt.  The leader warp fetches
+    // their table entries 32 at a time, one per lane, before the context
+    // length is known (every index stays inside the table row); entries past
+    // the context are masked once it is.
+    const int32_t* table_row = p.block_tables + (size_t)b * p.max_blocks;
+    const int pb = part * p.part_pages;
+    const int pe_row = min(pb + p.part_pages, p.max_blocks);
+    const int n_row = pe_row - pb > stream ? (pe_row - pb - stream + p.nt - 1) / p.nt : 0;
+    auto fetch = [&](int chunk) -> int {
+        const int li = chunk * 32 + lane;
+        return li < n_row ? __ldg(table_row + pb + stream + li * p.nt) : -1;
+    };
+    int ent_cur = -1, ent_next = -1, cur_chunk = 0;
+    if (ds == 0) {
+        ent_cur = fetch(0);
+        ent_next = fetch(1);
+    }
+
     const int T = reachable_tokens(p.context_lens, b, p.max_blocks, BS);
     const int npages = (T + BS - 1) / BS;
-    const int pb = part * p.part_pages;
     const int pe = min(pb + p.part_pages, npages);
     if (pb >= pe) {
         // Nothing of this sequence falls in the partition.  The single pass
@@ -123,88 +134,84 @@ __global__ void __launch_bounds__(256, 1)
         }
         return;
     }
+    __syncthreads();  // barrier initialisation visible to every warp
 
-    uint64_t* full = reinterpret_cast<uint64_t*>(smem + L.full_off);
-    uint64_t* empty = reinterpret_cast<uint64_t*>(smem + L.empty_off);
-    int32_t* phys_of = reinterpret_cast<int32_t*>(smem + L.phys_off);
-    float* pbuf = reinterpret_cast<float*>(smem + L.pbuf_off);
-    float* mrg = reinterpret_cast<float*>(smem + L.mrg_off);
-
-    if (tid == 0) {
-        for (int i = 0; i < p.nt * p.ns; ++i) {
-            mbar_init(smem_u32(full + i), 1);
-            mbar_init(smem_u32(empty + i), p.nh);
-        }
-        mbar_init_fence();
-    }
-    __syncthreads();
-
-    const int32_t* table_row = p.block_tables + (size_t)b * p.max_blocks;
     const int span = pe - pb;
     const int n_s = span > stream ? (span - stream + p.nt - 1) / p.nt : 0;  // pages of this stream
-    const bool leader = hg == 0 && lane == 0;
-    const uint64_t policy = l2_policy_evict_first();
+    const bool leader = ds == 0 && lane == 0;
     int n_issued = 0;
 
-    // Stage local page i of this stream: one table read, then one TMA copy
-    // each for the K and V page of this kv head (bs rows of head_dim).
-    auto issue = [&](int i) {
-        const int sidx = stream * p.ns + i % p.ns;
+    // Stage local page i of this stream (whole leader warp): the page's table
+    // entry, then one TMA copy per 64-column block of its K and V tiles.
+    auto issue = [&](int i, int sidx) {
+        if ((i >> 5) != cur_chunk) {  // slide the prefetched window
+            cur_chunk = i >> 5;
+            ent_cur = ent_next;
+            ent_next = fetch(cur_chunk + 1);
+        }
+        const int e = __shfl_sync(kFullMask, ent_cur, i & 31);
         const int j = pb + stream + i * p.nt;
-        const int phys = page_phys(table_row, j, npages, p.num_blocks);
-        phys_of[sidx] = phys;
-        const uint32_t bar = smem_u32(full + sidx);
-        if (phys >= 0) {
-            mbar_arrive_expect_tx(bar, L.stage_bytes);
-            const uint32_t dst = smem_u32(smem + L.stages_off + (size_t)sidx * L.stage_bytes);
-            tma_load_4d(dst, &tmap_k, 0, kvh, 0, phys, bar, policy);
-            tma_load_4d(dst + L.stage_bytes / 2, &tmap_v, 0, kvh, 0, phys, bar, policy);
-        } else {
-            mbar_arrive(bar);
+        const int phys = (j < npages && e >= 0 && (int64_t)e < p.num_blocks) ? e : -1;
+        if (lane == 0) {
+            phys_of[sidx] = phys;
+            const uint32_t bar = smem_u32(full + sidx);
+            if (phys >= 0) {
+                const uint64_t policy = l2_policy_evict_first();
+                mbar_arrive_expect_tx(bar, L.stage_bytes);
+                const uint32_t dst = smem_u32(smem + L.stages_off + (size_t)sidx * L.stage_bytes);
+#pragma unroll
+                for (int blk = 0; blk < DBLK; ++blk) {
+                    tma_load_4d(dst + blk * BS * 128, &tmap_k, blk * 64, kvh, 0, phys, bar, policy);
+                    tma_load_4d(dst + L.tile_bytes + blk * BS * 128, &tmap_v, blk * 64, kvh, 0,
+                                phys, bar, policy);
+                }
+            } else {
+                mbar_arrive(bar);
+            }
         }
     };
 
-    if (leader) {
-        prefetch_tensormap(&tmap_k);
-        prefetch_tensormap(&tmap_v);
+    if (ds == 0) {
         const int pro = n_s < p.ns ? n_s : p.ns;
-        for (int i = 0; i < pro; ++i) issue(i);
+        for (int i = 0; i < pro; ++i) issue(i, stream * p.ns + i);
         n_issued = pro;
     }
 
-    // This warp's query heads, pre-scaled into base-2 score units.
-    const int lig = lane & (LPT - 1);  // 16-byte slice of the head dimension
-    const int ts = lane / LPT;         // row within a step
-    float qf[GW][8];
+    // ---- Q fragments (A operand of S = Q K^T): rows = the group's heads ----
+    const int g = lane >> 2, tig = lane & 3;
+    const bool real0 = g < G, real1 = g + 8 < G;
+    uint32_t qa[KSTEPS][4];
+    {
+        const KV* q = static_cast<const KV*>(p.q) + ((size_t)b * p.num_heads + kvh * G) * D;
+        const uint32_t* q0 = reinterpret_cast<const uint32_t*>(q + (size_t)g * D);
+        const uint32_t* q1 = reinterpret_cast<const uint32_t*>(q + (size_t)(g + 8) * D);
 #pragma unroll
-    for (int g = 0; g < GW; ++g) {
-        const int h = kvh * G + hg * GW + g;
-        const uint4 raw = __ldg(reinterpret_cast<const uint4*>(
-            static_cast<const KV*>(p.q) + ((size_t)b * p.num_heads + h) * D + lig * 8));
-        Vec8<KV>::to_float(raw, qf[g]);
-#pragma unroll
-        for (int e = 0; e < 8; ++e) qf[g][e] *= p.qscale;
+        for (int kk = 0; kk < KSTEPS; ++kk) {
+            const int w = (kk * 16 + tig * 2) >> 1;  // 32-bit word index of the element pair
+            qa[kk][0] = real0 ? __ldg(q0 + w) : 0u;
+            qa[kk][1] = real1 ? __ldg(q1 + w) : 0u;
+            qa[kk][2] = real0 ? __ldg(q0 + w + 4) : 0u;
+            qa[kk][3] = real1 ? __ldg(q1 + w + 4) : 0u;
+        }
     }
 
-    float m[GW], acc[GW][8];
+    // Running state of rows g and g+8 (padded rows stay at m = 0, p = 0).
+    float m0 = real0 ? NEG_INF : 0.f, m1 = real1 ? NEG_INF : 0.f;
+    float l0 = 0.f, l1 = 0.f;  // this lane's share of the normalisers
+    float acc[ONT][4];
 #pragma unroll
-    for (int g = 0; g < GW; ++g) {
-        m[g] = NEG_INF;
-#pragma unroll
-        for (int e = 0; e < 8; ++e) acc[g][e] = 0.f;
-    }
-    float l_own = 0.f;  // normaliser share of this lane's head
+    for (int n = 0; n < ONT; ++n) acc[n][0] = acc[n][1] = acc[n][2] = acc[n][3] = 0.f;
 
-    const int vbase = (NVAL >= LPT) ? lig * NOUT : lig / DUP;  // first reduced dot of this lane
-    const int gown = vbase / STEPS;                            // its head
-    const bool designated = (DUP == 1) || (lig % DUP) == 0;
-    float* pw_base = pbuf + (size_t)(warp * TPS + ts) * STEPS * GW;
+    const float qscale = p.qscale;
+    const int ldsm_t = lane & 7;         // row supplied to ldmatrix
+    const int ldsm_m = lane >> 3;        // matrix supplied to ldmatrix
+    const int col0 = ds * (DW / 8);      // first 16-byte output chunk of this warp
 
     bool aborted = false;
-    int i = 0;
+    int i = 0, slot = 0;
+    uint32_t par = 0;
     for (; i < n_s; ++i) {
-        const int sidx = stream * p.ns + i % p.ns;
-        const uint32_t par = (uint32_t)(i / p.ns) & 1u;
+        const int sidx = stream * p.ns + slot;
         const bool ok = __all_sync(kFullMask, mbar_wait_bounded(smem_u32(full + sidx), par,
                                                                 p.timeout_ns));
         if (!ok) {
@@ -216,103 +223,130 @@ __global__ void __launch_bounds__(256, 1)
         if (phys >= 0) {
             const int j = pb + stream + i * p.nt;
             const int nvalid = min(BS, T - j * BS);
-            const KV* Kt = reinterpret_cast<const KV*>(smem + L.stages_off +
-                                                       (size_t)sidx * L.stage_bytes);
-            const KV* Vt = Kt + BS * D;
+            uint8_t* kt = smem + L.stages_off + (size_t)sidx * L.stage_bytes;
+            uint8_t* vt = kt + L.tile_bytes;
+            const uint32_t kbase = smem_u32(kt), vbase = smem_u32(vt);
 
-            for (int c0 = 0; c0 < nvalid; c0 += CHUNK) {
-                // ---- q.K partial dots over this lane's 8 dims ----
-                float v[NVAL];
-#pragma unroll
-                for (int st = 0; st < STEPS; ++st) {
-                    const int row = c0 + st * TPS + ts;
-                    const uint4 raw = *reinterpret_cast<const uint4*>(Kt + row * D + lig * 8);
-                    float kf[8];
-                    Vec8<KV>::to_float(raw, kf);
-#pragma unroll
-                    for (int g = 0; g < GW; ++g) {
-                        float a = qf[g][0] * kf[0];
-#pragma unroll
-                        for (int e = 1; e < 8; ++e) a = fmaf(qf[g][e], kf[e], a);
-                        v[g * STEPS + st] = a;
-                    }
+            if (nvalid < BS) {
+                // Zero this warp's columns of the V rows past the context.
+                const int rows = BS - nvalid;
+                for (int idx = lane; idx < rows * 8 * (DW / 64); idx += 32) {
+                    const int blk = ds * (DW / 64) + idx / (rows * 8);
+                    const int rem = idx % (rows * 8);
+                    *reinterpret_cast<uint4*>(vt + blk * BS * 128 + (nvalid + rem / 8) * 128 +
+                                              (rem % 8) * 16) = make_uint4(0, 0, 0, 0);
                 }
-                transpose_reduce<NVAL, LPT>(v, lane);
-
-                // ---- chunk max per head, online-softmax rescale ----
-                float cmax = NEG_INF;
-#pragma unroll
-                for (int k = 0; k < NOUT; ++k) {
-                    const int row = c0 + ((vbase + k) % STEPS) * TPS + ts;
-                    v[k] = row < nvalid ? v[k] : NEG_INF;
-                    cmax = fmaxf(cmax, v[k]);
-                }
-#pragma unroll
-                for (int mask = 1; mask < HL; mask <<= 1)
-                    cmax = fmaxf(cmax, __shfl_xor_sync(kFullMask, cmax, mask));
-#pragma unroll
-                for (int mask = LPT; mask < 32; mask <<= 1)
-                    cmax = fmaxf(cmax, __shfl_xor_sync(kFullMask, cmax, mask));
-
-                float alpha_own = 1.f, m_own = NEG_INF;
-#pragma unroll
-                for (int g = 0; g < GW; ++g) {
-                    const float cm = __shfl_sync(kFullMask, cmax, g * HL);
-                    const float mn = fmaxf(m[g], cm);
-                    const float alpha = (m[g] == mn) ? 1.f : exp2f(m[g] - mn);
-                    m[g] = mn;
-#pragma unroll
-                    for (int e = 0; e < 8; ++e) acc[g][e] *= alpha;
-                    if (g == gown) {
-                        alpha_own = alpha;
-                        m_own = mn;
-                    }
-                }
-
-                // ---- probabilities of this lane's dots ----
-                float psum = 0.f;
-#pragma unroll
-                for (int k = 0; k < NOUT; ++k) {
-                    const float pk = exp2f(v[k] - m_own);  // exp2(-inf) = 0 for masked rows
-                    psum += pk;
-                    if (designated) pw_base[((vbase + k) % STEPS) * GW + gown] = pk;
-                }
-                l_own = l_own * alpha_own + (designated ? psum : 0.f);
+                fence_proxy_async_smem();
                 __syncwarp();
+            }
 
-                // ---- acc += p * V over the chunk's rows ----
+            // ---- S = Q K^T (fp32) ----
+            float s[NT][4];
 #pragma unroll
-                for (int st = 0; st < STEPS; ++st) {
-                    const int row = c0 + st * TPS + ts;
-                    if (row < nvalid) {
-                        const uint4 raw = *reinterpret_cast<const uint4*>(Vt + row * D + lig * 8);
-                        float vf[8];
-                        Vec8<KV>::to_float(raw, vf);
-                        float pw[GW];
+            for (int nt = 0; nt < NT; ++nt) {
+                s[nt][0] = s[nt][1] = s[nt][2] = s[nt][3] = 0.f;
 #pragma unroll
-                        for (int g = 0; g < GW; ++g) pw[g] = pw_base[st * GW + g];
-#pragma unroll
-                        for (int g = 0; g < GW; ++g)
-#pragma unroll
-                            for (int e = 0; e < 8; ++e) acc[g][e] = fmaf(pw[g], vf[e], acc[g][e]);
-                    }
+                for (int kk = 0; kk < KSTEPS; kk += 2) {
+                    uint32_t b0, b1, b2, b3;
+                    ldsm_x4(kbase + swz<BS>(nt * 8 + ldsm_t, 2 * kk + ldsm_m), b0, b1, b2, b3);
+                    Mma<KV>::mma(s[nt], qa[kk], b0, b1);
+                    Mma<KV>::mma(s[nt], qa[kk + 1], b2, b3);
                 }
-                __syncwarp();
+            }
+
+            // ---- page max per row, conditional rescale ----
+            float mx0 = NEG_INF, mx1 = NEG_INF;
+#pragma unroll
+            for (int nt = 0; nt < NT; ++nt)
+#pragma unroll
+                for (int e = 0; e < 2; ++e) {
+                    const bool v = nt * 8 + tig * 2 + e < nvalid;
+                    s[nt][e] = v ? s[nt][e] : NEG_INF;
+                    s[nt][2 + e] = v ? s[nt][2 + e] : NEG_INF;
+                    mx0 = fmaxf(mx0, s[nt][e]);
+                    mx1 = fmaxf(mx1, s[nt][2 + e]);
+                }
+            mx0 = fmaxf(mx0, __shfl_xor_sync(kFullMask, mx0, 1));
+            mx1 = fmaxf(mx1, __shfl_xor_sync(kFullMask, mx1, 1));
+            mx0 = fmaxf(mx0, __shfl_xor_sync(kFullMask, mx0, 2));
+            mx1 = fmaxf(mx1, __shfl_xor_sync(kFullMask, mx1, 2));
+            const float ms0 = mx0 * qscale, ms1 = mx1 * qscale;
+            const bool need = (real0 && ms0 > m0 + kRescaleSlack) ||
+                              (real1 && ms1 > m1 + kRescaleSlack);
+            if (__any_sync(kFullMask, need)) {
+                const float n0 = real0 ? fmaxf(m0, ms0) : m0;
+                const float n1 = real1 ? fmaxf(m1, ms1) : m1;
+                const float a0 = (n0 == m0) ? 1.f : fast_exp2(m0 - n0);
+                const float a1 = (n1 == m1) ? 1.f : fast_exp2(m1 - n1);
+                m0 = n0;
+                m1 = n1;
+                l0 *= a0;
+                l1 *= a1;
+#pragma unroll
+                for (int n = 0; n < ONT; ++n) {
+                    acc[n][0] *= a0;
+                    acc[n][1] *= a0;
+                    acc[n][2] *= a1;
+                    acc[n][3] *= a1;
+                }
+            }
+
+            // ---- P = 2^(S*scale*log2e - m), and its hi/lo 16-bit split ----
+#pragma unroll
+            for (int nt = 0; nt < NT; ++nt)
+#pragma unroll
+                for (int e = 0; e < 2; ++e) {
+                    s[nt][e] = real0 ? fast_exp2(fmaf(s[nt][e], qscale, -m0)) : 0.f;
+                    s[nt][2 + e] = real1 ? fast_exp2(fmaf(s[nt][2 + e], qscale, -m1)) : 0.f;
+                    l0 += s[nt][e];
+                    l1 += s[nt][2 + e];
+                }
+
+            // ---- O += P V on this warp's columns ----
+#pragma unroll
+            for (int ks = 0; ks < PKS; ++ks) {
+                uint32_t ph[4], pl[4];
+#pragma unroll
+                for (int r = 0; r < 4; ++r) {
+                    // a0: n-tile 2ks rows g; a1: rows g+8; a2/a3: n-tile 2ks+1
+                    const float x0 = s[2 * ks + (r >> 1)][(r & 1) * 2];
+                    const float x1 = s[2 * ks + (r >> 1)][(r & 1) * 2 + 1];
+                    ph[r] = Mma<KV>::pack(x0, x1);
+                    float h0, h1;
+                    Mma<KV>::unpack(ph[r], h0, h1);
+                    pl[r] = Mma<KV>::pack(x0 - h0, x1 - h1);
+                }
+#pragma unroll
+                for (int n = 0; n < ONT; n += 2) {
+                    uint32_t b0, b1, b2, b3;
+                    const int t = ks * 16 + ((ldsm_m & 1) << 3) + ldsm_t;
+                    ldsm_x4_trans(vbase + swz<BS>(t, col0 + n + (ldsm_m >> 1)), b0, b1, b2, b3);
+                    Mma<KV>::mma(acc[n], ph, b0, b1);
+                    Mma<KV>::mma(acc[n], pl, b0, b1);
+                    Mma<KV>::mma(acc[n + 1], ph, b2, b3);
+                    Mma<KV>::mma(acc[n + 1], pl, b2, b3);
+                }
             }
         }
         __syncwarp();
         if (lane == 0) mbar_arrive(smem_u32(empty + sidx));
         // Refill the stage just released with this stream's page i + ns.
         int refill_failed = 0;
-        if (leader && i + p.ns < n_s) {
-            if (mbar_wait_bounded(smem_u32(empty + sidx), par, p.timeout_ns)) {
+        if (ds == 0 && i + p.ns < n_s) {
+            const bool freed = __all_sync(
+                kFullMask, mbar_wait_bounded(smem_u32(empty + sidx), par, p.timeout_ns));
+            if (freed) {
                 fence_proxy_async_smem();
-                issue(i + p.ns);
+                issue(i + p.ns, sidx);
                 ++n_issued;
             } else {
-                record_error(p.err, PA_ERR_TIMEOUT);
+                if (lane == 0) record_error(p.err, PA_ERR_TIMEOUT);
                 refill_failed = 1;
             }
+        }
+        if (++slot == p.ns) {
+            slot = 0;
+            par ^= 1u;
         }
         if (__shfl_sync(kFullMask, refill_failed, 0)) {
             aborted = true;
@@ -327,60 +361,64 @@ __global__ void __launch_bounds__(256, 1)
                                     (uint32_t)(k / p.ns) & 1u, p.timeout_ns);
     }
 
-    // ---- per-warp totals: rows of a step share m, so plain sums ----
-#pragma unroll
-    for (int mask = LPT; mask < 32; mask <<= 1)
-#pragma unroll
-        for (int g = 0; g < GW; ++g)
-#pragma unroll
-            for (int e = 0; e < 8; ++e) acc[g][e] += __shfl_xor_sync(kFullMask, acc[g][e], mask);
-#pragma unroll
-    for (int mask = 1; mask < HL; mask <<= 1) l_own += __shfl_xor_sync(kFullMask, l_own, mask);
-#pragma unroll
-    for (int mask = LPT; mask < 32; mask <<= 1) l_own += __shfl_xor_sync(kFullMask, l_own, mask);
+    // ---- per-warp normalisers: sum the quad's shares ----
+    l0 += __shfl_xor_sync(kFullMask, l0, 1);
+    l1 += __shfl_xor_sync(kFullMask, l1, 1);
+    l0 += __shfl_xor_sync(kFullMask, l0, 2);
+    l1 += __shfl_xor_sync(kFullMask, l1, 2);
 
-    const uint32_t MS = merge_stride(D, GW);
-    float* wm = mrg + (size_t)warp * MS;  // acc [GW][D], then m [GW], l [GW]
+    // Every stage has been consumed: the stage area now holds the merge data.
+    __syncthreads();
+    const int nw = p.nt * DS;
+    float* macc = reinterpret_cast<float*>(smem + L.stages_off);   // [nw][G][DW]
+    float* mm = macc + (size_t)nw * G * DW;                         // [nw][G]
+    float* ml = mm + nw * G;                                        // [nw][G]
 #pragma unroll
-    for (int g = 0; g < GW; ++g) {
-        const float lg = __shfl_sync(kFullMask, l_own, g * HL);
-        if (lane < LPT) {
-            float4* dst = reinterpret_cast<float4*>(wm + g * D + lig * 8);
-            dst[0] = make_float4(acc[g][0], acc[g][1], acc[g][2], acc[g][3]);
-            dst[1] = make_float4(acc[g][4], acc[g][5], acc[g][6], acc[g][7]);
+    for (int n = 0; n < ONT; ++n) {
+        const int c = n * 8 + tig * 2;
+        if (real0)
+            *reinterpret_cast<float2*>(macc + ((size_t)warp * G + g) * DW + c) =
+                make_float2(acc[n][0], acc[n][1]);
+        if (real1)
+            *reinterpret_cast<float2*>(macc + ((size_t)warp * G + g + 8) * DW + c) =
+                make_float2(acc[n][2], acc[n][3]);
+    }
+    if (tig == 0) {
+        if (real0) {
+            mm[warp * G + g] = m0;
+            ml[warp * G + g] = l0;
         }
-        if (lane == 0) {
-            wm[GW * D + g] = m[g];
-            wm[GW * D + GW + g] = lg;
+        if (real1) {
+            mm[warp * G + g + 8] = m1;
+            ml[warp * G + g + 8] = l1;
         }
     }
     __syncthreads();
 
     // ---- merge the token streams (log-sum-exp), then write ----
     for (int idx = tid; idx < G * D; idx += blockDim.x) {
-        const int gfull = idx / D, d = idx % D;
-        const int hgx = gfull / GW, gi = gfull % GW;
+        const int r = idx / D, d = idx % D;
+        const int dsx = d / DW, dd = d % DW;
         float M = NEG_INF;
-        for (int s2 = 0; s2 < p.nt; ++s2)
-            M = fmaxf(M, mrg[(size_t)(s2 * p.nh + hgx) * MS + GW * D + gi]);
+        for (int s2 = 0; s2 < p.nt; ++s2) M = fmaxf(M, mm[(s2 * DS + dsx) * G + r]);
         float A = 0.f, Ls = 0.f;
         if (M != NEG_INF) {
             for (int s2 = 0; s2 < p.nt; ++s2) {
-                const float* w2 = mrg + (size_t)(s2 * p.nh + hgx) * MS;
-                const float ms = w2[GW * D + gi];
+                const int w2 = s2 * DS + dsx;
+                const float ms = mm[w2 * G + r];
                 if (ms != NEG_INF) {
                     const float f = exp2f(ms - M);
-                    A = fmaf(f, w2[gi * D + d], A);
-                    Ls = fmaf(f, w2[GW * D + GW + gi], Ls);
+                    A = fmaf(f, macc[((size_t)w2 * G + r) * DW + dd], A);
+                    Ls = fmaf(f, ml[w2 * G + r], Ls);
                 }
             }
         }
-        const int h = kvh * G + gfull;
+        const int h = kvh * G + r;
         if (p.final_out) {
             store_out(p.out, ((size_t)b * p.num_heads + h) * D + d, Ls > 0.f ? A / Ls : 0.f,
                       p.out_dtype);
         } else {
-            const size_t row = (((size_t)b * p.num_kv_heads + kvh) * p.num_parts + part) * G + gfull;
+            const size_t row = (((size_t)b * p.num_kv_heads + kvh) * p.num_parts + part) * G + r;
             p.part_acc[row * D + d] = A;
             if (d == 0) {
                 p.part_ml[row * 2] = M;
@@ -390,35 +428,34 @@ __global__ void __launch_bounds__(256, 1)
     }
 }
 
-template <int D, int BS, typename KV, int GW>
+template <int D, int BS, typename KV>
 cudaError_t launch_attn_inst(const AttnLaunch& L, cudaStream_t stream) {
-    auto kern = attn_kernel<D, BS, KV, GW>;
+    auto kern = attn_kernel<D, BS, KV>;
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          (int)L.smem_bytes);
     if (e != cudaSuccess) return e;
-    kern<<<L.grid, L.threads, L.smem_bytes, stream>>>(L.tmap_k, L.tmap_v, L.p);
-    return cudaGetLastError();
-}
-
-template <int D, int BS, typename KV>
-cudaError_t launch_attn_gw(const AttnLaunch& L, cudaStream_t stream) {
-    switch (L.heads_per_warp) {
-        case 1: return launch_attn_inst<D, BS, KV, 1>(L, stream);
-        case 2: return launch_attn_inst<D, BS, KV, 2>(L, stream);
-        case 4: return launch_attn_inst<D, BS, KV, 4>(L, stream);
-        default: return cudaErrorInvalidValue;
-    }
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = L.grid;
+    cfg.blockDim = dim3(L.threads);
+    cfg.dynamicSmemBytes = L.smem_bytes;
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = L.pdl ? 1 : 0;
+    return cudaLaunchKernelEx(&cfg, kern, L.tmap_k, L.tmap_v, L.p);
 }
 
 template <int D>
 cudaError_t launch_attn_for_d(const AttnLaunch& L, cudaStream_t stream) {
     const bool bf = L.kv_dtype == PA_BF16;
     if (L.block_size == 16)
-        return bf ? launch_attn_gw<D, 16, __nv_bfloat16>(L, stream)
-                  : launch_attn_gw<D, 16, __half>(L, stream);
+        return bf ? launch_attn_inst<D, 16, __nv_bfloat16>(L, stream)
+                  : launch_attn_inst<D, 16, __half>(L, stream);
     if (L.block_size == 32)
-        return bf ? launch_attn_gw<D, 32, __nv_bfloat16>(L, stream)
-                  : launch_attn_gw<D, 32, __half>(L, stream);
+        return bf ? launch_attn_inst<D, 32, __nv_bfloat16>(L, stream)
+                  : launch_attn_inst<D, 32, __half>(L, stream);
     return cudaErrorInvalidValue;
 }
 

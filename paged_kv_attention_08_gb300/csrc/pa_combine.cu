@@ -15,69 +15,72 @@ namespace pa {
 
 namespace {
 
-__device__ __forceinline__ float block_reduce(float v, bool is_max, float* red) {
-    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-    const int nw = (blockDim.x + 31) >> 5;
-#pragma unroll
-    for (int mask = 16; mask >= 1; mask >>= 1) {
-        const float o = __shfl_xor_sync(kFullMask, v, mask);
-        v = is_max ? fmaxf(v, o) : v + o;
-    }
-    __syncthreads();  // `red` may still be read from a previous reduction
-    if (lane == 0) red[warp] = v;
-    __syncthreads();
-    float r = red[0];
-    for (int w = 1; w < nw; ++w) r = is_max ? fmaxf(r, red[w]) : r + red[w];
-    return r;
-}
-
-__global__ void __launch_bounds__(256) combine_kernel(const CombineParams p, int D) {
-    extern __shared__ float weight[];  // [num_parts]
-    __shared__ float red[32];
+// One CTA per (query head, sequence); each warp computes the partition
+// weights itself (lanes stride over partitions, shuffles reduce), then every
+// thread accumulates VEC output columns over the partitions with up to eight
+// independent loads in flight.  Two dependent memory round trips in all.
+template <int D>
+__global__ void __launch_bounds__(64) combine_kernel(const CombineParams p) {
+    constexpr int VEC = D <= 128 ? D / 32 : 4;
     constexpr float NEG_INF = -INFINITY;
+    extern __shared__ float weight_all[];  // [warps][num_parts]
+    grid_dependency_wait();                // partials come from the attention kernel
+    grid_launch_dependents();
 
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    float* weight = weight_all + (size_t)warp * p.num_parts;
     const int h = blockIdx.x, b = blockIdx.y;
     const int kvh = h / p.group, g = h % p.group;
     const int T = reachable_tokens(p.context_lens, b, p.max_blocks, p.block_size);
     const int npages = (T + p.block_size - 1) / p.block_size;
-    int nparts = (npages + p.part_pages - 1) / p.part_pages;
-    nparts = min(nparts, p.num_parts);
+    const int nparts = min((npages + p.part_pages - 1) / p.part_pages, p.num_parts);
 
     const size_t row0 = ((size_t)b * p.num_kv_heads + kvh) * p.num_parts;  // partition 0 of (b, kvh)
-    auto ml_at = [&](int part) { return p.part_ml + ((row0 + part) * p.group + g) * 2; };
+    const float2* ml = reinterpret_cast<const float2*>(p.part_ml);
+    auto ml_at = [&](int part) { return ml[(row0 + part) * p.group + g]; };
 
     float mx = NEG_INF;
-    for (int q = threadIdx.x; q < nparts; q += blockDim.x) mx = fmaxf(mx, ml_at(q)[0]);
-    const float M = block_reduce(mx, true, red);
-
+    for (int q = lane; q < nparts; q += 32) mx = fmaxf(mx, ml_at(q).x);
+#pragma unroll
+    for (int m = 16; m >= 1; m >>= 1) mx = fmaxf(mx, __shfl_xor_sync(kFullMask, mx, m));
     float ls = 0.f;
-    for (int q = threadIdx.x; q < nparts; q += blockDim.x) {
-        const float mq = ml_at(q)[0];
-        const float w = (mq == NEG_INF) ? 0.f : exp2f(mq - M);
+    for (int q = lane; q < nparts; q += 32) {
+        const float2 v = ml_at(q);
+        const float w = (v.x == NEG_INF) ? 0.f : exp2f(v.x - mx);
         weight[q] = w;
-        ls = fmaf(w, ml_at(q)[1], ls);
+        ls = fmaf(w, v.y, ls);
     }
-    const float Ls = block_reduce(ls, false, red);  // its barriers also publish `weight`
+#pragma unroll
+    for (int m = 16; m >= 1; m >>= 1) ls += __shfl_xor_sync(kFullMask, ls, m);
+    __syncwarp();
 
-    const bool empty = (M == NEG_INF) || !(Ls > 0.f);
-    for (int d = threadIdx.x; d < D; d += blockDim.x) {
-        float a = 0.f;
-        if (!empty) {
-            const float* src = p.part_acc + (row0 * p.group + g) * D + d;
-            const size_t stride = (size_t)p.group * D;
-            int q = 0;
-            for (; q + 4 <= nparts; q += 4) {
-                const float a0 = src[(size_t)q * stride], a1 = src[(size_t)(q + 1) * stride];
-                const float a2 = src[(size_t)(q + 2) * stride], a3 = src[(size_t)(q + 3) * stride];
-                a = fmaf(weight[q], a0, a);
-                a = fmaf(weight[q + 1], a1, a);
-                a = fmaf(weight[q + 2], a2, a);
-                a = fmaf(weight[q + 3], a3, a);
+    const int d0 = threadIdx.x * VEC;
+    float a[VEC];
+#pragma unroll
+    for (int v = 0; v < VEC; ++v) a[v] = 0.f;
+    const bool empty = (mx == NEG_INF) || !(ls > 0.f);
+    if (!empty) {
+        const float* src = p.part_acc + (row0 * p.group + g) * D + d0;
+        const size_t stride = (size_t)p.group * D;
+#pragma unroll 8
+        for (int q = 0; q < nparts; ++q) {
+            const float w = weight[q];
+            if constexpr (VEC == 4) {
+                const float4 x = *reinterpret_cast<const float4*>(src + (size_t)q * stride);
+                a[0] = fmaf(w, x.x, a[0]);
+                a[1] = fmaf(w, x.y, a[1]);
+                a[2] = fmaf(w, x.z, a[2]);
+                a[3] = fmaf(w, x.w, a[3]);
+            } else {
+                const float2 x = *reinterpret_cast<const float2*>(src + (size_t)q * stride);
+                a[0] = fmaf(w, x.x, a[0]);
+                a[1] = fmaf(w, x.y, a[1]);
             }
-            for (; q < nparts; ++q) a = fmaf(weight[q], src[(size_t)q * stride], a);
         }
-        store_out(p.out, ((size_t)b * p.num_heads + h) * D + d, empty ? 0.f : a / Ls, p.out_dtype);
     }
+    const size_t o = ((size_t)b * p.num_heads + h) * D + d0;
+#pragma unroll
+    for (int v = 0; v < VEC; ++v) store_out(p.out, o + v, empty ? 0.f : a[v] / ls, p.out_dtype);
 }
 
 __global__ void resolve_kernel(int32_t* out_phys, const int32_t* block_tables,
@@ -93,16 +96,32 @@ __global__ void resolve_kernel(int32_t* out_phys, const int32_t* block_tables,
 
 }  // namespace
 
-cudaError_t launch_combine(const CombineParams& p, int head_dim, dim3 grid, int threads,
-                           uint32_t smem_bytes, cudaStream_t stream) {
-    if (smem_bytes > 48 * 1024) {
-        cudaError_t e = cudaFuncSetAttribute(combine_kernel,
-                                             cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                             (int)smem_bytes);
+cudaError_t launch_combine(const CombineParams& p, int head_dim, dim3 grid, bool pdl,
+                           cudaStream_t stream) {
+    void (*kern)(const CombineParams);
+    switch (head_dim) {
+        case 64: kern = combine_kernel<64>; break;
+        case 128: kern = combine_kernel<128>; break;
+        default: kern = combine_kernel<256>; break;
+    }
+    const int threads = head_dim <= 128 ? 32 : 64;
+    const uint32_t smem = (uint32_t)(threads / 32) * p.num_parts * sizeof(float);
+    if (smem > 48 * 1024) {
+        cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                             (int)smem);
         if (e != cudaSuccess) return e;
     }
-    combine_kernel<<<grid, threads, smem_bytes, stream>>>(p, head_dim);
-    return cudaGetLastError();
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = grid;
+    cfg.blockDim = dim3(threads);
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = pdl ? 1 : 0;
+    return cudaLaunchKernelEx(&cfg, kern, p);
 }
 
 cudaError_t launch_resolve(int32_t* out_phys, const int32_t* block_tables,

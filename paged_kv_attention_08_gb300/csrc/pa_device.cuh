@@ -119,6 +119,20 @@ __device__ __forceinline__ void prefetch_tensormap(const CUtensorMap* map) {
     asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(map)) : "memory");
 }
 
+// Programmatic dependent launch: a kernel launched with the programmatic
+// stream-serialization attribute may start while its predecessor in the stream
+// is finishing; it must wait here before touching memory the predecessor may
+// write.  Without that attribute the wait returns at once.
+__device__ __forceinline__ void grid_dependency_wait() {
+    asm volatile("griddepcontrol.wait;" ::: "memory");
+}
+
+// Allow the next kernel in the stream to begin launching (it still waits for
+// this grid's completion before it reads anything this grid writes).
+__device__ __forceinline__ void grid_launch_dependents() {
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+
 __device__ __forceinline__ void record_error(int32_t* err, int32_t code) {
     if (err) atomicCAS(err, 0, code);
 }
@@ -152,6 +166,79 @@ struct Vec8<__nv_bfloat16> {
             f[2 * i] = x.x;
             f[2 * i + 1] = x.y;
         }
+    }
+};
+
+// ---------------------------------------------------------------------------
+// Warp-level tensor-core pieces: ldmatrix from shared memory and the
+// m16n8k16 MMA with fp32 accumulation, for fp16 and bf16 operands.
+// ---------------------------------------------------------------------------
+__device__ __forceinline__ void ldsm_x4(uint32_t addr, uint32_t& r0, uint32_t& r1, uint32_t& r2,
+                                        uint32_t& r3) {
+    asm volatile("ldmatrix.sync.aligned.m8n8.x4.shared.b16 {%0, %1, %2, %3}, [%4];"
+                 : "=r"(r0), "=r"(r1), "=r"(r2), "=r"(r3)
+                 : "r"(addr)
+                 : "memory");
+}
+
+__device__ __forceinline__ void ldsm_x4_trans(uint32_t addr, uint32_t& r0, uint32_t& r1,
+                                              uint32_t& r2, uint32_t& r3) {
+    asm volatile("ldmatrix.sync.aligned.m8n8.x4.trans.shared.b16 {%0, %1, %2, %3}, [%4];"
+                 : "=r"(r0), "=r"(r1), "=r"(r2), "=r"(r3)
+                 : "r"(addr)
+                 : "memory");
+}
+
+// 2^x on the special-function unit (relative error ~2^-22; -inf -> +0).
+__device__ __forceinline__ float fast_exp2(float x) {
+    float y;
+    asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+    return y;
+}
+
+template <typename KV>
+struct Mma;
+
+template <>
+struct Mma<__half> {
+    // c += a (16x16, row major) * b (16x8, column major)
+    static __device__ __forceinline__ void mma(float (&c)[4], const uint32_t (&a)[4], uint32_t b0,
+                                               uint32_t b1) {
+        asm("mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 {%0, %1, %2, %3}, "
+            "{%4, %5, %6, %7}, {%8, %9}, {%0, %1, %2, %3};"
+            : "+f"(c[0]), "+f"(c[1]), "+f"(c[2]), "+f"(c[3])
+            : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
+    }
+    // x0 in the low half, x1 in the high half, round to nearest even
+    static __device__ __forceinline__ uint32_t pack(float x0, float x1) {
+        uint32_t r;
+        asm("cvt.rn.f16x2.f32 %0, %1, %2;" : "=r"(r) : "f"(x1), "f"(x0));
+        return r;
+    }
+    static __device__ __forceinline__ void unpack(uint32_t v, float& x0, float& x1) {
+        const float2 f = __half22float2(*reinterpret_cast<const __half2*>(&v));
+        x0 = f.x;
+        x1 = f.y;
+    }
+};
+
+template <>
+struct Mma<__nv_bfloat16> {
+    static __device__ __forceinline__ void mma(float (&c)[4], const uint32_t (&a)[4], uint32_t b0,
+                                               uint32_t b1) {
+        asm("mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 {%0, %1, %2, %3}, "
+            "{%4, %5, %6, %7}, {%8, %9}, {%0, %1, %2, %3};"
+            : "+f"(c[0]), "+f"(c[1]), "+f"(c[2]), "+f"(c[3])
+            : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
+    }
+    static __device__ __forceinline__ uint32_t pack(float x0, float x1) {
+        uint32_t r;
+        asm("cvt.rn.bf16x2.f32 %0, %1, %2;" : "=r"(r) : "f"(x1), "f"(x0));
+        return r;
+    }
+    static __device__ __forceinline__ void unpack(uint32_t v, float& x0, float& x1) {
+        x0 = __uint_as_float(v << 16);
+        x1 = __uint_as_float(v & 0xffff0000u);
     }
 };
 

@@ -13,8 +13,6 @@ namespace pa {
 
 // Up to this many query heads share one kv head (num_heads / num_kv_heads).
 constexpr int kMaxGroup = 16;
-// Query heads one warp carries through a page (its share of the group).
-constexpr int kHeadsPerWarpMax = 4;
 
 struct AttnParams {
     const void* q;            // [B, H, D] kv dtype
@@ -30,7 +28,7 @@ struct AttnParams {
     int32_t part_pages;       // pages per partition
     int32_t num_parts;        // partitions per (sequence, kv head) = gridDim.x
     int32_t nt;               // token streams (independent page rings) per CTA
-    int32_t nh;               // warps per stream, each holding a slice of the head group
+    int32_t nh;               // warps per stream, each producing a slice of the output columns
     int32_t ns;               // pipeline stages per stream
     int32_t out_dtype;        // pa_dtype
     int32_t final_out;        // 1: write out; 0: write partials
@@ -47,30 +45,26 @@ struct CombineParams {
 };
 
 // Shared-memory layout of the attention kernel, identical on host and device.
+// Each stage holds one page of one kv head: the K tile then the V tile, each
+// head_dim/64 column blocks of [block_size rows][128 bytes], written by TMA
+// with the 128-byte swizzle.  After the page loop the stage area is reused
+// for the final merge of the warps' partial results.
 struct AttnSmem {
-    uint32_t stage_bytes;   // one stage: K tile then V tile, each block_size x head_dim
-    uint32_t stages_off;    // [nt][ns] stages
+    uint32_t tile_bytes;    // one K (or V) page tile: block_size * head_dim * 2
+    uint32_t stage_bytes;   // K tile + V tile
+    uint32_t stages_off;    // [nt][ns] stages (1024-byte aligned)
     uint32_t full_off;      // [nt][ns] uint64 mbarriers: page landed
     uint32_t empty_off;     // [nt][ns] uint64 mbarriers: page consumed
     uint32_t phys_off;      // [nt][ns] int32 physical block of the staged page (-1 = masked)
-    uint32_t pbuf_off;      // per warp: probabilities of one chunk
-    uint32_t mrg_off;       // per warp: acc [GW][D] then m [GW], l [GW] for the final merge
     uint32_t total;         // bytes, excluding the alignment slack
 };
 
 __host__ __device__ inline uint32_t pa_align_up(uint32_t x, uint32_t a) { return (x + a - 1) / a * a; }
 
-// Floats of one warp's merge block (acc [GW][D], m [GW], l [GW]), padded to a
-// multiple of four so that every block starts on a 16-byte boundary.
-__host__ __device__ inline uint32_t merge_stride(int D, int GW) {
-    return pa_align_up((uint32_t)(GW * (D + 2)), 4u);
-}
-
-__host__ __device__ inline AttnSmem attn_smem_layout(int D, int BS, int esize, int GW, int TPS,
-                                                     int STEPS, int nt, int nh, int ns) {
+__host__ __device__ inline AttnSmem attn_smem_layout(int D, int BS, int nt, int ns) {
     AttnSmem L;
-    const int nw = nt * nh;
-    L.stage_bytes = 2u * BS * D * esize;
+    L.tile_bytes = (uint32_t)BS * D * 2u;
+    L.stage_bytes = 2u * L.tile_bytes;
     L.stages_off = 0;
     uint32_t o = L.stage_bytes * nt * ns;
     L.full_off = o;
@@ -78,14 +72,15 @@ __host__ __device__ inline AttnSmem attn_smem_layout(int D, int BS, int esize, i
     L.empty_off = o;
     o += 8u * nt * ns;
     L.phys_off = o;
-    o = pa_align_up(o + 4u * nt * ns, 16);
-    L.pbuf_off = o;
-    o += 4u * nw * TPS * STEPS * GW;
-    o = pa_align_up(o, 16);
-    L.mrg_off = o;
-    o += 4u * nw * merge_stride(D, GW);
+    o += 4u * nt * ns;
     L.total = pa_align_up(o, 16);
     return L;
+}
+
+// Floats the final merge needs in the stage area: per warp, acc rows of the
+// group's heads over that warp's output columns, then m and l per head.
+__host__ __device__ inline uint32_t merge_floats(int nw, int G, int cols_per_warp) {
+    return (uint32_t)nw * G * cols_per_warp + 2u * nw * G;
 }
 
 // Slack added to the dynamic shared-memory request so that the kernel can
@@ -96,7 +91,8 @@ struct AttnLaunch {
     AttnParams p;
     CUtensorMap tmap_k;
     CUtensorMap tmap_v;
-    int head_dim, block_size, kv_dtype, heads_per_warp;
+    int head_dim, block_size, kv_dtype;
+    bool pdl;  // launch with programmatic stream serialization
     dim3 grid;
     int threads;
     uint32_t smem_bytes;
@@ -107,8 +103,8 @@ cudaError_t launch_attn_d64(const AttnLaunch& L, cudaStream_t stream);
 cudaError_t launch_attn_d128(const AttnLaunch& L, cudaStream_t stream);
 cudaError_t launch_attn_d256(const AttnLaunch& L, cudaStream_t stream);
 
-cudaError_t launch_combine(const CombineParams& p, int head_dim, dim3 grid, int threads,
-                           uint32_t smem_bytes, cudaStream_t stream);
+cudaError_t launch_combine(const CombineParams& p, int head_dim, dim3 grid, bool pdl,
+                           cudaStream_t stream);
 cudaError_t launch_resolve(int32_t* out_phys, const int32_t* block_tables,
                            const int32_t* context_lens, int32_t batch, int32_t max_blocks,
                            int32_t block_size, int64_t num_blocks, cudaStream_t stream);

@@ -84,6 +84,8 @@ GROUPS = {
              "long_b4_t8192", "long_b4_t32768", "long_b4_t131072"],
     "mqa": ["mqa_b32_t16384"],
 }
+# every single workload is also a group of its own
+GROUPS.update({name: [name] for name in SPECS if name not in GROUPS})
 
 
 @dataclass
