@@ -286,12 +286,22 @@ def main(argv=None):
 
     outs = [[torch.empty(x.q.shape, dtype=torch.float32, device=dev) for x in st] for st in sets]
     ws = []
-    for i, x in enumerate(set0):
-        need = pa.workspace_size(x.q, x.k_cache, x.block_tables, torch.float32,
-                                 x.max_context_len, pts[i])
+    for i in range(len(set0)):
+        # every rotated set has its own longest context, hence its own plan
+        need = max(pa.workspace_size(st[i].q, st[i].k_cache, st[i].block_tables, torch.float32,
+                                     st[i].max_context_len, pts[i]) for st in sets)
         ws.append(torch.empty(max(need, 16), dtype=torch.uint8, device=dev))
-    splits = [ws[i].numel() > 16 for i in range(len(set0))]
+    splits = [ws[i].numel() > 16 for i in range(len(set0))]      # partials combined by a 2nd kernel
     launches_per_step = sum(2 if s else 1 for s in splits)
+    sms = props.multi_processor_count
+    plans = {}
+    for i, x in enumerate(set0):
+        pt = pts[i] or pa.choose_partition_tokens(x.q, x.k_cache, x.block_tables,
+                                                  x.max_context_len, sms)
+        parts = -(-max(x.max_context_len, 1) // pt)
+        plans[names[i]] = {"partition_tokens": pt, "partitions": parts,
+                           "reduce": "none" if parts <= 1 else
+                                     ("workspace+combine kernel" if splits[i] else "cluster DSMEM")}
 
     stream = torch.cuda.Stream(device=dev)
 
@@ -462,7 +472,7 @@ def main(argv=None):
                 "per_call_us": {n: round(u, 3) for n, u in zip(names, call_us)},
                 "algorithmic_bytes_per_step": step_bytes,
                 "partition_tokens": {n: (p if p else "auto") for n, p in zip(names, pts)},
-                "split": {n: s for n, s in zip(names, splits)},
+                "plan": plans,
                 "l2": f"rotating {nsets} input sets of {set_bytes / 1e6:.1f} MB "
                       f"({nsets * set_bytes / 1e6:.0f} MB > 3x L2 {l2 / 1e6:.0f} MB)",
                 "launch": "CUDA graph replay per step" if graphs else "eager",
@@ -474,7 +484,8 @@ def main(argv=None):
             "roofline": {"bound": "hbm", "achieved": dom_gbs, "peak": peak, "unit": "GB/s",
                          "frac": dom_gbs / peak, "peak_kind": peak_kind,
                          "kernel": f"decode call on {dom_name} "
-                                   f"({'partial+combine' if splits[dom] else 'single pass'})",
+                                   f"({plans[dom_name]['partitions']} partition(s), reduce: "
+                                   f"{plans[dom_name]['reduce']})",
                          "traffic": ncu_traffic("pa_attn", dom_name),
                          "step_frac": value / world / peak},
             "cpu_baseline": cpu,

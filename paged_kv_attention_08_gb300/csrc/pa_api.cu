@@ -2,6 +2,7 @@
 // plan, TMA descriptors, and the launches.
 #include <cudaTypedefs.h>
 
+#include <algorithm>
 #include <atomic>
 #include <cstdlib>
 #include <cstring>
@@ -136,13 +137,38 @@ int pages_for(const pa_shape* s, int32_t max_context_len) {
     return (int)((t + s->block_size - 1) / s->block_size);
 }
 
-// Automatic partition size.  Cost model, in units of one page's time at a
-// fair share of bandwidth: a wave of resident CTAs costs (pages per CTA + a
-// fixed start-up of kCtaStartPages); splitting adds the combine pass
-// (kCombinePages).  The sequence length assumed is the longest one.
-int32_t choose_partition_tokens(const pa_shape* s, int32_t max_context_len, int num_sms) {
-    constexpr double kCtaStartPages = 4.0;
-    constexpr double kCombinePages = 8.0;
+// How a call is split: pages per partition, partitions per (sequence, kv
+// head), and whether the partitions reduce inside a thread-block cluster
+// (no workspace, no combine launch) or through the workspace and the combine
+// kernel.
+struct Plan {
+    int part_pages, num_parts;
+    bool cluster;
+};
+
+Plan plan_with(const pa_shape* s, int pages, int pp, bool cluster_ok) {
+    Plan p;
+    if (pp < 1) pp = 1;
+    p.num_parts = (pages + pp - 1) / pp;
+    if (p.num_parts < 1) p.num_parts = 1;
+    p.part_pages = p.num_parts <= 1 ? s->max_blocks_per_seq : pp;
+    p.cluster = cluster_ok && p.num_parts > 1 && p.num_parts <= kMaxClusterParts;
+    return p;
+}
+
+// Automatic split (the design notes only say the chunk size follows the KV
+// length; these rules are this library's own, fitted to GB300 timings of the
+// workloads it is measured on).  With units = batch * kv heads CTAs unsplit
+// and `slots` CTAs resident at once:
+//  - a grid already a third full or more is split only into partitions of
+//    about 64 pages, so that long and ragged sequences balance across waves;
+//    no cluster (the grid spans several waves);
+//  - a smaller grid is split to fill about 85% of one wave, either into at
+//    most 8 partitions of at least 4 pages reduced inside a cluster, or, when
+//    that would give less than half the parallelism, into partitions of at
+//    least 16 pages combined through the workspace.
+// The longest context stands for every sequence: the host reads no lengths.
+Plan auto_plan(const pa_shape* s, int32_t max_context_len, int num_sms) {
     const Tune t = pick_tune(s);
     const AttnSmem L = tune_smem(s, t);
     int ctas_per_sm = (int)((227u * 1024u) / (L.total + kSmemAlignSlack));
@@ -151,42 +177,41 @@ int32_t choose_partition_tokens(const pa_shape* s, int32_t max_context_len, int 
     const int64_t slots = (int64_t)num_sms * ctas_per_sm;
     const int pages = pages_for(s, max_context_len);
     const int64_t units = (int64_t)s->batch * s->num_kv_heads;
-    int best_pp = pages;
-    double best = 1e300;
-    int last_parts = 0;
-    for (int pp = pages; pp >= 1; --pp) {
-        const int parts = (pages + pp - 1) / pp;
-        if (parts == last_parts) continue;
-        last_parts = parts;
-        const int use_pp = (pages + parts - 1) / parts;  // smallest pp giving this count
-        const int64_t ctas = units * parts;
-        const int64_t waves = (ctas + slots - 1) / slots;
-        const double cost = (double)waves * (use_pp + kCtaStartPages) + (parts > 1 ? kCombinePages : 0.0);
-        if (cost < best - 1e-9) {
-            best = cost;
-            best_pp = use_pp;
-        }
+    auto ceil_div = [](int64_t a, int64_t b) { return (a + b - 1) / b; };
+    if (units * 3 >= slots) {
+        const int parts = (int)ceil_div(pages, 64);
+        return plan_with(s, pages, (int)ceil_div(pages, parts), false);
     }
-    return best_pp * s->block_size;
+    int64_t fill = (int64_t)(0.85 * (double)slots / (double)units);
+    if (fill < 1) fill = 1;
+    const int64_t p_cl = std::min<int64_t>(std::min<int64_t>(kMaxClusterParts, fill), ceil_div(pages, 4));
+    const int64_t p_ws = std::min<int64_t>(fill, ceil_div(pages, 16));
+    if (p_cl * 2 >= p_ws) return plan_with(s, pages, (int)ceil_div(pages, p_cl), true);
+    return plan_with(s, pages, (int)ceil_div(pages, p_ws), false);
 }
 
-struct Plan {
-    int part_pages, num_parts;
-};
+// The plan of a call: automatic for partition_tokens == 0, otherwise
+// partitions of exactly that many tokens (reduced in a cluster when there
+// are at most kMaxClusterParts of them).
+// PA_NO_CLUSTER=1 turns the in-cluster reduction off (partitions then always
+// go through the workspace); a tuning switch, results are the same.
+bool clusters_enabled() {
+    static const bool off = std::getenv("PA_NO_CLUSTER") && std::atoi(std::getenv("PA_NO_CLUSTER")) > 0;
+    return !off;
+}
 
-Plan make_plan(const pa_shape* s, int32_t max_context_len, int32_t partition_tokens) {
-    const int pages = pages_for(s, max_context_len);
-    const int pp = partition_tokens / s->block_size;
-    Plan p;
-    p.num_parts = (pages + pp - 1) / pp;
-    p.part_pages = p.num_parts <= 1 ? s->max_blocks_per_seq : pp;
-    if (p.num_parts < 1) p.num_parts = 1;
-    return p;
+Plan make_plan(const pa_shape* s, int32_t max_context_len, int32_t partition_tokens, int num_sms) {
+    Plan plan = partition_tokens == 0
+                    ? auto_plan(s, max_context_len, num_sms)
+                    : plan_with(s, pages_for(s, max_context_len), partition_tokens / s->block_size, true);
+    if (!clusters_enabled()) plan.cluster = false;
+    return plan;
 }
 
 // Workspace: part_acc [B, Hkv, P, G, D] fp32, then part_ml [B, Hkv, P, G, 2] fp32.
-size_t workspace_bytes_for(const pa_shape* s, int num_parts, size_t* ml_offset) {
-    if (num_parts <= 1) return 0;
+size_t workspace_bytes_for(const pa_shape* s, const Plan& plan, size_t* ml_offset) {
+    if (plan.num_parts <= 1 || plan.cluster) return 0;  // one pass, or reduced inside a cluster
+    const int num_parts = plan.num_parts;
     const size_t rows = (size_t)s->batch * s->num_heads * num_parts;  // B*Hkv*P*G
     const size_t acc = rows * s->head_dim * sizeof(float);
     const size_t off = (acc + 255) / 256 * 256;
@@ -238,7 +263,8 @@ pa_status launch_attention(void* out, const void* q, const void* k, const void* 
     const Tune t = pick_tune(s);
     const AttnSmem sm = tune_smem(s, t);
     const int G = s->num_heads / s->num_kv_heads;
-    if (4u * merge_floats(t.nt * t.nh, G, s->head_dim / t.nh) > sm.stage_bytes * t.nt * t.ns)
+    if (4u * (merge_floats(t.nt * t.nh, G, s->head_dim / t.nh) + cluster_part_floats(G, s->head_dim)) >
+        sm.stage_bytes * t.nt * t.ns)
         return PA_ERR_UNSUPPORTED;  // the final merge must fit in the stage area
     AttnParams& p = L.p;
     p.q = q;
@@ -262,11 +288,13 @@ pa_status launch_attention(void* out, const void* q, const void* k, const void* 
     p.ns = t.ns;
     p.out_dtype = s->out_dtype;
     p.final_out = plan.num_parts <= 1 ? 1 : 0;
+    p.cluster_reduce = plan.cluster ? 1 : 0;
     p.timeout_ns = kDefaultTimeoutNs;
     L.head_dim = s->head_dim;
     L.block_size = s->block_size;
     L.kv_dtype = s->kv_dtype;
     L.pdl = use_pdl();
+    L.cluster = p.cluster_reduce ? plan.num_parts : 1;
     L.grid = dim3((unsigned)plan.num_parts, (unsigned)s->num_kv_heads, (unsigned)s->batch);
     L.threads = 32 * t.nt * t.nh;
     L.smem_bytes = sm.total + kSmemAlignSlack;
@@ -301,20 +329,18 @@ const char* pa_status_string(pa_status status) {
 int32_t pa_choose_partition_tokens(const pa_shape* shape, int32_t max_context_len,
                                    int32_t num_sms) {
     if (check_shape(shape) != PA_OK || max_context_len < 0 || num_sms <= 0) return 0;
-    return choose_partition_tokens(shape, max_context_len, num_sms);
+    const Plan plan = auto_plan(shape, max_context_len, num_sms);
+    return plan.part_pages * shape->block_size;
 }
 
 size_t pa_workspace_size(const pa_shape* shape, int32_t max_context_len,
                          int32_t partition_tokens) {
     if (check_shape(shape) != PA_OK || max_context_len < 0 || partition_tokens < 0) return 0;
     if (partition_tokens % shape->block_size != 0) return 0;
-    if (partition_tokens == 0) {
-        int sms = 0;
-        if (device_state(&sms, nullptr) != PA_OK) return 0;
-        partition_tokens = choose_partition_tokens(shape, max_context_len, sms);
-    }
-    const Plan plan = make_plan(shape, max_context_len, partition_tokens);
-    return workspace_bytes_for(shape, plan.num_parts, nullptr);
+    int sms = 1;
+    if (partition_tokens == 0 && device_state(&sms, nullptr) != PA_OK) return 0;
+    const Plan plan = make_plan(shape, max_context_len, partition_tokens, sms);
+    return workspace_bytes_for(shape, plan, nullptr);
 }
 
 pa_status pa_decode(void* out, const void* q, const void* k_cache, const void* v_cache,
@@ -328,7 +354,7 @@ pa_status pa_decode(void* out, const void* q, const void* k_cache, const void* v
     int32_t* err = nullptr;
     st = device_state(nullptr, &err);
     if (st != PA_OK) return st;
-    Plan plan{shape->max_blocks_per_seq, 1};
+    Plan plan{shape->max_blocks_per_seq, 1, false};
     return launch_attention(out, q, k_cache, v_cache, block_tables, context_lens, shape, scale,
                             plan, nullptr, nullptr, err, static_cast<cudaStream_t>(stream));
 }
@@ -349,15 +375,14 @@ pa_status pa_decode_splitkv(void* out, const void* q, const void* k_cache, const
     int32_t* err = nullptr;
     st = device_state(&sms, &err);
     if (st != PA_OK) return st;
-    if (partition_tokens == 0) partition_tokens = choose_partition_tokens(shape, max_context_len, sms);
-    const Plan plan = make_plan(shape, max_context_len, partition_tokens);
+    const Plan plan = make_plan(shape, max_context_len, partition_tokens, sms);
     cudaStream_t cs = static_cast<cudaStream_t>(stream);
-    if (plan.num_parts <= 1)
+    if (plan.num_parts <= 1 || plan.cluster)
         return launch_attention(out, q, k_cache, v_cache, block_tables, context_lens, shape, scale,
                                 plan, nullptr, nullptr, err, cs);
 
     size_t ml_off = 0;
-    const size_t need = workspace_bytes_for(shape, plan.num_parts, &ml_off);
+    const size_t need = workspace_bytes_for(shape, plan, &ml_off);
     if (!workspace || !aligned(workspace, 16) || workspace_bytes < need) return PA_ERR_WORKSPACE;
     if ((size_t)plan.num_parts * 2 * sizeof(float) > 200u * 1024u) return PA_ERR_UNSUPPORTED;
     float* part_acc = static_cast<float*>(workspace);
@@ -429,9 +454,8 @@ pa_status pa_decode_splitkv_noalloc(void* out, const void* q, const void* k_cach
     int sms = 0;
     st = device_state(&sms, nullptr);
     if (st != PA_OK) return st;
-    if (partition_tokens == 0) partition_tokens = choose_partition_tokens(shape, max_context_len, sms);
-    const Plan plan = make_plan(shape, max_context_len, partition_tokens);
-    if (workspace_bytes_for(shape, plan.num_parts, nullptr) > kNoAllocScratchBytes)
+    const Plan plan = make_plan(shape, max_context_len, partition_tokens, sms);
+    if (workspace_bytes_for(shape, plan, nullptr) > kNoAllocScratchBytes)
         return PA_ERR_WORKSPACE;  // more partials than the fixed scratch holds
 
     // Device address of this device's copy of the scratch array, looked up

@@ -39,6 +39,8 @@
 //     PA_ERR_TIMEOUT in the device error word and abandons its work.
 #pragma once
 
+#include <cooperative_groups.h>
+
 #include "pa_device.cuh"
 
 namespace pa {
@@ -122,10 +124,11 @@ __global__ void __launch_bounds__(256, 1)
     const int T = reachable_tokens(p.context_lens, b, p.max_blocks, BS);
     const int npages = (T + BS - 1) / BS;
     const int pe = min(pb + p.part_pages, npages);
-    if (pb >= pe) {
+    if (pb >= pe && !p.cluster_reduce) {
         // Nothing of this sequence falls in the partition.  The single pass
         // writes the empty-context result; the combine kernel never reads
-        // partitions past the context.
+        // partitions past the context.  (Inside a cluster every CTA takes
+        // part in the reduction, so an empty one carries on with no pages.)
         if (p.final_out) {
             for (int idx = tid; idx < G * D; idx += blockDim.x) {
                 const int h = kvh * G + idx / D;
@@ -240,18 +243,21 @@ __global__ void __launch_bounds__(256, 1)
                 __syncwarp();
             }
 
-            // ---- S = Q K^T (fp32) ----
-            float s[NT][4];
+            // ---- S = Q K^T (fp32), even and odd k-steps in separate chains ----
+            float s[NT][4], s2[NT][4];
 #pragma unroll
             for (int nt = 0; nt < NT; ++nt) {
                 s[nt][0] = s[nt][1] = s[nt][2] = s[nt][3] = 0.f;
+                s2[nt][0] = s2[nt][1] = s2[nt][2] = s2[nt][3] = 0.f;
 #pragma unroll
                 for (int kk = 0; kk < KSTEPS; kk += 2) {
                     uint32_t b0, b1, b2, b3;
                     ldsm_x4(kbase + swz<BS>(nt * 8 + ldsm_t, 2 * kk + ldsm_m), b0, b1, b2, b3);
                     Mma<KV>::mma(s[nt], qa[kk], b0, b1);
-                    Mma<KV>::mma(s[nt], qa[kk + 1], b2, b3);
+                    Mma<KV>::mma(s2[nt], qa[kk + 1], b2, b3);
                 }
+#pragma unroll
+                for (int e = 0; e < 4; ++e) s[nt][e] += s2[nt][e];
             }
 
             // ---- page max per row, conditional rescale ----
@@ -329,11 +335,12 @@ __global__ void __launch_bounds__(256, 1)
             }
         }
         __syncwarp();
-        if (lane == 0) mbar_arrive(smem_u32(empty + sidx));
+        // A stream of one warp frees its own stage; with two, both must be done.
+        if (DS > 1 && lane == 0) mbar_arrive(smem_u32(empty + sidx));
         // Refill the stage just released with this stream's page i + ns.
         int refill_failed = 0;
         if (ds == 0 && i + p.ns < n_s) {
-            const bool freed = __all_sync(
+            const bool freed = DS == 1 || __all_sync(
                 kFullMask, mbar_wait_bounded(smem_u32(empty + sidx), par, p.timeout_ns));
             if (freed) {
                 fence_proxy_async_smem();
@@ -373,6 +380,7 @@ __global__ void __launch_bounds__(256, 1)
     float* macc = reinterpret_cast<float*>(smem + L.stages_off);   // [nw][G][DW]
     float* mm = macc + (size_t)nw * G * DW;                         // [nw][G]
     float* ml = mm + nw * G;                                        // [nw][G]
+    float* cpart = ml + nw * G;  // this CTA's partial when the cluster reduces: acc [G][D], m [G], l [G]
 #pragma unroll
     for (int n = 0; n < ONT; ++n) {
         const int c = n * 8 + tig * 2;
@@ -417,6 +425,12 @@ __global__ void __launch_bounds__(256, 1)
         if (p.final_out) {
             store_out(p.out, ((size_t)b * p.num_heads + h) * D + d, Ls > 0.f ? A / Ls : 0.f,
                       p.out_dtype);
+        } else if (p.cluster_reduce) {
+            cpart[idx] = A;
+            if (d == 0) {
+                cpart[G * D + r] = M;
+                cpart[G * D + G + r] = Ls;
+            }
         } else {
             const size_t row = (((size_t)b * p.num_kv_heads + kvh) * p.num_parts + part) * G + r;
             p.part_acc[row * D + d] = A;
@@ -425,6 +439,39 @@ __global__ void __launch_bounds__(256, 1)
                 p.part_ml[row * 2 + 1] = Ls;
             }
         }
+    }
+
+    if (p.cluster_reduce) {
+        // Log-sum-exp over the cluster's partitions, read from each CTA's
+        // shared memory; each CTA finalises a 1/P share of the outputs.
+        namespace cg = cooperative_groups;
+        cg::cluster_group cluster = cg::this_cluster();
+        cluster.sync();
+        const int P = p.num_parts;
+        const int rank = (int)cluster.block_rank();
+        const int chunk = (G * D + P - 1) / P;
+        const int i1 = min((rank + 1) * chunk, G * D);
+        for (int idx = rank * chunk + tid; idx < i1; idx += blockDim.x) {
+            const int r = idx / D;
+            float M = NEG_INF;
+            for (int q = 0; q < P; ++q)
+                M = fmaxf(M, cluster.map_shared_rank(cpart, q)[G * D + r]);
+            float A = 0.f, Ls = 0.f;
+            if (M != NEG_INF) {
+                for (int q = 0; q < P; ++q) {
+                    const float* rp = cluster.map_shared_rank(cpart, q);
+                    const float mq = rp[G * D + r];
+                    if (mq != NEG_INF) {
+                        const float f = exp2f(mq - M);
+                        A = fmaf(f, rp[idx], A);
+                        Ls = fmaf(f, rp[G * D + G + r], Ls);
+                    }
+                }
+            }
+            store_out(p.out, ((size_t)b * p.num_heads + kvh * G) * D + idx,
+                      Ls > 0.f ? A / Ls : 0.f, p.out_dtype);
+        }
+        cluster.sync();  // no CTA leaves while others still read its shared memory
     }
 }
 
@@ -439,11 +486,22 @@ cudaError_t launch_attn_inst(const AttnLaunch& L, cudaStream_t stream) {
     cfg.blockDim = dim3(L.threads);
     cfg.dynamicSmemBytes = L.smem_bytes;
     cfg.stream = stream;
-    cudaLaunchAttribute attr[1];
-    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
-    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cudaLaunchAttribute attr[2];
+    int n = 0;
+    if (L.pdl) {
+        attr[n].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+        attr[n].val.programmaticStreamSerializationAllowed = 1;
+        ++n;
+    }
+    if (L.cluster > 1) {
+        attr[n].id = cudaLaunchAttributeClusterDimension;
+        attr[n].val.clusterDim.x = (unsigned)L.cluster;
+        attr[n].val.clusterDim.y = 1;
+        attr[n].val.clusterDim.z = 1;
+        ++n;
+    }
     cfg.attrs = attr;
-    cfg.numAttrs = L.pdl ? 1 : 0;
+    cfg.numAttrs = n;
     return cudaLaunchKernelEx(&cfg, kern, L.tmap_k, L.tmap_v, L.p);
 }
 

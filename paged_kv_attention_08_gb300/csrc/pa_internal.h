@@ -31,7 +31,10 @@ struct AttnParams {
     int32_t nh;               // warps per stream, each producing a slice of the output columns
     int32_t ns;               // pipeline stages per stream
     int32_t out_dtype;        // pa_dtype
-    int32_t final_out;        // 1: write out; 0: write partials
+    int32_t final_out;        // 1: write out (one partition); 0: partitions reduce elsewhere
+    int32_t cluster_reduce;   // 1: the num_parts partitions of a (sequence, kv head) form one
+                              //    thread-block cluster and reduce through distributed shared
+                              //    memory; 0: partials go to the workspace for the combine kernel
     uint64_t timeout_ns;      // bound on every wait of the copy pipeline
 };
 
@@ -78,10 +81,18 @@ __host__ __device__ inline AttnSmem attn_smem_layout(int D, int BS, int nt, int 
 }
 
 // Floats the final merge needs in the stage area: per warp, acc rows of the
-// group's heads over that warp's output columns, then m and l per head.
+// group's heads over that warp's output columns, then m and l per head; then
+// the CTA's merged partial (acc [G][D], m [G], l [G]) that the other CTAs of a
+// cluster read.
 __host__ __device__ inline uint32_t merge_floats(int nw, int G, int cols_per_warp) {
     return (uint32_t)nw * G * cols_per_warp + 2u * nw * G;
 }
+__host__ __device__ inline uint32_t cluster_part_floats(int G, int D) {
+    return (uint32_t)G * D + 2u * G;
+}
+
+// Most partitions of one (sequence, kv head) reduced inside a cluster.
+constexpr int kMaxClusterParts = 8;
 
 // Slack added to the dynamic shared-memory request so that the kernel can
 // align its base to 1024 bytes (TMA destinations).
@@ -92,7 +103,8 @@ struct AttnLaunch {
     CUtensorMap tmap_k;
     CUtensorMap tmap_v;
     int head_dim, block_size, kv_dtype;
-    bool pdl;  // launch with programmatic stream serialization
+    bool pdl;     // launch with programmatic stream serialization
+    int cluster;  // > 1: cluster size along x (= partitions per sequence and kv head)
     dim3 grid;
     int threads;
     uint32_t smem_bytes;

@@ -104,10 +104,15 @@ def test_workspace_size_explicit_partition(lib):
     assert lib.pa_workspace_size(ctypes.byref(s), 131072, 131072) == 0      # one partition
     assert lib.pa_workspace_size(ctypes.byref(s), 131072, 100) == 0        # not a multiple of 16
     assert lib.pa_workspace_size(ctypes.byref(s), 0, 512) == 0
-    # tokens past the table row are not planned for
-    s2 = shape(batch=1, max_blocks_per_seq=4)
+    # tokens past the table row are not planned for: 16 pages in partitions of 1
+    s2 = shape(batch=1, max_blocks_per_seq=16)
     assert lib.pa_workspace_size(ctypes.byref(s2), 10_000, 16) == \
-        (1 * 32 * 4 * 128 * 4 + 255) // 256 * 256 + 1 * 32 * 4 * 2 * 4
+        (1 * 32 * 16 * 128 * 4 + 255) // 256 * 256 + 1 * 32 * 16 * 2 * 4
+    # up to 8 partitions reduce inside a thread-block cluster: no workspace
+    s3 = shape(batch=1, max_blocks_per_seq=4)
+    assert lib.pa_workspace_size(ctypes.byref(s3), 10_000, 16) == 0
+    assert lib.pa_workspace_size(ctypes.byref(s), 8 * 512, 512) == 0
+    assert lib.pa_workspace_size(ctypes.byref(s), 9 * 512, 512) > 0
 
 
 @pytest.mark.parametrize("B,T,Hkv", [(1, 512, 8), (16, 256, 8), (4, 2048, 8), (64, 4096, 8),
@@ -121,8 +126,10 @@ def test_partition_choice_properties(lib, B, T, Hkv):
         pt = lib.pa_choose_partition_tokens(ctypes.byref(s), T, sms)
         assert pt > 0 and pt % bs == 0
         assert pt <= ((T + bs - 1) // bs) * bs
-    # many (sequence, kv head) pairs per SM need no split
-    assert lib.pa_choose_partition_tokens(ctypes.byref(s), T, 1) >= T
+    # a grid that already fills the GPU is only cut into partitions of ~64 pages
+    pages = (T + bs - 1) // bs
+    pt1 = lib.pa_choose_partition_tokens(ctypes.byref(s), T, 1)
+    assert pt1 // bs == -(-pages // -(-pages // 64))
     assert lib.pa_choose_partition_tokens(ctypes.byref(s), T, 0) == 0     # invalid SM count
 
 
@@ -131,6 +138,14 @@ def test_single_sequence_long_context_is_split(lib):
     pt = lib.pa_choose_partition_tokens(ctypes.byref(s), 131072, 152)
     parts = -(-131072 // pt)
     assert parts * 8 >= 152           # at least one CTA per SM
+    assert parts * 8 <= 2 * 152       # and a single wave
+
+
+def test_small_grids_reduce_in_a_cluster(lib):
+    # batch 4 x 8 kv heads x 2048 tokens on 152 SMs: 8 partitions, no workspace needed
+    s = shape(batch=4, max_blocks_per_seq=128)
+    pt = lib.pa_choose_partition_tokens(ctypes.byref(s), 2048, 152)
+    assert -(-2048 // pt) == 8
 
 
 def test_binding_refuses_cpu_tensors():

@@ -143,6 +143,25 @@ def test_other_shapes(shape, dtype):
         assert_close_fp32(run(xd, mode, partition_tokens=pt), want)
 
 
+@pytest.mark.parametrize("parts", [2, 3, 5, 8])
+@pytest.mark.parametrize("shape", [SHAPES[2], SHAPES[3], SHAPES[4], SHAPES[0]],
+                         ids=lambda s: f"H{s['H']}kv{s['Hkv']}D{s['D']}bs{s['bs']}")
+def test_cluster_split_sizes(shape, parts):
+    """Splits of at most 8 partitions reduce inside one thread-block cluster."""
+    x = random_case(7, dtype=torch.bfloat16, **shape)
+    bs = shape["bs"]
+    pages = -(-max(shape["lens"]) // bs)
+    if pages < parts:
+        pytest.skip("fewer pages than partitions")
+    pt = -(-pages // parts) * bs
+    assert -(-max(shape["lens"]) // pt) <= 8
+    want = oracle.decode(x.q, x.k_cache, x.v_cache, x.block_tables, x.context_lens, x.scale)
+    xd = x.to(DEV)
+    assert pa.workspace_size(xd.q, xd.k_cache, xd.block_tables, torch.float32,
+                             xd.max_context_len, pt) == 0
+    assert_close_fp32(run(xd, "split", partition_tokens=pt), want)
+
+
 # ---------------------------------------------------------------------------
 # edge cases and invariances
 # ---------------------------------------------------------------------------
@@ -160,7 +179,7 @@ def test_edge_lengths_and_masking():
     want = oracle.decode(x.q, x.k_cache, x.v_cache, bt, lens, x.scale)
     xd = x.to(DEV)
     xd.max_context_len = 10_000
-    for mode, pt in [("single", 0), ("split", 16), ("split", 32), ("split", 0)]:
+    for mode, pt in [("single", 0), ("split", 16), ("split", 32), ("split", 48), ("split", 0)]:
         got = run(xd, mode, partition_tokens=pt)
         assert_close_fp32(got, want)
         assert torch.all(got[0] == 0)        # empty context -> zeros
@@ -170,7 +189,7 @@ def test_all_masked_and_empty_batch():
     x = random_case(6, B=2, H=4, Hkv=4, D=128, bs=16, lens=[40, 20], dtype=torch.float16)
     x.block_tables = torch.full_like(x.block_tables, -1)
     xd = x.to(DEV)
-    for mode, pt in [("single", 0), ("split", 16)]:
+    for mode, pt in [("single", 0), ("split", 16), ("split", 0)]:
         assert torch.all(run(xd, mode, partition_tokens=pt) == 0)
     e = workloads.make("tiny", device=DEV)
     out = torch.empty(0, 32, 128, device=DEV)
