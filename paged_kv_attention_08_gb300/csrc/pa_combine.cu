@@ -7,28 +7,33 @@
 //     out = sum_p 2^(m_p - M) acc_p / L.
 // Partitions past the sequence's context are never read; an empty partition
 // (m = -inf, l = 0, acc = 0) contributes nothing; a sequence with no attended
-// token gets zeros.  One CTA per (query head, sequence), one thread per
-// output element: the reads of acc are coalesced along head_dim.
+// token gets zeros.
 #include "pa_device.cuh"
 
 namespace pa {
 
 namespace {
 
-// One CTA per (query head, sequence); each warp computes the partition
-// weights itself (lanes stride over partitions, shuffles reduce), then every
-// thread accumulates VEC output columns over the partitions with up to eight
-// independent loads in flight.  Two dependent memory round trips in all.
+// One CTA of 256 threads per (query head, sequence).  Every thread loads the
+// (m, l) of a few partitions; two block reductions give the maximum and the
+// weighted normaliser.  The threads then form PGRP groups over the
+// partitions, each thread a 16-byte slice of the head dimension, so that all
+// acc loads of a head are in flight at once; a shared-memory sum over the
+// groups finishes the head.  Two dependent memory round trips in all.
+constexpr int kCombineThreads = 256;
+
 template <int D>
-__global__ void __launch_bounds__(64) combine_kernel(const CombineParams p) {
-    constexpr int VEC = D <= 128 ? D / 32 : 4;
+__global__ void __launch_bounds__(kCombineThreads) combine_kernel(const CombineParams p) {
+    constexpr int SLICES = D / 4;                      // float4 slices of one row
+    constexpr int PGRP = kCombineThreads / SLICES;     // partition groups
     constexpr float NEG_INF = -INFINITY;
-    extern __shared__ float weight_all[];  // [warps][num_parts]
-    grid_dependency_wait();                // partials come from the attention kernel
+    extern __shared__ float weight[];                  // [num_parts]
+    __shared__ float red[kCombineThreads / 32];
+    __shared__ float4 part[PGRP][SLICES];
+    grid_dependency_wait();                            // partials come from the attention kernel
     grid_launch_dependents();
 
-    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-    float* weight = weight_all + (size_t)warp * p.num_parts;
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     const int h = blockIdx.x, b = blockIdx.y;
     const int kvh = h / p.group, g = h % p.group;
     const int T = reachable_tokens(p.context_lens, b, p.max_blocks, p.block_size);
@@ -37,50 +42,66 @@ __global__ void __launch_bounds__(64) combine_kernel(const CombineParams p) {
 
     const size_t row0 = ((size_t)b * p.num_kv_heads + kvh) * p.num_parts;  // partition 0 of (b, kvh)
     const float2* ml = reinterpret_cast<const float2*>(p.part_ml);
-    auto ml_at = [&](int part) { return ml[(row0 + part) * p.group + g]; };
 
     float mx = NEG_INF;
-    for (int q = lane; q < nparts; q += 32) mx = fmaxf(mx, ml_at(q).x);
+    for (int q = tid; q < nparts; q += kCombineThreads) mx = fmaxf(mx, ml[(row0 + q) * p.group + g].x);
 #pragma unroll
     for (int m = 16; m >= 1; m >>= 1) mx = fmaxf(mx, __shfl_xor_sync(kFullMask, mx, m));
+    if (lane == 0) red[warp] = mx;
+    __syncthreads();
+    mx = red[0];
+#pragma unroll
+    for (int w = 1; w < kCombineThreads / 32; ++w) mx = fmaxf(mx, red[w]);
+    __syncthreads();
+
     float ls = 0.f;
-    for (int q = lane; q < nparts; q += 32) {
-        const float2 v = ml_at(q);
+    for (int q = tid; q < nparts; q += kCombineThreads) {
+        const float2 v = ml[(row0 + q) * p.group + g];
         const float w = (v.x == NEG_INF) ? 0.f : exp2f(v.x - mx);
         weight[q] = w;
         ls = fmaf(w, v.y, ls);
     }
 #pragma unroll
     for (int m = 16; m >= 1; m >>= 1) ls += __shfl_xor_sync(kFullMask, ls, m);
-    __syncwarp();
-
-    const int d0 = threadIdx.x * VEC;
-    float a[VEC];
+    if (lane == 0) red[warp] = ls;
+    __syncthreads();  // also publishes `weight`
+    ls = 0.f;
 #pragma unroll
-    for (int v = 0; v < VEC; ++v) a[v] = 0.f;
+    for (int w = 0; w < kCombineThreads / 32; ++w) ls += red[w];
+
     const bool empty = (mx == NEG_INF) || !(ls > 0.f);
+    const int pg = tid / SLICES, sl = tid % SLICES;
+    float4 a = make_float4(0.f, 0.f, 0.f, 0.f);
     if (!empty) {
-        const float* src = p.part_acc + (row0 * p.group + g) * D + d0;
-        const size_t stride = (size_t)p.group * D;
-#pragma unroll 8
-        for (int q = 0; q < nparts; ++q) {
+        const float4* src = reinterpret_cast<const float4*>(p.part_acc + (row0 * p.group + g) * D) + sl;
+        const size_t stride = (size_t)p.group * SLICES;  // float4s between partitions
+#pragma unroll 4
+        for (int q = pg; q < nparts; q += PGRP) {
             const float w = weight[q];
-            if constexpr (VEC == 4) {
-                const float4 x = *reinterpret_cast<const float4*>(src + (size_t)q * stride);
-                a[0] = fmaf(w, x.x, a[0]);
-                a[1] = fmaf(w, x.y, a[1]);
-                a[2] = fmaf(w, x.z, a[2]);
-                a[3] = fmaf(w, x.w, a[3]);
-            } else {
-                const float2 x = *reinterpret_cast<const float2*>(src + (size_t)q * stride);
-                a[0] = fmaf(w, x.x, a[0]);
-                a[1] = fmaf(w, x.y, a[1]);
-            }
+            const float4 x = src[(size_t)q * stride];
+            a.x = fmaf(w, x.x, a.x);
+            a.y = fmaf(w, x.y, a.y);
+            a.z = fmaf(w, x.z, a.z);
+            a.w = fmaf(w, x.w, a.w);
         }
     }
-    const size_t o = ((size_t)b * p.num_heads + h) * D + d0;
-#pragma unroll
-    for (int v = 0; v < VEC; ++v) store_out(p.out, o + v, empty ? 0.f : a[v] / ls, p.out_dtype);
+    part[pg][sl] = a;
+    __syncthreads();
+    if (pg == 0) {
+        for (int k = 1; k < PGRP; ++k) {
+            const float4 x = part[k][sl];
+            a.x += x.x;
+            a.y += x.y;
+            a.z += x.z;
+            a.w += x.w;
+        }
+        const float inv = empty ? 0.f : 1.f / ls;
+        const size_t o = ((size_t)b * p.num_heads + h) * D + sl * 4;
+        store_out(p.out, o, a.x * inv, p.out_dtype);
+        store_out(p.out, o + 1, a.y * inv, p.out_dtype);
+        store_out(p.out, o + 2, a.z * inv, p.out_dtype);
+        store_out(p.out, o + 3, a.w * inv, p.out_dtype);
+    }
 }
 
 __global__ void resolve_kernel(int32_t* out_phys, const int32_t* block_tables,
@@ -104,8 +125,7 @@ cudaError_t launch_combine(const CombineParams& p, int head_dim, dim3 grid, bool
         case 128: kern = combine_kernel<128>; break;
         default: kern = combine_kernel<256>; break;
     }
-    const int threads = head_dim <= 128 ? 32 : 64;
-    const uint32_t smem = (uint32_t)(threads / 32) * p.num_parts * sizeof(float);
+    const uint32_t smem = (uint32_t)p.num_parts * sizeof(float);
     if (smem > 48 * 1024) {
         cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                              (int)smem);
@@ -113,7 +133,7 @@ cudaError_t launch_combine(const CombineParams& p, int head_dim, dim3 grid, bool
     }
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = grid;
-    cfg.blockDim = dim3(threads);
+    cfg.blockDim = dim3(kCombineThreads);
     cfg.dynamicSmemBytes = smem;
     cfg.stream = stream;
     cudaLaunchAttribute attr[1];
