@@ -379,16 +379,18 @@ def main(argv=None):
             barrier()
             ms_total = e0.elapsed_time(e1)
 
-            # per-call durations: one graph per workload that runs its call once on
-            # every input set (L2-cold, back to back); replay time / sets = the
+            # per-call durations: one graph per workload that runs its call on the
+            # input sets in turn, at least 8 calls back to back (the sets together
+            # exceed 3x L2, so every call reads HBM); replay time / calls = the
             # call's device time (attention kernel plus, when it splits, combine)
             per_call = [[] for _ in set0]
             call_graphs = []
+            calls_per_graph = nsets * max(1, math.ceil(8 / nsets))   # at least 8 calls
             for i in range(len(set0)):
                 g = torch.cuda.CUDAGraph()
                 with torch.cuda.graph(g, stream=stream):
-                    for si in range(nsets):
-                        call(si, i, torch.cuda.current_stream())
+                    for k in range(calls_per_graph):
+                        call(k % nsets, i, torch.cuda.current_stream())
                 call_graphs.append(g)
             reps = max(3, min(args.steps // 10, 50))
             for _ in range(reps):
@@ -399,7 +401,7 @@ def main(argv=None):
                     g.replay()
                     b.record(stream)
                     b.synchronize()
-                    per_call[i].append(a.elapsed_time(b) / nsets)
+                    per_call[i].append(a.elapsed_time(b) / calls_per_graph)
     clk = clocks.summary() if rank == 0 else None
 
     ms_step = reduce_max(ms_total, dev) / args.steps

@@ -104,19 +104,42 @@ int env_int(const char* name, int fallback) {
     return v > 0 ? v : fallback;
 }
 
-Tune pick_tune(const pa_shape* s) {
+Tune pick_tune(const pa_shape* s, bool many_ctas) {
     Tune t;
     t.nh = s->head_dim == 256 ? 2 : 1;
-    const int stage = 2 * s->block_size * s->head_dim * 2;
-    t.nt = t.nh == 2 ? 2 : 4;
-    // Stages per stream: about 96 KB of pages in flight per CTA, at least two.
-    const int ns = (96 * 1024) / (t.nt * stage);
-    t.ns = ns < 2 ? 2 : (ns > 8 ? 8 : ns);
+    const uint32_t stage = 2u * s->block_size * s->head_dim * 2u;
+    if (many_ctas) {
+        // grids of several waves: four warps, ~96 KB of pages, two CTAs per SM
+        t.nt = 4 / t.nh;
+        const int ns = (96 * 1024) / (t.nt * (int)stage);
+        t.ns = ns < 2 ? 2 : (ns > 8 ? 8 : ns);
+    } else {
+        // grids of at most one wave: eight warps, one CTA per SM, two pages in
+        // flight per stream; fewer streams when the pages are too large
+        t.nt = 8 / t.nh;
+        t.ns = 2;
+        while (t.nt > 1 && (uint32_t)t.nt * t.ns * stage > 200u * 1024u) --t.nt;
+    }
     static const int env_nt = env_int("PA_TUNE_STREAMS", 0);
     static const int env_ns = env_int("PA_TUNE_STAGES", 0);
     if (env_nt > 0 && env_nt * t.nh <= 8) t.nt = env_nt;
     if (env_ns > 0 && env_ns <= 16) t.ns = env_ns;
+    // never ask for more shared memory than a CTA may have
+    while (t.ns > 1 && attn_smem_layout(s->head_dim, s->block_size, t.nt, t.ns).total +
+                               kSmemAlignSlack > 227u * 1024u)
+        --t.ns;
     return t;
+}
+
+// CTAs of this tune resident per SM: by shared memory, and by registers
+// (the kernels use about 200 registers a thread).
+int ctas_per_sm(const pa_shape* s, const Tune& t) {
+    const AttnSmem L = attn_smem_layout(s->head_dim, s->block_size, t.nt, t.ns);
+    int by_smem = (int)((227u * 1024u) / (L.total + kSmemAlignSlack));
+    const int threads = 32 * t.nt * t.nh;
+    int by_regs = 65536 / (200 * threads);
+    int n = by_smem < by_regs ? by_smem : by_regs;
+    return n < 1 ? 1 : (n > 8 ? 8 : n);
 }
 
 // Programmatic dependent launch lets each kernel's launch overlap the tail
@@ -126,9 +149,6 @@ bool use_pdl() {
     return !off;
 }
 
-AttnSmem tune_smem(const pa_shape* s, const Tune& t) {
-    return attn_smem_layout(s->head_dim, s->block_size, t.nt, t.ns);
-}
 
 int pages_for(const pa_shape* s, int32_t max_context_len) {
     int64_t t = max_context_len < 1 ? 1 : max_context_len;
@@ -144,10 +164,12 @@ int pages_for(const pa_shape* s, int32_t max_context_len) {
 struct Plan {
     int part_pages, num_parts;
     bool cluster;
+    bool many_ctas;  // the grid spans several waves: pick the two-CTAs-per-SM tune
 };
 
 Plan plan_with(const pa_shape* s, int pages, int pp, bool cluster_ok) {
     Plan p;
+    p.many_ctas = false;
     if (pp < 1) pp = 1;
     p.num_parts = (pages + pp - 1) / pp;
     if (p.num_parts < 1) p.num_parts = 1;
@@ -160,39 +182,34 @@ Plan plan_with(const pa_shape* s, int pages, int pp, bool cluster_ok) {
 // length; these rules are this library's own, fitted to GB300 timings of the
 // workloads it is measured on).  With units = batch * kv heads CTAs unsplit
 // and `slots` CTAs resident at once:
-//  - a grid already a third full or more is split only into partitions of
-//    about 64 pages, so that long and ragged sequences balance across waves;
-//    no cluster (the grid spans several waves);
+//  - a grid already a third full or more (at two CTAs per SM) is split only
+//    into partitions of about 64 pages, so that long and ragged sequences
+//    balance across waves; no cluster (the grid spans several waves);
 //  - a smaller grid is split to fill about 85% of one wave, either into at
 //    most 8 partitions of at least 4 pages reduced inside a cluster, or, when
-//    that would give less than half the parallelism, into partitions of at
-//    least 16 pages combined through the workspace.
+//    that gives less parallelism, into partitions of at least 16 pages
+//    combined through the workspace.
 // The longest context stands for every sequence: the host reads no lengths.
 Plan auto_plan(const pa_shape* s, int32_t max_context_len, int num_sms) {
-    const Tune t = pick_tune(s);
-    const AttnSmem L = tune_smem(s, t);
-    int ctas_per_sm = (int)((227u * 1024u) / (L.total + kSmemAlignSlack));
-    if (ctas_per_sm < 1) ctas_per_sm = 1;
-    if (ctas_per_sm > 8) ctas_per_sm = 8;
-    const int64_t slots = (int64_t)num_sms * ctas_per_sm;
     const int pages = pages_for(s, max_context_len);
     const int64_t units = (int64_t)s->batch * s->num_kv_heads;
     auto ceil_div = [](int64_t a, int64_t b) { return (a + b - 1) / b; };
-    if (units * 3 >= slots) {
+    const int64_t wide_slots = (int64_t)num_sms * ctas_per_sm(s, pick_tune(s, true));
+    if (units * 3 >= wide_slots) {
         const int parts = (int)ceil_div(pages, 64);
-        return plan_with(s, pages, (int)ceil_div(pages, parts), false);
+        Plan p = plan_with(s, pages, (int)ceil_div(pages, parts), false);
+        p.many_ctas = units * p.num_parts > num_sms;
+        return p;
     }
+    const int64_t slots = (int64_t)num_sms * ctas_per_sm(s, pick_tune(s, false));
     int64_t fill = (int64_t)(0.85 * (double)slots / (double)units);
     if (fill < 1) fill = 1;
     const int64_t p_cl = std::min<int64_t>(std::min<int64_t>(kMaxClusterParts, fill), ceil_div(pages, 4));
     const int64_t p_ws = std::min<int64_t>(fill, ceil_div(pages, 16));
-    if (p_cl * 2 >= p_ws) return plan_with(s, pages, (int)ceil_div(pages, p_cl), true);
+    if (p_cl >= p_ws) return plan_with(s, pages, (int)ceil_div(pages, p_cl), true);
     return plan_with(s, pages, (int)ceil_div(pages, p_ws), false);
 }
 
-// The plan of a call: automatic for partition_tokens == 0, otherwise
-// partitions of exactly that many tokens (reduced in a cluster when there
-// are at most kMaxClusterParts of them).
 // PA_NO_CLUSTER=1 turns the in-cluster reduction off (partitions then always
 // go through the workspace); a tuning switch, results are the same.
 bool clusters_enabled() {
@@ -201,9 +218,13 @@ bool clusters_enabled() {
 }
 
 Plan make_plan(const pa_shape* s, int32_t max_context_len, int32_t partition_tokens, int num_sms) {
-    Plan plan = partition_tokens == 0
-                    ? auto_plan(s, max_context_len, num_sms)
-                    : plan_with(s, pages_for(s, max_context_len), partition_tokens / s->block_size, true);
+    Plan plan;
+    if (partition_tokens == 0) {
+        plan = auto_plan(s, max_context_len, num_sms);
+    } else {
+        plan = plan_with(s, pages_for(s, max_context_len), partition_tokens / s->block_size, true);
+        plan.many_ctas = (int64_t)s->batch * s->num_kv_heads * plan.num_parts > num_sms;
+    }
     if (!clusters_enabled()) plan.cluster = false;
     return plan;
 }
@@ -260,8 +281,8 @@ pa_status launch_attention(void* out, const void* q, const void* k, const void* 
     std::memset(&L, 0, sizeof L);
     pa_status st = encode_maps(s, k, v, &L.tmap_k, &L.tmap_v);
     if (st != PA_OK) return st;
-    const Tune t = pick_tune(s);
-    const AttnSmem sm = tune_smem(s, t);
+    const Tune t = pick_tune(s, plan.many_ctas);
+    const AttnSmem sm = attn_smem_layout(s->head_dim, s->block_size, t.nt, t.ns);
     const int G = s->num_heads / s->num_kv_heads;
     if (4u * (merge_floats(t.nt * t.nh, G, s->head_dim / t.nh) + cluster_part_floats(G, s->head_dim)) >
         sm.stage_bytes * t.nt * t.ns)
@@ -352,9 +373,11 @@ pa_status pa_decode(void* out, const void* q, const void* k_cache, const void* v
     st = check_ptrs(out, q, k_cache, v_cache, block_tables, context_lens);
     if (st != PA_OK) return st;
     int32_t* err = nullptr;
-    st = device_state(nullptr, &err);
+    int sms = 0;
+    st = device_state(&sms, &err);
     if (st != PA_OK) return st;
-    Plan plan{shape->max_blocks_per_seq, 1, false};
+    Plan plan{shape->max_blocks_per_seq, 1, false,
+              (int64_t)shape->batch * shape->num_kv_heads > sms};
     return launch_attention(out, q, k_cache, v_cache, block_tables, context_lens, shape, scale,
                             plan, nullptr, nullptr, err, static_cast<cudaStream_t>(stream));
 }

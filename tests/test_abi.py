@@ -137,15 +137,16 @@ def test_single_sequence_long_context_is_split(lib):
     s = shape(batch=1, max_blocks_per_seq=8192, kv_dtype=pa.BF16)
     pt = lib.pa_choose_partition_tokens(ctypes.byref(s), 131072, 152)
     parts = -(-131072 // pt)
-    assert parts * 8 >= 152           # at least one CTA per SM
-    assert parts * 8 <= 2 * 152       # and a single wave
+    assert parts * 8 >= 100           # most SMs busy
+    assert parts * 8 <= 152           # in a single wave
 
 
 def test_small_grids_reduce_in_a_cluster(lib):
-    # batch 4 x 8 kv heads x 2048 tokens on 152 SMs: 8 partitions, no workspace needed
+    # batch 4 x 8 kv heads x 2048 tokens on 152 SMs: 4 partitions, no workspace needed
     s = shape(batch=4, max_blocks_per_seq=128)
     pt = lib.pa_choose_partition_tokens(ctypes.byref(s), 2048, 152)
-    assert -(-2048 // pt) == 8
+    assert -(-2048 // pt) == 4
+    assert lib.pa_workspace_size(ctypes.byref(s), 2048, pt) == 0
 
 
 def test_binding_refuses_cpu_tensors():
