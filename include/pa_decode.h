@@ -101,7 +101,8 @@ pa_status pa_decode(void* out, const void* q, const void* k_cache, const void* v
  * Bytes of device workspace pa_decode_splitkv needs for this shape, longest
  * context `max_context_len` and partition size `partition_tokens` (tokens per
  * split, a multiple of block_size; 0 = choose automatically for the current
- * device).  Returns 0 for invalid arguments or when no split is needed.
+ * device).  Returns 0 for invalid arguments and when no workspace is needed
+ * (one partition, or at most 8 reduced inside a cluster).
  */
 size_t pa_workspace_size(const pa_shape* shape, int32_t max_context_len,
                          int32_t partition_tokens);
@@ -111,8 +112,9 @@ size_t pa_workspace_size(const pa_shape* shape, int32_t max_context_len,
  * multiprocessors: 0 < result, a multiple of block_size; a result >=
  * max_context_len means "no split".  Host-only, no device access (a pure
  * function, exported so that its choice can be checked without a GPU).
- * This heuristic is this library's own: the flash-decoding-bench design notes
- * only say that the chunk size is picked from the KV length.
+ * The rules are this library's own, fitted to GB300 timings: the
+ * flash-decoding-bench design notes only say that the chunk size is picked
+ * from the KV length.
  */
 int32_t pa_choose_partition_tokens(const pa_shape* shape, int32_t max_context_len,
                                    int32_t num_sms);
@@ -121,17 +123,19 @@ int32_t pa_choose_partition_tokens(const pa_shape* shape, int32_t max_context_le
  * Flash-Decoding split-KV decode (flash-decoding-bench "design.md": the KV
  * cache is split into chunks, one thread block each, each computing its local
  * max, sum and weighted value sum, followed by a reduction of the partials).
- * Kernel 1 writes, per (sequence, kv head, partition of `partition_tokens`
- * tokens), fp32 partials (m, l, acc[head_dim]) for each query head of the
- * group into `workspace`; kernel 2 combines them with a log-sum-exp reduction
- * into out.  `max_context_len` must be >= every context_lens[b] that should be
- * attended in full (tokens beyond it are dropped; no device->host read is
- * made); `partition_tokens` = 0 chooses automatically, and a choice of one
- * partition runs the single pass without touching the workspace.
- * `workspace` (device, 16-byte aligned) must hold at least
- * pa_workspace_size(shape, max_context_len, partition_tokens) bytes; it is
- * scratch owned by the caller and may be reused once the stream has passed
- * this call.
+ * Each (sequence, kv head) is cut into partitions of `partition_tokens` tokens;
+ * one CTA per partition computes fp32 partials (m, l, acc[head_dim]) for each
+ * query head of the group.  At most 8 partitions are launched as one
+ * thread-block cluster and reduced through distributed shared memory inside
+ * the same kernel (no workspace needed); more partitions write their partials
+ * to `workspace` and a second kernel combines them with a log-sum-exp
+ * reduction into out.  `max_context_len` must be >= every context_lens[b] that
+ * should be attended in full (tokens beyond it are dropped; no device->host
+ * read is made); `partition_tokens` = 0 chooses the split automatically, and a
+ * choice of one partition runs the single pass.  `workspace` (device, 16-byte
+ * aligned) must hold at least pa_workspace_size(shape, max_context_len,
+ * partition_tokens) bytes (may be NULL when that is 0); it is scratch owned by
+ * the caller and may be reused once the stream has passed this call.
  */
 pa_status pa_decode_splitkv(void* out, const void* q, const void* k_cache, const void* v_cache,
                             const int32_t* block_tables, const int32_t* context_lens,
