@@ -190,6 +190,15 @@ pa_status pa_decode_splitkv_noalloc(void* out, const void* q, const void* k_cach
                                     float scale, int32_t max_context_len,
                                     int32_t partition_tokens, void* stream);
 
+/*
+ * Test export of the kernels' failure path (no counterpart in the pages): one
+ * CTA waits, with the decode kernels' bounded wait, on an mbarrier that nothing
+ * ever completes; after `timeout_ns` (1 ns .. 5 s) it gives up and records
+ * PA_ERR_TIMEOUT in the device error word, which pa_device_error then returns.
+ * The context stays usable.  Asynchronous on `stream`.
+ */
+pa_status pa_selftest_wait_timeout(uint64_t timeout_ns, void* stream);
+
 /* Static, human-readable name of a status. */
 const char* pa_status_string(pa_status status);
 

@@ -78,6 +78,8 @@ def _load():
             lib.pa_choose_partition_tokens.restype = i32
             lib.pa_resolve_blocks.argtypes = [P, P, P, S, P]
             lib.pa_resolve_blocks.restype = ctypes.c_int
+            lib.pa_selftest_wait_timeout.argtypes = [ctypes.c_uint64, P]
+            lib.pa_selftest_wait_timeout.restype = ctypes.c_int
             lib.pa_device_error.argtypes = [ctypes.POINTER(i32), P]
             lib.pa_device_error.restype = ctypes.c_int
             lib.pa_status_string.argtypes = [ctypes.c_int]
@@ -213,6 +215,12 @@ def resolve_blocks(out_phys, block_tables, context_lens, block_size: int, num_bl
                                      context_lens.data_ptr(), ctypes.byref(shape),
                                      _stream_ptr(stream)), "pa_resolve_blocks")
     return out_phys
+
+
+def selftest_wait_timeout(timeout_ns: int, stream=None):
+    """Run the bounded-wait self-test kernel (it records PA_ERR_TIMEOUT)."""
+    _check(_load().pa_selftest_wait_timeout(int(timeout_ns), _stream_ptr(stream)),
+           "pa_selftest_wait_timeout")
 
 
 def device_error(stream=None) -> int:

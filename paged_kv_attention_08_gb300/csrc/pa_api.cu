@@ -447,6 +447,16 @@ pa_status pa_resolve_blocks(int32_t* out_phys, const int32_t* block_tables,
     return e == cudaSuccess ? PA_OK : PA_ERR_CUDA;
 }
 
+pa_status pa_selftest_wait_timeout(uint64_t timeout_ns, void* stream) {
+    if (timeout_ns == 0 || timeout_ns > 5000000000ull) return PA_ERR_INVALID_ARG;
+    int32_t* err = nullptr;
+    pa_status st = device_state(nullptr, &err);
+    if (st != PA_OK) return st;
+    return launch_wait_timeout(err, timeout_ns, static_cast<cudaStream_t>(stream)) == cudaSuccess
+               ? PA_OK
+               : PA_ERR_CUDA;
+}
+
 pa_status pa_device_error(int32_t* code, void* stream) {
     if (!code) return PA_ERR_INVALID_ARG;
     int32_t* err = nullptr;

@@ -104,6 +104,20 @@ __global__ void __launch_bounds__(kCombineThreads) combine_kernel(const CombineP
     }
 }
 
+// Self-test of the bounded wait: an mbarrier that nothing ever arrives at.
+// The wait gives up after `timeout_ns` and records PA_ERR_TIMEOUT, exactly as
+// the decode kernels do when their copy pipeline stops delivering.
+__global__ void wait_timeout_kernel(int32_t* err, uint64_t timeout_ns) {
+    __shared__ uint64_t bar;
+    if (threadIdx.x == 0) {
+        mbar_init(smem_u32(&bar), 1);
+        mbar_init_fence();
+    }
+    __syncthreads();
+    const bool ok = mbar_wait_bounded(smem_u32(&bar), 0u, timeout_ns);
+    if (!ok && threadIdx.x == 0) record_error(err, PA_ERR_TIMEOUT);
+}
+
 __global__ void resolve_kernel(int32_t* out_phys, const int32_t* block_tables,
                                const int32_t* context_lens, int32_t batch, int32_t max_blocks,
                                int32_t block_size, int64_t num_blocks) {
@@ -142,6 +156,11 @@ cudaError_t launch_combine(const CombineParams& p, int head_dim, dim3 grid, bool
     cfg.attrs = attr;
     cfg.numAttrs = pdl ? 1 : 0;
     return cudaLaunchKernelEx(&cfg, kern, p);
+}
+
+cudaError_t launch_wait_timeout(int32_t* err, uint64_t timeout_ns, cudaStream_t stream) {
+    wait_timeout_kernel<<<1, 32, 0, stream>>>(err, timeout_ns);
+    return cudaGetLastError();
 }
 
 cudaError_t launch_resolve(int32_t* out_phys, const int32_t* block_tables,

@@ -35,7 +35,8 @@ def lib():
 def test_library_exports_every_declared_symbol(lib):
     names = declared_entry_points()
     assert {"pa_decode", "pa_decode_splitkv", "pa_workspace_size", "pa_resolve_blocks",
-            "pa_status_string", "pa_choose_partition_tokens", "pa_device_error"} <= set(names)
+            "pa_status_string", "pa_choose_partition_tokens", "pa_device_error",
+            "pa_selftest_wait_timeout", "pa_decode_splitkv_noalloc"} <= set(names)
     for n in names:
         assert hasattr(lib, n), f"{n} declared in include/ but not exported"
 
@@ -92,6 +93,11 @@ def test_pointer_validation(lib):
     e = shape(batch=0)
     assert lib.pa_decode(None, None, None, None, None, None, ctypes.byref(e), 0.1, None) == 0
     assert lib.pa_resolve_blocks(None, FAKE, FAKE, ctypes.byref(s), None) == 1
+
+
+def test_selftest_rejects_bad_limits(lib):
+    assert lib.pa_selftest_wait_timeout(0, None) == 1
+    assert lib.pa_selftest_wait_timeout(6_000_000_000, None) == 1
 
 
 def test_workspace_size_explicit_partition(lib):

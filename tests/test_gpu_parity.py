@@ -282,3 +282,16 @@ def test_workspace_errors_and_no_device_error():
         pa.decode_splitkv(out, x.q, x.k_cache, x.v_cache, x.block_tables, x.context_lens, x.scale,
                           x.max_context_len, 100)        # not a multiple of block_size
     assert pa.device_error() == 0
+
+
+def test_bounded_wait_reports_timeout_and_context_survives():
+    """A wait that can never complete gives up after its limit, the error word
+    says PA_ERR_TIMEOUT, and the context keeps working."""
+    assert pa.device_error() == 0
+    pa.selftest_wait_timeout(20_000_000)      # 20 ms
+    assert pa.device_error() == 5              # PA_ERR_TIMEOUT, and the word is cleared
+    assert pa.device_error() == 0
+    x = workloads.make("tiny", seed=0, device=DEV)
+    want = oracle.decode(x.q, x.k_cache, x.v_cache, x.block_tables, x.context_lens, x.scale)
+    assert_close_fp32(run(x, "split", partition_tokens=16), want)
+    assert pa.device_error() == 0
