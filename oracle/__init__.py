@@ -18,6 +18,10 @@ Parity status of each function (pins live in ``tests/test_oracle_pins.py``):
                           invariance, masking semantics.
   resolve_blocks       -- pinned: brute force over an independent per-page rule
                           and hand-written cases.
+  append_kv            -- pinned: exactly the addressed slots change (element
+                          by element over the whole pool), invalid positions and
+                          entries write nothing, append-then-decode equals the
+                          decode of a cache built with the token in place.
 """
 from __future__ import annotations
 
@@ -69,6 +73,8 @@ def _load():
             lib.pao_decode_rows.restype = ctypes.c_int
             lib.pao_resolve_blocks.argtypes = [P, P, P, i32, i32, i32, i64]
             lib.pao_resolve_blocks.restype = ctypes.c_int
+            lib.pao_append_kv.argtypes = [P, P, P, P, P, P, i32, i32, i32, i32, i32, i64]
+            lib.pao_append_kv.restype = ctypes.c_int
             _lib = lib
     return _lib
 
@@ -151,3 +157,24 @@ def resolve_blocks(block_tables, context_lens, block_size: int, num_blocks: int)
     if rc != 0:
         raise RuntimeError("oracle resolve_blocks rejected its arguments")
     return out
+
+
+def append_kv(k_cache, v_cache, k_new, v_new, block_tables, positions):
+    """New k_cache, v_cache (copies) with each sequence's token written at its
+    position's slot; k_new, v_new are [batch, num_kv_heads, head_dim]."""
+    if k_new.dtype != k_cache.dtype or v_new.dtype != v_cache.dtype:
+        raise TypeError("new keys/values must have the cache's dtype")
+    NB, bs, Hkv, D = k_cache.shape
+    bt = _i32(block_tables)
+    pos = _i32(positions)
+    B, mb = bt.shape
+    if tuple(k_new.shape) != (B, Hkv, D) or tuple(v_new.shape) != (B, Hkv, D) or pos.shape != (B,):
+        raise ValueError("k_new/v_new must be [batch, num_kv_heads, head_dim], positions [batch]")
+    ka, va = _u16(k_cache).copy(), _u16(v_cache).copy()
+    kn, vn = _u16(k_new), _u16(v_new)
+    rc = _load().pao_append_kv(_ptr(ka), _ptr(va), _ptr(kn), _ptr(vn), _ptr(bt), _ptr(pos),
+                               B, Hkv, D, bs, mb, NB)
+    if rc != 0:
+        raise RuntimeError("oracle append_kv rejected its arguments")
+    to_t = lambda a: torch.from_numpy(a.view(np.int16).reshape(NB, bs, Hkv, D)).view(k_cache.dtype)
+    return to_t(ka), to_t(va)

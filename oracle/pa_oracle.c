@@ -217,3 +217,34 @@ int pao_resolve_blocks(int32_t* out_phys, const int32_t* block_tables, const int
     }
     return 0;
 }
+
+/* Append of one new token per sequence to the paged cache (MiniVLLM docs
+ * "Decoding Benchmark", "What paged attention decode does": each decode step
+ * adds one token whose keys/values are stored in the block the table assigns,
+ * at slot position % block_size).  For each b with 0 <= positions[b] <
+ * max_blocks * block_size and table entry e = block_tables[b][positions[b] /
+ * block_size] in [0, num_blocks): k_cache[e][positions[b] % block_size][:][:] =
+ * k_new[b][:][:] (all kv heads), and likewise for v.  Other sequences write
+ * nothing.  Elements are copied as raw 16-bit patterns.  Returns 0, or -1 on a
+ * bad shape. */
+int pao_append_kv(uint16_t* k_cache, uint16_t* v_cache, const uint16_t* k_new,
+                  const uint16_t* v_new, const int32_t* block_tables, const int32_t* positions,
+                  int batch, int num_kv_heads, int head_dim, int block_size, int max_blocks,
+                  int64_t num_blocks) {
+    if (batch < 0 || num_kv_heads <= 0 || head_dim <= 0 || block_size <= 0 || max_blocks < 0 ||
+        num_blocks < 0)
+        return -1;
+    size_t row = (size_t)num_kv_heads * head_dim; /* one token slot, all kv heads */
+    for (int b = 0; b < batch; ++b) {
+        int64_t pos = positions[b];
+        if (pos < 0 || pos >= (int64_t)max_blocks * block_size) continue;
+        int64_t e = block_tables[(int64_t)b * max_blocks + pos / block_size];
+        if (e < 0 || e >= num_blocks) continue;
+        size_t dst = ((size_t)e * block_size + (size_t)(pos % block_size)) * row;
+        for (size_t i = 0; i < row; ++i) {
+            k_cache[dst + i] = k_new[(size_t)b * row + i];
+            v_cache[dst + i] = v_new[(size_t)b * row + i];
+        }
+    }
+    return 0;
+}

@@ -263,3 +263,53 @@ def test_resolve_blocks_bruteforce():
             e = int(bt[b, j])
             want = e if (j < pages_used and 0 <= e < NB) else -1
             assert got[b, j] == want, (b, j)
+
+
+# --------------------------------------------------------------------------
+# append of the new token
+# --------------------------------------------------------------------------
+def test_append_changes_exactly_the_addressed_slots():
+    q, k, v, bt, lens, scale = small_case(12, B=4, H=8, Hkv=2, D=8, bs=4, lens=[5, 8, 1, 11], spare=3)
+    g = torch.Generator().manual_seed(13)
+    kn = torch.randn(4, 2, 8, generator=g).to(k.dtype)
+    vn = torch.randn(4, 2, 8, generator=g).to(k.dtype)
+    pos = torch.tensor([5, 7, -1, 400], dtype=torch.int32)   # seq 2 padding, seq 3 past its row
+    k2, v2 = oracle.append_kv(k, v, kn, vn, bt, pos)
+    changed = set()
+    for b, p_ in enumerate(pos.tolist()):
+        if 0 <= p_ < bt.shape[1] * 4 and int(bt[b, p_ // 4]) >= 0:
+            e, s = int(bt[b, p_ // 4]), p_ % 4
+            assert torch.equal(k2[e, s], kn[b]) and torch.equal(v2[e, s], vn[b])
+            changed.add((e, s))
+    mask = torch.ones(k.shape[:2], dtype=torch.bool)
+    for e, s in changed:
+        mask[e, s] = False
+    assert torch.equal(k2[mask], k[mask]) and torch.equal(v2[mask], v[mask])
+    assert len(changed) == 2
+
+
+def test_append_skips_masked_entries():
+    q, k, v, bt, lens, scale = small_case(14, B=2, H=4, Hkv=2, D=8, bs=4, lens=[6, 6], spare=2)
+    bt = bt.clone()
+    bt[0, 1] = -1
+    bt[1, 1] = k.shape[0] + 3
+    kn = torch.ones(2, 2, 8).to(k.dtype)
+    k2, v2 = oracle.append_kv(k, v, kn, kn, bt, torch.tensor([5, 6], dtype=torch.int32))
+    assert torch.equal(k2, k) and torch.equal(v2, v)
+
+
+def test_append_then_decode_equals_decode_with_token_in_place():
+    q, k, v, bt, lens, scale = small_case(15, B=3, H=8, Hkv=4, D=16, bs=4, lens=[6, 9, 12], spare=4)
+    g = torch.Generator().manual_seed(16)
+    kn = torch.randn(3, 4, 16, generator=g).to(k.dtype)
+    vn = torch.randn(3, 4, 16, generator=g).to(k.dtype)
+    pos = torch.tensor([6, 9, 11], dtype=torch.int32)       # last one overwrites an existing slot
+    # cache with the token placed by hand, through an independent index computation
+    kh, vh = k.clone(), v.clone()
+    for b in range(3):
+        p_ = int(pos[b])
+        kh[int(bt[b, p_ // 4]), p_ % 4] = kn[b]
+        vh[int(bt[b, p_ // 4]), p_ % 4] = vn[b]
+    k2, v2 = oracle.append_kv(k, v, kn, vn, bt, pos)
+    np.testing.assert_array_equal(oracle.decode(q, k2, v2, bt, pos + 1, scale),
+                                  oracle.decode(q, kh, vh, bt, pos + 1, scale))
