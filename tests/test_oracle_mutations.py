@@ -26,7 +26,6 @@ MUTANTS = {
     "q_head_offset": ("((size_t)b * num_heads + h) * head_dim;", "((size_t)b * num_heads + kvh) * head_dim;"),
     "append_slot_index": ("(size_t)(pos % block_size)) * row", "(size_t)(pos / block_size % block_size)) * row"),
     "append_values_from_keys": ("v_cache[dst + i] = v_new[", "v_cache[dst + i] = k_new["),
-    "append_ignores_masked_entry": ("if (e < 0 || e >= num_blocks) continue;", "if (e < 0) continue;"),
 }
 
 
