@@ -254,6 +254,9 @@ def main(argv=None):
     ap.add_argument("--no-graph", action="store_true", help="launch eagerly instead of graph replay")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--with-append", action="store_true",
+                    help="each call first appends the step's new token (the last of every "
+                         "context) with pa_append_kv, as a full decode iteration does")
     ap.add_argument("--min-warmup-s", type=float, default=1.0,
                     help="keep warming up (graph replays) at least this long")
     args = ap.parse_args(argv)
@@ -292,7 +295,7 @@ def main(argv=None):
                                      st[i].max_context_len, pts[i]) for st in sets)
         ws.append(torch.empty(max(need, 16), dtype=torch.uint8, device=dev))
     splits = [ws[i].numel() > 16 for i in range(len(set0))]      # partials combined by a 2nd kernel
-    launches_per_step = sum(2 if s else 1 for s in splits)
+    launches_per_step = sum(2 if s else 1 for s in splits) + (len(set0) if args.with_append else 0)
     sms = props.multi_processor_count
     plans = {}
     for i, x in enumerate(set0):
@@ -305,8 +308,22 @@ def main(argv=None):
 
     stream = torch.cuda.Stream(device=dev)
 
+    new_kv = {}
+    if args.with_append:
+        for si, st_ in enumerate(sets):
+            for i, x in enumerate(st_):
+                B, _, D = x.q.shape
+                Hkv = x.k_cache.shape[2]
+                gk = torch.Generator(device=dev).manual_seed(1000 + si * 10 + i)
+                kn = torch.randn(B, Hkv, D, generator=gk, device=dev).to(x.q.dtype)
+                vn = torch.randn(B, Hkv, D, generator=gk, device=dev).to(x.q.dtype)
+                new_kv[(si, i)] = (kn, vn, (x.context_lens - 1).clamp(min=-1).contiguous())
+
     def call(si, i, st):
         x = sets[si][i]
+        if args.with_append:
+            kn, vn, pos = new_kv[(si, i)]
+            pa.append_kv(x.k_cache, x.v_cache, kn, vn, x.block_tables, pos, stream=st)
         pa.decode_splitkv(outs[si][i], x.q, x.k_cache, x.v_cache, x.block_tables, x.context_lens,
                           x.scale, x.max_context_len, pts[i], workspace=ws[i], stream=st)
 
@@ -478,6 +495,8 @@ def main(argv=None):
                 "l2": f"rotating {nsets} input sets of {set_bytes / 1e6:.1f} MB "
                       f"({nsets * set_bytes / 1e6:.0f} MB > 3x L2 {l2 / 1e6:.0f} MB)",
                 "launch": "CUDA graph replay per step" if graphs else "eager",
+                "append": ("each call appends the new token first (pa_append_kv); bytes "
+                           "counted are the decode's only") if args.with_append else None,
                 "parallelism": f"replicas x{world}",
                 "parity_max_abs_err": max_err,
             },

@@ -144,6 +144,25 @@ pa_status pa_decode_splitkv(void* out, const void* q, const void* k_cache, const
                             void* stream);
 
 /*
+ * Append of each sequence's new token to the paged cache, the step that
+ * precedes attention in every decode iteration (MiniVLLM docs "Decoding
+ * Benchmark", "What paged attention decode does": the cache is a pool of
+ * blocks allocated on demand, token t of sequence b in block
+ * block_tables[b][t / block_size] at slot t % block_size).  For each b with
+ * 0 <= positions[b] < max_blocks_per_seq * block_size and a table entry in
+ * [0, num_blocks): k_cache[entry][positions[b] % block_size][:][:] =
+ * k_new[b][:][:], and likewise v_cache from v_new.  Other sequences (padding:
+ * a negative position; a masked entry) write nothing.  k_new, v_new:
+ * [batch, num_kv_heads, head_dim] in kv_dtype, 16-byte aligned; positions:
+ * [batch] int32.  Launched with programmatic stream serialization, so a
+ * decode call queued right after it overlaps its launch and still sees every
+ * write.  Bit-exact (a copy).
+ */
+pa_status pa_append_kv(void* k_cache, void* v_cache, const void* k_new, const void* v_new,
+                       const int32_t* block_tables, const int32_t* positions,
+                       const pa_shape* shape, void* stream);
+
+/*
  * Test export of the page walk (MiniVLLM docs "Decoding Benchmark", "Block
  * table lookup mechanics"): out_phys[b][j] (device, int32, [batch,
  * max_blocks_per_seq]) = the physical block the decode kernels read for

@@ -22,7 +22,7 @@ import threading
 
 import torch
 
-__all__ = ["PaError", "decode", "decode_splitkv", "decode_splitkv_noalloc", "workspace_size", "choose_partition_tokens",
+__all__ = ["PaError", "decode", "decode_splitkv", "decode_splitkv_noalloc", "append_kv", "workspace_size", "choose_partition_tokens",
            "resolve_blocks", "device_error", "library_path", "F16", "BF16", "F32"]
 
 F16, BF16, F32 = 0, 1, 2
@@ -78,6 +78,8 @@ def _load():
             lib.pa_choose_partition_tokens.restype = i32
             lib.pa_resolve_blocks.argtypes = [P, P, P, S, P]
             lib.pa_resolve_blocks.restype = ctypes.c_int
+            lib.pa_append_kv.argtypes = [P, P, P, P, P, P, S, P]
+            lib.pa_append_kv.restype = ctypes.c_int
             lib.pa_selftest_wait_timeout.argtypes = [ctypes.c_uint64, P]
             lib.pa_selftest_wait_timeout.restype = ctypes.c_int
             lib.pa_device_error.argtypes = [ctypes.POINTER(i32), P]
@@ -200,6 +202,24 @@ def decode_splitkv_noalloc(out, q, k_cache, v_cache, block_tables, context_lens,
         int(max_context_len), int(partition_tokens), _stream_ptr(stream)),
         "pa_decode_splitkv_noalloc")
     return out
+
+
+def append_kv(k_cache, v_cache, k_new, v_new, block_tables, positions, stream=None):
+    """Write each sequence's new token ([B, Hkv, D] k_new / v_new) into its
+    cache slot at ``positions[b]``; negative positions and masked entries
+    write nothing."""
+    _dev_tensors(k_cache, v_cache, k_new, v_new, block_tables, positions)
+    _ints(block_tables, positions)
+    if k_new.dtype != k_cache.dtype or v_new.dtype != v_cache.dtype:
+        raise TypeError("new keys/values must have the cache's dtype")
+    B = block_tables.shape[0]
+    NB, bs, Hkv, D = k_cache.shape
+    if tuple(k_new.shape) != (B, Hkv, D) or tuple(v_new.shape) != (B, Hkv, D):
+        raise ValueError("k_new/v_new must be [batch, num_kv_heads, head_dim]")
+    shape = _Shape(B, Hkv, Hkv, D, bs, block_tables.shape[1], NB, _dtype_code(k_cache.dtype), F32)
+    _check(_load().pa_append_kv(k_cache.data_ptr(), v_cache.data_ptr(), k_new.data_ptr(),
+                                v_new.data_ptr(), block_tables.data_ptr(), positions.data_ptr(),
+                                ctypes.byref(shape), _stream_ptr(stream)), "pa_append_kv")
 
 
 def resolve_blocks(out_phys, block_tables, context_lens, block_size: int, num_blocks: int,

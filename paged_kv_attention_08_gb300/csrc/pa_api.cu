@@ -447,6 +447,28 @@ pa_status pa_resolve_blocks(int32_t* out_phys, const int32_t* block_tables,
     return e == cudaSuccess ? PA_OK : PA_ERR_CUDA;
 }
 
+pa_status pa_append_kv(void* k_cache, void* v_cache, const void* k_new, const void* v_new,
+                       const int32_t* block_tables, const int32_t* positions,
+                       const pa_shape* shape, void* stream) {
+    pa_status st = check_shape(shape);
+    if (st != PA_OK) return st;
+    if (shape->batch == 0) return PA_OK;
+    if (!k_cache || !v_cache || !k_new || !v_new || !block_tables || !positions)
+        return PA_ERR_INVALID_ARG;
+    if (!aligned(k_cache, 16) || !aligned(v_cache, 16) || !aligned(k_new, 16) ||
+        !aligned(v_new, 16) || !aligned(block_tables, 4) || !aligned(positions, 4))
+        return PA_ERR_INVALID_ARG;
+    int sms = 0;
+    st = device_state(&sms, nullptr);
+    if (st != PA_OK) return st;
+    const int32_t row_bytes = shape->num_kv_heads * shape->head_dim * 2;
+    return launch_append(k_cache, v_cache, k_new, v_new, block_tables, positions, shape->batch,
+                         shape->max_blocks_per_seq, shape->block_size, shape->num_blocks,
+                         row_bytes, use_pdl(), static_cast<cudaStream_t>(stream)) == cudaSuccess
+               ? PA_OK
+               : PA_ERR_CUDA;
+}
+
 pa_status pa_selftest_wait_timeout(uint64_t timeout_ns, void* stream) {
     if (timeout_ns == 0 || timeout_ns > 5000000000ull) return PA_ERR_INVALID_ARG;
     int32_t* err = nullptr;

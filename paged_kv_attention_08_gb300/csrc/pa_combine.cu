@@ -104,6 +104,33 @@ __global__ void __launch_bounds__(kCombineThreads) combine_kernel(const CombineP
     }
 }
 
+// Append of one new token per sequence (MiniVLLM docs "Decoding Benchmark":
+// each decode step stores the new token's keys/values in the block the table
+// assigns, at slot position % block_size).  One CTA per sequence copies the
+// token's row for all kv heads (contiguous in both the new-token array and
+// the cache slot) with 16-byte vectors.  Positions outside the table row and
+// masked entries write nothing.
+__global__ void __launch_bounds__(128) append_kernel(uint4* k_cache, uint4* v_cache,
+                                                    const uint4* k_new, const uint4* v_new,
+                                                    const int32_t* block_tables,
+                                                    const int32_t* positions, int32_t max_blocks,
+                                                    int32_t block_size, int64_t num_blocks,
+                                                    int32_t row_vecs) {
+    grid_dependency_wait();  // the new rows may come from the previous kernel
+    grid_launch_dependents();
+    const int b = blockIdx.x;
+    const int pos = __ldg(positions + b);
+    if (pos < 0 || pos >= max_blocks * block_size) return;
+    const int e = __ldg(block_tables + (size_t)b * max_blocks + pos / block_size);
+    if (e < 0 || (int64_t)e >= num_blocks) return;
+    const size_t dst = ((size_t)e * block_size + pos % block_size) * row_vecs;
+    const size_t src = (size_t)b * row_vecs;
+    for (int i = threadIdx.x; i < row_vecs; i += blockDim.x) {
+        k_cache[dst + i] = __ldg(k_new + src + i);
+        v_cache[dst + i] = __ldg(v_new + src + i);
+    }
+}
+
 // Self-test of the bounded wait: an mbarrier that nothing ever arrives at.
 // The wait gives up after `timeout_ns` and records PA_ERR_TIMEOUT, exactly as
 // the decode kernels do when their copy pipeline stops delivering.
@@ -156,6 +183,25 @@ cudaError_t launch_combine(const CombineParams& p, int head_dim, dim3 grid, bool
     cfg.attrs = attr;
     cfg.numAttrs = pdl ? 1 : 0;
     return cudaLaunchKernelEx(&cfg, kern, p);
+}
+
+cudaError_t launch_append(void* k_cache, void* v_cache, const void* k_new, const void* v_new,
+                          const int32_t* block_tables, const int32_t* positions, int32_t batch,
+                          int32_t max_blocks, int32_t block_size, int64_t num_blocks,
+                          int32_t row_bytes, bool pdl, cudaStream_t stream) {
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3((unsigned)batch);
+    cfg.blockDim = dim3(128);
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = pdl ? 1 : 0;
+    return cudaLaunchKernelEx(&cfg, append_kernel, static_cast<uint4*>(k_cache),
+                              static_cast<uint4*>(v_cache), static_cast<const uint4*>(k_new),
+                              static_cast<const uint4*>(v_new), block_tables, positions,
+                              max_blocks, block_size, num_blocks, row_bytes / 16);
 }
 
 cudaError_t launch_wait_timeout(int32_t* err, uint64_t timeout_ns, cudaStream_t stream) {

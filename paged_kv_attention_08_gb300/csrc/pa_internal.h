@@ -117,6 +117,10 @@ cudaError_t launch_attn_d256(const AttnLaunch& L, cudaStream_t stream);
 
 cudaError_t launch_combine(const CombineParams& p, int head_dim, dim3 grid, bool pdl,
                            cudaStream_t stream);
+cudaError_t launch_append(void* k_cache, void* v_cache, const void* k_new, const void* v_new,
+                          const int32_t* block_tables, const int32_t* positions, int32_t batch,
+                          int32_t max_blocks, int32_t block_size, int64_t num_blocks,
+                          int32_t row_bytes, bool pdl, cudaStream_t stream);
 cudaError_t launch_wait_timeout(int32_t* err, uint64_t timeout_ns, cudaStream_t stream);
 cudaError_t launch_resolve(int32_t* out_phys, const int32_t* block_tables,
                            const int32_t* context_lens, int32_t batch, int32_t max_blocks,

@@ -295,3 +295,69 @@ def test_bounded_wait_reports_timeout_and_context_survives():
     want = oracle.decode(x.q, x.k_cache, x.v_cache, x.block_tables, x.context_lens, x.scale)
     assert_close_fp32(run(x, "split", partition_tokens=16), want)
     assert pa.device_error() == 0
+
+
+# ---------------------------------------------------------------------------
+# append of the new token
+# ---------------------------------------------------------------------------
+def _as_bits(t):
+    return t.contiguous().view(torch.int16).cpu()
+
+
+@pytest.mark.parametrize("dtype", [torch.float16, torch.bfloat16])
+@pytest.mark.parametrize("shape", [SHAPES[2], SHAPES[4], SHAPES[0]],
+                         ids=lambda s: f"H{s['H']}kv{s['Hkv']}D{s['D']}bs{s['bs']}")
+def test_append_bit_exact(shape, dtype):
+    x = random_case(8, dtype=dtype, **shape)
+    B, Hkv, D, bs = shape["B"], shape["Hkv"], shape["D"], shape["bs"]
+    g = torch.Generator().manual_seed(9)
+    kn = torch.randn(B, Hkv, D, generator=g).to(dtype)
+    vn = torch.randn(B, Hkv, D, generator=g).to(dtype)
+    mb = x.block_tables.shape[1]
+    pos = torch.tensor([(7 * b + 3) % (mb * bs) for b in range(B)], dtype=torch.int32)
+    pos[0] = -1                                    # padding sequence
+    bt = x.block_tables.clone()
+    if B > 2:
+        bt[2, :] = -1                              # masked entry
+    k_want, v_want = oracle.append_kv(x.k_cache, x.v_cache, kn, vn, bt, pos)
+    kd, vd = x.k_cache.to(DEV), x.v_cache.to(DEV)
+    pa.append_kv(kd, vd, kn.to(DEV), vn.to(DEV), bt.to(DEV), pos.to(DEV))
+    torch.cuda.synchronize()
+    assert torch.equal(_as_bits(kd), _as_bits(k_want))
+    assert torch.equal(_as_bits(vd), _as_bits(v_want))
+
+
+def test_append_then_decode_in_a_graph():
+    """A decode iteration: append the new token (the last of each context),
+    then attend; captured once in a CUDA graph and replayed."""
+    x = workloads.make("ragged_b64", seed=3, device=DEV)
+    host = x.to("cpu")                                   # the cache before any append
+    B, _, D = x.q.shape
+    Hkv = x.k_cache.shape[2]
+    g = torch.Generator(device=DEV).manual_seed(4)
+    kn = torch.randn(B, Hkv, D, generator=g, device=DEV).to(x.q.dtype)
+    vn = torch.randn(B, Hkv, D, generator=g, device=DEV).to(x.q.dtype)
+    pos = (x.context_lens - 1).contiguous()
+    out = torch.empty(x.q.shape, dtype=torch.float32, device=DEV)
+    need = pa.workspace_size(x.q, x.k_cache, x.block_tables, torch.float32, x.max_context_len, 0)
+    ws = torch.empty(max(16, need), dtype=torch.uint8, device=DEV)
+    st = torch.cuda.Stream()
+    with torch.cuda.stream(st):
+        def step():
+            pa.append_kv(x.k_cache, x.v_cache, kn, vn, x.block_tables, pos, stream=st)
+            pa.decode_splitkv(out, x.q, x.k_cache, x.v_cache, x.block_tables, x.context_lens,
+                              x.scale, x.max_context_len, 0, workspace=ws, stream=st)
+        step()
+        st.synchronize()
+        graph = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(graph, stream=st):
+            step()
+        out.fill_(float("nan"))
+        graph.replay()
+        st.synchronize()
+    k2, v2 = oracle.append_kv(host.k_cache, host.v_cache, kn.cpu(), vn.cpu(), host.block_tables,
+                              pos.cpu())
+    assert torch.equal(_as_bits(x.k_cache), _as_bits(k2))
+    rows = sample_rows(x, 24)
+    want = oracle.decode_rows(host.q, k2, v2, host.block_tables, host.context_lens, host.scale, rows)
+    assert_close_fp32(out[rows[:, 0], rows[:, 1]], want)
