@@ -301,6 +301,10 @@ def main(argv=None):
     for i, x in enumerate(set0):
         pt = pts[i] or pa.choose_partition_tokens(x.q, x.k_cache, x.block_tables,
                                                   x.max_context_len, sms)
+        if pt == pa.PARTITION_BALANCED:
+            plans[names[i]] = {"partition_tokens": "balanced", "partitions": f"{sms} equal shares",
+                               "reduce": "balanced records + combine kernel"}
+            continue
         parts = -(-max(x.max_context_len, 1) // pt)
         plans[names[i]] = {"partition_tokens": pt, "partitions": parts,
                            "reduce": "none" if parts <= 1 else

@@ -72,6 +72,12 @@ typedef enum pa_status {
 
 typedef enum pa_dtype { PA_F16 = 0, PA_BF16 = 1, PA_F32 = 2 } pa_dtype;
 
+/* partition_tokens value requesting the balanced split: one CTA per SM, each
+ * taking an equal share of all (sequence, kv head, page) triples in order,
+ * pieces of a (sequence, kv head) that straddle CTAs combined afterwards.
+ * Needs batch <= 512 (otherwise the automatic choice is used). */
+#define PA_PARTITION_BALANCED (-1)
+
 typedef struct pa_shape {
     int32_t batch;              /* B >= 0 (B = 0 launches nothing) */
     int32_t num_heads;          /* H, query heads */
@@ -101,16 +107,18 @@ pa_status pa_decode(void* out, const void* q, const void* k_cache, const void* v
  * Bytes of device workspace pa_decode_splitkv needs for this shape, longest
  * context `max_context_len` and partition size `partition_tokens` (tokens per
  * split, a multiple of block_size; 0 = choose automatically for the current
- * device).  Returns 0 for invalid arguments and when no workspace is needed
- * (one partition, or at most 8 reduced inside a cluster).
+ * device; PA_PARTITION_BALANCED = the balanced split).  Returns 0 for invalid
+ * arguments and when no workspace is needed (one partition, or at most 8
+ * reduced inside a cluster).
  */
 size_t pa_workspace_size(const pa_shape* shape, int32_t max_context_len,
                          int32_t partition_tokens);
 
 /*
  * Partition size (tokens) the automatic choice picks for `num_sms`
- * multiprocessors: 0 < result, a multiple of block_size; a result >=
- * max_context_len means "no split".  Host-only, no device access (a pure
+ * multiprocessors: a multiple of block_size (a result >= max_context_len
+ * means "no split"), or PA_PARTITION_BALANCED when it picks the balanced
+ * split; 0 for invalid arguments.  Host-only, no device access (a pure
  * function, exported so that its choice can be checked without a GPU).
  * The rules are this library's own, fitted to GB300 timings: the
  * flash-decoding-bench design notes only say that the chunk size is picked
@@ -123,7 +131,10 @@ int32_t pa_choose_partition_tokens(const pa_shape* shape, int32_t max_context_le
  * Flash-Decoding split-KV decode (flash-decoding-bench "design.md": the KV
  * cache is split into chunks, one thread block each, each computing its local
  * max, sum and weighted value sum, followed by a reduction of the partials).
- * Each (sequence, kv head) is cut into partitions of `partition_tokens` tokens;
+ * Each (sequence, kv head) is cut into partitions of `partition_tokens` tokens
+ * (or, with PA_PARTITION_BALANCED, the flattened pages of all of them are cut
+ * into one equal share per SM, and a piece that straddles two shares leaves
+ * a partial record for the combine kernel);
  * one CTA per partition computes fp32 partials (m, l, acc[head_dim]) for each
  * query head of the group.  At most 8 partitions are launched as one
  * thread-block cluster and reduced through distributed shared memory inside

@@ -26,6 +26,7 @@ __all__ = ["PaError", "decode", "decode_splitkv", "decode_splitkv_noalloc", "app
            "resolve_blocks", "device_error", "library_path", "F16", "BF16", "F32"]
 
 F16, BF16, F32 = 0, 1, 2
+PARTITION_BALANCED = -1   # partition_tokens value requesting the balanced split
 _STATUS = {0: "PA_OK", 1: "PA_ERR_INVALID_ARG", 2: "PA_ERR_UNSUPPORTED", 3: "PA_ERR_WORKSPACE",
            4: "PA_ERR_CUDA", 5: "PA_ERR_TIMEOUT"}
 

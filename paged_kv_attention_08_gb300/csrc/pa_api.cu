@@ -165,11 +165,15 @@ struct Plan {
     int part_pages, num_parts;
     bool cluster;
     bool many_ctas;  // the grid spans several waves: pick the two-CTAs-per-SM tune
+    bool balanced;   // one CTA per SM, equal shares of the flattened page order
+    int num_ctas;    // balanced: grid size
 };
 
 Plan plan_with(const pa_shape* s, int pages, int pp, bool cluster_ok) {
     Plan p;
     p.many_ctas = false;
+    p.balanced = false;
+    p.num_ctas = 0;
     if (pp < 1) pp = 1;
     p.num_parts = (pages + pp - 1) / pp;
     if (p.num_parts < 1) p.num_parts = 1;
@@ -190,12 +194,40 @@ Plan plan_with(const pa_shape* s, int pages, int pp, bool cluster_ok) {
 //    that gives less parallelism, into partitions of at least 16 pages
 //    combined through the workspace.
 // The longest context stands for every sequence: the host reads no lengths.
+// The automatic choice does not pick the balanced split (on GB300 it was
+// slower than equal partitions for every workload measured: once ~128 CTAs
+// stream, HBM is the limit and the split's extra reduction costs more than
+// the idle SMs); PA_BALANCED=1 lets it pick the balanced split where equal
+// partitions leave SMs idle, PA_BALANCED=2 wherever the batch allows.  A
+// tuning switch; results agree.
+int balanced_mode() {
+    static const int m = [] {
+        const char* v = std::getenv("PA_BALANCED");
+        if (!v || !*v) return 0;
+        const int x = std::atoi(v);
+        return x < 0 ? 0 : (x > 2 ? 2 : x);
+    }();
+    return m;
+}
+
+Plan balanced_plan(const pa_shape* s, int pages, int num_sms) {
+    Plan p = plan_with(s, pages, pages, false);
+    p.balanced = true;
+    p.num_ctas = num_sms;
+    p.many_ctas = false;
+    return p;
+}
+
 Plan auto_plan(const pa_shape* s, int32_t max_context_len, int num_sms) {
     const int pages = pages_for(s, max_context_len);
     const int64_t units = (int64_t)s->batch * s->num_kv_heads;
     auto ceil_div = [](int64_t a, int64_t b) { return (a + b - 1) / b; };
+    const bool can_balance = s->batch <= kMaxBalancedBatch && balanced_mode() > 0;
+    // enough pages that every SM gets at least eight
+    const bool big = units * pages >= 8LL * num_sms;
     const int64_t wide_slots = (int64_t)num_sms * ctas_per_sm(s, pick_tune(s, true));
     if (units * 3 >= wide_slots) {
+        if (can_balance && balanced_mode() == 2 && big) return balanced_plan(s, pages, num_sms);
         const int parts = (int)ceil_div(pages, 64);
         Plan p = plan_with(s, pages, (int)ceil_div(pages, parts), false);
         p.many_ctas = units * p.num_parts > num_sms;
@@ -206,8 +238,14 @@ Plan auto_plan(const pa_shape* s, int32_t max_context_len, int num_sms) {
     if (fill < 1) fill = 1;
     const int64_t p_cl = std::min<int64_t>(std::min<int64_t>(kMaxClusterParts, fill), ceil_div(pages, 4));
     const int64_t p_ws = std::min<int64_t>(fill, ceil_div(pages, 16));
-    if (p_cl >= p_ws) return plan_with(s, pages, (int)ceil_div(pages, p_cl), true);
-    return plan_with(s, pages, (int)ceil_div(pages, p_ws), false);
+    Plan p = p_cl >= p_ws ? plan_with(s, pages, (int)ceil_div(pages, p_cl), true)
+                          : plan_with(s, pages, (int)ceil_div(pages, p_ws), false);
+    // Equal partitions of few units leave SMs idle (e.g. 32 units x 4 = 128
+    // CTAs on 152 SMs); the balanced split gives every SM the same share.
+    const double coverage = (double)(units * p.num_parts) / (double)slots;
+    if (can_balance && big && (balanced_mode() == 2 || coverage < 0.9))
+        return balanced_plan(s, pages, (int)slots);
+    return p;
 }
 
 // PA_NO_CLUSTER=1 turns the in-cluster reduction off (partitions then always
@@ -219,7 +257,10 @@ bool clusters_enabled() {
 
 Plan make_plan(const pa_shape* s, int32_t max_context_len, int32_t partition_tokens, int num_sms) {
     Plan plan;
-    if (partition_tokens == 0) {
+    if (partition_tokens == PA_PARTITION_BALANCED && s->batch <= kMaxBalancedBatch) {
+        plan = balanced_plan(s, pages_for(s, max_context_len),
+                             num_sms * ctas_per_sm(s, pick_tune(s, false)));
+    } else if (partition_tokens <= 0) {
         plan = auto_plan(s, max_context_len, num_sms);
     } else {
         plan = plan_with(s, pages_for(s, max_context_len), partition_tokens / s->block_size, true);
@@ -229,11 +270,20 @@ Plan make_plan(const pa_shape* s, int32_t max_context_len, int32_t partition_tok
     return plan;
 }
 
+bool partition_arg_ok(const pa_shape* s, int32_t partition_tokens) {
+    return partition_tokens == PA_PARTITION_BALANCED ||
+           (partition_tokens >= 0 && partition_tokens % s->block_size == 0);
+}
+
 // Workspace: part_acc [B, Hkv, P, G, D] fp32, then part_ml [B, Hkv, P, G, 2] fp32.
 size_t workspace_bytes_for(const pa_shape* s, const Plan& plan, size_t* ml_offset) {
-    if (plan.num_parts <= 1 || plan.cluster) return 0;  // one pass, or reduced inside a cluster
-    const int num_parts = plan.num_parts;
-    const size_t rows = (size_t)s->batch * s->num_heads * num_parts;  // B*Hkv*P*G
+    size_t rows;  // (m, l, acc) rows of the group's heads
+    if (plan.balanced) {
+        rows = (size_t)plan.num_ctas * 2 * (s->num_heads / s->num_kv_heads);  // [C][2][G]
+    } else {
+        if (plan.num_parts <= 1 || plan.cluster) return 0;  // one pass, or reduced in a cluster
+        rows = (size_t)s->batch * s->num_heads * plan.num_parts;           // [B][Hkv][P][G]
+    }
     const size_t acc = rows * s->head_dim * sizeof(float);
     const size_t off = (acc + 255) / 256 * 256;
     if (ml_offset) *ml_offset = off;
@@ -310,13 +360,17 @@ pa_status launch_attention(void* out, const void* q, const void* k, const void* 
     p.out_dtype = s->out_dtype;
     p.final_out = plan.num_parts <= 1 ? 1 : 0;
     p.cluster_reduce = plan.cluster ? 1 : 0;
+    p.balanced = plan.balanced ? 1 : 0;
+    if (plan.balanced) p.final_out = 0;
     p.timeout_ns = kDefaultTimeoutNs;
     L.head_dim = s->head_dim;
     L.block_size = s->block_size;
     L.kv_dtype = s->kv_dtype;
     L.pdl = use_pdl();
     L.cluster = p.cluster_reduce ? plan.num_parts : 1;
-    L.grid = dim3((unsigned)plan.num_parts, (unsigned)s->num_kv_heads, (unsigned)s->batch);
+    L.grid = plan.balanced ? dim3((unsigned)plan.num_ctas)
+                           : dim3((unsigned)plan.num_parts, (unsigned)s->num_kv_heads,
+                                  (unsigned)s->batch);
     L.threads = 32 * t.nt * t.nh;
     L.smem_bytes = sm.total + kSmemAlignSlack;
     cudaError_t e;
@@ -351,15 +405,16 @@ int32_t pa_choose_partition_tokens(const pa_shape* shape, int32_t max_context_le
                                    int32_t num_sms) {
     if (check_shape(shape) != PA_OK || max_context_len < 0 || num_sms <= 0) return 0;
     const Plan plan = auto_plan(shape, max_context_len, num_sms);
+    if (plan.balanced) return PA_PARTITION_BALANCED;
     return plan.part_pages * shape->block_size;
 }
 
 size_t pa_workspace_size(const pa_shape* shape, int32_t max_context_len,
                          int32_t partition_tokens) {
-    if (check_shape(shape) != PA_OK || max_context_len < 0 || partition_tokens < 0) return 0;
-    if (partition_tokens % shape->block_size != 0) return 0;
+    if (check_shape(shape) != PA_OK || max_context_len < 0) return 0;
+    if (!partition_arg_ok(shape, partition_tokens)) return 0;
     int sms = 1;
-    if (partition_tokens == 0 && device_state(&sms, nullptr) != PA_OK) return 0;
+    if (partition_tokens <= 0 && device_state(&sms, nullptr) != PA_OK) return 0;
     const Plan plan = make_plan(shape, max_context_len, partition_tokens, sms);
     return workspace_bytes_for(shape, plan, nullptr);
 }
@@ -377,7 +432,7 @@ pa_status pa_decode(void* out, const void* q, const void* k_cache, const void* v
     st = device_state(&sms, &err);
     if (st != PA_OK) return st;
     Plan plan{shape->max_blocks_per_seq, 1, false,
-              (int64_t)shape->batch * shape->num_kv_heads > sms};
+              (int64_t)shape->batch * shape->num_kv_heads > sms, false, 0};
     return launch_attention(out, q, k_cache, v_cache, block_tables, context_lens, shape, scale,
                             plan, nullptr, nullptr, err, static_cast<cudaStream_t>(stream));
 }
@@ -389,8 +444,7 @@ pa_status pa_decode_splitkv(void* out, const void* q, const void* k_cache, const
                             void* stream) {
     pa_status st = check_shape(shape);
     if (st != PA_OK) return st;
-    if (max_context_len < 0 || partition_tokens < 0 || partition_tokens % shape->block_size != 0)
-        return PA_ERR_INVALID_ARG;
+    if (max_context_len < 0 || !partition_arg_ok(shape, partition_tokens)) return PA_ERR_INVALID_ARG;
     if (shape->batch == 0) return PA_OK;
     st = check_ptrs(out, q, k_cache, v_cache, block_tables, context_lens);
     if (st != PA_OK) return st;
@@ -400,7 +454,7 @@ pa_status pa_decode_splitkv(void* out, const void* q, const void* k_cache, const
     if (st != PA_OK) return st;
     const Plan plan = make_plan(shape, max_context_len, partition_tokens, sms);
     cudaStream_t cs = static_cast<cudaStream_t>(stream);
-    if (plan.num_parts <= 1 || plan.cluster)
+    if (!plan.balanced && (plan.num_parts <= 1 || plan.cluster))
         return launch_attention(out, q, k_cache, v_cache, block_tables, context_lens, shape, scale,
                                 plan, nullptr, nullptr, err, cs);
 
@@ -427,9 +481,11 @@ pa_status pa_decode_splitkv(void* out, const void* q, const void* k_cache, const
     c.part_pages = plan.part_pages;
     c.num_parts = plan.num_parts;
     c.out_dtype = shape->out_dtype;
-    const cudaError_t e = launch_combine(c, shape->head_dim,
-                                         dim3((unsigned)shape->num_heads, (unsigned)shape->batch),
-                                         use_pdl(), cs);
+    c.num_ctas = plan.num_ctas;
+    const dim3 cgrid((unsigned)shape->num_heads, (unsigned)shape->batch);
+    const cudaError_t e = plan.balanced ? launch_combine_balanced(c, shape->head_dim, cgrid,
+                                                                  use_pdl(), cs)
+                                        : launch_combine(c, shape->head_dim, cgrid, use_pdl(), cs);
     return e == cudaSuccess ? PA_OK : PA_ERR_CUDA;
 }
 
@@ -501,8 +557,7 @@ pa_status pa_decode_splitkv_noalloc(void* out, const void* q, const void* k_cach
                                     int32_t partition_tokens, void* stream) {
     pa_status st = check_shape(shape);
     if (st != PA_OK) return st;
-    if (max_context_len < 0 || partition_tokens < 0 || partition_tokens % shape->block_size != 0)
-        return PA_ERR_INVALID_ARG;
+    if (max_context_len < 0 || !partition_arg_ok(shape, partition_tokens)) return PA_ERR_INVALID_ARG;
     if (shape->batch == 0) return PA_OK;
     st = check_ptrs(out, q, k_cache, v_cache, block_tables, context_lens);
     if (st != PA_OK) return st;

@@ -67,6 +67,9 @@ __device__ __forceinline__ uint32_t swz(int t, int c) {
 
 constexpr float kRescaleSlack = 8.0f;  // log2 units: p may reach 2^8 before a rescale
 
+// Where the merged result of a segment goes.
+enum SegOut { kOutFinal = 0, kOutPartial = 1, kOutCluster = 2, kOutRecord = 3 };
+
 template <int D, int BS, typename KV>
 __global__ void __launch_bounds__(256, 1)
     attn_kernel(const __grid_constant__ CUtensorMap tmap_k,
@@ -84,12 +87,12 @@ __global__ void __launch_bounds__(256, 1)
 
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const int stream = warp / DS, ds = warp % DS;
-    const int part = blockIdx.x, kvh = blockIdx.y, b = blockIdx.z;
     const int G = p.group;
 
     uint64_t* full = reinterpret_cast<uint64_t*>(smem + L.full_off);
     uint64_t* empty = reinterpret_cast<uint64_t*>(smem + L.empty_off);
     int32_t* phys_of = reinterpret_cast<int32_t*>(smem + L.phys_off);
+    int32_t* seq_pages = reinterpret_cast<int32_t*>(smem + L.seq_off);  // balanced split only
     if (tid == 0) {
         for (int i = 0; i < p.nt * p.ns; ++i) {
             mbar_init(smem_u32(full + i), 1);
@@ -103,24 +106,435 @@ __global__ void __launch_bounds__(256, 1)
     grid_dependency_wait();
     grid_launch_dependents();
 
-    // This stream's pages are pb + stream + i*nt.  The leader warp fetches
-    // their table entries 32 at a time, one per lane, before the context
-    // length is known (every index stays inside the table row); entries past
-    // the context are masked once it is.
-    const int32_t* table_row = p.block_tables + (size_t)b * p.max_blocks;
-    const int pb = part * p.part_pages;
-    const int pe_row = min(pb + p.part_pages, p.max_blocks);
-    const int n_row = pe_row - pb > stream ? (pe_row - pb - stream + p.nt - 1) / p.nt : 0;
+    const int g = lane >> 2, tig = lane & 3;
+    const bool real0 = g < G, real1 = g + 8 < G;
+    const float qscale = p.qscale;
+    const int ldsm_t = lane & 7;         // row supplied to ldmatrix
+    const int ldsm_m = lane >> 3;        // matrix supplied to ldmatrix
+    const int col0 = ds * (DW / 8);      // first 16-byte output chunk of this warp
+    const int nw = p.nt * DS;
+    // After a segment's pages are consumed the stage area holds the merge data.
+    float* macc = reinterpret_cast<float*>(smem + L.stages_off);   // [nw][G][DW]
+    float* mm = macc + (size_t)nw * G * DW;                         // [nw][G]
+    float* mls = mm + nw * G;                                       // [nw][G]
+    float* cpart = mls + nw * G;  // this CTA's partial when the cluster reduces: acc [G][D], m [G], l [G]
+
+    // Pipeline state of this warp's stream, carried across segments.
+    int slot = 0;
+    uint32_t par = 0;
+    bool aborted = false;
+
+    // Table entries of this stream's pages of the current segment, 32 at a
+    // time, one per lane of the leader warp.
+    const int32_t* table_row = nullptr;
+    int seg_pb = 0, seg_fetch_end = 0;
+    int ent_cur = -1, ent_next = -1, cur_chunk = 0;
     auto fetch = [&](int chunk) -> int {
         const int li = chunk * 32 + lane;
-        return li < n_row ? __ldg(table_row + pb + stream + li * p.nt) : -1;
+        const int j = seg_pb + stream + li * p.nt;
+        return j < seg_fetch_end ? __ldg(table_row + j) : -1;
     };
-    int ent_cur = -1, ent_next = -1, cur_chunk = 0;
-    if (ds == 0) {
-        ent_cur = fetch(0);
-        ent_next = fetch(1);
+    auto start_fetch = [&](int b, int pb, int fetch_end) {
+        table_row = p.block_tables + (size_t)b * p.max_blocks;
+        seg_pb = pb;
+        seg_fetch_end = fetch_end;
+        cur_chunk = 0;
+        if (ds == 0) {
+            ent_cur = fetch(0);
+            ent_next = fetch(1);
+        }
+    };
+
+    // Pages [pb, pe) of (sequence b, kv head kvh), whose context holds T
+    // tokens; the leader warp has already called start_fetch(b, pb, >= pe).
+    // The streams take the pages in turn; the merged (m, l, acc) of every
+    // query head of the group is handed to emit(idx = r*D + d, A, M, L).
+    auto run_segment = [&](int b, int kvh, int pb, int pe, int T, auto&& emit) {
+        const int npages = (T + BS - 1) / BS;
+        const int span = pe - pb;
+        const int n_s = span > stream ? (span - stream + p.nt - 1) / p.nt : 0;
+        const int slot0 = slot;
+        const uint32_t par0 = par;
+        int n_issued = 0;
+
+        // Stage local page i of this stream (whole leader warp): its table
+        // entry, then one TMA copy per 64-column block of its K and V tiles.
+        auto issue = [&](int i, int sidx) {
+            if ((i >> 5) != cur_chunk) {  // slide the prefetched window
+                cur_chunk = i >> 5;
+                ent_cur = ent_next;
+                ent_next = fetch(cur_chunk + 1);
+            }
+            const int e = __shfl_sync(kFullMask, ent_cur, i & 31);
+            const int j = pb + stream + i * p.nt;
+            const int phys = (j < npages && e >= 0 && (int64_t)e < p.num_blocks) ? e : -1;
+            if (lane == 0) {
+                phys_of[sidx] = phys;
+                const uint32_t bar = smem_u32(full + sidx);
+                if (phys >= 0) {
+                    const uint64_t policy = l2_policy_evict_first();
+                    mbar_arrive_expect_tx(bar, L.stage_bytes);
+                    const uint32_t dst =
+                        smem_u32(smem + L.stages_off + (size_t)sidx * L.stage_bytes);
+#pragma unroll
+                    for (int blk = 0; blk < DBLK; ++blk) {
+                        tma_load_4d(dst + blk * BS * 128, &tmap_k, blk * 64, kvh, 0, phys, bar,
+                                    policy);
+                        tma_load_4d(dst + L.tile_bytes + blk * BS * 128, &tmap_v, blk * 64, kvh,
+                                    0, phys, bar, policy);
+                    }
+                } else {
+                    mbar_arrive(bar);
+                }
+            }
+        };
+
+        if (ds == 0 && !aborted) {
+            const int pro = n_s < p.ns ? n_s : p.ns;
+            int sl = slot0;
+            for (int i = 0; i < pro; ++i) {
+                issue(i, stream * p.ns + sl);
+                if (++sl == p.ns) sl = 0;
+            }
+            n_issued = pro;
+        }
+
+        // ---- Q fragments (A operand of S = Q K^T): rows = the group's heads ----
+        uint32_t qa[KSTEPS][4];
+        {
+            const KV* q = static_cast<const KV*>(p.q) + ((size_t)b * p.num_heads + kvh * G) * D;
+            const uint32_t* q0 = reinterpret_cast<const uint32_t*>(q + (size_t)g * D);
+            const uint32_t* q1 = reinterpret_cast<const uint32_t*>(q + (size_t)(g + 8) * D);
+#pragma unroll
+            for (int kk = 0; kk < KSTEPS; ++kk) {
+                const int w = (kk * 16 + tig * 2) >> 1;  // 32-bit word index of the element pair
+                qa[kk][0] = real0 ? __ldg(q0 + w) : 0u;
+                qa[kk][1] = real1 ? __ldg(q1 + w) : 0u;
+                qa[kk][2] = real0 ? __ldg(q0 + w + 4) : 0u;
+                qa[kk][3] = real1 ? __ldg(q1 + w + 4) : 0u;
+            }
+        }
+
+        // Running state of rows g and g+8 (padded rows stay at m = 0, p = 0).
+        float m0 = real0 ? NEG_INF : 0.f, m1 = real1 ? NEG_INF : 0.f;
+        float l0 = 0.f, l1 = 0.f;  // this lane's share of the normalisers
+        float acc[ONT][4];
+#pragma unroll
+        for (int n = 0; n < ONT; ++n) acc[n][0] = acc[n][1] = acc[n][2] = acc[n][3] = 0.f;
+
+        int i = 0;
+        for (; i < n_s && !aborted; ++i) {
+            const int sidx = stream * p.ns + slot;
+            const bool ok = __all_sync(kFullMask, mbar_wait_bounded(smem_u32(full + sidx), par,
+                                                                    p.timeout_ns));
+            if (!ok) {
+                if (lane == 0) record_error(p.err, PA_ERR_TIMEOUT);
+                aborted = true;
+                break;
+            }
+            const int phys = phys_of[sidx];
+            if (phys >= 0) {
+                const int j = pb + stream + i * p.nt;
+                const int nvalid = min(BS, T - j * BS);
+                uint8_t* kt = smem + L.stages_off + (size_t)sidx * L.stage_bytes;
+                uint8_t* vt = kt + L.tile_bytes;
+                const uint32_t kbase = smem_u32(kt), vbase = smem_u32(vt);
+
+                if (nvalid < BS) {
+                    // Zero this warp's columns of the V rows past the context.
+                    const int rows = BS - nvalid;
+                    for (int idx = lane; idx < rows * 8 * (DW / 64); idx += 32) {
+                        const int blk = ds * (DW / 64) + idx / (rows * 8);
+                        const int rem = idx % (rows * 8);
+                        *reinterpret_cast<uint4*>(vt + blk * BS * 128 + (nvalid + rem / 8) * 128 +
+                                                  (rem % 8) * 16) = make_uint4(0, 0, 0, 0);
+                    }
+                    fence_proxy_async_smem();
+                    __syncwarp();
+                }
+
+                // ---- S = Q K^T (fp32), even and odd k-steps in separate chains ----
+                float s[NT][4], s2[NT][4];
+#pragma unroll
+                for (int nt = 0; nt < NT; ++nt) {
+                    s[nt][0] = s[nt][1] = s[nt][2] = s[nt][3] = 0.f;
+                    s2[nt][0] = s2[nt][1] = s2[nt][2] = s2[nt][3] = 0.f;
+#pragma unroll
+                    for (int kk = 0; kk < KSTEPS; kk += 2) {
+                        uint32_t b0, b1, b2, b3;
+                        ldsm_x4(kbase + swz<BS>(nt * 8 + ldsm_t, 2 * kk + ldsm_m), b0, b1, b2, b3);
+                        Mma<KV>::mma(s[nt], qa[kk], b0, b1);
+                        Mma<KV>::mma(s2[nt], qa[kk + 1], b2, b3);
+                    }
+#pragma unroll
+                    for (int e = 0; e < 4; ++e) s[nt][e] += s2[nt][e];
+                }
+
+                // ---- page max per row, conditional rescale ----
+                float mx0 = NEG_INF, mx1 = NEG_INF;
+#pragma unroll
+                for (int nt = 0; nt < NT; ++nt)
+#pragma unroll
+                    for (int e = 0; e < 2; ++e) {
+                        const bool v = nt * 8 + tig * 2 + e < nvalid;
+                        s[nt][e] = v ? s[nt][e] : NEG_INF;
+                        s[nt][2 + e] = v ? s[nt][2 + e] : NEG_INF;
+                        mx0 = fmaxf(mx0, s[nt][e]);
+                        mx1 = fmaxf(mx1, s[nt][2 + e]);
+                    }
+                mx0 = fmaxf(mx0, __shfl_xor_sync(kFullMask, mx0, 1));
+                mx1 = fmaxf(mx1, __shfl_xor_sync(kFullMask, mx1, 1));
+                mx0 = fmaxf(mx0, __shfl_xor_sync(kFullMask, mx0, 2));
+                mx1 = fmaxf(mx1, __shfl_xor_sync(kFullMask, mx1, 2));
+                const float ms0 = mx0 * qscale, ms1 = mx1 * qscale;
+                const bool need = (real0 && ms0 > m0 + kRescaleSlack) ||
+                                  (real1 && ms1 > m1 + kRescaleSlack);
+                if (__any_sync(kFullMask, need)) {
+                    const float n0 = real0 ? fmaxf(m0, ms0) : m0;
+                    const float n1 = real1 ? fmaxf(m1, ms1) : m1;
+                    const float a0 = (n0 == m0) ? 1.f : fast_exp2(m0 - n0);
+                    const float a1 = (n1 == m1) ? 1.f : fast_exp2(m1 - n1);
+                    m0 = n0;
+                    m1 = n1;
+                    l0 *= a0;
+                    l1 *= a1;
+#pragma unroll
+                    for (int n = 0; n < ONT; ++n) {
+                        acc[n][0] *= a0;
+                        acc[n][1] *= a0;
+                        acc[n][2] *= a1;
+                        acc[n][3] *= a1;
+                    }
+                }
+
+                // ---- P = 2^(S*scale*log2e - m), and its hi/lo 16-bit split ----
+#pragma unroll
+                for (int nt = 0; nt < NT; ++nt)
+#pragma unroll
+                    for (int e = 0; e < 2; ++e) {
+                        s[nt][e] = real0 ? fast_exp2(fmaf(s[nt][e], qscale, -m0)) : 0.f;
+                        s[nt][2 + e] = real1 ? fast_exp2(fmaf(s[nt][2 + e], qscale, -m1)) : 0.f;
+                        l0 += s[nt][e];
+                        l1 += s[nt][2 + e];
+                    }
+
+                // ---- O += P V on this warp's columns ----
+#pragma unroll
+                for (int ks = 0; ks < PKS; ++ks) {
+                    uint32_t ph[4], pl[4];
+#pragma unroll
+                    for (int r = 0; r < 4; ++r) {
+                        // a0: n-tile 2ks rows g; a1: rows g+8; a2/a3: n-tile 2ks+1
+                        const float x0 = s[2 * ks + (r >> 1)][(r & 1) * 2];
+                        const float x1 = s[2 * ks + (r >> 1)][(r & 1) * 2 + 1];
+                        ph[r] = Mma<KV>::pack(x0, x1);
+                        float h0, h1;
+                        Mma<KV>::unpack(ph[r], h0, h1);
+                        pl[r] = Mma<KV>::pack(x0 - h0, x1 - h1);
+                    }
+#pragma unroll
+                    for (int n = 0; n < ONT; n += 2) {
+                        uint32_t b0, b1, b2, b3;
+                        const int t = ks * 16 + ((ldsm_m & 1) << 3) + ldsm_t;
+                        ldsm_x4_trans(vbase + swz<BS>(t, col0 + n + (ldsm_m >> 1)), b0, b1, b2,
+                                      b3);
+                        Mma<KV>::mma(acc[n], ph, b0, b1);
+                        Mma<KV>::mma(acc[n], pl, b0, b1);
+                        Mma<KV>::mma(acc[n + 1], ph, b2, b3);
+                        Mma<KV>::mma(acc[n + 1], pl, b2, b3);
+                    }
+                }
+            }
+            __syncwarp();
+            // A stream of one warp frees its own stage; with two, both must be done.
+            if (DS > 1 && lane == 0) mbar_arrive(smem_u32(empty + sidx));
+            // Refill the stage just released with this stream's page i + ns.
+            int refill_failed = 0;
+            if (ds == 0 && i + p.ns < n_s) {
+                const bool freed = DS == 1 || __all_sync(kFullMask,
+                                                         mbar_wait_bounded(smem_u32(empty + sidx),
+                                                                           par, p.timeout_ns));
+                if (freed) {
+                    fence_proxy_async_smem();
+                    issue(i + p.ns, sidx);
+                    ++n_issued;
+                } else {
+                    if (lane == 0) record_error(p.err, PA_ERR_TIMEOUT);
+                    refill_failed = 1;
+                }
+            }
+            if (++slot == p.ns) {
+                slot = 0;
+                par ^= 1u;
+            }
+            if (__shfl_sync(kFullMask, refill_failed, 0)) {
+                aborted = true;
+                ++i;
+                break;
+            }
+        }
+        if (aborted && ds == 0 && lane == 0) {
+            // Let copies this stream still has in flight land before moving on.
+            for (int k = i; k < n_issued; ++k) {
+                const int ks = (slot0 + k) % p.ns;
+                const uint32_t kp = par0 ^ (uint32_t)(((slot0 + k) / p.ns) & 1);
+                (void)mbar_wait_bounded(smem_u32(full + stream * p.ns + ks), kp, p.timeout_ns);
+            }
+        }
+
+        // ---- per-warp normalisers: sum the quad's shares ----
+        l0 += __shfl_xor_sync(kFullMask, l0, 1);
+        l1 += __shfl_xor_sync(kFullMask, l1, 1);
+        l0 += __shfl_xor_sync(kFullMask, l0, 2);
+        l1 += __shfl_xor_sync(kFullMask, l1, 2);
+
+        // Every stage of the segment has been consumed: the stage area now
+        // holds the merge data.
+        __syncthreads();
+#pragma unroll
+        for (int n = 0; n < ONT; ++n) {
+            const int c = n * 8 + tig * 2;
+            if (real0)
+                *reinterpret_cast<float2*>(macc + ((size_t)warp * G + g) * DW + c) =
+                    make_float2(acc[n][0], acc[n][1]);
+            if (real1)
+                *reinterpret_cast<float2*>(macc + ((size_t)warp * G + g + 8) * DW + c) =
+                    make_float2(acc[n][2], acc[n][3]);
+        }
+        if (tig == 0) {
+            if (real0) {
+                mm[warp * G + g] = m0;
+                mls[warp * G + g] = l0;
+            }
+            if (real1) {
+                mm[warp * G + g + 8] = m1;
+                mls[warp * G + g + 8] = l1;
+            }
+        }
+        __syncthreads();
+
+        // ---- merge the token streams (log-sum-exp) ----
+        for (int idx = tid; idx < G * D; idx += blockDim.x) {
+            const int r = idx / D, d = idx % D;
+            const int dsx = d / DW, dd = d % DW;
+            float M = NEG_INF;
+            for (int s2 = 0; s2 < p.nt; ++s2) M = fmaxf(M, mm[(s2 * DS + dsx) * G + r]);
+            float A = 0.f, Ls = 0.f;
+            if (M != NEG_INF) {
+                for (int s2 = 0; s2 < p.nt; ++s2) {
+                    const int w2 = s2 * DS + dsx;
+                    const float ms = mm[w2 * G + r];
+                    if (ms != NEG_INF) {
+                        const float f = exp2f(ms - M);
+                        A = fmaf(f, macc[((size_t)w2 * G + r) * DW + dd], A);
+                        Ls = fmaf(f, mls[w2 * G + r], Ls);
+                    }
+                }
+            }
+            emit(idx, A, M, Ls);
+        }
+        __syncthreads();  // the next segment's copies may now reuse the stage area
+    };
+
+    auto emit_final = [&](int b, int kvh) {
+        return [&, b, kvh](int idx, float A, float M, float Ls) {
+            store_out(p.out, ((size_t)b * p.num_heads + kvh * G) * D + idx,
+                      Ls > 0.f ? A / Ls : 0.f, p.out_dtype);
+        };
+    };
+    // (m, l, acc) of the group's heads into workspace row `row0 + r`.
+    auto emit_rows = [&](size_t row0) {
+        return [&, row0](int idx, float A, float M, float Ls) {
+            const int r = idx / D, d = idx % D;
+            p.part_acc[(row0 + r) * D + d] = A;
+            if (d == 0) {
+                p.part_ml[(row0 + r) * 2] = M;
+                p.part_ml[(row0 + r) * 2 + 1] = Ls;
+            }
+        };
+    };
+
+    if (p.balanced) {
+        // ---- balanced split: CTA c takes pages [c*W/C, (c+1)*W/C) of the
+        // flattened (sequence, kv head, page) order, W pages in all ----
+        const int Hkv = p.num_kv_heads;
+        int* totals = seq_pages + p.batch;  // [0]: W
+        if (warp == 0) {
+            int w = 0;
+            for (int b0 = lane; b0 < p.batch; b0 += 32) {
+                const int T = reachable_tokens(p.context_lens, b0, p.max_blocks, BS);
+                const int np = (T + BS - 1) / BS;
+                seq_pages[b0] = np;
+                w += np;
+            }
+#pragma unroll
+            for (int m = 16; m >= 1; m >>= 1) w += __shfl_xor_sync(kFullMask, w, m);
+            if (lane == 0) totals[0] = w * Hkv;
+        }
+        __syncthreads();
+        const int64_t W = totals[0];
+        const int64_t Cn = gridDim.x, c = blockIdx.x;
+        const int64_t start = c * W / Cn, end = (c + 1) * W / Cn;
+        if (start >= end) return;
+        // locate the sequence holding flat page `start` (each thread of the
+        // warp scans the same prefix, 32 sequences at a time)
+        int b = 0;
+        int64_t base = 0;  // flat index of sequence b's first page
+        for (;;) {
+            const int bb = b + lane;
+            const int64_t v = bb < p.batch ? (int64_t)seq_pages[bb] * Hkv : 0;
+            int64_t incl = v;
+#pragma unroll
+            for (int m = 1; m < 32; m <<= 1) {
+                const int64_t o = __shfl_up_sync(kFullMask, incl, m);
+                if (lane >= m) incl += o;
+            }
+            const unsigned hit = __ballot_sync(kFullMask, bb < p.batch && base + incl > start);
+            if (hit) {
+                const int k = __ffs(hit) - 1;
+                base += __shfl_sync(kFullMask, incl - v, k);
+                b += k;
+                break;
+            }
+            base += __shfl_sync(kFullMask, incl, 31);
+            b += 32;
+        }
+        int64_t cur = start;
+        bool first = true;
+        while (cur < end) {
+            const int np = seq_pages[b];
+            const int kvh = (int)((cur - base) / np);
+            const int j = (int)((cur - base) % np);
+            const int64_t room = np - j;
+            const int len = (int)((end - cur) < room ? (end - cur) : room);
+            const int T = reachable_tokens(p.context_lens, b, p.max_blocks, BS);
+            start_fetch(b, j, j + len);
+            const bool whole = j == 0 && len == np;
+            const bool last = cur + len >= end;
+            if (whole) {
+                run_segment(b, kvh, j, j + len, T, emit_final(b, kvh));
+            } else {
+                const size_t row0 = ((size_t)c * 2 + (first ? 0 : 1)) * G;
+                run_segment(b, kvh, j, j + len, T, emit_rows(row0));
+            }
+            (void)last;
+            cur += len;
+            first = false;
+            if (cur - base >= (int64_t)np * Hkv) {  // next sequence with pages
+                base += (int64_t)np * Hkv;
+                ++b;
+                while (b < p.batch && seq_pages[b] == 0) ++b;
+            }
+        }
+        return;
     }
 
+    // ---- one CTA per (sequence, kv head, partition) ----
+    const int part = blockIdx.x, kvh = blockIdx.y, b = blockIdx.z;
+    const int pb = part * p.part_pages;
+    // the table entries are fetched before the context length is known
+    // (every index stays inside the table row); those past it are masked
+    start_fetch(b, pb, min(pb + p.part_pages, p.max_blocks));
     const int T = reachable_tokens(p.context_lens, b, p.max_blocks, BS);
     const int npages = (T + BS - 1) / BS;
     const int pe = min(pb + p.part_pages, npages);
@@ -139,306 +553,19 @@ __global__ void __launch_bounds__(256, 1)
     }
     __syncthreads();  // barrier initialisation visible to every warp
 
-    const int span = pe - pb;
-    const int n_s = span > stream ? (span - stream + p.nt - 1) / p.nt : 0;  // pages of this stream
-    const bool leader = ds == 0 && lane == 0;
-    int n_issued = 0;
-
-    // Stage local page i of this stream (whole leader warp): the page's table
-    // entry, then one TMA copy per 64-column block of its K and V tiles.
-    auto issue = [&](int i, int sidx) {
-        if ((i >> 5) != cur_chunk) {  // slide the prefetched window
-            cur_chunk = i >> 5;
-            ent_cur = ent_next;
-            ent_next = fetch(cur_chunk + 1);
-        }
-        const int e = __shfl_sync(kFullMask, ent_cur, i & 31);
-        const int j = pb + stream + i * p.nt;
-        const int phys = (j < npages && e >= 0 && (int64_t)e < p.num_blocks) ? e : -1;
-        if (lane == 0) {
-            phys_of[sidx] = phys;
-            const uint32_t bar = smem_u32(full + sidx);
-            if (phys >= 0) {
-                const uint64_t policy = l2_policy_evict_first();
-                mbar_arrive_expect_tx(bar, L.stage_bytes);
-                const uint32_t dst = smem_u32(smem + L.stages_off + (size_t)sidx * L.stage_bytes);
-#pragma unroll
-                for (int blk = 0; blk < DBLK; ++blk) {
-                    tma_load_4d(dst + blk * BS * 128, &tmap_k, blk * 64, kvh, 0, phys, bar, policy);
-                    tma_load_4d(dst + L.tile_bytes + blk * BS * 128, &tmap_v, blk * 64, kvh, 0,
-                                phys, bar, policy);
-                }
-            } else {
-                mbar_arrive(bar);
-            }
-        }
-    };
-
-    if (ds == 0) {
-        const int pro = n_s < p.ns ? n_s : p.ns;
-        for (int i = 0; i < pro; ++i) issue(i, stream * p.ns + i);
-        n_issued = pro;
-    }
-
-    // ---- Q fragments (A operand of S = Q K^T): rows = the group's heads ----
-    const int g = lane >> 2, tig = lane & 3;
-    const bool real0 = g < G, real1 = g + 8 < G;
-    uint32_t qa[KSTEPS][4];
-    {
-        const KV* q = static_cast<const KV*>(p.q) + ((size_t)b * p.num_heads + kvh * G) * D;
-        const uint32_t* q0 = reinterpret_cast<const uint32_t*>(q + (size_t)g * D);
-        const uint32_t* q1 = reinterpret_cast<const uint32_t*>(q + (size_t)(g + 8) * D);
-#pragma unroll
-        for (int kk = 0; kk < KSTEPS; ++kk) {
-            const int w = (kk * 16 + tig * 2) >> 1;  // 32-bit word index of the element pair
-            qa[kk][0] = real0 ? __ldg(q0 + w) : 0u;
-            qa[kk][1] = real1 ? __ldg(q1 + w) : 0u;
-            qa[kk][2] = real0 ? __ldg(q0 + w + 4) : 0u;
-            qa[kk][3] = real1 ? __ldg(q1 + w + 4) : 0u;
-        }
-    }
-
-    // Running state of rows g and g+8 (padded rows stay at m = 0, p = 0).
-    float m0 = real0 ? NEG_INF : 0.f, m1 = real1 ? NEG_INF : 0.f;
-    float l0 = 0.f, l1 = 0.f;  // this lane's share of the normalisers
-    float acc[ONT][4];
-#pragma unroll
-    for (int n = 0; n < ONT; ++n) acc[n][0] = acc[n][1] = acc[n][2] = acc[n][3] = 0.f;
-
-    const float qscale = p.qscale;
-    const int ldsm_t = lane & 7;         // row supplied to ldmatrix
-    const int ldsm_m = lane >> 3;        // matrix supplied to ldmatrix
-    const int col0 = ds * (DW / 8);      // first 16-byte output chunk of this warp
-
-    bool aborted = false;
-    int i = 0, slot = 0;
-    uint32_t par = 0;
-    for (; i < n_s; ++i) {
-        const int sidx = stream * p.ns + slot;
-        const bool ok = __all_sync(kFullMask, mbar_wait_bounded(smem_u32(full + sidx), par,
-                                                                p.timeout_ns));
-        if (!ok) {
-            if (lane == 0) record_error(p.err, PA_ERR_TIMEOUT);
-            aborted = true;
-            break;
-        }
-        const int phys = phys_of[sidx];
-        if (phys >= 0) {
-            const int j = pb + stream + i * p.nt;
-            const int nvalid = min(BS, T - j * BS);
-            uint8_t* kt = smem + L.stages_off + (size_t)sidx * L.stage_bytes;
-            uint8_t* vt = kt + L.tile_bytes;
-            const uint32_t kbase = smem_u32(kt), vbase = smem_u32(vt);
-
-            if (nvalid < BS) {
-                // Zero this warp's columns of the V rows past the context.
-                const int rows = BS - nvalid;
-                for (int idx = lane; idx < rows * 8 * (DW / 64); idx += 32) {
-                    const int blk = ds * (DW / 64) + idx / (rows * 8);
-                    const int rem = idx % (rows * 8);
-                    *reinterpret_cast<uint4*>(vt + blk * BS * 128 + (nvalid + rem / 8) * 128 +
-                                              (rem % 8) * 16) = make_uint4(0, 0, 0, 0);
-                }
-                fence_proxy_async_smem();
-                __syncwarp();
-            }
-
-            // ---- S = Q K^T (fp32), even and odd k-steps in separate chains ----
-            float s[NT][4], s2[NT][4];
-#pragma unroll
-            for (int nt = 0; nt < NT; ++nt) {
-                s[nt][0] = s[nt][1] = s[nt][2] = s[nt][3] = 0.f;
-                s2[nt][0] = s2[nt][1] = s2[nt][2] = s2[nt][3] = 0.f;
-#pragma unroll
-                for (int kk = 0; kk < KSTEPS; kk += 2) {
-                    uint32_t b0, b1, b2, b3;
-                    ldsm_x4(kbase + swz<BS>(nt * 8 + ldsm_t, 2 * kk + ldsm_m), b0, b1, b2, b3);
-                    Mma<KV>::mma(s[nt], qa[kk], b0, b1);
-                    Mma<KV>::mma(s2[nt], qa[kk + 1], b2, b3);
-                }
-#pragma unroll
-                for (int e = 0; e < 4; ++e) s[nt][e] += s2[nt][e];
-            }
-
-            // ---- page max per row, conditional rescale ----
-            float mx0 = NEG_INF, mx1 = NEG_INF;
-#pragma unroll
-            for (int nt = 0; nt < NT; ++nt)
-#pragma unroll
-                for (int e = 0; e < 2; ++e) {
-                    const bool v = nt * 8 + tig * 2 + e < nvalid;
-                    s[nt][e] = v ? s[nt][e] : NEG_INF;
-                    s[nt][2 + e] = v ? s[nt][2 + e] : NEG_INF;
-                    mx0 = fmaxf(mx0, s[nt][e]);
-                    mx1 = fmaxf(mx1, s[nt][2 + e]);
-                }
-            mx0 = fmaxf(mx0, __shfl_xor_sync(kFullMask, mx0, 1));
-            mx1 = fmaxf(mx1, __shfl_xor_sync(kFullMask, mx1, 1));
-            mx0 = fmaxf(mx0, __shfl_xor_sync(kFullMask, mx0, 2));
-            mx1 = fmaxf(mx1, __shfl_xor_sync(kFullMask, mx1, 2));
-            const float ms0 = mx0 * qscale, ms1 = mx1 * qscale;
-            const bool need = (real0 && ms0 > m0 + kRescaleSlack) ||
-                              (real1 && ms1 > m1 + kRescaleSlack);
-            if (__any_sync(kFullMask, need)) {
-                const float n0 = real0 ? fmaxf(m0, ms0) : m0;
-                const float n1 = real1 ? fmaxf(m1, ms1) : m1;
-                const float a0 = (n0 == m0) ? 1.f : fast_exp2(m0 - n0);
-                const float a1 = (n1 == m1) ? 1.f : fast_exp2(m1 - n1);
-                m0 = n0;
-                m1 = n1;
-                l0 *= a0;
-                l1 *= a1;
-#pragma unroll
-                for (int n = 0; n < ONT; ++n) {
-                    acc[n][0] *= a0;
-                    acc[n][1] *= a0;
-                    acc[n][2] *= a1;
-                    acc[n][3] *= a1;
-                }
-            }
-
-            // ---- P = 2^(S*scale*log2e - m), and its hi/lo 16-bit split ----
-#pragma unroll
-            for (int nt = 0; nt < NT; ++nt)
-#pragma unroll
-                for (int e = 0; e < 2; ++e) {
-                    s[nt][e] = real0 ? fast_exp2(fmaf(s[nt][e], qscale, -m0)) : 0.f;
-                    s[nt][2 + e] = real1 ? fast_exp2(fmaf(s[nt][2 + e], qscale, -m1)) : 0.f;
-                    l0 += s[nt][e];
-                    l1 += s[nt][2 + e];
-                }
-
-            // ---- O += P V on this warp's columns ----
-#pragma unroll
-            for (int ks = 0; ks < PKS; ++ks) {
-                uint32_t ph[4], pl[4];
-#pragma unroll
-                for (int r = 0; r < 4; ++r) {
-                    // a0: n-tile 2ks rows g; a1: rows g+8; a2/a3: n-tile 2ks+1
-                    const float x0 = s[2 * ks + (r >> 1)][(r & 1) * 2];
-                    const float x1 = s[2 * ks + (r >> 1)][(r & 1) * 2 + 1];
-                    ph[r] = Mma<KV>::pack(x0, x1);
-                    float h0, h1;
-                    Mma<KV>::unpack(ph[r], h0, h1);
-                    pl[r] = Mma<KV>::pack(x0 - h0, x1 - h1);
-                }
-#pragma unroll
-                for (int n = 0; n < ONT; n += 2) {
-                    uint32_t b0, b1, b2, b3;
-                    const int t = ks * 16 + ((ldsm_m & 1) << 3) + ldsm_t;
-                    ldsm_x4_trans(vbase + swz<BS>(t, col0 + n + (ldsm_m >> 1)), b0, b1, b2, b3);
-                    Mma<KV>::mma(acc[n], ph, b0, b1);
-                    Mma<KV>::mma(acc[n], pl, b0, b1);
-                    Mma<KV>::mma(acc[n + 1], ph, b2, b3);
-                    Mma<KV>::mma(acc[n + 1], pl, b2, b3);
-                }
-            }
-        }
-        __syncwarp();
-        // A stream of one warp frees its own stage; with two, both must be done.
-        if (DS > 1 && lane == 0) mbar_arrive(smem_u32(empty + sidx));
-        // Refill the stage just released with this stream's page i + ns.
-        int refill_failed = 0;
-        if (ds == 0 && i + p.ns < n_s) {
-            const bool freed = DS == 1 || __all_sync(
-                kFullMask, mbar_wait_bounded(smem_u32(empty + sidx), par, p.timeout_ns));
-            if (freed) {
-                fence_proxy_async_smem();
-                issue(i + p.ns, sidx);
-                ++n_issued;
-            } else {
-                if (lane == 0) record_error(p.err, PA_ERR_TIMEOUT);
-                refill_failed = 1;
-            }
-        }
-        if (++slot == p.ns) {
-            slot = 0;
-            par ^= 1u;
-        }
-        if (__shfl_sync(kFullMask, refill_failed, 0)) {
-            aborted = true;
-            ++i;
-            break;
-        }
-    }
-    if (aborted && leader) {
-        // Let copies this stream still has in flight land before the CTA exits.
-        for (int k = i; k < n_issued; ++k)
-            (void)mbar_wait_bounded(smem_u32(full + stream * p.ns + k % p.ns),
-                                    (uint32_t)(k / p.ns) & 1u, p.timeout_ns);
-    }
-
-    // ---- per-warp normalisers: sum the quad's shares ----
-    l0 += __shfl_xor_sync(kFullMask, l0, 1);
-    l1 += __shfl_xor_sync(kFullMask, l1, 1);
-    l0 += __shfl_xor_sync(kFullMask, l0, 2);
-    l1 += __shfl_xor_sync(kFullMask, l1, 2);
-
-    // Every stage has been consumed: the stage area now holds the merge data.
-    __syncthreads();
-    const int nw = p.nt * DS;
-    float* macc = reinterpret_cast<float*>(smem + L.stages_off);   // [nw][G][DW]
-    float* mm = macc + (size_t)nw * G * DW;                         // [nw][G]
-    float* ml = mm + nw * G;                                        // [nw][G]
-    float* cpart = ml + nw * G;  // this CTA's partial when the cluster reduces: acc [G][D], m [G], l [G]
-#pragma unroll
-    for (int n = 0; n < ONT; ++n) {
-        const int c = n * 8 + tig * 2;
-        if (real0)
-            *reinterpret_cast<float2*>(macc + ((size_t)warp * G + g) * DW + c) =
-                make_float2(acc[n][0], acc[n][1]);
-        if (real1)
-            *reinterpret_cast<float2*>(macc + ((size_t)warp * G + g + 8) * DW + c) =
-                make_float2(acc[n][2], acc[n][3]);
-    }
-    if (tig == 0) {
-        if (real0) {
-            mm[warp * G + g] = m0;
-            ml[warp * G + g] = l0;
-        }
-        if (real1) {
-            mm[warp * G + g + 8] = m1;
-            ml[warp * G + g + 8] = l1;
-        }
-    }
-    __syncthreads();
-
-    // ---- merge the token streams (log-sum-exp), then write ----
-    for (int idx = tid; idx < G * D; idx += blockDim.x) {
-        const int r = idx / D, d = idx % D;
-        const int dsx = d / DW, dd = d % DW;
-        float M = NEG_INF;
-        for (int s2 = 0; s2 < p.nt; ++s2) M = fmaxf(M, mm[(s2 * DS + dsx) * G + r]);
-        float A = 0.f, Ls = 0.f;
-        if (M != NEG_INF) {
-            for (int s2 = 0; s2 < p.nt; ++s2) {
-                const int w2 = s2 * DS + dsx;
-                const float ms = mm[w2 * G + r];
-                if (ms != NEG_INF) {
-                    const float f = exp2f(ms - M);
-                    A = fmaf(f, macc[((size_t)w2 * G + r) * DW + dd], A);
-                    Ls = fmaf(f, ml[w2 * G + r], Ls);
-                }
-            }
-        }
-        const int h = kvh * G + r;
-        if (p.final_out) {
-            store_out(p.out, ((size_t)b * p.num_heads + h) * D + d, Ls > 0.f ? A / Ls : 0.f,
-                      p.out_dtype);
-        } else if (p.cluster_reduce) {
+    if (p.final_out) {
+        run_segment(b, kvh, pb, max(pb, pe), T, emit_final(b, kvh));
+    } else if (p.cluster_reduce) {
+        run_segment(b, kvh, pb, max(pb, pe), T, [&](int idx, float A, float M, float Ls) {
             cpart[idx] = A;
-            if (d == 0) {
-                cpart[G * D + r] = M;
-                cpart[G * D + G + r] = Ls;
+            if (idx % D == 0) {
+                cpart[G * D + idx / D] = M;
+                cpart[G * D + G + idx / D] = Ls;
             }
-        } else {
-            const size_t row = (((size_t)b * p.num_kv_heads + kvh) * p.num_parts + part) * G + r;
-            p.part_acc[row * D + d] = A;
-            if (d == 0) {
-                p.part_ml[row * 2] = M;
-                p.part_ml[row * 2 + 1] = Ls;
-            }
-        }
+        });
+    } else {
+        run_segment(b, kvh, pb, max(pb, pe), T,
+                    emit_rows((((size_t)b * p.num_kv_heads + kvh) * p.num_parts + part) * G));
     }
 
     if (p.cluster_reduce) {

@@ -104,6 +104,125 @@ __global__ void __launch_bounds__(kCombineThreads) combine_kernel(const CombineP
     }
 }
 
+// Combine for the balanced split: the attention kernel's CTA c covered pages
+// [c*W/C, (c+1)*W/C) of the flattened (sequence, kv head, page) order and
+// wrote every unit it covered whole; a unit spread over CTAs c0..c1 left one
+// record in each: slot 1 of c0 when the unit began inside c0's range (slot 0
+// when exactly at its start), slot 0 of every later CTA.  One CTA per (query
+// head, sequence) finds its unit's CTAs from the same arithmetic and merges
+// their records as the partition combine does.
+template <int D>
+__global__ void __launch_bounds__(kCombineThreads) combine_balanced_kernel(const CombineParams p) {
+    constexpr int SLICES = D / 4;
+    constexpr int PGRP = kCombineThreads / SLICES;
+    constexpr float NEG_INF = -INFINITY;
+    extern __shared__ float weight[];                  // [records]
+    __shared__ float red[kCombineThreads / 32];
+    __shared__ float4 part[PGRP][SLICES];
+    __shared__ long long span[2];                      // W, flat start of sequence b
+    grid_dependency_wait();
+    grid_launch_dependents();
+
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    const int h = blockIdx.x, b = blockIdx.y;
+    const int Hkv = p.num_kv_heads;
+    const int kvh = h / p.group, g = h % p.group;
+    if (warp == 0) {
+        long long all = 0, before = 0;
+        for (int b0 = lane; b0 < p.batch; b0 += 32) {
+            const int T = reachable_tokens(p.context_lens, b0, p.max_blocks, p.block_size);
+            const int np = (T + p.block_size - 1) / p.block_size;
+            all += np;
+            if (b0 < b) before += np;
+        }
+#pragma unroll
+        for (int m = 16; m >= 1; m >>= 1) {
+            all += __shfl_xor_sync(kFullMask, all, m);
+            before += __shfl_xor_sync(kFullMask, before, m);
+        }
+        if (lane == 0) {
+            span[0] = all * Hkv;
+            span[1] = before * Hkv;
+        }
+    }
+    __syncthreads();
+    const long long W = span[0];
+    const int T = reachable_tokens(p.context_lens, b, p.max_blocks, p.block_size);
+    const int np = (T + p.block_size - 1) / p.block_size;
+    const size_t o = ((size_t)b * p.num_heads + h) * D;
+    if (np == 0) {  // no page, no CTA: the empty-context result
+        for (int d = tid; d < D; d += kCombineThreads) store_out(p.out, o + d, 0.f, p.out_dtype);
+        return;
+    }
+    const long long Cn = p.num_ctas;
+    const long long A = span[1] + (long long)kvh * np, E = A + np;
+    const long long c0 = ((A + 1) * Cn - 1) / W, c1 = (E * Cn - 1) / W;
+    if (c0 == c1) return;  // one CTA covered the unit and wrote it
+    const int nrec = (int)(c1 - c0 + 1);
+    const bool c0_tail = A != c0 * W / Cn;
+    auto rec_row = [&](int k) -> size_t {
+        const long long c = c0 + k;
+        const int slotk = (k == 0 && c0_tail) ? 1 : 0;
+        return ((size_t)c * 2 + slotk) * p.group + g;
+    };
+    const float2* ml = reinterpret_cast<const float2*>(p.part_ml);
+
+    float mx = NEG_INF;
+    for (int k = tid; k < nrec; k += kCombineThreads) mx = fmaxf(mx, ml[rec_row(k)].x);
+#pragma unroll
+    for (int m = 16; m >= 1; m >>= 1) mx = fmaxf(mx, __shfl_xor_sync(kFullMask, mx, m));
+    if (lane == 0) red[warp] = mx;
+    __syncthreads();
+    mx = red[0];
+#pragma unroll
+    for (int w = 1; w < kCombineThreads / 32; ++w) mx = fmaxf(mx, red[w]);
+    __syncthreads();
+    float ls = 0.f;
+    for (int k = tid; k < nrec; k += kCombineThreads) {
+        const float2 v = ml[rec_row(k)];
+        const float w = (v.x == NEG_INF) ? 0.f : exp2f(v.x - mx);
+        weight[k] = w;
+        ls = fmaf(w, v.y, ls);
+    }
+#pragma unroll
+    for (int m = 16; m >= 1; m >>= 1) ls += __shfl_xor_sync(kFullMask, ls, m);
+    if (lane == 0) red[warp] = ls;
+    __syncthreads();  // also publishes `weight`
+    ls = 0.f;
+#pragma unroll
+    for (int w = 0; w < kCombineThreads / 32; ++w) ls += red[w];
+
+    const bool empty = (mx == NEG_INF) || !(ls > 0.f);
+    const int pg = tid / SLICES, sl = tid % SLICES;
+    float4 a = make_float4(0.f, 0.f, 0.f, 0.f);
+    if (!empty) {
+        for (int k = pg; k < nrec; k += PGRP) {
+            const float w = weight[k];
+            const float4 x = reinterpret_cast<const float4*>(p.part_acc + rec_row(k) * D)[sl];
+            a.x = fmaf(w, x.x, a.x);
+            a.y = fmaf(w, x.y, a.y);
+            a.z = fmaf(w, x.z, a.z);
+            a.w = fmaf(w, x.w, a.w);
+        }
+    }
+    part[pg][sl] = a;
+    __syncthreads();
+    if (pg == 0) {
+        for (int k = 1; k < PGRP; ++k) {
+            const float4 x = part[k][sl];
+            a.x += x.x;
+            a.y += x.y;
+            a.z += x.z;
+            a.w += x.w;
+        }
+        const float inv = empty ? 0.f : 1.f / ls;
+        store_out(p.out, o + sl * 4, a.x * inv, p.out_dtype);
+        store_out(p.out, o + sl * 4 + 1, a.y * inv, p.out_dtype);
+        store_out(p.out, o + sl * 4 + 2, a.z * inv, p.out_dtype);
+        store_out(p.out, o + sl * 4 + 3, a.w * inv, p.out_dtype);
+    }
+}
+
 // Append of one new token per sequence (MiniVLLM docs "Decoding Benchmark":
 // each decode step stores the new token's keys/values in the block the table
 // assigns, at slot position % block_size).  One CTA per sequence copies the
@@ -167,6 +286,33 @@ cudaError_t launch_combine(const CombineParams& p, int head_dim, dim3 grid, bool
         default: kern = combine_kernel<256>; break;
     }
     const uint32_t smem = (uint32_t)p.num_parts * sizeof(float);
+    if (smem > 48 * 1024) {
+        cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                             (int)smem);
+        if (e != cudaSuccess) return e;
+    }
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = grid;
+    cfg.blockDim = dim3(kCombineThreads);
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = pdl ? 1 : 0;
+    return cudaLaunchKernelEx(&cfg, kern, p);
+}
+
+cudaError_t launch_combine_balanced(const CombineParams& p, int head_dim, dim3 grid, bool pdl,
+                                    cudaStream_t stream) {
+    void (*kern)(const CombineParams);
+    switch (head_dim) {
+        case 64: kern = combine_balanced_kernel<64>; break;
+        case 128: kern = combine_balanced_kernel<128>; break;
+        default: kern = combine_balanced_kernel<256>; break;
+    }
+    const uint32_t smem = (uint32_t)(p.num_ctas + 1) * sizeof(float);
     if (smem > 48 * 1024) {
         cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                              (int)smem);

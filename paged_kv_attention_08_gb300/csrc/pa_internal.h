@@ -32,6 +32,9 @@ struct AttnParams {
     int32_t ns;               // pipeline stages per stream
     int32_t out_dtype;        // pa_dtype
     int32_t final_out;        // 1: write out (one partition); 0: partitions reduce elsewhere
+    int32_t balanced;         // 1: CTA c takes pages [c*W/C, (c+1)*W/C) of the flattened
+                              //    (sequence, kv head, page) order; units it covers whole are
+                              //    written out, pieces become records [C][2][G] in part_acc/ml
     int32_t cluster_reduce;   // 1: the num_parts partitions of a (sequence, kv head) form one
                               //    thread-block cluster and reduce through distributed shared
                               //    memory; 0: partials go to the workspace for the combine kernel
@@ -45,7 +48,12 @@ struct CombineParams {
     const float* part_ml;
     int32_t batch, num_heads, num_kv_heads, group, max_blocks, block_size;
     int32_t part_pages, num_parts, out_dtype;
+    int32_t num_ctas;  // balanced split: CTAs of the attention kernel (records [C][2][G])
 };
+
+// Largest batch the balanced split handles (its per-sequence page counts live
+// in shared memory).
+constexpr int kMaxBalancedBatch = 512;
 
 // Shared-memory layout of the attention kernel, identical on host and device.
 // Each stage holds one page of one kv head: the K tile then the V tile, each
@@ -59,8 +67,11 @@ struct AttnSmem {
     uint32_t full_off;      // [nt][ns] uint64 mbarriers: page landed
     uint32_t empty_off;     // [nt][ns] uint64 mbarriers: page consumed
     uint32_t phys_off;      // [nt][ns] int32 physical block of the staged page (-1 = masked)
+    uint32_t seq_off;       // balanced split: pages of each sequence, then the total
     uint32_t total;         // bytes, excluding the alignment slack
 };
+
+
 
 __host__ __device__ inline uint32_t pa_align_up(uint32_t x, uint32_t a) { return (x + a - 1) / a * a; }
 
@@ -75,7 +86,9 @@ __host__ __device__ inline AttnSmem attn_smem_layout(int D, int BS, int nt, int 
     L.empty_off = o;
     o += 8u * nt * ns;
     L.phys_off = o;
-    o += 4u * nt * ns;
+    o = pa_align_up(o + 4u * nt * ns, 16);
+    L.seq_off = o;
+    o += 4u * (kMaxBalancedBatch + 1);
     L.total = pa_align_up(o, 16);
     return L;
 }
@@ -117,6 +130,8 @@ cudaError_t launch_attn_d256(const AttnLaunch& L, cudaStream_t stream);
 
 cudaError_t launch_combine(const CombineParams& p, int head_dim, dim3 grid, bool pdl,
                            cudaStream_t stream);
+cudaError_t launch_combine_balanced(const CombineParams& p, int head_dim, dim3 grid, bool pdl,
+                                    cudaStream_t stream);
 cudaError_t launch_append(void* k_cache, void* v_cache, const void* k_new, const void* v_new,
                           const int32_t* block_tables, const int32_t* positions, int32_t batch,
                           int32_t max_blocks, int32_t block_size, int64_t num_blocks,

@@ -89,6 +89,8 @@ def test_pointer_validation(lib):
                                  FAKE, 1 << 20, None) == 1
     assert lib.pa_decode_splitkv(FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, ctypes.byref(s), 0.1, 100, 24,
                                  FAKE, 1 << 20, None) == 1
+    assert lib.pa_decode_splitkv(FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, ctypes.byref(s), 0.1, 100, -2,
+                                 FAKE, 1 << 20, None) == 1
     # an empty batch is a no-op, whatever the pointers
     e = shape(batch=0)
     assert lib.pa_decode(None, None, None, None, None, None, ctypes.byref(e), 0.1, None) == 0
@@ -130,7 +132,7 @@ def test_partition_choice_properties(lib, B, T, Hkv):
               max_blocks_per_seq=(T + bs - 1) // bs)
     for sms in (1, 8, 148, 152):
         pt = lib.pa_choose_partition_tokens(ctypes.byref(s), T, sms)
-        assert pt > 0 and pt % bs == 0
+        assert pt == pa.PARTITION_BALANCED or (pt > 0 and pt % bs == 0)
         assert pt <= ((T + bs - 1) // bs) * bs
     # a grid that already fills the GPU is only cut into partitions of ~64 pages
     pages = (T + bs - 1) // bs
@@ -148,11 +150,11 @@ def test_single_sequence_long_context_is_split(lib):
 
 
 def test_small_grids_reduce_in_a_cluster(lib):
-    # batch 4 x 8 kv heads x 2048 tokens on 152 SMs: 4 partitions, no workspace needed
-    s = shape(batch=4, max_blocks_per_seq=128)
-    pt = lib.pa_choose_partition_tokens(ctypes.byref(s), 2048, 152)
-    assert -(-2048 // pt) == 4
-    assert lib.pa_workspace_size(ctypes.byref(s), 2048, pt) == 0
+    # batch 1 x 8 kv heads x 512 tokens: too few pages to balance; 8 partitions in a cluster
+    s = shape(batch=1, max_blocks_per_seq=32)
+    pt = lib.pa_choose_partition_tokens(ctypes.byref(s), 512, 152)
+    assert -(-512 // pt) == 8
+    assert lib.pa_workspace_size(ctypes.byref(s), 512, pt) == 0
 
 
 def test_binding_refuses_cpu_tensors():

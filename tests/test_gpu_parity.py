@@ -162,6 +162,30 @@ def test_cluster_split_sizes(shape, parts):
     assert_close_fp32(run(xd, "split", partition_tokens=pt), want)
 
 
+BALANCED_CASES = [
+    dict(B=9, H=8, Hkv=2, D=128, bs=16, lens=[300, 0, 17, 1, 2000, 64, 0, 999, 15]),
+    dict(B=3, H=16, Hkv=1, D=256, bs=32, lens=[5000, 31, 2900]),
+    dict(B=5, H=8, Hkv=8, D=64, bs=16, lens=[1, 2, 3, 4, 5]),
+    dict(B=1, H=32, Hkv=8, D=128, bs=32, lens=[7777]),
+    dict(B=4, H=16, Hkv=2, D=64, bs=32, lens=[0, 0, 0, 0]),
+]
+
+
+@pytest.mark.parametrize("dtype", [torch.float16, torch.bfloat16])
+@pytest.mark.parametrize("case", BALANCED_CASES, ids=lambda s: f"B{s['B']}H{s['H']}kv{s['Hkv']}D{s['D']}")
+def test_balanced_split(case, dtype):
+    """The balanced split: equal shares of all pages per SM, straddling pieces
+    combined afterwards (empty sequences, one-page units, units spread over
+    many CTAs, CTAs holding several whole units)."""
+    x = random_case(11, dtype=dtype, **case)
+    want = oracle.decode(x.q, x.k_cache, x.v_cache, x.block_tables, x.context_lens, x.scale)
+    xd = x.to(DEV)
+    assert pa.workspace_size(xd.q, xd.k_cache, xd.block_tables, torch.float32,
+                             xd.max_context_len, pa.PARTITION_BALANCED) > 0
+    for _ in range(2):      # the second call reuses the workspace records
+        assert_close_fp32(run(xd, "split", partition_tokens=pa.PARTITION_BALANCED), want)
+
+
 # ---------------------------------------------------------------------------
 # edge cases and invariances
 # ---------------------------------------------------------------------------
@@ -239,7 +263,7 @@ def test_split_count_invariance():
                               host.context_lens, host.scale, rows)
     outs = []
     for mode, pt in [("single", 0), ("split", 16), ("split", 256), ("split", 512), ("split", 4096),
-                     ("split", 0)]:
+                     ("split", 0), ("split", pa.PARTITION_BALANCED)]:
         got = run(x, mode, partition_tokens=pt)
         assert_close_fp32(got[rows[:, 0], rows[:, 1]], want)
         outs.append(got)
