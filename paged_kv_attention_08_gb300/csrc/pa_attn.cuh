@@ -39,8 +39,6 @@
 //     PA_ERR_TIMEOUT in the device error word and abandons its work.
 #pragma once
 
-#include <cooperative_groups.h>
-
 #include "pa_device.cuh"
 
 namespace pa {
@@ -115,8 +113,8 @@ __global__ void __launch_bounds__(256, 1)
     const int nw = p.nt * DS;
     // After a segment's pages are consumed the stage area holds the merge data.
     float* macc = reinterpret_cast<float*>(smem + L.stages_off);   // [nw][G][DW]
-    float* mm = macc + (size_t)nw * G * DW;                         // [nw][G]
-    float* mls = mm + nw * G;                                       // [nw][G]
+    float* mm = macc + (size_t)nw * G * DW;                         // [nw][G] running max
+    float* mls = mm + nw * G;                                       // [nw][G] normaliser
     float* cpart = mls + nw * G;  // this CTA's partial when the cluster reduces: acc [G][D], m [G], l [G]
 
     // Pipeline state of this warp's stream, carried across segments.
@@ -420,16 +418,12 @@ __global__ void __launch_bounds__(256, 1)
             float M = NEG_INF;
             for (int s2 = 0; s2 < p.nt; ++s2) M = fmaxf(M, mm[(s2 * DS + dsx) * G + r]);
             float A = 0.f, Ls = 0.f;
-            if (M != NEG_INF) {
-                for (int s2 = 0; s2 < p.nt; ++s2) {
-                    const int w2 = s2 * DS + dsx;
-                    const float ms = mm[w2 * G + r];
-                    if (ms != NEG_INF) {
-                        const float f = exp2f(ms - M);
-                        A = fmaf(f, macc[((size_t)w2 * G + r) * DW + dd], A);
-                        Ls = fmaf(f, mls[w2 * G + r], Ls);
-                    }
-                }
+            for (int s2 = 0; s2 < p.nt; ++s2) {
+                const int w2 = s2 * DS + dsx;
+                const float ms = mm[w2 * G + r];
+                const float f = (ms == NEG_INF) ? 0.f : fast_exp2(ms - M);
+                A = fmaf(f, macc[((size_t)w2 * G + r) * DW + dd], A);
+                Ls = fmaf(f, mls[w2 * G + r], Ls);
             }
             emit(idx, A, M, Ls);
         }
@@ -569,36 +563,47 @@ __global__ void __launch_bounds__(256, 1)
     }
 
     if (p.cluster_reduce) {
-        // Log-sum-exp over the cluster's partitions, read from each CTA's
-        // shared memory; each CTA finalises a 1/P share of the outputs.
-        namespace cg = cooperative_groups;
-        cg::cluster_group cluster = cg::this_cluster();
-        cluster.sync();
+        // Log-sum-exp over the cluster's partitions through distributed shared
+        // memory: each CTA finalises a 1/P share of the outputs; for an
+        // element, the (m, l, acc) of every rank are loaded at once.
+        cluster_sync_release_acquire();  // every CTA's partial is in place
         const int P = p.num_parts;
-        const int rank = (int)cluster.block_rank();
+        const uint32_t rank = (uint32_t)blockIdx.x;  // the cluster spans grid x
+        const uint32_t cp = smem_u32(cpart);
+        uint32_t rbase[kMaxClusterParts];
+#pragma unroll
+        for (int q = 0; q < kMaxClusterParts; ++q)
+            rbase[q] = q < P ? map_cluster_rank(cp, (uint32_t)q) : cp;
         const int chunk = (G * D + P - 1) / P;
-        const int i1 = min((rank + 1) * chunk, G * D);
-        for (int idx = rank * chunk + tid; idx < i1; idx += blockDim.x) {
+        const int i1 = min(((int)rank + 1) * chunk, G * D);
+        for (int idx = (int)rank * chunk + tid; idx < i1; idx += blockDim.x) {
             const int r = idx / D;
+            float m[kMaxClusterParts], l[kMaxClusterParts], a[kMaxClusterParts];
+#pragma unroll
+            for (int q = 0; q < kMaxClusterParts; ++q) {
+                if (q < P) {
+                    m[q] = ld_cluster_f32(rbase[q] + 4u * (G * D + r));
+                    l[q] = ld_cluster_f32(rbase[q] + 4u * (G * D + G + r));
+                    a[q] = ld_cluster_f32(rbase[q] + 4u * idx);
+                }
+            }
             float M = NEG_INF;
-            for (int q = 0; q < P; ++q)
-                M = fmaxf(M, cluster.map_shared_rank(cpart, q)[G * D + r]);
+#pragma unroll
+            for (int q = 0; q < kMaxClusterParts; ++q)
+                if (q < P) M = fmaxf(M, m[q]);
             float A = 0.f, Ls = 0.f;
-            if (M != NEG_INF) {
-                for (int q = 0; q < P; ++q) {
-                    const float* rp = cluster.map_shared_rank(cpart, q);
-                    const float mq = rp[G * D + r];
-                    if (mq != NEG_INF) {
-                        const float f = exp2f(mq - M);
-                        A = fmaf(f, rp[idx], A);
-                        Ls = fmaf(f, rp[G * D + G + r], Ls);
-                    }
+#pragma unroll
+            for (int q = 0; q < kMaxClusterParts; ++q) {
+                if (q < P && m[q] != NEG_INF) {
+                    const float f = fast_exp2(m[q] - M);
+                    A = fmaf(f, a[q], A);
+                    Ls = fmaf(f, l[q], Ls);
                 }
             }
             store_out(p.out, ((size_t)b * p.num_heads + kvh * G) * D + idx,
                       Ls > 0.f ? A / Ls : 0.f, p.out_dtype);
         }
-        cluster.sync();  // no CTA leaves while others still read its shared memory
+        cluster_sync_relaxed();  // no CTA leaves while others still read its shared memory
     }
 }
 

@@ -196,6 +196,29 @@ __device__ __forceinline__ float fast_exp2(float x) {
     return y;
 }
 
+// Thread-block cluster barrier.  arrive.release / wait.acquire publishes this
+// CTA's shared-memory writes to the cluster; the relaxed form only waits.
+__device__ __forceinline__ void cluster_sync_release_acquire() {
+    asm volatile("barrier.cluster.arrive.release.aligned;\n\tbarrier.cluster.wait.acquire.aligned;" ::
+                     : "memory");
+}
+__device__ __forceinline__ void cluster_sync_relaxed() {
+    asm volatile("barrier.cluster.arrive.relaxed.aligned;\n\tbarrier.cluster.wait.aligned;" ::
+                     : "memory");
+}
+// Address of the same shared-memory location in CTA `rank` of the cluster,
+// and a load through it (distributed shared memory).
+__device__ __forceinline__ uint32_t map_cluster_rank(uint32_t smem_addr, uint32_t rank) {
+    uint32_t r;
+    asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(r) : "r"(smem_addr), "r"(rank));
+    return r;
+}
+__device__ __forceinline__ float ld_cluster_f32(uint32_t addr) {
+    float v;
+    asm volatile("ld.shared::cluster.f32 %0, [%1];" : "=f"(v) : "r"(addr) : "memory");
+    return v;
+}
+
 template <typename KV>
 struct Mma;
 

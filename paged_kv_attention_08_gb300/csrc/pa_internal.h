@@ -94,14 +94,15 @@ __host__ __device__ inline AttnSmem attn_smem_layout(int D, int BS, int nt, int 
 }
 
 // Floats the final merge needs in the stage area: per warp, acc rows of the
-// group's heads over that warp's output columns, then m and l per head; then
-// the CTA's merged partial (acc [G][D], m [G], l [G]) that the other CTAs of a
-// cluster read.
+// group's heads over that warp's output columns, m and l per head, the
+// streams' weights and per-row totals; then the CTA's merged partial
+// (acc [G][D], m [G], l [G]) that the other CTAs of a cluster read, and the
+// cluster's per-rank statistics.
 __host__ __device__ inline uint32_t merge_floats(int nw, int G, int cols_per_warp) {
-    return (uint32_t)nw * G * cols_per_warp + 2u * nw * G;
+    return (uint32_t)nw * G * cols_per_warp + 3u * nw * G + 4u * G;
 }
 __host__ __device__ inline uint32_t cluster_part_floats(int G, int D) {
-    return (uint32_t)G * D + 2u * G;
+    return (uint32_t)G * D + 2u * G + 3u * 8u * G;
 }
 
 // Most partitions of one (sequence, kv head) reduced inside a cluster.
