@@ -439,9 +439,10 @@ def main(argv=None):
 
     # ---- end to end: host buffers, copies inside the timed region ----
     # Every input of the step (q, K, V, tables, lengths of each workload) sits
-    # in one pinned host buffer and every output in another; a step copies the
-    # inputs to the device in one transfer, runs the decode calls through the
-    # public API on views of that device buffer, and copies the outputs back.
+    # in one pinned host buffer; a step copies the inputs to the device in one
+    # transfer, runs the decode calls through the public API on views of that
+    # device buffer, and copies the outputs back to pinned host memory.  Steps
+    # are double-buffered: a step's input copy overlaps the previous decode.
     e2e = None
     if not args.no_e2e:
         host = [x.to("cpu") for x in set0]
@@ -457,43 +458,62 @@ def main(argv=None):
         for (_, _, t), o in zip(fields, offs):
             n = t.numel() * t.element_size()
             pin_in[o:o + n].copy_(t.contiguous().view(-1).view(torch.uint8))
-        dev_in = torch.empty(total, dtype=torch.uint8, device=dev)
-        views = [dict() for _ in host]
-        for (i, name, t), o in zip(fields, offs):
-            n = t.numel() * t.element_size()
-            views[i][name] = dev_in[o:o + n].view(t.dtype).view(t.shape)
+        # two device copies of the inputs and outputs: step k+1's inputs
+        # arrive (copy stream) while step k decodes (compute stream)
         out_elems = [x.q.numel() for x in set0]
         out_offs = [sum(out_elems[:i]) for i in range(len(out_elems))]
-        dev_out = torch.empty(sum(out_elems), dtype=torch.float32, device=dev)
-        pin_out = torch.empty(sum(out_elems), dtype=torch.float32).pin_memory()
-        h2d, d2h = total, pin_out.numel() * 4
-        e2e_steps = max(3, min(args.steps, 50))
-        with torch.cuda.stream(stream):
-            def e2e_step():
-                dev_in.copy_(pin_in, non_blocking=True)
+        nbuf = 2
+        dev_in = [torch.empty(total, dtype=torch.uint8, device=dev) for _ in range(nbuf)]
+        dev_out = [torch.empty(sum(out_elems), dtype=torch.float32, device=dev) for _ in range(nbuf)]
+        pin_out = [torch.empty(sum(out_elems), dtype=torch.float32).pin_memory() for _ in range(nbuf)]
+        views = [[dict() for _ in host] for _ in range(nbuf)]
+        for k in range(nbuf):
+            for (i, name, t), o in zip(fields, offs):
+                n = t.numel() * t.element_size()
+                views[k][i][name] = dev_in[k][o:o + n].view(t.dtype).view(t.shape)
+        ws2 = [[torch.empty_like(w) for w in ws] for _ in range(nbuf)]
+        h2d, d2h = total, pin_out[0].numel() * 4
+        e2e_steps = max(4, min(args.steps, 50))
+        copy_stream = torch.cuda.Stream(device=dev)
+        copied = [torch.cuda.Event() for _ in range(nbuf)]
+        consumed = [torch.cuda.Event() for _ in range(nbuf)]
+
+        def e2e_step(k):
+            buf = k % nbuf
+            with torch.cuda.stream(copy_stream):
+                copy_stream.wait_event(consumed[buf])          # the decode of step k-2 is done
+                dev_in[buf].copy_(pin_in, non_blocking=True)
+                copied[buf].record(copy_stream)
+            stream.wait_event(copied[buf])
+            with torch.cuda.stream(stream):
                 for i, x in enumerate(set0):
-                    v = views[i]
-                    o = dev_out[out_offs[i]:out_offs[i] + out_elems[i]].view(x.q.shape)
+                    v = views[buf][i]
+                    o = dev_out[buf][out_offs[i]:out_offs[i] + out_elems[i]].view(x.q.shape)
                     pa.decode_splitkv(o, v["q"], v["k_cache"], v["v_cache"], v["block_tables"],
                                       v["context_lens"], x.scale, x.max_context_len, pts[i],
-                                      workspace=ws[i], stream=stream)
-                pin_out.copy_(dev_out, non_blocking=True)
-            for _ in range(3):
-                e2e_step()
-            stream.synchronize()
-            barrier()
-            a = torch.cuda.Event(enable_timing=True)
-            b = torch.cuda.Event(enable_timing=True)
-            a.record(stream)
-            for _ in range(e2e_steps):
-                e2e_step()
-            b.record(stream)
-            b.synchronize()
+                                      workspace=ws2[buf][i], stream=stream)
+                pin_out[buf].copy_(dev_out[buf], non_blocking=True)
+                consumed[buf].record(stream)
+
+        for k in range(nbuf):
+            consumed[k].record(stream)
+        for k in range(3):
+            e2e_step(k)
+        torch.cuda.synchronize()
+        barrier()
+        a = torch.cuda.Event(enable_timing=True)
+        b = torch.cuda.Event(enable_timing=True)
+        a.record(stream)
+        copy_stream.wait_event(a)
+        for k in range(e2e_steps):
+            e2e_step(k)
+        b.record(stream)
+        b.synchronize()
         ms_e2e = reduce_max(a.elapsed_time(b), dev) / e2e_steps
         e2e = {"value": total_bytes / (ms_e2e * 1e-3) / 1e9, "unit": "GB/s",
                "ms_per_step": ms_e2e, "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
-               "steps": e2e_steps,
-               "h2d_GBps": h2d / (ms_e2e * 1e-3) / 1e9}
+               "steps": e2e_steps, "h2d_GBps": h2d / (ms_e2e * 1e-3) / 1e9,
+               "pipeline": "2 buffers; step k+1 H2D (copy stream) overlaps step k decode"}
 
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
