@@ -1,5 +1,5 @@
-// Device helpers of the decode library: the page walk, mbarrier / TMA inline
-// PTX with bounded waits, and 16-byte vector conversions.
+// Device helpers of the decode library: the page walk, mbarrier / TMA /
+// cluster inline PTX with bounded waits, and the warp-level MMA pieces.
 #pragma once
 
 #include <cuda.h>
@@ -136,38 +136,6 @@ __device__ __forceinline__ void grid_launch_dependents() {
 __device__ __forceinline__ void record_error(int32_t* err, int32_t code) {
     if (err) atomicCAS(err, 0, code);
 }
-
-// ---------------------------------------------------------------------------
-// 16-byte vectors of eight fp16 / bf16 values -> fp32
-// ---------------------------------------------------------------------------
-template <typename KV>
-struct Vec8;
-
-template <>
-struct Vec8<__half> {
-    static __device__ __forceinline__ void to_float(const uint4& r, float (&f)[8]) {
-        const __half2* h = reinterpret_cast<const __half2*>(&r);
-#pragma unroll
-        for (int i = 0; i < 4; ++i) {
-            const float2 x = __half22float2(h[i]);
-            f[2 * i] = x.x;
-            f[2 * i + 1] = x.y;
-        }
-    }
-};
-
-template <>
-struct Vec8<__nv_bfloat16> {
-    static __device__ __forceinline__ void to_float(const uint4& r, float (&f)[8]) {
-        const __nv_bfloat162* h = reinterpret_cast<const __nv_bfloat162*>(&r);
-#pragma unroll
-        for (int i = 0; i < 4; ++i) {
-            const float2 x = __bfloat1622float2(h[i]);
-            f[2 * i] = x.x;
-            f[2 * i + 1] = x.y;
-        }
-    }
-};
 
 // ---------------------------------------------------------------------------
 // Warp-level tensor-core pieces: ldmatrix from shared memory and the

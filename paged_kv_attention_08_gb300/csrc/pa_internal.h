@@ -11,8 +11,6 @@
 
 namespace pa {
 
-// Up to this many query heads share one kv head (num_heads / num_kv_heads).
-constexpr int kMaxGroup = 16;
 
 struct AttnParams {
     const void* q;            // [B, H, D] kv dtype
