@@ -18,6 +18,9 @@ Parity status of each function (pins live in ``tests/test_oracle_pins.py``):
                           invariance, masking semantics.
   resolve_blocks       -- pinned: brute force over an independent per-page rule
                           and hand-written cases.
+  decode_multi         -- pinned: each query row equals the one-token decode of
+                          its causal prefix (bit-exact), q_len = 1 equals
+                          decode, dense brute force with an explicit causal mask.
   append_kv            -- pinned: exactly the addressed slots change (element
                           by element over the whole pool), invalid positions and
                           entries write nothing, append-then-decode equals the
@@ -73,6 +76,9 @@ def _load():
             lib.pao_decode_rows.restype = ctypes.c_int
             lib.pao_resolve_blocks.argtypes = [P, P, P, i32, i32, i32, i64]
             lib.pao_resolve_blocks.restype = ctypes.c_int
+            lib.pao_decode_multi.argtypes = [P, P, P, P, P, P, i32, i32, i32, i32, i32, i32, i32,
+                                             i64, i32, f64]
+            lib.pao_decode_multi.restype = ctypes.c_int
             lib.pao_append_kv.argtypes = [P, P, P, P, P, P, i32, i32, i32, i32, i32, i64]
             lib.pao_append_kv.restype = ctypes.c_int
             _lib = lib
@@ -178,3 +184,21 @@ def append_kv(k_cache, v_cache, k_new, v_new, block_tables, positions):
         raise RuntimeError("oracle append_kv rejected its arguments")
     to_t = lambda a: torch.from_numpy(a.view(np.int16).reshape(NB, bs, Hkv, D)).view(k_cache.dtype)
     return to_t(ka), to_t(va)
+
+
+def decode_multi(q, k_cache, v_cache, block_tables, context_lens, scale: float) -> np.ndarray:
+    """Several query tokens per sequence: q [B, Q, H, D] -> out [B, Q, H, D]
+    float64; query token i attends causally to tokens <= T - Q + i."""
+    if q.dim() != 4:
+        raise ValueError("q must be [batch, q_len, num_heads, head_dim]")
+    B, Q, H, D = q.shape
+    (_, _, Hkv, _, bs, mb, NB), bt, lens = _common(q[:, 0], k_cache, v_cache, block_tables,
+                                                  context_lens)
+    qa, ka, va = _u16(q), _u16(k_cache), _u16(v_cache)
+    out = np.zeros((B, Q, H, D), dtype=np.float64)
+    rc = _load().pao_decode_multi(_ptr(out), _ptr(qa), _ptr(ka), _ptr(va), _ptr(bt), _ptr(lens),
+                                  B, Q, H, Hkv, D, bs, mb, NB, _dtype_code(q),
+                                  float(np.float32(scale)))
+    if rc != 0:
+        raise RuntimeError("oracle decode_multi rejected its arguments")
+    return out

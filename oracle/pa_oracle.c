@@ -88,22 +88,18 @@ static int64_t pao_lookup(const int32_t* block_tables, int b, int64_t t, int blo
     return e;
 }
 
-/* Attention output of one (b, h) pair into out[0..head_dim).  Returns 0, or
- * -1 if scratch memory could not be had. */
-static int pao_one(double* out, const uint16_t* q, const uint16_t* k_cache,
-                   const uint16_t* v_cache, const int32_t* block_tables,
-                   const int32_t* context_lens, int b, int h, int num_heads, int num_kv_heads,
-                   int head_dim, int block_size, int max_blocks, int64_t num_blocks, int dtype,
-                   double scale) {
-    int group = num_heads / num_kv_heads;
-    int kvh = h / group;
-    int64_t n = pao_reachable(context_lens, b, block_size, max_blocks);
+/* Attention of one query row against tokens t < n of sequence b, kv head
+ * `kvh`, into out[0..head_dim).  `qoff` is the row's element offset in q.
+ * Returns 0, or -1 if scratch memory could not be had. */
+static int pao_attend(double* out, const uint16_t* q, size_t qoff, const uint16_t* k_cache,
+                      const uint16_t* v_cache, const int32_t* block_tables, int b, int kvh,
+                      int64_t n, int num_kv_heads, int head_dim, int block_size, int max_blocks,
+                      int64_t num_blocks, int dtype, double scale) {
     size_t row_stride = (size_t)num_kv_heads * head_dim;          /* one token slot */
     size_t block_stride = (size_t)block_size * row_stride;        /* one physical block */
-    const size_t qoff = ((size_t)b * num_heads + h) * head_dim;
 
     for (int d = 0; d < head_dim; ++d) out[d] = 0.0;
-    if (n == 0) return 0;
+    if (n <= 0) return 0;
 
     double* s = (double*)malloc(sizeof(double) * (size_t)n);
     unsigned char* keep = (unsigned char*)malloc((size_t)n);
@@ -147,6 +143,20 @@ static int pao_one(double* out, const uint16_t* q, const uint16_t* k_cache,
     free(s);
     free(keep);
     return 0;
+}
+
+/* Attention output of one (b, h) pair of a one-token decode. */
+static int pao_one(double* out, const uint16_t* q, const uint16_t* k_cache,
+                   const uint16_t* v_cache, const int32_t* block_tables,
+                   const int32_t* context_lens, int b, int h, int num_heads, int num_kv_heads,
+                   int head_dim, int block_size, int max_blocks, int64_t num_blocks, int dtype,
+                   double scale) {
+    int group = num_heads / num_kv_heads;
+    int kvh = h / group;
+    int64_t n = pao_reachable(context_lens, b, block_size, max_blocks);
+    const size_t qoff = ((size_t)b * num_heads + h) * head_dim;
+    return pao_attend(out, q, qoff, k_cache, v_cache, block_tables, b, kvh, n, num_kv_heads,
+                      head_dim, block_size, max_blocks, num_blocks, dtype, scale);
 }
 
 static int pao_shape_ok(int batch, int num_heads, int num_kv_heads, int head_dim, int block_size,
@@ -244,6 +254,40 @@ int pao_append_kv(uint16_t* k_cache, uint16_t* v_cache, const uint16_t* k_new,
         for (size_t i = 0; i < row; ++i) {
             k_cache[dst + i] = k_new[(size_t)b * row + i];
             v_cache[dst + i] = v_new[(size_t)b * row + i];
+        }
+    }
+    return 0;
+}
+
+/* Several query tokens per sequence (a multi-token decode step, e.g. the
+ * verification of drafted tokens): q and out are [batch, q_len, num_heads,
+ * head_dim]; context_lens[b] counts the q_len new tokens, which are already
+ * in the cache at positions T - q_len .. T - 1.  Query token i sits at
+ * position p = T - q_len + i and attends causally to the tokens t <= p that a
+ * table row reaches (the same masking as the one-token decode); a query with
+ * no attended token gets zeros.  With q_len = 1 this is pao_decode. */
+int pao_decode_multi(double* out, const uint16_t* q, const uint16_t* k_cache,
+                     const uint16_t* v_cache, const int32_t* block_tables,
+                     const int32_t* context_lens, int batch, int q_len, int num_heads,
+                     int num_kv_heads, int head_dim, int block_size, int max_blocks,
+                     int64_t num_blocks, int dtype, double scale) {
+    if (!pao_shape_ok(batch, num_heads, num_kv_heads, head_dim, block_size, max_blocks,
+                      num_blocks, dtype) || q_len <= 0)
+        return -1;
+    int group = num_heads / num_kv_heads;
+    for (int b = 0; b < batch; ++b) {
+        int64_t reach = pao_reachable(context_lens, b, block_size, max_blocks);
+        int64_t T = context_lens[b];
+        for (int i = 0; i < q_len; ++i) {
+            int64_t n = T - q_len + i + 1; /* tokens 0 .. p */
+            if (n > reach) n = reach;
+            for (int h = 0; h < num_heads; ++h) {
+                size_t row = ((size_t)b * q_len + i) * num_heads + h;
+                if (pao_attend(out + row * head_dim, q, row * head_dim, k_cache, v_cache,
+                               block_tables, b, h / group, n, num_kv_heads, head_dim, block_size,
+                               max_blocks, num_blocks, dtype, scale))
+                    return -1;
+            }
         }
     }
     return 0;

@@ -24,6 +24,7 @@ MUTANTS = {
     "no_normalisation": ("out[d] /= wsum;", "out[d] /= 1.0;"),
     "clamp_off_by_one": ("if (t > cap) t = cap;", "if (t > cap) t = cap - 1;"),
     "q_head_offset": ("((size_t)b * num_heads + h) * head_dim;", "((size_t)b * num_heads + kvh) * head_dim;"),
+    "causal_off_by_one": ("int64_t n = T - q_len + i + 1; /* tokens 0 .. p */", "int64_t n = T - q_len + i; /* tokens 0 .. p */"),
     "append_slot_index": ("(size_t)(pos % block_size)) * row", "(size_t)(pos / block_size % block_size)) * row"),
     "append_values_from_keys": ("v_cache[dst + i] = v_new[", "v_cache[dst + i] = k_new["),
 }

@@ -313,3 +313,46 @@ def test_append_then_decode_equals_decode_with_token_in_place():
     k2, v2 = oracle.append_kv(k, v, kn, vn, bt, pos)
     np.testing.assert_array_equal(oracle.decode(q, k2, v2, bt, pos + 1, scale),
                                   oracle.decode(q, kh, vh, bt, pos + 1, scale))
+
+
+# --------------------------------------------------------------------------
+# several query tokens per sequence (causal over the new tokens)
+# --------------------------------------------------------------------------
+def test_multi_token_rows_equal_one_token_decodes_of_their_prefix():
+    B, Q, H, Hkv, D, bs = 3, 4, 8, 2, 16, 4
+    _, k, v, bt, lens, scale = small_case(21, B=B, H=H, Hkv=Hkv, D=D, bs=bs, lens=[9, 14, 3])
+    g = torch.Generator().manual_seed(22)
+    q = torch.randn(B, Q, H, D, generator=g).to(k.dtype)
+    got = oracle.decode_multi(q, k, v, bt, lens, scale)
+    for i in range(Q):
+        prefix = torch.clamp(lens - Q + i + 1, min=0)
+        want = oracle.decode(q[:, i].contiguous(), k, v, bt, prefix, scale)
+        np.testing.assert_array_equal(got[:, i], want)
+    assert np.all(got[2, :1] == 0)          # T = 3 < Q: the first query sees no token
+
+
+def test_multi_token_with_one_token_is_decode():
+    q, k, v, bt, lens, scale = small_case(23, B=2, H=4, Hkv=4, D=8, bs=2, lens=[5, 7])
+    np.testing.assert_array_equal(oracle.decode_multi(q[:, None], k, v, bt, lens, scale)[:, 0],
+                                  oracle.decode(q, k, v, bt, lens, scale))
+
+
+def test_multi_token_matches_causal_bruteforce():
+    B, Q, H, Hkv, D, bs = 2, 3, 6, 3, 8, 4
+    _, k, v, bt, lens, scale = small_case(24, B=B, H=H, Hkv=Hkv, D=D, bs=bs, lens=[10, 6])
+    q = torch.randn(B, Q, H, D, generator=torch.Generator().manual_seed(25)).to(k.dtype)
+    got = oracle.decode_multi(q, k, v, bt, lens, scale)
+    kd, vd, qd = (t.to(torch.float64).numpy() for t in (k, v, q))
+    sc = float(np.float32(scale))
+    for b in range(B):
+        T = int(lens[b])
+        toks = np.arange(T)
+        ent = bt.numpy()[b, toks // bs]
+        Kb, Vb = kd[ent, toks % bs], vd[ent, toks % bs]       # [T, Hkv, D]
+        for i in range(Q):
+            mask = toks <= T - Q + i
+            for h in range(H):
+                s = sc * (Kb[:, h // (H // Hkv)] @ qd[b, i, h])
+                s = np.where(mask, s, -np.inf)
+                np.testing.assert_allclose(got[b, i, h], scipy.special.softmax(s) @ Vb[:, h // (H // Hkv)],
+                                           rtol=0, atol=1e-12)
