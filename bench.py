@@ -7,7 +7,9 @@ the pages' sweep, (batch, ctx) in {(1,512), (16,256), (4,2048)}, 32 query /
 single pass when one partition suffices).  Inputs rotate among enough
 independent seeded sets that every step reads from HBM, not L2.  The step is
 captured once per input set as a CUDA graph and replayed, so host launch
-overhead does not pace the GPU.
+overhead does not pace the GPU.  Multi-token workloads (``--workload multi``:
+q_len > 1 query tokens per sequence, causal over the new tokens) run through
+``pa_decode_multi`` instead.
 
 Prints one JSON line (rank 0).  ``--impl reference`` times the fp64 CPU oracle
 on the same workload instead.  Under torchrun each rank runs an independent
@@ -44,14 +46,41 @@ DTYPE_NAME = {torch.float16: "f16", torch.bfloat16: "bf16", torch.float32: "f32"
 # ---------------------------------------------------------------------------
 def algorithmic_bytes(x: workloads.Inputs, out_elem: int = 4) -> int:
     """Bytes one decode call must move at least once: K and V of every attended
-    token for each kv head, q, the output, the block table and the lengths."""
-    B, H, D = x.q.shape
+    token for each kv head, q, the output, the block table and the lengths.
+    (With several query tokens the last one attends every cached token.)"""
+    B, D = x.q.shape[0], x.q.shape[-1]
     _, bs, Hkv, _ = x.k_cache.shape
     e = x.q.element_size()
     mb = x.block_tables.shape[1]
     tokens = sum(min(max(t, 0), mb * bs) for t in x.lens_host)
-    return (tokens * Hkv * D * 2 * e + B * H * D * e + B * H * D * out_elem
+    return (tokens * Hkv * D * 2 * e + x.q.numel() * e + x.q.numel() * out_elem
             + B * mb * 4 + B * 4)
+
+
+def decode_call(pa, out, q, k_cache, v_cache, block_tables, context_lens, scale, max_context_len,
+                partition_tokens, workspace, stream):
+    """One decode call through the public API: one query token per sequence
+    (q [B, H, D]) or several (q [B, Q, H, D])."""
+    fn = pa.decode_multi if q.dim() == 4 else pa.decode_splitkv
+    fn(out, q, k_cache, v_cache, block_tables, context_lens, scale, max_context_len,
+       partition_tokens, workspace=workspace, stream=stream)
+
+
+def workspace_bytes(pa, x, partition_tokens) -> int:
+    fn = pa.workspace_size_multi if x.q.dim() == 4 else pa.workspace_size
+    return fn(x.q, x.k_cache, x.block_tables, torch.float32, x.max_context_len, partition_tokens)
+
+
+def oracle_rows(oracle, h, rows, token=None):
+    """fp64 oracle output of (b, h) rows; for several query tokens, those of
+    query token `token` (the one-token decode of its causal prefix)."""
+    if h.q.dim() == 3:
+        return oracle.decode_rows(h.q, h.k_cache, h.v_cache, h.block_tables, h.context_lens,
+                                  h.scale, rows)
+    Q = h.q.shape[1]
+    prefix = torch.clamp(h.context_lens - Q + token + 1, min=0)
+    return oracle.decode_rows(h.q[:, token].contiguous(), h.k_cache, h.v_cache, h.block_tables,
+                              prefix, h.scale, rows)
 
 
 def input_bytes(x: workloads.Inputs) -> int:
@@ -188,7 +217,8 @@ def ncu_traffic(kernel: str, workload: str):
 def oracle_step(sets_host):
     import oracle
     for x in sets_host:
-        oracle.decode(x.q, x.k_cache, x.v_cache, x.block_tables, x.context_lens, x.scale)
+        fn = oracle.decode_multi if x.q.dim() == 4 else oracle.decode
+        fn(x.q, x.k_cache, x.v_cache, x.block_tables, x.context_lens, x.scale)
 
 
 def time_oracle(sets_host, min_s=10.0, max_steps=None):
@@ -207,10 +237,19 @@ def time_oracle(sets_host, min_s=10.0, max_steps=None):
 # ---------------------------------------------------------------------------
 def describe(group):
     specs = [workloads.SPECS[n] for n in workloads.GROUPS[group]]
-    s0 = specs[0]
-    return (f"{group}: (batch, ctx) in {{{', '.join(f'({s.batch},{s.lens})' for s in specs)}}}, "
-            f"H{s0.num_heads}/Hkv{s0.num_kv_heads}, D{s0.head_dim}, bs{s0.block_size}, "
-            f"{DTYPE_NAME[s0.dtype]} K/V, fp32 out")
+
+    def shape(s):
+        return (f"H{s.num_heads}/Hkv{s.num_kv_heads}, D{s.head_dim}, bs{s.block_size}, "
+                f"{DTYPE_NAME[s.dtype]} K/V")
+
+    def case(s):
+        return f"({s.batch},{s.lens}" + (f",{s.q_len})" if s.q_len > 1 else ")")
+
+    head = f"(batch, ctx{', q_len' if any(s.q_len > 1 for s in specs) else ''})"
+    if len({shape(s) for s in specs}) == 1:
+        return (f"{group}: {head} in {{{', '.join(case(s) for s in specs)}}}, "
+                f"{shape(specs[0])}, fp32 out")
+    return f"{group}: {head}: " + "; ".join(f"{case(s)} {shape(s)}" for s in specs) + "; fp32 out"
 
 
 def run_reference(args):
@@ -256,7 +295,8 @@ def main(argv=None):
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--with-append", action="store_true",
                     help="each call first appends the step's new token (the last of every "
-                         "context) with pa_append_kv, as a full decode iteration does")
+                         "context) with pa_append_kv, as a full decode iteration does "
+                         "(one-token workloads only)")
     ap.add_argument("--min-warmup-s", type=float, default=1.0,
                     help="keep warming up (graph replays) at least this long")
     args = ap.parse_args(argv)
@@ -286,19 +326,31 @@ def main(argv=None):
     sets = [set0] + [[workloads.make(n, seed=100 * r + rank, device=dev) for n in names]
                      for r in range(1, nsets)]
     pts = [s.partition_tokens if args.partition_tokens < 0 else args.partition_tokens for s in specs]
+    if args.with_append and any(s.q_len > 1 for s in specs):
+        print(json.dumps({"metric": METRIC, "error": "--with-append needs one-token workloads"}))
+        return 1
 
     outs = [[torch.empty(x.q.shape, dtype=torch.float32, device=dev) for x in st] for st in sets]
     ws = []
     for i in range(len(set0)):
         # every rotated set has its own longest context, hence its own plan
-        need = max(pa.workspace_size(st[i].q, st[i].k_cache, st[i].block_tables, torch.float32,
-                                     st[i].max_context_len, pts[i]) for st in sets)
+        need = max(workspace_bytes(pa, st[i], pts[i]) for st in sets)
         ws.append(torch.empty(max(need, 16), dtype=torch.uint8, device=dev))
     splits = [ws[i].numel() > 16 for i in range(len(set0))]      # partials combined by a 2nd kernel
     launches_per_step = sum(2 if s else 1 for s in splits) + (len(set0) if args.with_append else 0)
     sms = props.multi_processor_count
     plans = {}
     for i, x in enumerate(set0):
+        if x.q.dim() == 4:
+            G = x.q.shape[2] // x.k_cache.shape[2]
+            Q = x.q.shape[1]
+            plans[names[i]] = {"partition_tokens": pts[i] or "auto", "q_len": Q,
+                               "query_chunks": -(-Q // min(Q, 16 // G)),
+                               "partitions": "auto" if not pts[i] else
+                                             -(-max(x.max_context_len, 1) // pts[i]),
+                               "reduce": "workspace+combine kernel" if splits[i] else
+                                         "cluster DSMEM or none"}
+            continue
         pt = pts[i] or pa.choose_partition_tokens(x.q, x.k_cache, x.block_tables,
                                                   x.max_context_len, sms)
         if pt == pa.PARTITION_BALANCED:
@@ -328,8 +380,8 @@ def main(argv=None):
         if args.with_append:
             kn, vn, pos = new_kv[(si, i)]
             pa.append_kv(x.k_cache, x.v_cache, kn, vn, x.block_tables, pos, stream=st)
-        pa.decode_splitkv(outs[si][i], x.q, x.k_cache, x.v_cache, x.block_tables, x.context_lens,
-                          x.scale, x.max_context_len, pts[i], workspace=ws[i], stream=st)
+        decode_call(pa, outs[si][i], x.q, x.k_cache, x.v_cache, x.block_tables, x.context_lens,
+                    x.scale, x.max_context_len, pts[i], ws[i], st)
 
     # ---- parity before timing (sampled rows against the fp64 oracle) ----
     import oracle
@@ -341,13 +393,15 @@ def main(argv=None):
     if rank == 0:
         for i, x in enumerate(set0):
             g = np.random.default_rng(i)
-            B, H = x.q.shape[:2]
+            B, H = x.q.shape[0], x.q.shape[-2]
             rows = np.stack([g.integers(0, B, 16), g.integers(0, H, 16)], 1).astype(np.int32)
             h = x.to("cpu")
-            want = oracle.decode_rows(h.q, h.k_cache, h.v_cache, h.block_tables, h.context_lens,
-                                      h.scale, rows)
-            got = outs[0][i][rows[:, 0], rows[:, 1]].double().cpu().numpy()
-            max_err = max(max_err, float(np.abs(got - want).max()))
+            tokens = [None] if x.q.dim() == 3 else sorted({0, x.q.shape[1] - 1})
+            for tok in tokens:
+                want = oracle_rows(oracle, h, rows, tok)
+                o = outs[0][i] if tok is None else outs[0][i][:, tok]
+                got = o[rows[:, 0], rows[:, 1]].double().cpu().numpy()
+                max_err = max(max_err, float(np.abs(got - want).max()))
         if not max_err <= 2e-3:
             print(json.dumps({"metric": METRIC, "error": f"parity failed: max_err {max_err}"}))
             return 1
@@ -489,9 +543,9 @@ def main(argv=None):
                 for i, x in enumerate(set0):
                     v = views[buf][i]
                     o = dev_out[buf][out_offs[i]:out_offs[i] + out_elems[i]].view(x.q.shape)
-                    pa.decode_splitkv(o, v["q"], v["k_cache"], v["v_cache"], v["block_tables"],
-                                      v["context_lens"], x.scale, x.max_context_len, pts[i],
-                                      workspace=ws2[buf][i], stream=stream)
+                    decode_call(pa, o, v["q"], v["k_cache"], v["v_cache"], v["block_tables"],
+                                v["context_lens"], x.scale, x.max_context_len, pts[i],
+                                ws2[buf][i], stream)
                 pin_out[buf].copy_(dev_out[buf], non_blocking=True)
                 consumed[buf].record(stream)
 

@@ -36,7 +36,8 @@
  *   - a sequence with no attended token gets an all-zero output row.
  *
  * Arithmetic: scores, the online softmax (running max m and normaliser l) and
- * the value accumulation are fp32; K/V/q are fp16 or bf16.
+ * the value accumulation are fp32; K/V/q are fp16 or bf16.  `scale` must be
+ * finite and > 0 (PA_ERR_INVALID_ARG otherwise).
  *
  * Calls.  All entry points validate on the host and either launch work on
  * `stream` (a cudaStream_t; NULL = the legacy default stream) and return
@@ -153,6 +154,41 @@ pa_status pa_decode_splitkv(void* out, const void* q, const void* k_cache, const
                             const pa_shape* shape, float scale, int32_t max_context_len,
                             int32_t partition_tokens, void* workspace, size_t workspace_bytes,
                             void* stream);
+
+/*
+ * Several query tokens per sequence in one call: the decode step of
+ * speculative decoding's verification, or a short chunk of new tokens (the
+ * pages define only the one-token decode; this is its causal extension, the
+ * q_len > 1 attention that the flash-decoding-bench design notes contrast
+ * with the q_len = 1 decode).  Layouts:
+ *   q    [batch, q_len, num_heads, head_dim]  kv_dtype
+ *   out  [batch, q_len, num_heads, head_dim]  out_dtype
+ * context_lens[b] counts the q_len new tokens, whose keys and values are
+ * already in the cache at positions T - q_len .. T - 1 (T = context_lens[b]).
+ * Query token i sits at position T - q_len + i and attends to the tokens
+ * t <= T - q_len + i that the table reaches, with the same masking as
+ * pa_decode; a query token with no such token gets zeros.  With q_len = 1
+ * this is pa_decode_splitkv.
+ *
+ * The MMA tile's 16 rows hold (query token, head) pairs, so one CTA serves
+ * floor(16 / group) query tokens of a kv head; larger q_len launches
+ * ceil(q_len / that) CTAs per (sequence, kv head, partition), each reading
+ * the pages again (num_kv_heads * that count must be <= 65535, else
+ * PA_ERR_UNSUPPORTED).  Partitions, workspace and max_context_len as in
+ * pa_decode_splitkv; PA_PARTITION_BALANCED is honoured only when
+ * q_len * group <= 16 (otherwise the automatic choice is used).  The
+ * workspace must hold pa_workspace_size_multi(shape, q_len, ...) bytes.
+ */
+pa_status pa_decode_multi(void* out, const void* q, const void* k_cache, const void* v_cache,
+                          const int32_t* block_tables, const int32_t* context_lens,
+                          const pa_shape* shape, int32_t q_len, float scale,
+                          int32_t max_context_len, int32_t partition_tokens, void* workspace,
+                          size_t workspace_bytes, void* stream);
+
+/* Workspace bytes of pa_decode_multi (0 for invalid arguments or when none is
+ * needed); pa_workspace_size(shape, ...) is this with q_len = 1. */
+size_t pa_workspace_size_multi(const pa_shape* shape, int32_t q_len, int32_t max_context_len,
+                               int32_t partition_tokens);
 
 /*
  * Append of each sequence's new token to the paged cache, the step that

@@ -9,6 +9,8 @@ or a call is rejected, an exception is raised.
     decode(out, q, k_cache, v_cache, block_tables, context_lens, scale)
     decode_splitkv(out, q, k_cache, v_cache, block_tables, context_lens, scale,
                    max_context_len, partition_tokens=0, workspace=None)
+    decode_multi(out, q, k_cache, v_cache, block_tables, context_lens, scale,
+                 max_context_len, partition_tokens=0, workspace=None)
     workspace_size(q, k_cache, block_tables, out_dtype, max_context_len, partition_tokens=0)
     choose_partition_tokens(q, k_cache, block_tables, max_context_len, num_sms)
     resolve_blocks(out_phys, block_tables, context_lens, block_size, num_blocks)
@@ -22,7 +24,8 @@ import threading
 
 import torch
 
-__all__ = ["PaError", "decode", "decode_splitkv", "decode_splitkv_noalloc", "append_kv", "workspace_size", "choose_partition_tokens",
+__all__ = ["PaError", "decode", "decode_splitkv", "decode_splitkv_noalloc", "decode_multi",
+           "append_kv", "workspace_size", "workspace_size_multi", "choose_partition_tokens",
            "resolve_blocks", "device_error", "library_path", "F16", "BF16", "F32"]
 
 F16, BF16, F32 = 0, 1, 2
@@ -73,6 +76,10 @@ def _load():
             lib.pa_decode_splitkv.restype = ctypes.c_int
             lib.pa_decode_splitkv_noalloc.argtypes = [P, P, P, P, P, P, S, f32, i32, i32, P]
             lib.pa_decode_splitkv_noalloc.restype = ctypes.c_int
+            lib.pa_decode_multi.argtypes = [P, P, P, P, P, P, S, i32, f32, i32, i32, P, sz, P]
+            lib.pa_decode_multi.restype = ctypes.c_int
+            lib.pa_workspace_size_multi.argtypes = [S, i32, i32, i32]
+            lib.pa_workspace_size_multi.restype = sz
             lib.pa_workspace_size.argtypes = [S, i32, i32]
             lib.pa_workspace_size.restype = sz
             lib.pa_choose_partition_tokens.argtypes = [S, i32, i32]
@@ -202,6 +209,44 @@ def decode_splitkv_noalloc(out, q, k_cache, v_cache, block_tables, context_lens,
         block_tables.data_ptr(), context_lens.data_ptr(), ctypes.byref(shape), float(scale),
         int(max_context_len), int(partition_tokens), _stream_ptr(stream)),
         "pa_decode_splitkv_noalloc")
+    return out
+
+
+def _multi_shape(q, k_cache, block_tables, out_dtype):
+    if q.dim() != 4:
+        raise ValueError("q must be [batch, q_len, num_heads, head_dim]")
+    return make_shape(q[:, 0], k_cache, block_tables, out_dtype), int(q.shape[1])
+
+
+def workspace_size_multi(q, k_cache, block_tables, out_dtype, max_context_len: int,
+                         partition_tokens: int = 0) -> int:
+    shape, q_len = _multi_shape(q, k_cache, block_tables, out_dtype)
+    return int(_load().pa_workspace_size_multi(ctypes.byref(shape), q_len, int(max_context_len),
+                                               int(partition_tokens)))
+
+
+def decode_multi(out, q, k_cache, v_cache, block_tables, context_lens, scale: float,
+                 max_context_len: int, partition_tokens: int = 0, workspace=None, stream=None):
+    """Several query tokens per sequence (q, out: [B, Q, H, D]); query token i
+    of sequence b attends causally to the cached tokens t <= context_lens[b] - Q + i."""
+    _dev_tensors(out, q, k_cache, v_cache, block_tables, context_lens)
+    _ints(block_tables, context_lens)
+    if out.shape != q.shape:
+        raise ValueError("out must be shaped like q")
+    shape, q_len = _multi_shape(q, k_cache, block_tables, out.dtype)
+    lib = _load()
+    if workspace is None:
+        need = lib.pa_workspace_size_multi(ctypes.byref(shape), q_len, int(max_context_len),
+                                           int(partition_tokens))
+        workspace = torch.empty(max(int(need), 16), dtype=torch.uint8, device=q.device)
+    else:
+        _dev_tensors(workspace)
+    _check(lib.pa_decode_multi(out.data_ptr(), q.data_ptr(), k_cache.data_ptr(),
+                               v_cache.data_ptr(), block_tables.data_ptr(),
+                               context_lens.data_ptr(), ctypes.byref(shape), q_len, float(scale),
+                               int(max_context_len), int(partition_tokens), workspace.data_ptr(),
+                               workspace.numel() * workspace.element_size(), _stream_ptr(stream)),
+           "pa_decode_multi")
     return out
 
 

@@ -4,6 +4,7 @@
 
 #include <algorithm>
 #include <atomic>
+#include <cmath>
 #include <cstdlib>
 #include <cstring>
 #include <mutex>
@@ -55,6 +56,21 @@ pa_status check_shape(const pa_shape* s) {
     if ((int64_t)s->max_blocks_per_seq * s->block_size >= (int64_t(1) << 31))
         return PA_ERR_UNSUPPORTED;
     return PA_OK;
+}
+
+// The scores are scaled by `scale` before the softmax; the kernels take the
+// running maximum of the unscaled scores, which needs scale > 0.
+bool scale_ok(float scale) { return std::isfinite(scale) && scale > 0.f; }
+
+// Query tokens one CTA serves: q_chunk * group rows fill at most the 16 rows
+// of the MMA tile.
+int q_chunk_for(const pa_shape* s, int32_t q_len) {
+    const int per = 16 / (s->num_heads / s->num_kv_heads);
+    return q_len < per ? q_len : per;
+}
+int q_chunks_for(const pa_shape* s, int32_t q_len) {
+    const int c = q_chunk_for(s, q_len);
+    return (q_len + c - 1) / c;
 }
 
 pa_status check_ptrs(const void* out, const void* q, const void* k, const void* v,
@@ -218,11 +234,12 @@ Plan balanced_plan(const pa_shape* s, int pages, int num_sms) {
     return p;
 }
 
-Plan auto_plan(const pa_shape* s, int32_t max_context_len, int num_sms) {
+Plan auto_plan(const pa_shape* s, int32_t max_context_len, int num_sms, int q_chunks = 1) {
     const int pages = pages_for(s, max_context_len);
-    const int64_t units = (int64_t)s->batch * s->num_kv_heads;
+    const int64_t units = (int64_t)s->batch * s->num_kv_heads * q_chunks;
     auto ceil_div = [](int64_t a, int64_t b) { return (a + b - 1) / b; };
-    const bool can_balance = s->batch <= kMaxBalancedBatch && balanced_mode() > 0;
+    const bool can_balance =
+        s->batch <= kMaxBalancedBatch && q_chunks == 1 && balanced_mode() > 0;
     // enough pages that every SM gets at least eight
     const bool big = units * pages >= 8LL * num_sms;
     const int64_t wide_slots = (int64_t)num_sms * ctas_per_sm(s, pick_tune(s, true));
@@ -255,16 +272,22 @@ bool clusters_enabled() {
     return !off;
 }
 
-Plan make_plan(const pa_shape* s, int32_t max_context_len, int32_t partition_tokens, int num_sms) {
+// The balanced split keeps every query token of a (sequence, kv head) in
+// one CTA: it needs q_len * group <= 16, and batch <= kMaxBalancedBatch.
+Plan make_plan(const pa_shape* s, int32_t max_context_len, int32_t partition_tokens, int num_sms,
+               int32_t q_len = 1) {
     Plan plan;
-    if (partition_tokens == PA_PARTITION_BALANCED && s->batch <= kMaxBalancedBatch) {
+    const int q_chunks = q_chunks_for(s, q_len);
+    if (partition_tokens == PA_PARTITION_BALANCED && s->batch <= kMaxBalancedBatch &&
+        q_chunks == 1) {
         plan = balanced_plan(s, pages_for(s, max_context_len),
                              num_sms * ctas_per_sm(s, pick_tune(s, false)));
     } else if (partition_tokens <= 0) {
-        plan = auto_plan(s, max_context_len, num_sms);
+        plan = auto_plan(s, max_context_len, num_sms, q_chunks);
     } else {
         plan = plan_with(s, pages_for(s, max_context_len), partition_tokens / s->block_size, true);
-        plan.many_ctas = (int64_t)s->batch * s->num_kv_heads * plan.num_parts > num_sms;
+        plan.many_ctas =
+            (int64_t)s->batch * s->num_kv_heads * q_chunks * plan.num_parts > num_sms;
     }
     if (!clusters_enabled()) plan.cluster = false;
     return plan;
@@ -275,14 +298,16 @@ bool partition_arg_ok(const pa_shape* s, int32_t partition_tokens) {
            (partition_tokens >= 0 && partition_tokens % s->block_size == 0);
 }
 
-// Workspace: part_acc [B, Hkv, P, G, D] fp32, then part_ml [B, Hkv, P, G, 2] fp32.
-size_t workspace_bytes_for(const pa_shape* s, const Plan& plan, size_t* ml_offset) {
-    size_t rows;  // (m, l, acc) rows of the group's heads
+// Workspace: part_acc [B, Hkv, P, Q*G, D] fp32, then part_ml [B, Hkv, P, Q*G, 2]
+// fp32 (rows of a (sequence, kv head, partition): query token, then head).
+size_t workspace_bytes_for(const pa_shape* s, const Plan& plan, size_t* ml_offset,
+                           int32_t q_len = 1) {
+    size_t rows;  // (m, l, acc) rows
     if (plan.balanced) {
-        rows = (size_t)plan.num_ctas * 2 * (s->num_heads / s->num_kv_heads);  // [C][2][G]
+        rows = (size_t)plan.num_ctas * 2 * (s->num_heads / s->num_kv_heads) * q_len;  // [C][2][QG]
     } else {
         if (plan.num_parts <= 1 || plan.cluster) return 0;  // one pass, or reduced in a cluster
-        rows = (size_t)s->batch * s->num_heads * plan.num_parts;           // [B][Hkv][P][G]
+        rows = (size_t)s->batch * s->num_heads * q_len * plan.num_parts;  // [B][Hkv][P][Q*G]
     }
     const size_t acc = rows * s->head_dim * sizeof(float);
     const size_t off = (acc + 255) / 256 * 256;
@@ -326,17 +351,21 @@ pa_status encode_maps(const pa_shape* s, const void* k, const void* v, CUtensorM
 pa_status launch_attention(void* out, const void* q, const void* k, const void* v,
                            const int32_t* bt, const int32_t* lens, const pa_shape* s, float scale,
                            const Plan& plan, float* part_acc, float* part_ml, int32_t* err,
-                           cudaStream_t stream) {
+                           cudaStream_t stream, int32_t q_len = 1) {
     AttnLaunch L;
     std::memset(&L, 0, sizeof L);
-    pa_status st = encode_maps(s, k, v, &L.tmap_k, &L.tmap_v);
-    if (st != PA_OK) return st;
+    const int G = s->num_heads / s->num_kv_heads;
+    const int q_chunk = q_chunk_for(s, q_len);
+    const int64_t grid_y = (int64_t)s->num_kv_heads * q_chunks_for(s, q_len);
+    if (grid_y > 65535) return PA_ERR_UNSUPPORTED;
     const Tune t = pick_tune(s, plan.many_ctas);
     const AttnSmem sm = attn_smem_layout(s->head_dim, s->block_size, t.nt, t.ns);
-    const int G = s->num_heads / s->num_kv_heads;
-    if (4u * (merge_floats(t.nt * t.nh, G, s->head_dim / t.nh) + cluster_part_floats(G, s->head_dim)) >
-        sm.stage_bytes * t.nt * t.ns)
+    const int rows = q_chunk * G;  // MMA rows in use
+    if (4u * (merge_floats(t.nt * t.nh, rows, s->head_dim / t.nh) +
+              cluster_part_floats(rows, s->head_dim)) > sm.stage_bytes * t.nt * t.ns)
         return PA_ERR_UNSUPPORTED;  // the final merge must fit in the stage area
+    pa_status st = encode_maps(s, k, v, &L.tmap_k, &L.tmap_v);
+    if (st != PA_OK) return st;
     AttnParams& p = L.p;
     p.q = q;
     p.out = out;
@@ -348,7 +377,10 @@ pa_status launch_attention(void* out, const void* q, const void* k, const void* 
     p.batch = s->batch;
     p.num_heads = s->num_heads;
     p.num_kv_heads = s->num_kv_heads;
-    p.group = s->num_heads / s->num_kv_heads;
+    p.group = G;
+    p.q_len = q_len;
+    p.q_chunk = q_chunk;
+    p.unit_rows = q_len * G;
     p.max_blocks = s->max_blocks_per_seq;
     p.num_blocks = s->num_blocks;
     p.qscale = scale * 1.4426950408889634f;  // log2(e)
@@ -369,7 +401,7 @@ pa_status launch_attention(void* out, const void* q, const void* k, const void* 
     L.pdl = use_pdl();
     L.cluster = p.cluster_reduce ? plan.num_parts : 1;
     L.grid = plan.balanced ? dim3((unsigned)plan.num_ctas)
-                           : dim3((unsigned)plan.num_parts, (unsigned)s->num_kv_heads,
+                           : dim3((unsigned)plan.num_parts, (unsigned)grid_y,
                                   (unsigned)s->batch);
     L.threads = 32 * t.nt * t.nh;
     L.smem_bytes = sm.total + kSmemAlignSlack;
@@ -411,12 +443,7 @@ int32_t pa_choose_partition_tokens(const pa_shape* shape, int32_t max_context_le
 
 size_t pa_workspace_size(const pa_shape* shape, int32_t max_context_len,
                          int32_t partition_tokens) {
-    if (check_shape(shape) != PA_OK || max_context_len < 0) return 0;
-    if (!partition_arg_ok(shape, partition_tokens)) return 0;
-    int sms = 1;
-    if (partition_tokens <= 0 && device_state(&sms, nullptr) != PA_OK) return 0;
-    const Plan plan = make_plan(shape, max_context_len, partition_tokens, sms);
-    return workspace_bytes_for(shape, plan, nullptr);
+    return pa_workspace_size_multi(shape, 1, max_context_len, partition_tokens);
 }
 
 pa_status pa_decode(void* out, const void* q, const void* k_cache, const void* v_cache,
@@ -424,6 +451,7 @@ pa_status pa_decode(void* out, const void* q, const void* k_cache, const void* v
                     const pa_shape* shape, float scale, void* stream) {
     pa_status st = check_shape(shape);
     if (st != PA_OK) return st;
+    if (!scale_ok(scale)) return PA_ERR_INVALID_ARG;
     if (shape->batch == 0) return PA_OK;
     st = check_ptrs(out, q, k_cache, v_cache, block_tables, context_lens);
     if (st != PA_OK) return st;
@@ -437,13 +465,14 @@ pa_status pa_decode(void* out, const void* q, const void* k_cache, const void* v
                             plan, nullptr, nullptr, err, static_cast<cudaStream_t>(stream));
 }
 
-pa_status pa_decode_splitkv(void* out, const void* q, const void* k_cache, const void* v_cache,
-                            const int32_t* block_tables, const int32_t* context_lens,
-                            const pa_shape* shape, float scale, int32_t max_context_len,
-                            int32_t partition_tokens, void* workspace, size_t workspace_bytes,
-                            void* stream) {
+pa_status pa_decode_multi(void* out, const void* q, const void* k_cache, const void* v_cache,
+                          const int32_t* block_tables, const int32_t* context_lens,
+                          const pa_shape* shape, int32_t q_len, float scale,
+                          int32_t max_context_len, int32_t partition_tokens, void* workspace,
+                          size_t workspace_bytes, void* stream) {
     pa_status st = check_shape(shape);
     if (st != PA_OK) return st;
+    if (q_len < 1 || !scale_ok(scale)) return PA_ERR_INVALID_ARG;
     if (max_context_len < 0 || !partition_arg_ok(shape, partition_tokens)) return PA_ERR_INVALID_ARG;
     if (shape->batch == 0) return PA_OK;
     st = check_ptrs(out, q, k_cache, v_cache, block_tables, context_lens);
@@ -452,20 +481,21 @@ pa_status pa_decode_splitkv(void* out, const void* q, const void* k_cache, const
     int32_t* err = nullptr;
     st = device_state(&sms, &err);
     if (st != PA_OK) return st;
-    const Plan plan = make_plan(shape, max_context_len, partition_tokens, sms);
+    const Plan plan = make_plan(shape, max_context_len, partition_tokens, sms, q_len);
     cudaStream_t cs = static_cast<cudaStream_t>(stream);
     if (!plan.balanced && (plan.num_parts <= 1 || plan.cluster))
         return launch_attention(out, q, k_cache, v_cache, block_tables, context_lens, shape, scale,
-                                plan, nullptr, nullptr, err, cs);
+                                plan, nullptr, nullptr, err, cs, q_len);
 
     size_t ml_off = 0;
-    const size_t need = workspace_bytes_for(shape, plan, &ml_off);
+    const size_t need = workspace_bytes_for(shape, plan, &ml_off, q_len);
     if (!workspace || !aligned(workspace, 16) || workspace_bytes < need) return PA_ERR_WORKSPACE;
     if ((size_t)plan.num_parts * 2 * sizeof(float) > 200u * 1024u) return PA_ERR_UNSUPPORTED;
+    if ((int64_t)q_len * shape->num_heads > 0x7fffffff) return PA_ERR_UNSUPPORTED;
     float* part_acc = static_cast<float*>(workspace);
     float* part_ml = reinterpret_cast<float*>(static_cast<char*>(workspace) + ml_off);
     st = launch_attention(out, q, k_cache, v_cache, block_tables, context_lens, shape, scale, plan,
-                          part_acc, part_ml, err, cs);
+                          part_acc, part_ml, err, cs, q_len);
     if (st != PA_OK) return st;
     CombineParams c;
     c.out = out;
@@ -478,15 +508,35 @@ pa_status pa_decode_splitkv(void* out, const void* q, const void* k_cache, const
     c.group = shape->num_heads / shape->num_kv_heads;
     c.max_blocks = shape->max_blocks_per_seq;
     c.block_size = shape->block_size;
+    c.q_len = q_len;
     c.part_pages = plan.part_pages;
     c.num_parts = plan.num_parts;
     c.out_dtype = shape->out_dtype;
     c.num_ctas = plan.num_ctas;
-    const dim3 cgrid((unsigned)shape->num_heads, (unsigned)shape->batch);
+    const dim3 cgrid((unsigned)(q_len * shape->num_heads), (unsigned)shape->batch);
     const cudaError_t e = plan.balanced ? launch_combine_balanced(c, shape->head_dim, cgrid,
                                                                   use_pdl(), cs)
                                         : launch_combine(c, shape->head_dim, cgrid, use_pdl(), cs);
     return e == cudaSuccess ? PA_OK : PA_ERR_CUDA;
+}
+
+pa_status pa_decode_splitkv(void* out, const void* q, const void* k_cache, const void* v_cache,
+                            const int32_t* block_tables, const int32_t* context_lens,
+                            const pa_shape* shape, float scale, int32_t max_context_len,
+                            int32_t partition_tokens, void* workspace, size_t workspace_bytes,
+                            void* stream) {
+    return pa_decode_multi(out, q, k_cache, v_cache, block_tables, context_lens, shape, 1, scale,
+                           max_context_len, partition_tokens, workspace, workspace_bytes, stream);
+}
+
+size_t pa_workspace_size_multi(const pa_shape* shape, int32_t q_len, int32_t max_context_len,
+                               int32_t partition_tokens) {
+    if (check_shape(shape) != PA_OK || max_context_len < 0 || q_len < 1) return 0;
+    if (!partition_arg_ok(shape, partition_tokens)) return 0;
+    int sms = 1;
+    if (partition_tokens <= 0 && device_state(&sms, nullptr) != PA_OK) return 0;
+    const Plan plan = make_plan(shape, max_context_len, partition_tokens, sms, q_len);
+    return workspace_bytes_for(shape, plan, nullptr, q_len);
 }
 
 pa_status pa_resolve_blocks(int32_t* out_phys, const int32_t* block_tables,
@@ -557,6 +607,7 @@ pa_status pa_decode_splitkv_noalloc(void* out, const void* q, const void* k_cach
                                     int32_t partition_tokens, void* stream) {
     pa_status st = check_shape(shape);
     if (st != PA_OK) return st;
+    if (!scale_ok(scale)) return PA_ERR_INVALID_ARG;
     if (max_context_len < 0 || !partition_arg_ok(shape, partition_tokens)) return PA_ERR_INVALID_ARG;
     if (shape->batch == 0) return PA_OK;
     st = check_ptrs(out, q, k_cache, v_cache, block_tables, context_lens);

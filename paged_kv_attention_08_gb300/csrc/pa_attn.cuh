@@ -68,7 +68,9 @@ constexpr float kRescaleSlack = 8.0f;  // log2 units: p may reach 2^8 before a r
 // Where the merged result of a segment goes.
 enum SegOut { kOutFinal = 0, kOutPartial = 1, kOutCluster = 2, kOutRecord = 3 };
 
-template <int D, int BS, typename KV>
+// MULTI: several query tokens per sequence (rows are (query token, head)
+// pairs with a causal limit each); otherwise one token, rows = the group's heads.
+template <int D, int BS, typename KV, bool MULTI>
 __global__ void __launch_bounds__(256, 1)
     attn_kernel(const __grid_constant__ CUtensorMap tmap_k,
                 const __grid_constant__ CUtensorMap tmap_v, const AttnParams p) {
@@ -85,7 +87,13 @@ __global__ void __launch_bounds__(256, 1)
 
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const int stream = warp / DS, ds = warp % DS;
-    const int G = p.group;
+    const int G = p.group, Hkv = p.num_kv_heads;
+    const int Q = MULTI ? p.q_len : 1;
+    const int gshift = __ffs(G) - 1;  // the group is a power of two
+    // MMA rows are (query token, head) pairs: row r is query token qi0 + r / G
+    // and head kvh * G + r % G.  A CTA takes the query tokens of one chunk.
+    const int qi0 = MULTI ? ((int)blockIdx.y / Hkv) * p.q_chunk : 0;
+    const int R = MULTI ? min(p.q_chunk, Q - qi0) * G : G;
 
     uint64_t* full = reinterpret_cast<uint64_t*>(smem + L.full_off);
     uint64_t* empty = reinterpret_cast<uint64_t*>(smem + L.empty_off);
@@ -105,17 +113,26 @@ __global__ void __launch_bounds__(256, 1)
     grid_launch_dependents();
 
     const int g = lane >> 2, tig = lane & 3;
-    const bool real0 = g < G, real1 = g + 8 < G;
+    const bool real0 = g < R, real1 = g + 8 < R;
     const float qscale = p.qscale;
     const int ldsm_t = lane & 7;         // row supplied to ldmatrix
     const int ldsm_m = lane >> 3;        // matrix supplied to ldmatrix
     const int col0 = ds * (DW / 8);      // first 16-byte output chunk of this warp
     const int nw = p.nt * DS;
     // After a segment's pages are consumed the stage area holds the merge data.
-    float* macc = reinterpret_cast<float*>(smem + L.stages_off);   // [nw][G][DW]
-    float* mm = macc + (size_t)nw * G * DW;                         // [nw][G] running max
-    float* mls = mm + nw * G;                                       // [nw][G] normaliser
-    float* cpart = mls + nw * G;  // this CTA's partial when the cluster reduces: acc [G][D], m [G], l [G]
+    float* macc = reinterpret_cast<float*>(smem + L.stages_off);   // [nw][R][DW]
+    float* mm = macc + (size_t)nw * R * DW;                         // [nw][R] running max
+    float* mls = mm + nw * R;                                       // [nw][R] normaliser
+    float* cpart = mls + nw * R;  // this CTA's partial when the cluster reduces: acc [R][D], m [R], l [R]
+
+    // Element offset of row r's query (and output) vector: [B, Q, H, D].
+    auto row_off = [&](int b, int kvh, int r) -> size_t {
+        if constexpr (MULTI)
+            return (((size_t)b * Q + qi0 + (r >> gshift)) * p.num_heads + kvh * G +
+                    (r & (G - 1))) * D;
+        else
+            return ((size_t)b * p.num_heads + kvh * G + r) * D;
+    };
 
     // Pipeline state of this warp's stream, carried across segments.
     int slot = 0;
@@ -143,10 +160,11 @@ __global__ void __launch_bounds__(256, 1)
         }
     };
 
-    // Pages [pb, pe) of (sequence b, kv head kvh), whose context holds T
+    // Pages [pb, pe) of (sequence b, kv head kvh), whose table reaches T
     // tokens; the leader warp has already called start_fetch(b, pb, >= pe).
     // The streams take the pages in turn; the merged (m, l, acc) of every
-    // query head of the group is handed to emit(idx = r*D + d, A, M, L).
+    // row is handed to emit(idx = r*D + d, A, M, L).  Query token qi sits at
+    // position ctx - Q + qi and attends to the tokens before and at it.
     auto run_segment = [&](int b, int kvh, int pb, int pe, int T, auto&& emit) {
         const int npages = (T + BS - 1) / BS;
         const int span = pe - pb;
@@ -197,12 +215,13 @@ __global__ void __launch_bounds__(256, 1)
             n_issued = pro;
         }
 
-        // ---- Q fragments (A operand of S = Q K^T): rows = the group's heads ----
+        // ---- Q fragments (A operand of S = Q K^T): rows g and g + 8 ----
         uint32_t qa[KSTEPS][4];
         {
-            const KV* q = static_cast<const KV*>(p.q) + ((size_t)b * p.num_heads + kvh * G) * D;
-            const uint32_t* q0 = reinterpret_cast<const uint32_t*>(q + (size_t)g * D);
-            const uint32_t* q1 = reinterpret_cast<const uint32_t*>(q + (size_t)(g + 8) * D);
+            // (the rows of padded lanes are never loaded)
+            const KV* q = static_cast<const KV*>(p.q);
+            const uint32_t* q0 = reinterpret_cast<const uint32_t*>(q + row_off(b, kvh, g));
+            const uint32_t* q1 = reinterpret_cast<const uint32_t*>(q + row_off(b, kvh, g + 8));
 #pragma unroll
             for (int kk = 0; kk < KSTEPS; ++kk) {
                 const int w = (kk * 16 + tig * 2) >> 1;  // 32-bit word index of the element pair
@@ -211,6 +230,15 @@ __global__ void __launch_bounds__(256, 1)
                 qa[kk][2] = real0 ? __ldg(q0 + w + 4) : 0u;
                 qa[kk][3] = real1 ? __ldg(q1 + w + 4) : 0u;
             }
+        }
+
+        // Tokens each row attends: the causal limit of its query token, inside
+        // the table's reach (with one query token, every row attends T).
+        int lim0 = T, lim1 = T;
+        if constexpr (MULTI) {
+            const int ctx = max(__ldg(p.context_lens + b), 0);
+            lim0 = min(T, ctx - Q + qi0 + (g >> gshift) + 1);
+            lim1 = min(T, ctx - Q + qi0 + ((g + 8) >> gshift) + 1);
         }
 
         // Running state of rows g and g+8 (padded rows stay at m = 0, p = 0).
@@ -269,14 +297,17 @@ __global__ void __launch_bounds__(256, 1)
                 }
 
                 // ---- page max per row, conditional rescale ----
+                // this page's attended tokens of rows g and g + 8
+                const int v0 = MULTI ? lim0 - j * BS : nvalid;
+                const int v1 = MULTI ? lim1 - j * BS : nvalid;
                 float mx0 = NEG_INF, mx1 = NEG_INF;
 #pragma unroll
                 for (int nt = 0; nt < NT; ++nt)
 #pragma unroll
                     for (int e = 0; e < 2; ++e) {
-                        const bool v = nt * 8 + tig * 2 + e < nvalid;
-                        s[nt][e] = v ? s[nt][e] : NEG_INF;
-                        s[nt][2 + e] = v ? s[nt][2 + e] : NEG_INF;
+                        const int c = nt * 8 + tig * 2 + e;
+                        s[nt][e] = c < v0 ? s[nt][e] : NEG_INF;
+                        s[nt][2 + e] = c < v1 ? s[nt][2 + e] : NEG_INF;
                         mx0 = fmaxf(mx0, s[nt][e]);
                         mx1 = fmaxf(mx1, s[nt][2 + e]);
                     }
@@ -306,12 +337,18 @@ __global__ void __launch_bounds__(256, 1)
                 }
 
                 // ---- P = 2^(S*scale*log2e - m), and its hi/lo 16-bit split ----
+                // (with several query tokens, a row that has attended nothing
+                // yet still has m = -inf and only -inf scores; its P must come
+                // out 0, not NaN.  With one token every real row has a finite
+                // max once a page is read.)
+                const float e0 = (MULTI && m0 == NEG_INF) ? 0.f : m0;
+                const float e1 = (MULTI && m1 == NEG_INF) ? 0.f : m1;
 #pragma unroll
                 for (int nt = 0; nt < NT; ++nt)
 #pragma unroll
                     for (int e = 0; e < 2; ++e) {
-                        s[nt][e] = real0 ? fast_exp2(fmaf(s[nt][e], qscale, -m0)) : 0.f;
-                        s[nt][2 + e] = real1 ? fast_exp2(fmaf(s[nt][2 + e], qscale, -m1)) : 0.f;
+                        s[nt][e] = real0 ? fast_exp2(fmaf(s[nt][e], qscale, -e0)) : 0.f;
+                        s[nt][2 + e] = real1 ? fast_exp2(fmaf(s[nt][2 + e], qscale, -e1)) : 0.f;
                         l0 += s[nt][e];
                         l1 += s[nt][2 + e];
                     }
@@ -393,37 +430,37 @@ __global__ void __launch_bounds__(256, 1)
         for (int n = 0; n < ONT; ++n) {
             const int c = n * 8 + tig * 2;
             if (real0)
-                *reinterpret_cast<float2*>(macc + ((size_t)warp * G + g) * DW + c) =
+                *reinterpret_cast<float2*>(macc + ((size_t)warp * R + g) * DW + c) =
                     make_float2(acc[n][0], acc[n][1]);
             if (real1)
-                *reinterpret_cast<float2*>(macc + ((size_t)warp * G + g + 8) * DW + c) =
+                *reinterpret_cast<float2*>(macc + ((size_t)warp * R + g + 8) * DW + c) =
                     make_float2(acc[n][2], acc[n][3]);
         }
         if (tig == 0) {
             if (real0) {
-                mm[warp * G + g] = m0;
-                mls[warp * G + g] = l0;
+                mm[warp * R + g] = m0;
+                mls[warp * R + g] = l0;
             }
             if (real1) {
-                mm[warp * G + g + 8] = m1;
-                mls[warp * G + g + 8] = l1;
+                mm[warp * R + g + 8] = m1;
+                mls[warp * R + g + 8] = l1;
             }
         }
         __syncthreads();
 
         // ---- merge the token streams (log-sum-exp) ----
-        for (int idx = tid; idx < G * D; idx += blockDim.x) {
+        for (int idx = tid; idx < R * D; idx += blockDim.x) {
             const int r = idx / D, d = idx % D;
             const int dsx = d / DW, dd = d % DW;
             float M = NEG_INF;
-            for (int s2 = 0; s2 < p.nt; ++s2) M = fmaxf(M, mm[(s2 * DS + dsx) * G + r]);
+            for (int s2 = 0; s2 < p.nt; ++s2) M = fmaxf(M, mm[(s2 * DS + dsx) * R + r]);
             float A = 0.f, Ls = 0.f;
             for (int s2 = 0; s2 < p.nt; ++s2) {
                 const int w2 = s2 * DS + dsx;
-                const float ms = mm[w2 * G + r];
+                const float ms = mm[w2 * R + r];
                 const float f = (ms == NEG_INF) ? 0.f : fast_exp2(ms - M);
-                A = fmaf(f, macc[((size_t)w2 * G + r) * DW + dd], A);
-                Ls = fmaf(f, mls[w2 * G + r], Ls);
+                A = fmaf(f, macc[((size_t)w2 * R + r) * DW + dd], A);
+                Ls = fmaf(f, mls[w2 * R + r], Ls);
             }
             emit(idx, A, M, Ls);
         }
@@ -432,11 +469,11 @@ __global__ void __launch_bounds__(256, 1)
 
     auto emit_final = [&](int b, int kvh) {
         return [&, b, kvh](int idx, float A, float M, float Ls) {
-            store_out(p.out, ((size_t)b * p.num_heads + kvh * G) * D + idx,
-                      Ls > 0.f ? A / Ls : 0.f, p.out_dtype);
+            store_out(p.out, row_off(b, kvh, idx / D) + idx % D, Ls > 0.f ? A / Ls : 0.f,
+                      p.out_dtype);
         };
     };
-    // (m, l, acc) of the group's heads into workspace row `row0 + r`.
+    // (m, l, acc) of the CTA's rows into workspace row `row0 + r`.
     auto emit_rows = [&](size_t row0) {
         return [&, row0](int idx, float A, float M, float Ls) {
             const int r = idx / D, d = idx % D;
@@ -450,8 +487,8 @@ __global__ void __launch_bounds__(256, 1)
 
     if (p.balanced) {
         // ---- balanced split: CTA c takes pages [c*W/C, (c+1)*W/C) of the
-        // flattened (sequence, kv head, page) order, W pages in all ----
-        const int Hkv = p.num_kv_heads;
+        // flattened (sequence, kv head, page) order, W pages in all; every
+        // query token of a unit is in the CTA's rows ----
         int* totals = seq_pages + p.batch;  // [0]: W
         if (warp == 0) {
             int w = 0;
@@ -508,7 +545,7 @@ __global__ void __launch_bounds__(256, 1)
             if (whole) {
                 run_segment(b, kvh, j, j + len, T, emit_final(b, kvh));
             } else {
-                const size_t row0 = ((size_t)c * 2 + (first ? 0 : 1)) * G;
+                const size_t row0 = ((size_t)c * 2 + (first ? 0 : 1)) * R;
                 run_segment(b, kvh, j, j + len, T, emit_rows(row0));
             }
             (void)last;
@@ -523,8 +560,9 @@ __global__ void __launch_bounds__(256, 1)
         return;
     }
 
-    // ---- one CTA per (sequence, kv head, partition) ----
-    const int part = blockIdx.x, kvh = blockIdx.y, b = blockIdx.z;
+    // ---- one CTA per (sequence, query chunk and kv head, partition) ----
+    const int part = blockIdx.x, b = blockIdx.z;
+    const int kvh = MULTI ? (int)blockIdx.y % Hkv : (int)blockIdx.y;
     const int pb = part * p.part_pages;
     // the table entries are fetched before the context length is known
     // (every index stays inside the table row); those past it are masked
@@ -538,10 +576,8 @@ __global__ void __launch_bounds__(256, 1)
         // partitions past the context.  (Inside a cluster every CTA takes
         // part in the reduction, so an empty one carries on with no pages.)
         if (p.final_out) {
-            for (int idx = tid; idx < G * D; idx += blockDim.x) {
-                const int h = kvh * G + idx / D;
-                store_out(p.out, ((size_t)b * p.num_heads + h) * D + idx % D, 0.f, p.out_dtype);
-            }
+            for (int idx = tid; idx < R * D; idx += blockDim.x)
+                store_out(p.out, row_off(b, kvh, idx / D) + idx % D, 0.f, p.out_dtype);
         }
         return;
     }
@@ -553,13 +589,15 @@ __global__ void __launch_bounds__(256, 1)
         run_segment(b, kvh, pb, max(pb, pe), T, [&](int idx, float A, float M, float Ls) {
             cpart[idx] = A;
             if (idx % D == 0) {
-                cpart[G * D + idx / D] = M;
-                cpart[G * D + G + idx / D] = Ls;
+                cpart[R * D + idx / D] = M;
+                cpart[R * D + R + idx / D] = Ls;
             }
         });
     } else {
+        // workspace rows [B][Hkv][P][Q * G]: this CTA's rows start at qi0 * G
         run_segment(b, kvh, pb, max(pb, pe), T,
-                    emit_rows((((size_t)b * p.num_kv_heads + kvh) * p.num_parts + part) * G));
+                    emit_rows((((size_t)b * Hkv + kvh) * p.num_parts + part) *
+                                  (MULTI ? p.unit_rows : G) + (size_t)qi0 * G));
     }
 
     if (p.cluster_reduce) {
@@ -574,16 +612,16 @@ __global__ void __launch_bounds__(256, 1)
 #pragma unroll
         for (int q = 0; q < kMaxClusterParts; ++q)
             rbase[q] = q < P ? map_cluster_rank(cp, (uint32_t)q) : cp;
-        const int chunk = (G * D + P - 1) / P;
-        const int i1 = min(((int)rank + 1) * chunk, G * D);
+        const int chunk = (R * D + P - 1) / P;
+        const int i1 = min(((int)rank + 1) * chunk, R * D);
         for (int idx = (int)rank * chunk + tid; idx < i1; idx += blockDim.x) {
             const int r = idx / D;
             float m[kMaxClusterParts], l[kMaxClusterParts], a[kMaxClusterParts];
 #pragma unroll
             for (int q = 0; q < kMaxClusterParts; ++q) {
                 if (q < P) {
-                    m[q] = ld_cluster_f32(rbase[q] + 4u * (G * D + r));
-                    l[q] = ld_cluster_f32(rbase[q] + 4u * (G * D + G + r));
+                    m[q] = ld_cluster_f32(rbase[q] + 4u * (R * D + r));
+                    l[q] = ld_cluster_f32(rbase[q] + 4u * (R * D + R + r));
                     a[q] = ld_cluster_f32(rbase[q] + 4u * idx);
                 }
             }
@@ -600,16 +638,16 @@ __global__ void __launch_bounds__(256, 1)
                     Ls = fmaf(f, l[q], Ls);
                 }
             }
-            store_out(p.out, ((size_t)b * p.num_heads + kvh * G) * D + idx,
-                      Ls > 0.f ? A / Ls : 0.f, p.out_dtype);
+            store_out(p.out, row_off(b, kvh, r) + idx % D, Ls > 0.f ? A / Ls : 0.f,
+                      p.out_dtype);
         }
         cluster_sync_relaxed();  // no CTA leaves while others still read its shared memory
     }
 }
 
-template <int D, int BS, typename KV>
+template <int D, int BS, typename KV, bool MULTI>
 cudaError_t launch_attn_inst(const AttnLaunch& L, cudaStream_t stream) {
-    auto kern = attn_kernel<D, BS, KV>;
+    auto kern = attn_kernel<D, BS, KV, MULTI>;
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          (int)L.smem_bytes);
     if (e != cudaSuccess) return e;
@@ -637,15 +675,15 @@ cudaError_t launch_attn_inst(const AttnLaunch& L, cudaStream_t stream) {
     return cudaLaunchKernelEx(&cfg, kern, L.tmap_k, L.tmap_v, L.p);
 }
 
-template <int D>
+template <int D, bool MULTI>
 cudaError_t launch_attn_for_d(const AttnLaunch& L, cudaStream_t stream) {
     const bool bf = L.kv_dtype == PA_BF16;
     if (L.block_size == 16)
-        return bf ? launch_attn_inst<D, 16, __nv_bfloat16>(L, stream)
-                  : launch_attn_inst<D, 16, __half>(L, stream);
+        return bf ? launch_attn_inst<D, 16, __nv_bfloat16, MULTI>(L, stream)
+                  : launch_attn_inst<D, 16, __half, MULTI>(L, stream);
     if (L.block_size == 32)
-        return bf ? launch_attn_inst<D, 32, __nv_bfloat16>(L, stream)
-                  : launch_attn_inst<D, 32, __half>(L, stream);
+        return bf ? launch_attn_inst<D, 32, __nv_bfloat16, MULTI>(L, stream)
+                  : launch_attn_inst<D, 32, __half, MULTI>(L, stream);
     return cudaErrorInvalidValue;
 }
 

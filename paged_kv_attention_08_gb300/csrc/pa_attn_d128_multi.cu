@@ -1,0 +1,9 @@
+// Instantiations of the multi-token decode kernel (several query tokens per
+// sequence) for head_dim 128.
+#include "pa_attn.cuh"
+
+namespace pa {
+cudaError_t launch_attn_d128_multi(const AttnLaunch& L, cudaStream_t stream) {
+    return launch_attn_for_d<128, true>(L, stream);
+}
+}  // namespace pa

@@ -1,9 +1,10 @@
-// Instantiations of the decode kernel for head_dim 256 (kept in their own
-// translation unit so that the library builds in parallel).
+// Instantiations of the one-token decode kernel for head_dim 256 (kept in
+// their own translation unit so that the library builds in parallel).
 #include "pa_attn.cuh"
 
 namespace pa {
 cudaError_t launch_attn_d256(const AttnLaunch& L, cudaStream_t stream) {
-    return launch_attn_for_d<256>(L, stream);
+    if (L.p.q_len > 1) return launch_attn_d256_multi(L, stream);
+    return launch_attn_for_d<256, false>(L, stream);
 }
 }  // namespace pa

@@ -2,7 +2,8 @@
 //
 // Combine (flash-decoding-bench "design.md": each chunk's local max, sum and
 // weighted values are reduced into the final output): for query head h of
-// sequence b, with partitions p holding (m_p, l_p, acc_p) in base-2 units,
+// query token qi of sequence b, with partitions p holding (m_p, l_p, acc_p)
+// in base-2 units,
 //     M = max_p m_p,   L = sum_p 2^(m_p - M) l_p,
 //     out = sum_p 2^(m_p - M) acc_p / L.
 // Partitions past the sequence's context are never read; an empty partition
@@ -14,7 +15,7 @@ namespace pa {
 
 namespace {
 
-// One CTA of 256 threads per (query head, sequence).  Every thread loads the
+// One CTA of 256 threads per (query token and head, sequence).  Every thread loads the
 // (m, l) of a few partitions; two block reductions give the maximum and the
 // weighted normaliser.  The threads then form PGRP groups over the
 // partitions, each thread a 16-byte slice of the head dimension, so that all
@@ -34,8 +35,10 @@ __global__ void __launch_bounds__(kCombineThreads) combine_kernel(const CombineP
     grid_launch_dependents();
 
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-    const int h = blockIdx.x, b = blockIdx.y;
-    const int kvh = h / p.group, g = h % p.group;
+    const int h = (int)blockIdx.x % p.num_heads, qi = (int)blockIdx.x / p.num_heads;
+    const int b = blockIdx.y;
+    const int kvh = h / p.group;
+    const int U = p.q_len * p.group, u = qi * p.group + h % p.group;  // rows of a unit; this row
     const int T = reachable_tokens(p.context_lens, b, p.max_blocks, p.block_size);
     const int npages = (T + p.block_size - 1) / p.block_size;
     const int nparts = min((npages + p.part_pages - 1) / p.part_pages, p.num_parts);
@@ -44,7 +47,7 @@ __global__ void __launch_bounds__(kCombineThreads) combine_kernel(const CombineP
     const float2* ml = reinterpret_cast<const float2*>(p.part_ml);
 
     float mx = NEG_INF;
-    for (int q = tid; q < nparts; q += kCombineThreads) mx = fmaxf(mx, ml[(row0 + q) * p.group + g].x);
+    for (int q = tid; q < nparts; q += kCombineThreads) mx = fmaxf(mx, ml[(row0 + q) * U + u].x);
 #pragma unroll
     for (int m = 16; m >= 1; m >>= 1) mx = fmaxf(mx, __shfl_xor_sync(kFullMask, mx, m));
     if (lane == 0) red[warp] = mx;
@@ -56,7 +59,7 @@ __global__ void __launch_bounds__(kCombineThreads) combine_kernel(const CombineP
 
     float ls = 0.f;
     for (int q = tid; q < nparts; q += kCombineThreads) {
-        const float2 v = ml[(row0 + q) * p.group + g];
+        const float2 v = ml[(row0 + q) * U + u];
         const float w = (v.x == NEG_INF) ? 0.f : exp2f(v.x - mx);
         weight[q] = w;
         ls = fmaf(w, v.y, ls);
@@ -73,8 +76,8 @@ __global__ void __launch_bounds__(kCombineThreads) combine_kernel(const CombineP
     const int pg = tid / SLICES, sl = tid % SLICES;
     float4 a = make_float4(0.f, 0.f, 0.f, 0.f);
     if (!empty) {
-        const float4* src = reinterpret_cast<const float4*>(p.part_acc + (row0 * p.group + g) * D) + sl;
-        const size_t stride = (size_t)p.group * SLICES;  // float4s between partitions
+        const float4* src = reinterpret_cast<const float4*>(p.part_acc + (row0 * U + u) * D) + sl;
+        const size_t stride = (size_t)U * SLICES;  // float4s between partitions
 #pragma unroll 4
         for (int q = pg; q < nparts; q += PGRP) {
             const float w = weight[q];
@@ -96,7 +99,7 @@ __global__ void __launch_bounds__(kCombineThreads) combine_kernel(const CombineP
             a.w += x.w;
         }
         const float inv = empty ? 0.f : 1.f / ls;
-        const size_t o = ((size_t)b * p.num_heads + h) * D + sl * 4;
+        const size_t o = (((size_t)b * p.q_len + qi) * p.num_heads + h) * D + sl * 4;
         store_out(p.out, o, a.x * inv, p.out_dtype);
         store_out(p.out, o + 1, a.y * inv, p.out_dtype);
         store_out(p.out, o + 2, a.z * inv, p.out_dtype);
@@ -108,9 +111,11 @@ __global__ void __launch_bounds__(kCombineThreads) combine_kernel(const CombineP
 // [c*W/C, (c+1)*W/C) of the flattened (sequence, kv head, page) order and
 // wrote every unit it covered whole; a unit spread over CTAs c0..c1 left one
 // record in each: slot 1 of c0 when the unit began inside c0's range (slot 0
-// when exactly at its start), slot 0 of every later CTA.  One CTA per (query
+// when exactly at its start), slot 0 of every later CTA whose share is not
+// empty (with more CTAs than pages, some CTAs take no page and write nothing).  One CTA per (query
 // head, sequence) finds its unit's CTAs from the same arithmetic and merges
-// their records as the partition combine does.
+// their records as the partition combine does.  Records hold every row of a
+// unit: [C][2][Q * G].
 template <int D>
 __global__ void __launch_bounds__(kCombineThreads) combine_balanced_kernel(const CombineParams p) {
     constexpr int SLICES = D / 4;
@@ -124,9 +129,11 @@ __global__ void __launch_bounds__(kCombineThreads) combine_balanced_kernel(const
     grid_launch_dependents();
 
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-    const int h = blockIdx.x, b = blockIdx.y;
+    const int h = (int)blockIdx.x % p.num_heads, qi = (int)blockIdx.x / p.num_heads;
+    const int b = blockIdx.y;
     const int Hkv = p.num_kv_heads;
-    const int kvh = h / p.group, g = h % p.group;
+    const int kvh = h / p.group;
+    const int U = p.q_len * p.group, u = qi * p.group + h % p.group;
     if (warp == 0) {
         long long all = 0, before = 0;
         for (int b0 = lane; b0 < p.batch; b0 += 32) {
@@ -149,7 +156,7 @@ __global__ void __launch_bounds__(kCombineThreads) combine_balanced_kernel(const
     const long long W = span[0];
     const int T = reachable_tokens(p.context_lens, b, p.max_blocks, p.block_size);
     const int np = (T + p.block_size - 1) / p.block_size;
-    const size_t o = ((size_t)b * p.num_heads + h) * D;
+    const size_t o = (((size_t)b * p.q_len + qi) * p.num_heads + h) * D;
     if (np == 0) {  // no page, no CTA: the empty-context result
         for (int d = tid; d < D; d += kCombineThreads) store_out(p.out, o + d, 0.f, p.out_dtype);
         return;
@@ -163,12 +170,18 @@ __global__ void __launch_bounds__(kCombineThreads) combine_balanced_kernel(const
     auto rec_row = [&](int k) -> size_t {
         const long long c = c0 + k;
         const int slotk = (k == 0 && c0_tail) ? 1 : 0;
-        return ((size_t)c * 2 + slotk) * p.group + g;
+        return ((size_t)c * 2 + slotk) * U + u;
+    };
+    // CTA c0 + k wrote a record only if its share [c*W/C, (c+1)*W/C) is not empty
+    auto live = [&](int k) -> bool {
+        const long long c = c0 + k;
+        return (c + 1) * W / Cn > c * W / Cn;
     };
     const float2* ml = reinterpret_cast<const float2*>(p.part_ml);
 
     float mx = NEG_INF;
-    for (int k = tid; k < nrec; k += kCombineThreads) mx = fmaxf(mx, ml[rec_row(k)].x);
+    for (int k = tid; k < nrec; k += kCombineThreads)
+        if (live(k)) mx = fmaxf(mx, ml[rec_row(k)].x);
 #pragma unroll
     for (int m = 16; m >= 1; m >>= 1) mx = fmaxf(mx, __shfl_xor_sync(kFullMask, mx, m));
     if (lane == 0) red[warp] = mx;
@@ -179,10 +192,13 @@ __global__ void __launch_bounds__(kCombineThreads) combine_balanced_kernel(const
     __syncthreads();
     float ls = 0.f;
     for (int k = tid; k < nrec; k += kCombineThreads) {
-        const float2 v = ml[rec_row(k)];
-        const float w = (v.x == NEG_INF) ? 0.f : exp2f(v.x - mx);
+        float w = 0.f;
+        if (live(k)) {
+            const float2 v = ml[rec_row(k)];
+            w = (v.x == NEG_INF) ? 0.f : exp2f(v.x - mx);
+            ls = fmaf(w, v.y, ls);
+        }
         weight[k] = w;
-        ls = fmaf(w, v.y, ls);
     }
 #pragma unroll
     for (int m = 16; m >= 1; m >>= 1) ls += __shfl_xor_sync(kFullMask, ls, m);
@@ -198,6 +214,7 @@ __global__ void __launch_bounds__(kCombineThreads) combine_balanced_kernel(const
     if (!empty) {
         for (int k = pg; k < nrec; k += PGRP) {
             const float w = weight[k];
+            if (w == 0.f) continue;  // no record (or an empty one): nothing to add
             const float4 x = reinterpret_cast<const float4*>(p.part_acc + rec_row(k) * D)[sl];
             a.x = fmaf(w, x.x, a.x);
             a.y = fmaf(w, x.y, a.y);

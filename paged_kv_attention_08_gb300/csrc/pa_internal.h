@@ -13,14 +13,18 @@ namespace pa {
 
 
 struct AttnParams {
-    const void* q;            // [B, H, D] kv dtype
-    void* out;                // [B, H, D] out dtype (final mode)
+    const void* q;            // [B, Q, H, D] kv dtype
+    void* out;                // [B, Q, H, D] out dtype (final mode)
     const int32_t* block_tables;
     const int32_t* context_lens;
-    float* part_acc;          // [B, Hkv, P, G, D] fp32 (split mode)
-    float* part_ml;           // [B, Hkv, P, G, 2] fp32 (split mode): running max (log2 units), normaliser
+    float* part_acc;          // [B, Hkv, P, Q*G, D] fp32 (split mode)
+    float* part_ml;           // [B, Hkv, P, Q*G, 2] fp32 (split mode): running max (log2 units), normaliser
     int32_t* err;             // device error word
     int32_t batch, num_heads, num_kv_heads, group, max_blocks;
+    int32_t q_len;            // Q: query tokens per sequence (1 for a one-token decode)
+    int32_t q_chunk;          // query tokens per CTA (q_chunk * group <= 16 MMA rows);
+                              // gridDim.y = num_kv_heads * ceil(Q / q_chunk)
+    int32_t unit_rows;        // Q * group: workspace rows of one (sequence, kv head, partition)
     int64_t num_blocks;
     float qscale;             // scale * log2(e): scores are kept in base-2 units
     int32_t part_pages;       // pages per partition
@@ -45,6 +49,7 @@ struct CombineParams {
     const float* part_acc;
     const float* part_ml;
     int32_t batch, num_heads, num_kv_heads, group, max_blocks, block_size;
+    int32_t q_len;     // query tokens per sequence; gridDim.x = q_len * num_heads
     int32_t part_pages, num_parts, out_dtype;
     int32_t num_ctas;  // balanced split: CTAs of the attention kernel (records [C][2][G])
 };
@@ -91,10 +96,10 @@ __host__ __device__ inline AttnSmem attn_smem_layout(int D, int BS, int nt, int 
     return L;
 }
 
-// Floats the final merge needs in the stage area: per warp, acc rows of the
-// group's heads over that warp's output columns, m and l per head, the
-// streams' weights and per-row totals; then the CTA's merged partial
-// (acc [G][D], m [G], l [G]) that the other CTAs of a cluster read, and the
+// Floats the final merge needs in the stage area for R rows (query token,
+// head pairs): per warp, acc rows over that warp's output columns, m and l per
+// row, the streams' weights and per-row totals; then the CTA's merged partial
+// (acc [R][D], m [R], l [R]) that the other CTAs of a cluster read, and the
 // cluster's per-rank statistics.
 __host__ __device__ inline uint32_t merge_floats(int nw, int G, int cols_per_warp) {
     return (uint32_t)nw * G * cols_per_warp + 3u * nw * G + 4u * G;
@@ -122,10 +127,14 @@ struct AttnLaunch {
     uint32_t smem_bytes;
 };
 
-// Per-head_dim launchers (one translation unit each, compiled in parallel).
+// Per-head_dim launchers (one translation unit each, compiled in parallel);
+// with q_len > 1 they hand over to the multi-token instantiations.
 cudaError_t launch_attn_d64(const AttnLaunch& L, cudaStream_t stream);
 cudaError_t launch_attn_d128(const AttnLaunch& L, cudaStream_t stream);
 cudaError_t launch_attn_d256(const AttnLaunch& L, cudaStream_t stream);
+cudaError_t launch_attn_d64_multi(const AttnLaunch& L, cudaStream_t stream);
+cudaError_t launch_attn_d128_multi(const AttnLaunch& L, cudaStream_t stream);
+cudaError_t launch_attn_d256_multi(const AttnLaunch& L, cudaStream_t stream);
 
 cudaError_t launch_combine(const CombineParams& p, int head_dim, dim3 grid, bool pdl,
                            cudaStream_t stream);

@@ -13,7 +13,10 @@ Shapes and distributions follow the benchmark set-up on the pages:
   - MiniVLLM docs "Decoding Benchmark", table "Benchmark configurations": the
     (batch, seq_len) sweep with 32 query heads, 8 kv heads, head_dim 128 and
     block_size 16.
-plus the ragged, long-context and MQA workloads this library is measured on.
+plus the ragged, long-context and MQA workloads this library is measured on,
+and multi-token steps (q_len > 1: speculative verification of drafted
+tokens, a short chunk of new tokens) whose query is [batch, q_len,
+num_heads, head_dim] and whose context lengths count the new tokens.
 
 Recipe (identical for every workload):
   1. The index structure (context lengths, block tables) is drawn on the CPU
@@ -52,6 +55,7 @@ class Spec:
     q_std: float = 1.0
     kv_std: float = 1.0
     partition_tokens: int = 0  # split-KV partition size this workload runs with (0: automatic)
+    q_len: int = 1             # query tokens per sequence (q is [B, H, D] when 1, else [B, Q, H, D])
 
 
 def _sweep(b, t):
@@ -73,6 +77,15 @@ SPECS = {s.name: s for s in [
     _long(4, 8192), _long(4, 32768), _long(4, 131072),
     Spec("mqa_b32_t16384", 32, 16, 1, 256, 32, torch.bfloat16, "fixed:16384", pool="factor:1.1",
          q_std=1.0, kv_std=0.5),
+    # multi-token steps: a small case with a sequence shorter than q_len, four
+    # drafted tokens per sequence (4 tokens x 4 heads fill the 16 MMA rows),
+    # eight (two CTAs per kv head), and a 64-token chunk with MQA-like groups
+    Spec("tiny_q3", 3, 32, 8, 128, 16, torch.float16, "list:2,37,60", pool="fixed:12",
+         max_blocks=4, q_len=3),
+    Spec("spec_b16_t2048_q4", 16, 32, 8, 128, 16, torch.float16, "fixed:2048", q_len=4),
+    Spec("spec_b4_t8192_q8", 4, 32, 8, 128, 16, torch.bfloat16, "fixed:8192", q_len=8),
+    Spec("chunk_b2_t4096_q64", 2, 16, 1, 256, 32, torch.bfloat16, "fixed:4096", pool="factor:1.1",
+         kv_std=0.5, q_len=64),
 ]}
 
 # Named groups of workloads; a group is run as a sequence of decode calls.
@@ -83,6 +96,7 @@ GROUPS = {
     "long": ["long_b1_t8192", "long_b1_t32768", "long_b1_t131072",
              "long_b4_t8192", "long_b4_t32768", "long_b4_t131072"],
     "mqa": ["mqa_b32_t16384"],
+    "multi": ["spec_b16_t2048_q4", "spec_b4_t8192_q8", "chunk_b2_t4096_q64"],
 }
 # every single workload is also a group of its own
 GROUPS.update({name: [name] for name in SPECS if name not in GROUPS})
@@ -170,7 +184,9 @@ def make(spec, seed: int = 0, device="cpu") -> Inputs:
         cursor += n
 
     gv = torch.Generator(device=device).manual_seed(seed + 1)
-    q = torch.empty(spec.batch, spec.num_heads, spec.head_dim, dtype=spec.dtype, device=device)
+    qshape = (spec.batch, spec.num_heads, spec.head_dim) if spec.q_len == 1 else \
+        (spec.batch, spec.q_len, spec.num_heads, spec.head_dim)
+    q = torch.empty(qshape, dtype=spec.dtype, device=device)
     k = torch.empty(pool, bs, spec.num_kv_heads, spec.head_dim, dtype=spec.dtype, device=device)
     v = torch.empty_like(k)
     _randn_into(q, spec.q_std, gv)

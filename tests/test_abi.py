@@ -36,7 +36,8 @@ def test_library_exports_every_declared_symbol(lib):
     names = declared_entry_points()
     assert {"pa_decode", "pa_decode_splitkv", "pa_workspace_size", "pa_resolve_blocks",
             "pa_status_string", "pa_choose_partition_tokens", "pa_device_error",
-            "pa_selftest_wait_timeout", "pa_decode_splitkv_noalloc"} <= set(names)
+            "pa_selftest_wait_timeout", "pa_decode_splitkv_noalloc", "pa_decode_multi",
+            "pa_workspace_size_multi"} <= set(names)
     for n in names:
         assert hasattr(lib, n), f"{n} declared in include/ but not exported"
 
@@ -95,6 +96,45 @@ def test_pointer_validation(lib):
     e = shape(batch=0)
     assert lib.pa_decode(None, None, None, None, None, None, ctypes.byref(e), 0.1, None) == 0
     assert lib.pa_resolve_blocks(None, FAKE, FAKE, ctypes.byref(s), None) == 1
+
+
+@pytest.mark.parametrize("scale", [0.0, -0.1, float("inf"), float("nan")])
+def test_scale_must_be_positive_and_finite(lib, scale):
+    s = shape()
+    assert lib.pa_decode(FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, ctypes.byref(s), scale, None) == 1
+    assert lib.pa_decode_splitkv(FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, ctypes.byref(s), scale, 100, 0,
+                                 FAKE, 1 << 20, None) == 1
+    assert lib.pa_decode_multi(FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, ctypes.byref(s), 2, scale, 100,
+                               0, FAKE, 1 << 20, None) == 1
+    assert lib.pa_decode_splitkv_noalloc(FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, ctypes.byref(s), scale,
+                                         100, 0, None) == 1
+
+
+def test_multi_token_validation(lib):
+    s = shape()
+    for q_len in (0, -3):
+        assert lib.pa_decode_multi(FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, ctypes.byref(s), q_len, 0.1,
+                                   100, 0, FAKE, 1 << 20, None) == 1
+        assert lib.pa_workspace_size_multi(ctypes.byref(s), q_len, 100, 16) == 0
+    bad = shape(head_dim=96)
+    assert lib.pa_decode_multi(FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, ctypes.byref(bad), 2, 0.1, 100,
+                               0, FAKE, 1 << 20, None) == 2
+    e = shape(batch=0)
+    assert lib.pa_decode_multi(None, None, None, None, None, None, ctypes.byref(e), 4, 0.1, 0, 0,
+                               None, 0, None) == 0
+
+
+def test_multi_token_workspace_size(lib):
+    # B=4, H=32 (G=4), q_len 6: rows per partition B*H*Q; 131072 tokens in 256 partitions of 512
+    s = shape(batch=4, max_blocks_per_seq=8192)
+    rows = 4 * 32 * 6 * 256
+    acc = rows * 128 * 4
+    want = (acc + 255) // 256 * 256 + rows * 2 * 4
+    assert lib.pa_workspace_size_multi(ctypes.byref(s), 6, 131072, 512) == want
+    assert lib.pa_workspace_size_multi(ctypes.byref(s), 1, 131072, 512) == \
+        lib.pa_workspace_size(ctypes.byref(s), 131072, 512)
+    assert lib.pa_workspace_size_multi(ctypes.byref(s), 6, 131072, 131072) == 0   # one partition
+    assert lib.pa_workspace_size_multi(ctypes.byref(s), 6, 8 * 512, 512) == 0     # cluster
 
 
 def test_selftest_rejects_bad_limits(lib):

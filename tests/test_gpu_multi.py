@@ -1,0 +1,167 @@
+"""GPU parity of the multi-token step (q_len > 1, causal over the new tokens)
+through the C ABI, against the fp64 oracle.
+
+Bar: max |gpu - oracle| <= 2e-3 on fp32 output, as for the one-token decode.
+Covered: every group size with q_len up to and past one CTA's 16 MMA rows
+(query chunks), sequences shorter than q_len (query tokens that see nothing),
+masked table entries, every split mode (one pass, cluster, workspace,
+balanced), the q-dtype output, and the full-size multi-token workloads on
+sampled rows.
+"""
+import math
+
+import numpy as np
+import pytest
+import torch
+
+import oracle
+import paged_kv_attention_08_gb300 as pa
+from paged_kv_attention_08_gb300 import workloads
+
+pytestmark = pytest.mark.gpu
+
+TOL = 2e-3
+DEV = "cuda:0"
+
+
+def run(x, partition_tokens=0, out_dtype=torch.float32):
+    """One call; the workspace is filled with NaN first, so that a read of a
+    partial that no CTA wrote shows in the output."""
+    out = torch.full(x.q.shape, float("nan"), dtype=out_dtype, device=x.q.device)
+    need = pa.workspace_size_multi(x.q, x.k_cache, x.block_tables, out_dtype, x.max_context_len,
+                                   partition_tokens)
+    ws = torch.full((max(need, 16) // 4 + 1,), float("nan"), dtype=torch.float32, device=x.q.device)
+    pa.decode_multi(out, x.q, x.k_cache, x.v_cache, x.block_tables, x.context_lens, x.scale,
+                    x.max_context_len, partition_tokens, workspace=ws)
+    torch.cuda.synchronize()
+    return out
+
+
+def check(got, want, tol=TOL):
+    g = got.double().cpu().numpy()
+    assert np.isfinite(g).all(), "non-finite output"
+    err = np.abs(g - want).max()
+    assert err <= tol, f"max abs err {err:.3e} > {tol}"
+
+
+def multi_case(seed, B, Q, H, Hkv, D, bs, lens, dtype=torch.bfloat16, spare=3, mb_extra=1):
+    g = torch.Generator().manual_seed(seed)
+    pages = [(t + bs - 1) // bs for t in lens]
+    mb = max(1, max(pages)) + mb_extra
+    pool = sum(pages) + spare
+    perm = torch.randperm(pool, generator=g)
+    bt = torch.full((B, mb), -1, dtype=torch.int32)
+    c = 0
+    for b, n in enumerate(pages):
+        bt[b, :n] = perm[c:c + n].to(torch.int32)
+        c += n
+    spec = workloads.Spec("case", B, H, Hkv, D, bs, dtype, "list:" + ",".join(map(str, lens)),
+                          q_len=Q)
+    return workloads.Inputs(spec, torch.randn(B, Q, H, D, generator=g).to(dtype),
+                            torch.randn(pool, bs, Hkv, D, generator=g).to(dtype),
+                            torch.randn(pool, bs, Hkv, D, generator=g).to(dtype),
+                            bt, torch.tensor(lens, dtype=torch.int32), 1.0 / math.sqrt(D),
+                            max(lens), list(lens))
+
+
+def oracle_of(x):
+    return oracle.decode_multi(x.q, x.k_cache, x.v_cache, x.block_tables, x.context_lens, x.scale)
+
+
+# (B, Q, H, Hkv, D, bs, lens): groups 1..16, Q below, at and past 16 / group
+CASES = [
+    (3, 2, 8, 8, 64, 16, [1, 37, 200]),       # G=1, 2 rows of 16
+    (2, 16, 8, 8, 64, 32, [16, 333]),          # G=1, exactly 16 rows; T = Q
+    (2, 17, 4, 4, 128, 16, [40, 129]),         # G=1, two chunks (16 + 1)
+    (2, 3, 16, 8, 128, 16, [129, 7]),          # G=2
+    (3, 4, 32, 8, 128, 16, [2, 64, 300]),      # G=4, 16 rows, one sequence shorter than Q
+    (2, 5, 32, 8, 128, 32, [500, 31]),         # G=4, two chunks (4 + 1)
+    (2, 2, 16, 2, 128, 16, [77, 1]),           # G=8
+    (2, 3, 16, 1, 256, 32, [1000, 33]),        # G=16, three chunks of one token
+    (2, 6, 8, 4, 256, 16, [100, 401]),         # G=2, 12 rows
+]
+IDS = [f"B{c[0]}Q{c[1]}H{c[2]}kv{c[3]}D{c[4]}bs{c[5]}" for c in CASES]
+
+
+@pytest.mark.parametrize("dtype", [torch.float16, torch.bfloat16])
+@pytest.mark.parametrize("case", CASES, ids=IDS)
+def test_multi_token_vs_oracle(case, dtype):
+    B, Q, H, Hkv, D, bs, lens = case
+    x = multi_case(13, B, Q, H, Hkv, D, bs, lens, dtype)
+    want = oracle_of(x)
+    xd = x.to(DEV)
+    pages = -(-max(lens) // bs)
+    # one pass, automatic, two-page partitions (workspace), <= 8 partitions (cluster)
+    for pt in [pages * bs, 0, 2 * bs, -(-pages // min(pages, 8)) * bs]:
+        check(run(xd, pt), want)
+
+
+@pytest.mark.parametrize("case", [CASES[0], CASES[3], CASES[4], CASES[6]], ids=lambda c: f"Q{c[1]}H{c[2]}kv{c[3]}")
+def test_multi_token_balanced(case):
+    """The balanced split keeps all of a unit's query tokens in one CTA."""
+    B, Q, H, Hkv, D, bs, lens = case
+    x = multi_case(17, B, Q, H, Hkv, D, bs, lens)
+    want = oracle_of(x)
+    xd = x.to(DEV)
+    assert Q * (H // Hkv) <= 16
+    for _ in range(2):
+        check(run(xd, pa.PARTITION_BALANCED), want)
+
+
+def test_multi_token_one_token_equals_decode():
+    """q_len = 1 through the multi-token entry point is the one-token decode, bit for bit."""
+    x = workloads.make("sweep_b4_t2048", seed=3, device=DEV)
+    ref = torch.empty(x.q.shape, dtype=torch.float32, device=DEV)
+    pa.decode_splitkv(ref, x.q, x.k_cache, x.v_cache, x.block_tables, x.context_lens, x.scale,
+                      x.max_context_len, 0)
+    got = torch.empty((x.q.shape[0], 1) + tuple(x.q.shape[1:]), dtype=torch.float32, device=DEV)
+    pa.decode_multi(got, x.q[:, None].contiguous(), x.k_cache, x.v_cache, x.block_tables,
+                    x.context_lens, x.scale, x.max_context_len, 0)
+    torch.cuda.synchronize()
+    assert torch.equal(got[:, 0], ref)
+
+
+def test_multi_token_masking_and_qdtype_output():
+    x = multi_case(19, 4, 4, 16, 4, 128, 16, [0, 3, 50, 90], torch.float16, mb_extra=0)
+    NB = x.k_cache.shape[0]
+    bt = x.block_tables.clone()
+    bt[3, 1] = -1           # an unallocated page inside the context
+    bt[2, 0] = NB + 3       # an id outside the pool
+    x.block_tables = bt
+    want = oracle_of(x)
+    assert np.all(want[0] == 0) and np.all(want[1, 3] != 0) and np.all(want[1, 0] == 0)
+    xd = x.to(DEV)
+    for pt in [0, 16, 32]:
+        check(run(xd, pt), want)
+    got = run(xd, 0, out_dtype=torch.float16).double().cpu().numpy()
+    want_r = torch.from_numpy(want).to(torch.float16).double().numpy()
+    a = np.abs(want_r)
+    ulp = np.where(a > 0, 2.0 ** (np.floor(np.log2(np.where(a > 0, a, 1.0))) - 10), 2.0 ** -24)
+    assert (np.abs(got - want_r) <= TOL + ulp).all()
+
+
+def test_tiny_q3_workload():
+    x = workloads.make("tiny_q3", seed=0, device=DEV)
+    want = oracle_of(x.to("cpu"))
+    for pt in [0, 16, 64]:
+        check(run(x, pt), want)
+
+
+@pytest.mark.parametrize("name", ["spec_b16_t2048_q4", "spec_b4_t8192_q8", "chunk_b2_t4096_q64"])
+def test_multi_token_full_size_sampled(name):
+    """Full-size multi-token workloads, automatic split; sampled (b, token, head)
+    rows through the oracle's one-token decode of each token's causal prefix."""
+    x = workloads.make(name, seed=0, device=DEV)
+    got = run(x, 0)
+    assert torch.isfinite(got).all()
+    host = x.to("cpu")
+    B, Q, H, _ = host.q.shape
+    g = np.random.default_rng(1)
+    for i in sorted({0, Q - 1, int(g.integers(Q))}):
+        rows = np.array(sorted({(0, 0), (B - 1, H - 1)} |
+                               {(int(g.integers(B)), int(g.integers(H))) for _ in range(6)}),
+                        dtype=np.int32)
+        prefix = torch.clamp(host.context_lens - Q + i + 1, min=0)
+        want = oracle.decode_rows(host.q[:, i].contiguous(), host.k_cache, host.v_cache,
+                                  host.block_tables, prefix, host.scale, rows)
+        check(got[rows[:, 0], i, rows[:, 1]], want)

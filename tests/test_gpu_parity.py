@@ -26,8 +26,13 @@ def run(x, mode="single", out_dtype=torch.float32, partition_tokens=0):
     if mode == "single":
         pa.decode(out, x.q, x.k_cache, x.v_cache, x.block_tables, x.context_lens, x.scale)
     else:
+        # a NaN-filled workspace: a read of a partial that no CTA wrote shows
+        need = pa.workspace_size(x.q, x.k_cache, x.block_tables, out_dtype, x.max_context_len,
+                                 partition_tokens)
+        ws = torch.full((max(need, 16) // 4 + 1,), float("nan"), dtype=torch.float32,
+                        device=x.q.device)
         pa.decode_splitkv(out, x.q, x.k_cache, x.v_cache, x.block_tables, x.context_lens, x.scale,
-                          x.max_context_len, partition_tokens)
+                          x.max_context_len, partition_tokens, workspace=ws)
     torch.cuda.synchronize()
     return out
 
@@ -168,6 +173,10 @@ BALANCED_CASES = [
     dict(B=5, H=8, Hkv=8, D=64, bs=16, lens=[1, 2, 3, 4, 5]),
     dict(B=1, H=32, Hkv=8, D=128, bs=32, lens=[7777]),
     dict(B=4, H=16, Hkv=2, D=64, bs=32, lens=[0, 0, 0, 0]),
+    # fewer pages than CTAs: empty shares lie between a unit's CTAs
+    dict(B=2, H=16, Hkv=8, D=128, bs=16, lens=[129, 7]),
+    dict(B=2, H=16, Hkv=2, D=128, bs=16, lens=[77, 1]),
+    dict(B=3, H=8, Hkv=8, D=64, bs=16, lens=[1, 37, 200]),
 ]
 
 
