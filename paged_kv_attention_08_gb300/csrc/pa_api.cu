@@ -183,6 +183,7 @@ struct Plan {
     bool many_ctas;  // the grid spans several waves: pick the two-CTAs-per-SM tune
     bool balanced;   // one CTA per SM, equal shares of the flattened page order
     int num_ctas;    // balanced: grid size
+    bool tile;       // several query tokens on the tcgen05 tile kernel (128-row tiles)
 };
 
 Plan plan_with(const pa_shape* s, int pages, int pp, bool cluster_ok) {
@@ -190,6 +191,7 @@ Plan plan_with(const pa_shape* s, int pages, int pp, bool cluster_ok) {
     p.many_ctas = false;
     p.balanced = false;
     p.num_ctas = 0;
+    p.tile = false;
     if (pp < 1) pp = 1;
     p.num_parts = (pages + pp - 1) / pp;
     if (p.num_parts < 1) p.num_parts = 1;
@@ -272,10 +274,60 @@ bool clusters_enabled() {
     return !off;
 }
 
+// Which kernel serves several query tokens: the tcgen05 tile kernel once
+// the rows of a (sequence, kv head) -- q_len * group -- exceed the 16 rows
+// of the warp-level MMA path (which would otherwise read the pages once per
+// 16 rows).  PA_MULTI_KERNEL=mma or =tile forces one of them for every
+// q_len > 1 (a testing and tuning switch; read on every call, results agree).
+bool use_tile(const pa_shape* s, int32_t q_len) {
+    if (q_len <= 1) return false;
+    const char* v = std::getenv("PA_MULTI_KERNEL");
+    if (v && std::strcmp(v, "mma") == 0) return false;
+    if (v && std::strcmp(v, "tile") == 0) return true;
+    return (int64_t)q_len * (s->num_heads / s->num_kv_heads) > 16;
+}
+
+int tile_ctas_per_sm(const pa_shape* s) {
+    const TileSmem L = tile_smem_layout(s->head_dim, s->block_size);
+    int n = (int)((227u * 1024u) / (L.total + kSmemAlignSlack));
+    const int by_tmem = (int)(512u / tile_tmem_cols(s->head_dim));
+    n = n < by_tmem ? n : by_tmem;
+    n = n < 2 ? n : 2;  // registers: 256 threads of up to ~128
+    return n < 1 ? 1 : n;
+}
+
+// Tile kernel split: units = B * Hkv * ceil(q_len*G / 128) CTAs unsplit; cut
+// each unit's pages into as many partitions (of at least 4 pages) as fit in
+// one wave of resident CTAs.  Partitions reduce through the workspace.
+Plan tile_plan(const pa_shape* s, int32_t max_context_len, int32_t partition_tokens, int num_sms,
+               int32_t q_len) {
+    const int pages = pages_for(s, max_context_len);
+    int pp;
+    if (partition_tokens > 0) {
+        pp = partition_tokens / s->block_size;
+    } else {
+        const int64_t rows = (int64_t)q_len * (s->num_heads / s->num_kv_heads);
+        const int64_t units = (int64_t)s->batch * s->num_kv_heads * ((rows + kTileRows - 1) / kTileRows);
+        const int64_t slots = (int64_t)num_sms * tile_ctas_per_sm(s);
+        int64_t parts = slots / units;  // whole waves: one partition more would add a wave
+        const int64_t max_parts = (pages + 3) / 4;
+        if (parts > max_parts) parts = max_parts;
+        if (parts < 1) parts = 1;
+        pp = (int)((pages + parts - 1) / parts);
+    }
+    Plan p = plan_with(s, pages, pp, false);
+    p.tile = true;
+    return p;
+}
+
 // The balanced split keeps every query token of a (sequence, kv head) in
 // one CTA: it needs q_len * group <= 16, and batch <= kMaxBalancedBatch.
 Plan make_plan(const pa_shape* s, int32_t max_context_len, int32_t partition_tokens, int num_sms,
                int32_t q_len = 1) {
+    if (use_tile(s, q_len))
+        return tile_plan(s, max_context_len,
+                         partition_tokens == PA_PARTITION_BALANCED ? 0 : partition_tokens, num_sms,
+                         q_len);
     Plan plan;
     const int q_chunks = q_chunks_for(s, q_len);
     if (partition_tokens == PA_PARTITION_BALANCED && s->batch <= kMaxBalancedBatch &&
@@ -414,6 +466,58 @@ pa_status launch_attention(void* out, const void* q, const void* k, const void* 
     return e == cudaSuccess ? PA_OK : PA_ERR_CUDA;
 }
 
+pa_status launch_tile(void* out, const void* q, const void* k, const void* v, const int32_t* bt,
+                      const int32_t* lens, const pa_shape* s, float scale, const Plan& plan,
+                      float* part_acc, float* part_ml, int32_t* err, cudaStream_t stream,
+                      int32_t q_len) {
+    AttnLaunch L;
+    std::memset(&L, 0, sizeof L);
+    const int G = s->num_heads / s->num_kv_heads;
+    const int64_t rows = (int64_t)q_len * G;
+    const int64_t grid_y = (int64_t)s->num_kv_heads * ((rows + kTileRows - 1) / kTileRows);
+    if (grid_y > 65535 || rows > 0x7fffffff) return PA_ERR_UNSUPPORTED;
+    pa_status st = encode_maps(s, k, v, &L.tmap_k, &L.tmap_v);
+    if (st != PA_OK) return st;
+    AttnParams& p = L.p;
+    p.q = q;
+    p.out = out;
+    p.block_tables = bt;
+    p.context_lens = lens;
+    p.part_acc = part_acc;
+    p.part_ml = part_ml;
+    p.err = err;
+    p.batch = s->batch;
+    p.num_heads = s->num_heads;
+    p.num_kv_heads = s->num_kv_heads;
+    p.group = G;
+    p.q_len = q_len;
+    p.q_chunk = kTileRows / G;
+    p.unit_rows = (int32_t)rows;
+    p.max_blocks = s->max_blocks_per_seq;
+    p.num_blocks = s->num_blocks;
+    p.qscale = scale * 1.4426950408889634f;  // log2(e)
+    p.part_pages = plan.part_pages;
+    p.num_parts = plan.num_parts;
+    p.out_dtype = s->out_dtype;
+    p.final_out = plan.num_parts <= 1 ? 1 : 0;
+    p.timeout_ns = kDefaultTimeoutNs;
+    L.head_dim = s->head_dim;
+    L.block_size = s->block_size;
+    L.kv_dtype = s->kv_dtype;
+    L.pdl = use_pdl();
+    L.cluster = 1;
+    L.grid = dim3((unsigned)plan.num_parts, (unsigned)grid_y, (unsigned)s->batch);
+    L.threads = kTileThreads;
+    L.smem_bytes = tile_smem_layout(s->head_dim, s->block_size).total + kSmemAlignSlack;
+    cudaError_t e;
+    switch (s->head_dim) {
+        case 64: e = launch_tile_d64(L, stream); break;
+        case 128: e = launch_tile_d128(L, stream); break;
+        default: e = launch_tile_d256(L, stream); break;
+    }
+    return e == cudaSuccess ? PA_OK : PA_ERR_CUDA;
+}
+
 }  // namespace
 }  // namespace pa
 
@@ -460,7 +564,7 @@ pa_status pa_decode(void* out, const void* q, const void* k_cache, const void* v
     st = device_state(&sms, &err);
     if (st != PA_OK) return st;
     Plan plan{shape->max_blocks_per_seq, 1, false,
-              (int64_t)shape->batch * shape->num_kv_heads > sms, false, 0};
+              (int64_t)shape->batch * shape->num_kv_heads > sms, false, 0, false};
     return launch_attention(out, q, k_cache, v_cache, block_tables, context_lens, shape, scale,
                             plan, nullptr, nullptr, err, static_cast<cudaStream_t>(stream));
 }
@@ -483,7 +587,10 @@ pa_status pa_decode_multi(void* out, const void* q, const void* k_cache, const v
     if (st != PA_OK) return st;
     const Plan plan = make_plan(shape, max_context_len, partition_tokens, sms, q_len);
     cudaStream_t cs = static_cast<cudaStream_t>(stream);
-    if (!plan.balanced && (plan.num_parts <= 1 || plan.cluster))
+    if (plan.tile && plan.num_parts <= 1)
+        return launch_tile(out, q, k_cache, v_cache, block_tables, context_lens, shape, scale, plan,
+                           nullptr, nullptr, err, cs, q_len);
+    if (!plan.tile && !plan.balanced && (plan.num_parts <= 1 || plan.cluster))
         return launch_attention(out, q, k_cache, v_cache, block_tables, context_lens, shape, scale,
                                 plan, nullptr, nullptr, err, cs, q_len);
 
@@ -494,8 +601,10 @@ pa_status pa_decode_multi(void* out, const void* q, const void* k_cache, const v
     if ((int64_t)q_len * shape->num_heads > 0x7fffffff) return PA_ERR_UNSUPPORTED;
     float* part_acc = static_cast<float*>(workspace);
     float* part_ml = reinterpret_cast<float*>(static_cast<char*>(workspace) + ml_off);
-    st = launch_attention(out, q, k_cache, v_cache, block_tables, context_lens, shape, scale, plan,
-                          part_acc, part_ml, err, cs, q_len);
+    st = plan.tile ? launch_tile(out, q, k_cache, v_cache, block_tables, context_lens, shape, scale,
+                                 plan, part_acc, part_ml, err, cs, q_len)
+                   : launch_attention(out, q, k_cache, v_cache, block_tables, context_lens, shape,
+                                      scale, plan, part_acc, part_ml, err, cs, q_len);
     if (st != PA_OK) return st;
     CombineParams c;
     c.out = out;

@@ -115,6 +115,67 @@ constexpr int kMaxClusterParts = 8;
 // align its base to 1024 bytes (TMA destinations).
 constexpr uint32_t kSmemAlignSlack = 1024;
 
+// Tile kernel (several query tokens, tcgen05).  A CTA walks its pages in
+// KV blocks of BN tokens (128, or 64 at head_dim 256): the pages of a block
+// are copied into consecutive rows of one stage, so that one MMA covers the
+// whole block.  Shared memory: the Q tile (128 rows x head_dim, 128-byte
+// swizzle, head_dim/64 column blocks of 16 KB), `ns` stages of a block's K
+// and V tiles (head_dim/64 column blocks of BN rows x 128 bytes each), then
+// the mbarriers and the physical block of every staged page.  K and V have
+// rings of their own (a K stage is free once S is computed, long before P V
+// has read the V stage), each fed by its own copy warp.
+constexpr int kTileRows = 128;
+constexpr int kTileThreads = 384;  // warp 0 copies K, warp 3 copies V, warp 1 issues
+                                   // MMAs, warp 2 owns tensor memory, warps 4-11 softmax
+                                   // (two warpgroups, one half of a block's columns each)
+
+__host__ __device__ constexpr int tile_block_tokens(int D) { return D == 256 ? 64 : 128; }
+// S / P buffers in tensor memory: S of block j + 2 may be computed while P of
+// block j still waits for its P V MMA.
+constexpr int kTileSBufs = 3;
+__host__ __device__ constexpr int tile_stages(int D) { return D == 64 ? 4 : 2; }
+
+struct TileSmem {
+    uint32_t tile_bytes;   // one K (or V) block tile: BN * head_dim * 2
+    uint32_t q_off;        // Q tile
+    uint32_t k_off;        // [ns] K stages
+    uint32_t v_off;        // [ns] V stages
+    uint32_t bar_off;      // mbarriers: k_full[ns], k_empty[ns], v_full[ns], v_empty[ns],
+                           // s_full[3], p_full[3], pv_done[3], final
+    uint32_t phys_off;     // [ns][BN / block_size] int32 physical block of each K stage's pages
+    uint32_t xchg_off;     // softmax exchange: row maxima [2][2][128], normalisers [2][128] (fp32),
+                           // then mbarriers xchg[2]
+    uint32_t misc_off;     // tensor-memory base address, abort flag
+    uint32_t total;
+    int ns;
+};
+
+__host__ __device__ inline TileSmem tile_smem_layout(int D, int BS) {
+    TileSmem L;
+    const int BN = tile_block_tokens(D);
+    L.ns = tile_stages(D);
+    L.tile_bytes = (uint32_t)BN * D * 2u;
+    L.q_off = 0;
+    L.k_off = 256u * D;
+    L.v_off = L.k_off + L.tile_bytes * L.ns;
+    uint32_t o = L.v_off + L.tile_bytes * L.ns;
+    L.bar_off = o;
+    o += 8u * (4 * L.ns + 3 * kTileSBufs + 1);
+    L.phys_off = o;
+    o += 4u * L.ns * (BN / BS);
+    L.xchg_off = pa_align_up(o, 16);
+    o = L.xchg_off + 4u * (2 * 2 * 128 + 2 * 128) + 16;
+    L.misc_off = pa_align_up(o, 16);
+    L.total = L.misc_off + 16;
+    return L;
+}
+
+// Tensor-memory columns of the tile kernel: O [head_dim], then kTileSBufs S
+// buffers of BN fp32 columns (P, as 16-bit high and low parts, overwrites S).
+__host__ __device__ constexpr uint32_t tile_tmem_cols(int D) {
+    return (uint32_t)D + kTileSBufs * tile_block_tokens(D) <= 256u ? 256u : 512u;
+}
+
 struct AttnLaunch {
     AttnParams p;
     CUtensorMap tmap_k;
@@ -135,6 +196,11 @@ cudaError_t launch_attn_d256(const AttnLaunch& L, cudaStream_t stream);
 cudaError_t launch_attn_d64_multi(const AttnLaunch& L, cudaStream_t stream);
 cudaError_t launch_attn_d128_multi(const AttnLaunch& L, cudaStream_t stream);
 cudaError_t launch_attn_d256_multi(const AttnLaunch& L, cudaStream_t stream);
+
+// Tile kernel (tcgen05) launchers, one translation unit per head_dim.
+cudaError_t launch_tile_d64(const AttnLaunch& L, cudaStream_t stream);
+cudaError_t launch_tile_d128(const AttnLaunch& L, cudaStream_t stream);
+cudaError_t launch_tile_d256(const AttnLaunch& L, cudaStream_t stream);
 
 cudaError_t launch_combine(const CombineParams& p, int head_dim, dim3 grid, bool pdl,
                            cudaStream_t stream);

@@ -1,0 +1,512 @@
+// Paged attention for many query rows per kv head on the Blackwell tensor
+// cores (tcgen05): several query tokens per sequence, causal over the new
+// tokens, where the rows of a (sequence, kv head) -- query token x head of
+// the group -- fill 128-row tiles.
+//
+// What it computes is the multi-token decode step (each query token i of
+// sequence b sits at position T - Q + i and attends to the cached tokens at
+// and before it; "benchmark_decoding.py" reference_output for the attention
+// itself, MiniVLLM docs "Decoding Benchmark" for the paged layout and the
+// online softmax, flash-decoding-bench "design.md" for the split into
+// partitions with a (max, sum, weighted values) partial each).
+//
+// One CTA per (sequence, 128-row tile and kv head, partition of pages); the
+// partition's pages are taken in KV blocks of BN tokens (128; 64 at
+// head_dim 256):
+//   - warp 0 streams the blocks: one lane per page reads its block-table entry
+//     and issues a 4-D TMA copy per 64-column block of the page's K and V
+//     tiles (128-byte swizzle) into consecutive rows of a stage, so that a
+//     block's pages form one BN-row operand;
+//   - warp 1 (one lane) issues the MMAs: S = Q K^T for a block (M = 128 rows,
+//     N = BN tokens, K = head_dim; Q and K from shared memory) into one of two
+//     S buffers in tensor memory, and O += P V (M = 128, N = head_dim,
+//     K = BN; P from tensor memory, V from shared memory, MN-major) into the
+//     O accumulator in tensor memory.  S of block j + 1 is computed while the
+//     softmax works on block j;
+//   - warps 4-11 (two warpgroups, one half of a block's columns each) own one
+//     row per thread (a tensor-memory lane): they read the row's scores, mask
+//     them (table reach and the row's causal limit), exchange the halves'
+//     maxima, keep the running max m and normaliser l in base-2 units,
+//     rescale O in tensor
+//     memory when the max moves by more than 2^8, and write P over S as a
+//     high and a low 16-bit part (two MMAs, ~16 significant bits), then the
+//     final O / l or the partial (m, l, O) for the combine kernel.
+// Every mbarrier wait is bounded: on timeout the kernel records
+// PA_ERR_TIMEOUT, the roles stop, and tensor memory is released.
+#pragma once
+
+#include <type_traits>
+
+#include "pa_device.cuh"
+#include "pa_tcgen05.cuh"
+
+namespace pa {
+
+constexpr float kTileRescaleSlack = 8.0f;  // log2 units: P may reach 2^8 before a rescale
+
+template <int D, int BS, typename KV>
+__global__ void __launch_bounds__(kTileThreads, 1)
+    tile_kernel(const __grid_constant__ CUtensorMap tmap_k,
+                const __grid_constant__ CUtensorMap tmap_v, const AttnParams p) {
+    constexpr int BN = tile_block_tokens(D);  // tokens per KV block
+    constexpr int NPB = BN / BS;              // pages per KV block
+    constexpr int NS = tile_stages(D);
+    constexpr int DBLK = D / 64;
+    constexpr int KSTEPS = D / 16;
+    constexpr float NEG_INF = -INFINITY;
+    constexpr bool kBF = std::is_same<KV, __nv_bfloat16>::value;
+    constexpr uint32_t kCols = tile_tmem_cols(D);
+    constexpr int NB = kTileSBufs;
+    constexpr uint32_t O_COL = 0, S_COL = D;  // S buffer b at S_COL + b*BN; P (hi, lo) over it
+    static_assert(D + NB * BN <= 512, "tensor memory");
+
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t* smem = reinterpret_cast<uint8_t*>(
+        (reinterpret_cast<uintptr_t>(smem_raw) + (kSmemAlignSlack - 1)) &
+        ~uintptr_t(kSmemAlignSlack - 1));
+    const TileSmem L = tile_smem_layout(D, BS);
+    uint64_t* bars = reinterpret_cast<uint64_t*>(smem + L.bar_off);
+    uint64_t* k_full = bars;
+    uint64_t* k_empty = bars + NS;
+    uint64_t* v_full = bars + 2 * NS;
+    uint64_t* v_empty = bars + 3 * NS;
+    uint64_t* s_full = bars + 4 * NS;
+    uint64_t* p_full = s_full + NB;
+    uint64_t* pv_done = s_full + 2 * NB;
+    uint64_t* final_bar = s_full + 3 * NB;
+    int32_t* phys_of = reinterpret_cast<int32_t*>(smem + L.phys_off);  // [NS][NPB] of K stages
+    float* xmax = reinterpret_cast<float*>(smem + L.xchg_off);    // [2][2][128]
+    float* xl = xmax + 2 * 2 * 128;                                   // [2][128]
+    uint64_t* xchg = reinterpret_cast<uint64_t*>(xl + 2 * 128);     // [2]
+    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + L.misc_off);
+    volatile uint32_t* abort_flag = tmem_slot + 1;
+
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    const int G = p.group, Q = p.q_len, Hkv = p.num_kv_heads, U = p.unit_rows;
+    const int gshift = __ffs(G) - 1;
+    const int part = blockIdx.x, b = blockIdx.z;
+    const int kvh = (int)blockIdx.y % Hkv, tile = (int)blockIdx.y / Hkv;
+
+    grid_dependency_wait();
+    grid_launch_dependents();
+
+    const int T = reachable_tokens(p.context_lens, b, p.max_blocks, BS);
+    const int npages = (T + BS - 1) / BS;
+    const int pb = part * p.part_pages;
+    const int pe = min(pb + p.part_pages, npages);
+    const int n = pe - pb;                      // pages of this partition (masked ones included)
+    const int nblk = (n + NPB - 1) / NPB;       // KV blocks
+    const int tend = min(T, pe * BS);           // tokens of this partition end here
+
+    // Element offset of unit row u's query / output vector ([B, Q, H, D]).
+    auto row_off = [&](int u) -> size_t {
+        return (((size_t)b * Q + (u >> gshift)) * p.num_heads + kvh * G + (u & (G - 1))) * D;
+    };
+
+    if (n <= 0) {
+        // Nothing of this sequence in the partition: the single pass writes the
+        // empty-context result; the combine never reads such partitions.
+        if (p.final_out) {
+            for (int idx = tid; idx < kTileRows * D; idx += kTileThreads) {
+                const int u = tile * kTileRows + idx / D;
+                if (u < U) store_out(p.out, row_off(u) + idx % D, 0.f, p.out_dtype);
+            }
+        }
+        return;
+    }
+
+    if (tid == 0) {
+        for (int i = 0; i < NS; ++i) {
+            mbar_init(smem_u32(k_full + i), 1);
+            mbar_init(smem_u32(k_empty + i), 1);
+            mbar_init(smem_u32(v_full + i), 1);
+            mbar_init(smem_u32(v_empty + i), 1);
+        }
+        for (int i = 0; i < NB; ++i) {
+            mbar_init(smem_u32(s_full + i), 1);
+            mbar_init(smem_u32(p_full + i), 256);
+            mbar_init(smem_u32(pv_done + i), 1);
+        }
+        mbar_init(smem_u32(final_bar), 1);
+        mbar_init(smem_u32(xchg), 256);
+        mbar_init(smem_u32(xchg + 1), 256);
+        *abort_flag = 0;
+        mbar_init_fence();
+        prefetch_tensormap(&tmap_k);
+        prefetch_tensormap(&tmap_v);
+    }
+    if (warp == 2) {  // tensor memory for O and the S / P buffers
+        tc::tmem_alloc(smem_u32(tmem_slot), kCols);
+        tc::tmem_relinquish();
+    }
+
+    // ---- Q tile: rows u = tile*128 + r, zero rows past the unit's rows;
+    // written with the 128-byte swizzle the MMA descriptors expect ----
+    {
+        uint8_t* qs = smem + L.q_off;
+        for (int i = tid; i < kTileRows * (D / 8); i += kTileThreads) {
+            const int r = i / (D / 8), c = i % (D / 8);
+            const int u = tile * kTileRows + r;
+            uint4 v = make_uint4(0, 0, 0, 0);
+            if (u < U)
+                v = __ldg(reinterpret_cast<const uint4*>(static_cast<const KV*>(p.q) + row_off(u)) + c);
+            *reinterpret_cast<uint4*>(qs + (c >> 3) * (kTileRows * 128) + r * 128 +
+                                      (((c & 7) ^ (r & 7)) << 4)) = v;
+        }
+        fence_proxy_async_smem();
+    }
+    tc::fence_before_sync();
+    __syncthreads();
+    tc::fence_after_sync();
+    const uint32_t tmem = *tmem_slot;
+
+    auto fail = [&]() {
+        if (lane == 0) record_error(p.err, PA_ERR_TIMEOUT);
+        *abort_flag = 1;
+    };
+    auto wait = [&](uint64_t* bar, uint32_t parity) -> bool {
+        const bool ok = mbar_wait_bounded(smem_u32(bar), parity, p.timeout_ns);
+        if (!ok) fail();
+        return ok;
+    };
+    // does KV block k (in stage st) hold at least one page?
+    auto block_live = [&](int st) -> bool {
+        bool any = false;
+#pragma unroll
+        for (int q = 0; q < NPB; ++q) any |= phys_of[st * NPB + q] >= 0;
+        return any;
+    };
+
+    if (warp == 0 || warp == 3) {
+        // ============ producers: warp 0 the K ring, warp 3 the V ring ============
+        // lane q < NPB reads the table entry of page q of a block and copies it
+        const bool is_k = warp == 0;
+        uint64_t* full = is_k ? k_full : v_full;
+        uint64_t* empty = is_k ? k_empty : v_empty;
+        const CUtensorMap* map = is_k ? &tmap_k : &tmap_v;
+        const uint32_t ring = smem_u32(smem + (is_k ? L.k_off : L.v_off));
+        const int32_t* table_row = p.block_tables + (size_t)b * p.max_blocks;
+        const uint64_t policy = l2_policy_evict_first();
+        int issued = 0;
+        for (int k = 0; k < nblk && !*abort_flag; ++k) {
+            const int st = k % NS, round = k / NS;
+            const int j = pb + k * NPB + lane;
+            const int e = (lane < NPB && j < pe) ? __ldg(table_row + j) : -1;
+            const int phys = (e >= 0 && (int64_t)e < p.num_blocks) ? e : -1;
+            bool ok = true;
+            if (round > 0 && lane == 0) ok = wait(empty + st, (round - 1) & 1);
+            if (!__shfl_sync(kFullMask, ok ? 1 : 0, 0)) break;
+            if (is_k && lane < NPB) phys_of[st * NPB + lane] = phys;
+            const unsigned live = __ballot_sync(kFullMask, lane < NPB && phys >= 0);
+            const uint32_t bar = smem_u32(full + st);
+            if (lane == 0) {
+                if (live) mbar_arrive_expect_tx(bar, (uint32_t)__popc(live) * 2u * BS * D);
+                else mbar_arrive(bar);
+            }
+            __syncwarp();
+            if (lane < NPB && phys >= 0) {
+                const uint32_t dst = ring + (uint32_t)st * L.tile_bytes + (uint32_t)lane * BS * 128;
+#pragma unroll
+                for (int blk = 0; blk < DBLK; ++blk)
+                    tma_load_4d(dst + blk * BN * 128, map, blk * 64, kvh, 0, phys, bar, policy);
+            }
+            ++issued;
+        }
+        if (*abort_flag && lane == 0) {
+            // let copies still in flight land before the CTA may exit
+            for (int k = issued > NS ? issued - NS : 0; k < issued; ++k)
+                (void)mbar_wait_bounded(smem_u32(full + k % NS), (k / NS) & 1, p.timeout_ns);
+        }
+    } else if (warp == 1) {
+        // ================= MMA issuer (one lane) =================
+        if (lane == 0) {
+            constexpr int kType = kBF ? 1 : 0;
+            constexpr uint32_t id_s = tc::idesc_f16(kType, false, kTileRows, BN);
+            constexpr uint32_t id_o = tc::idesc_f16(kType, true, kTileRows, D);
+            const uint32_t q_base = smem_u32(smem + L.q_off);
+            bool started = false;
+            bool live_prev = false;  // block i-1 holds a page (its K stage may be refilled)
+            for (int i = 0; i <= nblk && !*abort_flag; ++i) {
+                bool live_cur = false;
+                if (i < nblk) {
+                    // S_i = Q K_i^T into buffer i % NB, once P_{i-NB} there has been consumed
+                    const int st = i % NS;
+                    if (!wait(k_full + st, (i / NS) & 1)) break;
+                    if (i >= NB && !wait(pv_done + i % NB, ((i - NB) / NB) & 1)) break;
+                    tc::fence_after_sync();
+                    live_cur = block_live(st);
+                    if (live_cur) {
+                        const uint32_t k_base = smem_u32(smem + L.k_off) + (uint32_t)st * L.tile_bytes;
+#pragma unroll
+                        for (int s = 0; s < KSTEPS; ++s) {
+                            const uint64_t a = tc::smem_desc(
+                                q_base + (s >> 2) * (kTileRows * 128) + (s & 3) * 32, 16, 1024,
+                                tc::kSwizzle128B);
+                            const uint64_t bd = tc::smem_desc(
+                                k_base + (s >> 2) * (BN * 128) + (s & 3) * 32, 16, 1024,
+                                tc::kSwizzle128B);
+                            tc::mma_ss(tmem + S_COL + (i % NB) * BN, a, bd, id_s, s > 0);
+                        }
+                    }
+                    tc::commit(smem_u32(s_full + i % NB));
+                    tc::commit(smem_u32(k_empty + st));
+                }
+                if (i >= 1) {
+                    // O += P_j V_j with P's high and low parts
+                    const int j = i - 1, st = j % NS;
+                    if (!wait(p_full + j % NB, (j / NB) & 1)) break;
+                    if (!wait(v_full + st, (j / NS) & 1)) break;
+                    tc::fence_after_sync();
+                    if (live_prev) {
+                        const uint32_t v_base = smem_u32(smem + L.v_off) + (uint32_t)st * L.tile_bytes;
+                        const uint32_t p_hi = tmem + S_COL + (j % NB) * BN;
+                        const uint32_t p_lo = p_hi + BN / 2;
+#pragma unroll
+                        for (int ks = 0; ks < BN / 16; ++ks) {
+                            // V rows ks*16 .. +15: MN-major, 64-column blocks BN*128 bytes
+                            // apart, 8-row groups 1024 bytes apart
+                            const uint64_t vd = tc::smem_desc(v_base + ks * 16 * 128, BN * 128,
+                                                              1024, tc::kSwizzle128B);
+                            tc::mma_ts(tmem + O_COL, p_hi + ks * 8, vd, id_o,
+                                       (started || ks > 0) ? 1u : 0u);
+                            tc::mma_ts(tmem + O_COL, p_lo + ks * 8, vd, id_o, 1u);
+                        }
+                        started = true;
+                    }
+                    tc::commit(smem_u32(pv_done + j % NB));
+                    tc::commit(smem_u32(v_empty + st));
+                }
+                live_prev = live_cur;
+            }
+            // every MMA issued has completed before tensor memory is released
+            tc::commit(smem_u32(final_bar));
+            (void)mbar_wait_bounded(smem_u32(final_bar), 0, p.timeout_ns);
+        }
+        __syncwarp();
+    } else if (warp >= 4) {
+        // ============ softmax: two warpgroups, one row per thread each ============
+        // warpgroup wg takes columns [wg*BH, (wg+1)*BH) of every block and
+        // output columns [wg*D/2, (wg+1)*D/2); the two exchange row maxima (and,
+        // at the end, normalisers) through shared memory
+        constexpr int BH = BN / 2;
+        const int wg = (warp - 4) >> 2, w4 = warp & 3;
+        const int r = w4 * 32 + lane;
+        const int sr = wg * 128 + r;  // 0 .. 255 among the softmax threads
+        const uint32_t lane_base = tmem + ((uint32_t)(w4 * 32) << 16);
+        const int u = tile * kTileRows + r;
+        const int ctx = max(__ldg(p.context_lens + b), 0);
+        // tokens t < lim: the row's causal limit, the table's reach, the partition's end
+        const int lim = u < U ? min(tend, ctx - Q + (u >> gshift) + 1) : 0;
+        const float qscale = p.qscale;
+        const int32_t* table_row = p.block_tables + (size_t)b * p.max_blocks;
+        // which pages of block k hold data: bit q for page q (read from the
+        // table here; the K stage's record may already describe a later block)
+        auto page_bits = [&](int k) -> unsigned {
+            const int jj = pb + k * NPB + lane;
+            const int e = (lane < NPB && jj < pe && k < nblk) ? __ldg(table_row + jj) : -1;
+            return __ballot_sync(kFullMask, e >= 0 && (int64_t)e < p.num_blocks);
+        };
+        // exchange round nx: publish v, return the other warpgroup's value
+        int nx = 0;
+        auto exchange = [&](float* buf, float v, float& other) -> bool {
+            buf[wg * 128 + r] = v;
+            mbar_arrive(smem_u32(xchg + (nx & 1)));
+            const bool ok = __all_sync(kFullMask, wait(xchg + (nx & 1), (nx >> 1) & 1));
+            other = buf[(1 - wg) * 128 + r];
+            ++nx;
+            return ok;
+        };
+        float m = NEG_INF, l = 0.f;  // l: this half's share of the normaliser
+        unsigned bits_next = page_bits(0);
+        int j = 0;
+        for (; j < nblk && !*abort_flag; ++j) {
+            const int st = j % NS;
+            const unsigned bits = bits_next;
+            bits_next = page_bits(j + 1);
+            // (waits are decided warp-wide: the tensor-memory accesses below
+            // are warp-collective)
+            if (!__all_sync(kFullMask, wait(s_full + j % NB, (j / NB) & 1))) break;
+            tc::fence_after_sync();
+            if (bits) {
+                const int t0 = (pb + j * NPB) * BS + wg * BH;  // first token of this half
+                const uint32_t sb = lane_base + S_COL + (j % NB) * BN;
+                float s[BH];
+                {
+                    uint32_t x[32];
+#pragma unroll
+                    for (int c0 = 0; c0 < BH; c0 += 32) {
+                        tc::ld_32x32b_x32(sb + wg * BH + c0, x);
+                        tc::wait_ld();
+#pragma unroll
+                        for (int c = 0; c < 32; ++c) s[c0 + c] = __uint_as_float(x[c]);
+                    }
+                }
+                float mx = NEG_INF;
+#pragma unroll
+                for (int c = 0; c < BH; ++c) {
+                    const bool pl = (bits >> ((wg * BH + c) / BS)) & 1u;
+                    s[c] = (pl && t0 + c < lim) ? s[c] : NEG_INF;
+                    mx = fmaxf(mx, s[c]);
+                }
+                float mo;
+                if (!exchange(xmax + (nx & 1) * 256, mx, mo)) break;
+                const float ms = fmaxf(mx, mo) * qscale;
+                const bool need = ms > m + kTileRescaleSlack;
+                float alpha = 1.f;
+                if (need) {
+                    alpha = (m == NEG_INF) ? 1.f : fast_exp2(m - ms);
+                    l *= alpha;
+                    m = ms;
+                }
+                // O holds earlier blocks' sums only if this row had attended a token;
+                // each warpgroup rescales its half of O's columns
+                if (__any_sync(kFullMask, need && alpha != 1.f)) {
+                    if (j >= 1 && !__all_sync(kFullMask, wait(pv_done + (j - 1) % NB,
+                                                              ((j - 1) / NB) & 1)))
+                        break;
+                    tc::fence_after_sync();
+                    uint32_t x[16];
+#pragma unroll 1
+                    for (int c0 = wg * (D / 2); c0 < (wg + 1) * (D / 2); c0 += 16) {
+                        tc::ld_32x32b_x16(lane_base + O_COL + c0, x);
+                        tc::wait_ld();
+#pragma unroll
+                        for (int c = 0; c < 16; ++c)
+                            x[c] = __float_as_uint(__uint_as_float(x[c]) * alpha);
+                        tc::st_32x32b_x16(lane_base + O_COL + c0, x);
+                    }
+                    tc::wait_st();
+                }
+                // P = 2^(s*scale*log2e - m) as high and low 16-bit parts over S:
+                // hi in columns [0, BN/2), lo in [BN/2, BN) of the buffer
+                const float me = (m == NEG_INF) ? 0.f : m;
+#pragma unroll
+                for (int c0 = 0; c0 < BH; c0 += 32) {
+                    uint32_t ph[16], pl[16];
+#pragma unroll
+                    for (int c = 0; c < 32; c += 2) {
+                        const float x0 = fast_exp2(fmaf(s[c0 + c], qscale, -me));
+                        const float x1 = fast_exp2(fmaf(s[c0 + c + 1], qscale, -me));
+                        l += x0 + x1;
+                        const uint32_t h = Mma<KV>::pack(x0, x1);
+                        float h0, h1;
+                        Mma<KV>::unpack(h, h0, h1);
+                        ph[c / 2] = h;
+                        pl[c / 2] = Mma<KV>::pack(x0 - h0, x1 - h1);
+                    }
+                    const uint32_t col = (uint32_t)(wg * BH + c0) / 2;
+                    tc::st_32x32b_x16(sb + col, ph);
+                    tc::st_32x32b_x16(sb + BN / 2 + col, pl);
+                }
+                tc::wait_st();
+                // zero the V rows of masked pages and past the partition's last
+                // token (0 * NaN would otherwise reach O), once the stage's
+                // copies have landed
+                const int tb = (pb + j * NPB) * BS;
+                const bool holes = tb + BN > tend || bits != (1u << NPB) - 1u;
+                if (holes) {
+                    if (!__all_sync(kFullMask, wait(v_full + st, (j / NS) & 1))) break;
+                    uint8_t* vt = smem + L.v_off + (size_t)st * L.tile_bytes;
+                    for (int idx = sr; idx < BN * DBLK * 8; idx += 256) {
+                        const int row = idx / (DBLK * 8), rem = idx % (DBLK * 8);
+                        if (!((bits >> (row / BS)) & 1u) || tb + row >= tend)
+                            *reinterpret_cast<uint4*>(vt + (rem >> 3) * BN * 128 + row * 128 +
+                                                      (rem & 7) * 16) = make_uint4(0, 0, 0, 0);
+                    }
+                    fence_proxy_async_smem();
+                }
+            }
+            tc::fence_before_sync();
+            mbar_arrive(smem_u32(p_full + j % NB));
+        }
+        // ---- epilogue: O / l, or the partial (m, l, O); each warpgroup its
+        // half of the columns ----
+        bool have_o = __all_sync(kFullMask, j == nblk && !*abort_flag);
+        if (have_o)
+            have_o = __all_sync(kFullMask,
+                                wait(pv_done + (nblk - 1) % NB, ((nblk - 1) / NB) & 1));
+        float lo_half = 0.f;
+        if (have_o) have_o = exchange(xl, l, lo_half);
+        tc::fence_after_sync();
+        if (have_o) {
+            l += lo_half;
+            const bool live = u < U;
+            const float inv = l > 0.f ? 1.f / l : 0.f;
+            size_t orow = 0;
+            if (live) {
+                orow = p.final_out ? row_off(u)
+                                   : ((((size_t)b * Hkv + kvh) * p.num_parts + part) * U + u) * D;
+                if (!p.final_out && wg == 0) {
+                    p.part_ml[(orow / D) * 2] = l > 0.f ? m : NEG_INF;
+                    p.part_ml[(orow / D) * 2 + 1] = l;
+                }
+            }
+            uint32_t x[16];
+#pragma unroll 1
+            for (int c0 = wg * (D / 2); c0 < (wg + 1) * (D / 2); c0 += 16) {
+                tc::ld_32x32b_x16(lane_base + O_COL + c0, x);
+                tc::wait_ld();
+                if (!live) continue;
+                float v[16];
+#pragma unroll
+                for (int c = 0; c < 16; ++c)
+                    v[c] = l > 0.f ? __uint_as_float(x[c]) * (p.final_out ? inv : 1.f) : 0.f;
+                if (!p.final_out || p.out_dtype == PA_F32) {
+                    float* dst = (p.final_out ? static_cast<float*>(p.out) : p.part_acc) + orow + c0;
+#pragma unroll
+                    for (int c = 0; c < 16; c += 4)
+                        *reinterpret_cast<float4*>(dst + c) =
+                            make_float4(v[c], v[c + 1], v[c + 2], v[c + 3]);
+                } else {
+                    uint32_t w[8];
+#pragma unroll
+                    for (int c = 0; c < 16; c += 2) w[c / 2] = Mma<KV>::pack(v[c], v[c + 1]);
+                    uint4* dst = reinterpret_cast<uint4*>(static_cast<KV*>(p.out) + orow + c0);
+                    dst[0] = make_uint4(w[0], w[1], w[2], w[3]);
+                    dst[1] = make_uint4(w[4], w[5], w[6], w[7]);
+                }
+            }
+        }
+    }
+
+    // ---- release tensor memory once every role is done with it ----
+    tc::fence_before_sync();
+    __syncthreads();
+    if (warp == 2) {
+        tc::fence_after_sync();
+        tc::tmem_dealloc(tmem, kCols);
+    }
+}
+
+template <int D, int BS, typename KV>
+cudaError_t launch_tile_inst(const AttnLaunch& L, cudaStream_t stream) {
+    auto kern = tile_kernel<D, BS, KV>;
+    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         (int)L.smem_bytes);
+    if (e != cudaSuccess) return e;
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = L.grid;
+    cfg.blockDim = dim3(kTileThreads);
+    cfg.dynamicSmemBytes = L.smem_bytes;
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = L.pdl ? 1 : 0;
+    return cudaLaunchKernelEx(&cfg, kern, L.tmap_k, L.tmap_v, L.p);
+}
+
+template <int D>
+cudaError_t launch_tile_for_d(const AttnLaunch& L, cudaStream_t stream) {
+    const bool bf = L.kv_dtype == PA_BF16;
+    if (L.block_size == 16)
+        return bf ? launch_tile_inst<D, 16, __nv_bfloat16>(L, stream)
+                  : launch_tile_inst<D, 16, __half>(L, stream);
+    if (L.block_size == 32)
+        return bf ? launch_tile_inst<D, 32, __nv_bfloat16>(L, stream)
+                  : launch_tile_inst<D, 32, __half>(L, stream);
+    return cudaErrorInvalidValue;
+}
+
+}  // namespace pa

@@ -1,0 +1,9 @@
+// Instantiations of the tcgen05 tile kernel (several query tokens per
+// sequence) for head_dim 64.
+#include "pa_tile.cuh"
+
+namespace pa {
+cudaError_t launch_tile_d64(const AttnLaunch& L, cudaStream_t stream) {
+    return launch_tile_for_d<64>(L, stream);
+}
+}  // namespace pa

@@ -2,11 +2,13 @@
 through the C ABI, against the fp64 oracle.
 
 Bar: max |gpu - oracle| <= 2e-3 on fp32 output, as for the one-token decode.
-Covered: every group size with q_len up to and past one CTA's 16 MMA rows
-(query chunks), sequences shorter than q_len (query tokens that see nothing),
-masked table entries, every split mode (one pass, cluster, workspace,
-balanced), the q-dtype output, and the full-size multi-token workloads on
-sampled rows.
+Covered, on both kernels that serve several query tokens (the warp-level MMA
+path with up to 16 rows per CTA, and the tcgen05 tile kernel with 128-row
+tiles; PA_MULTI_KERNEL forces one of them): every group size with q_len up to
+and past 16 and 128 rows, sequences shorter than q_len (query tokens that see
+nothing), masked table entries, every split mode (one pass, cluster,
+workspace, balanced), the q-dtype output, and the full-size multi-token
+workloads on sampled rows.
 """
 import math
 
@@ -22,6 +24,16 @@ pytestmark = pytest.mark.gpu
 
 TOL = 2e-3
 DEV = "cuda:0"
+
+
+@pytest.fixture(params=["auto", "mma", "tile"])
+def kernel(request, monkeypatch):
+    """Which kernel serves the calls: the library's choice, or one forced."""
+    if request.param == "auto":
+        monkeypatch.delenv("PA_MULTI_KERNEL", raising=False)
+    else:
+        monkeypatch.setenv("PA_MULTI_KERNEL", request.param)
+    return request.param
 
 
 def run(x, partition_tokens=0, out_dtype=torch.float32):
@@ -79,13 +91,16 @@ CASES = [
     (2, 2, 16, 2, 128, 16, [77, 1]),           # G=8
     (2, 3, 16, 1, 256, 32, [1000, 33]),        # G=16, three chunks of one token
     (2, 6, 8, 4, 256, 16, [100, 401]),         # G=2, 12 rows
+    (2, 40, 16, 4, 128, 16, [45, 700]),        # G=4, 160 rows: two 128-row tiles
+    (1, 130, 8, 8, 64, 32, [520]),             # G=1, 130 rows: a tile of 2 rows after 128
+    (2, 24, 16, 1, 256, 32, [24, 1500]),       # G=16, 384 rows, a sequence exactly Q long
 ]
 IDS = [f"B{c[0]}Q{c[1]}H{c[2]}kv{c[3]}D{c[4]}bs{c[5]}" for c in CASES]
 
 
 @pytest.mark.parametrize("dtype", [torch.float16, torch.bfloat16])
 @pytest.mark.parametrize("case", CASES, ids=IDS)
-def test_multi_token_vs_oracle(case, dtype):
+def test_multi_token_vs_oracle(case, dtype, kernel):
     B, Q, H, Hkv, D, bs, lens = case
     x = multi_case(13, B, Q, H, Hkv, D, bs, lens, dtype)
     want = oracle_of(x)
@@ -121,7 +136,7 @@ def test_multi_token_one_token_equals_decode():
     assert torch.equal(got[:, 0], ref)
 
 
-def test_multi_token_masking_and_qdtype_output():
+def test_multi_token_masking_and_qdtype_output(kernel):
     x = multi_case(19, 4, 4, 16, 4, 128, 16, [0, 3, 50, 90], torch.float16, mb_extra=0)
     NB = x.k_cache.shape[0]
     bt = x.block_tables.clone()
@@ -140,7 +155,7 @@ def test_multi_token_masking_and_qdtype_output():
     assert (np.abs(got - want_r) <= TOL + ulp).all()
 
 
-def test_tiny_q3_workload():
+def test_tiny_q3_workload(kernel):
     x = workloads.make("tiny_q3", seed=0, device=DEV)
     want = oracle_of(x.to("cpu"))
     for pt in [0, 16, 64]:
@@ -148,7 +163,7 @@ def test_tiny_q3_workload():
 
 
 @pytest.mark.parametrize("name", ["spec_b16_t2048_q4", "spec_b4_t8192_q8", "chunk_b2_t4096_q64"])
-def test_multi_token_full_size_sampled(name):
+def test_multi_token_full_size_sampled(name, kernel):
     """Full-size multi-token workloads, automatic split; sampled (b, token, head)
     rows through the oracle's one-token decode of each token's causal prefix."""
     x = workloads.make(name, seed=0, device=DEV)
@@ -165,3 +180,37 @@ def test_multi_token_full_size_sampled(name):
         want = oracle.decode_rows(host.q[:, i].contiguous(), host.k_cache, host.v_cache,
                                   host.block_tables, prefix, host.scale, rows)
         check(got[rows[:, 0], i, rows[:, 1]], want)
+
+
+def test_tile_kernel_poison_and_permutation(monkeypatch):
+    """Tile kernel: NaN in every unreferenced block and in the slots past each
+    context leaves the output bit-identical; so does a permutation of the pool
+    with the table remapped."""
+    monkeypatch.setenv("PA_MULTI_KERNEL", "tile")
+    x = multi_case(23, 3, 20, 16, 2, 128, 16, [30, 250, 77], spare=6)
+    xd = x.to(DEV)
+    base = run(xd, 0)
+    NB = x.k_cache.shape[0]
+    used = set(x.block_tables[x.block_tables >= 0].tolist())
+    k, v = xd.k_cache.clone(), xd.v_cache.clone()
+    for blk in range(NB):
+        if blk not in used:
+            k[blk] = float("nan")
+            v[blk] = float("nan")
+    for b, t in enumerate(x.lens_host):
+        last = int(x.block_tables[b, (t - 1) // 16])
+        k[last, t % 16 or 16:] = float("nan")
+        v[last, t % 16 or 16:] = float("nan")
+    xp = workloads.Inputs(x.spec, xd.q, k, v, xd.block_tables, xd.context_lens, x.scale,
+                          x.max_context_len, x.lens_host)
+    assert torch.equal(run(xp, 0), base)
+    perm = torch.randperm(NB, generator=torch.Generator().manual_seed(5))
+    inv = torch.empty_like(perm)
+    inv[perm] = torch.arange(NB)
+    bt = x.block_tables.clone()
+    bt[bt >= 0] = inv[bt[bt >= 0].long()].to(torch.int32)
+    xq = workloads.Inputs(x.spec, xd.q, xd.k_cache[perm.to(DEV)].contiguous(),
+                          xd.v_cache[perm.to(DEV)].contiguous(), bt.to(DEV), xd.context_lens,
+                          x.scale, x.max_context_len, x.lens_host)
+    assert torch.equal(run(xq, 0), base)
+    assert pa.device_error() == 0
