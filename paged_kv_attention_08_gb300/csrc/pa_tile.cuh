@@ -316,6 +316,9 @@ __global__ void __launch_bounds__(kTileThreads, 1)
             ++nx;
             return ok;
         };
+        // a warp whose 32 rows all lie past the unit's rows (a partial tile)
+        // only keeps the barriers going: its P and O rows are never used
+        const bool dead = tile * kTileRows + w4 * 32 >= U;
         float m = NEG_INF, l = 0.f;  // l: this half's share of the normaliser
         unsigned bits_next = page_bits(0);
         int j = 0;
@@ -331,7 +334,8 @@ __global__ void __launch_bounds__(kTileThreads, 1)
                 const int t0 = (pb + j * NPB) * BS + wg * BH;  // first token of this half
                 const uint32_t sb = lane_base + S_COL + (j % NB) * BN;
                 float s[BH];
-                {
+                float mx = NEG_INF;
+                if (!dead) {
                     uint32_t x[32];
 #pragma unroll
                     for (int c0 = 0; c0 < BH; c0 += 32) {
@@ -340,13 +344,19 @@ __global__ void __launch_bounds__(kTileThreads, 1)
 #pragma unroll
                         for (int c = 0; c < 32; ++c) s[c0 + c] = __uint_as_float(x[c]);
                     }
-                }
-                float mx = NEG_INF;
+                    // every page live and the whole half inside every row's limit:
+                    // nothing to mask
+                    if (__all_sync(kFullMask, bits == (1u << NPB) - 1u && t0 + BH <= lim)) {
 #pragma unroll
-                for (int c = 0; c < BH; ++c) {
-                    const bool pl = (bits >> ((wg * BH + c) / BS)) & 1u;
-                    s[c] = (pl && t0 + c < lim) ? s[c] : NEG_INF;
-                    mx = fmaxf(mx, s[c]);
+                        for (int c = 0; c < BH; ++c) mx = fmaxf(mx, s[c]);
+                    } else {
+#pragma unroll
+                        for (int c = 0; c < BH; ++c) {
+                            const bool pl = (bits >> ((wg * BH + c) / BS)) & 1u;
+                            s[c] = (pl && t0 + c < lim) ? s[c] : NEG_INF;
+                            mx = fmaxf(mx, s[c]);
+                        }
+                    }
                 }
                 float mo;
                 if (!exchange(xmax + (nx & 1) * 256, mx, mo)) break;
@@ -380,23 +390,25 @@ __global__ void __launch_bounds__(kTileThreads, 1)
                 // P = 2^(s*scale*log2e - m) as high and low 16-bit parts over S:
                 // hi in columns [0, BN/2), lo in [BN/2, BN) of the buffer
                 const float me = (m == NEG_INF) ? 0.f : m;
+                if (!dead) {
 #pragma unroll
-                for (int c0 = 0; c0 < BH; c0 += 32) {
-                    uint32_t ph[16], pl[16];
+                    for (int c0 = 0; c0 < BH; c0 += 16) {
+                        uint32_t ph[8], pl[8];
 #pragma unroll
-                    for (int c = 0; c < 32; c += 2) {
-                        const float x0 = fast_exp2(fmaf(s[c0 + c], qscale, -me));
-                        const float x1 = fast_exp2(fmaf(s[c0 + c + 1], qscale, -me));
-                        l += x0 + x1;
-                        const uint32_t h = Mma<KV>::pack(x0, x1);
-                        float h0, h1;
-                        Mma<KV>::unpack(h, h0, h1);
-                        ph[c / 2] = h;
-                        pl[c / 2] = Mma<KV>::pack(x0 - h0, x1 - h1);
+                        for (int c = 0; c < 16; c += 2) {
+                            const float x0 = fast_exp2(fmaf(s[c0 + c], qscale, -me));
+                            const float x1 = fast_exp2(fmaf(s[c0 + c + 1], qscale, -me));
+                            l += x0 + x1;
+                            const uint32_t h = Mma<KV>::pack(x0, x1);
+                            float h0, h1;
+                            Mma<KV>::unpack(h, h0, h1);
+                            ph[c / 2] = h;
+                            pl[c / 2] = Mma<KV>::pack(x0 - h0, x1 - h1);
+                        }
+                        const uint32_t col = (uint32_t)(wg * BH + c0) / 2;
+                        tc::st_32x32b_x8(sb + col, ph);
+                        tc::st_32x32b_x8(sb + BN / 2 + col, pl);
                     }
-                    const uint32_t col = (uint32_t)(wg * BH + c0) / 2;
-                    tc::st_32x32b_x16(sb + col, ph);
-                    tc::st_32x32b_x16(sb + BN / 2 + col, pl);
                 }
                 tc::wait_st();
                 // zero the V rows of masked pages and past the partition's last
@@ -428,7 +440,7 @@ __global__ void __launch_bounds__(kTileThreads, 1)
         float lo_half = 0.f;
         if (have_o) have_o = exchange(xl, l, lo_half);
         tc::fence_after_sync();
-        if (have_o) {
+        if (have_o && !dead) {
             l += lo_half;
             const bool live = u < U;
             const float inv = l > 0.f ? 1.f / l : 0.f;
