@@ -57,6 +57,23 @@ def algorithmic_bytes(x: workloads.Inputs, out_elem: int = 4) -> int:
             + B * mb * 4 + B * 4)
 
 
+def algorithmic_flops(x: workloads.Inputs) -> int:
+    """Multiply-adds x 2 of one call: S = q.K and O = P.V over every attended
+    token of every query row (with several query tokens, token i of a sequence
+    attends its causal prefix of T - Q + i + 1 tokens)."""
+    D = x.q.shape[-1]
+    H = x.q.shape[-2]
+    _, bs, _, _ = x.k_cache.shape
+    cap = x.block_tables.shape[1] * bs
+    Q = x.q.shape[1] if x.q.dim() == 4 else 1
+    rows_tokens = 0
+    for t in x.lens_host:
+        t = max(t, 0)
+        for i in range(Q):
+            rows_tokens += max(0, min(t - Q + i + 1, cap))
+    return 4 * rows_tokens * H * D
+
+
 def decode_call(pa, out, q, k_cache, v_cache, block_tables, context_lens, scale, max_context_len,
                 partition_tokens, workspace, stream):
     """One decode call through the public API: one query token per sequence
@@ -190,6 +207,15 @@ class ClockSampler:
 # ---------------------------------------------------------------------------
 # peaks
 # ---------------------------------------------------------------------------
+def tensor_peak():
+    """Dense bf16 (= fp16) tensor peak in TFLOP/s for a kernel timed alone."""
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        return float(json.load(open(path))["bf16_tflops"]), "measured"
+    except (OSError, KeyError, ValueError):
+        return 1900.0, "fallback"
+
+
 def hbm_peak():
     path = os.path.join(ROOT, "MEASURED_PEAKS.json")
     try:
@@ -490,6 +516,16 @@ def main(argv=None):
     dom_bytes = algorithmic_bytes(set0[dom])
     dom_gbs = dom_bytes / (call_us[dom] * 1e-6) / 1e9
     dom_name = names[dom]
+    # the bound of the dominant call: its FLOPs per byte against the ridge of
+    # the measured peaks (a multi-token call with many query rows is a
+    # contraction, a decode call streams K and V)
+    tpeak, tpeak_kind = tensor_peak()
+    dom_flops = algorithmic_flops(set0[dom])
+    dom_tflops = dom_flops / (call_us[dom] * 1e-6) / 1e12
+    tensor_bound = dom_flops / dom_bytes > tpeak * 1e12 / (peak * 1e9)
+    per_call_rates = {n: {"GB/s": round(algorithmic_bytes(x) / (u * 1e-6) / 1e9, 1),
+                          "TFLOP/s": round(algorithmic_flops(x) / (u * 1e-6) / 1e12, 2)}
+                      for n, x, u in zip(names, set0, call_us)}
 
     # ---- end to end: host buffers, copies inside the timed region ----
     # Every input of the step (q, K, V, tables, lengths of each workload) sits
@@ -587,6 +623,7 @@ def main(argv=None):
                 "workload": describe(args.workload),
                 "us_per_step": ms_step * 1e3,
                 "per_call_us": {n: round(u, 3) for n, u in zip(names, call_us)},
+                "per_call_rate": per_call_rates,
                 "algorithmic_bytes_per_step": step_bytes,
                 "partition_tokens": {n: (p if p else "auto") for n, p in zip(names, pts)},
                 "plan": plans,
@@ -600,13 +637,18 @@ def main(argv=None):
             },
             "e2e": e2e,
             "gpu_launches": launches_per_step * args.steps,
-            "roofline": {"bound": "hbm", "achieved": dom_gbs, "peak": peak, "unit": "GB/s",
-                         "frac": dom_gbs / peak, "peak_kind": peak_kind,
-                         "kernel": f"decode call on {dom_name} "
-                                   f"({plans[dom_name]['partitions']} partition(s), reduce: "
-                                   f"{plans[dom_name]['reduce']})",
-                         "traffic": ncu_traffic("pa_attn", dom_name),
-                         "step_frac": value / world / peak},
+            "roofline": ({"bound": "tensor", "achieved": dom_tflops, "peak": tpeak,
+                          "unit": "TFLOP/s", "frac": dom_tflops / tpeak, "peak_kind": tpeak_kind,
+                          "flops_per_launch": dom_flops}
+                         if tensor_bound else
+                         {"bound": "hbm", "achieved": dom_gbs, "peak": peak, "unit": "GB/s",
+                          "frac": dom_gbs / peak, "peak_kind": peak_kind,
+                          "step_frac": value / world / peak}) | {
+                "kernel": f"decode call on {dom_name} "
+                          f"({plans[dom_name]['partitions']} partition(s), reduce: "
+                          f"{plans[dom_name]['reduce']})",
+                "bytes_per_launch": dom_bytes,
+                "traffic": ncu_traffic("pa_tile" if tensor_bound else "pa_attn", dom_name)},
             "cpu_baseline": cpu,
             "clocks": clk,
         }
