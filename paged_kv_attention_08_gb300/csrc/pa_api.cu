@@ -296,9 +296,37 @@ int tile_ctas_per_sm(const pa_shape* s) {
     return n < 1 ? 1 : n;
 }
 
+// Clusters of `cluster` tile-kernel CTAs that fit on the current device at
+// once (cached per device and instantiation; 0 when unknown).
+int tile_max_clusters(const pa_shape* s, int cluster) {
+    static std::atomic<int> cache[kMaxDevices][3][2][2][kMaxClusterParts + 1];  // n + 1; 0 = unset
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return 0;
+    const int di = s->head_dim == 64 ? 0 : (s->head_dim == 128 ? 1 : 2);
+    std::atomic<int>& slot =
+        cache[dev][di][s->block_size == 32][s->kv_dtype == PA_BF16][cluster];
+    int v = slot.load(std::memory_order_relaxed);
+    if (v == 0) {
+        const uint32_t smem = tile_smem_layout(s->head_dim, s->block_size).total + kSmemAlignSlack;
+        int n = 0;
+        switch (s->head_dim) {
+            case 64: n = tile_max_clusters_d64(s->block_size, s->kv_dtype, cluster, smem); break;
+            case 128: n = tile_max_clusters_d128(s->block_size, s->kv_dtype, cluster, smem); break;
+            default: n = tile_max_clusters_d256(s->block_size, s->kv_dtype, cluster, smem); break;
+        }
+        v = n + 1;
+        slot.store(v, std::memory_order_relaxed);
+    }
+    return v - 1;
+}
+
 // Tile kernel split: units = B * Hkv * ceil(q_len*G / 128) CTAs unsplit; cut
 // each unit's pages into as many partitions (of at least 4 pages) as fit in
-// one wave of resident CTAs.  Partitions reduce through the workspace.
+// one wave of resident CTAs.  Partitions reduce inside a cluster through
+// distributed shared memory when every unit's cluster (at most 8 CTAs) fits
+// on the device at once and the cluster split keeps at least 3/4 of those
+// partitions (the workspace round trip and the combine launch cost more than
+// the rest); otherwise through the workspace.
 Plan tile_plan(const pa_shape* s, int32_t max_context_len, int32_t partition_tokens, int num_sms,
                int32_t q_len) {
     const int pages = pages_for(s, max_context_len);
@@ -313,9 +341,20 @@ Plan tile_plan(const pa_shape* s, int32_t max_context_len, int32_t partition_tok
         const int64_t max_parts = (pages + 3) / 4;
         if (parts > max_parts) parts = max_parts;
         if (parts < 1) parts = 1;
+        int best_c = 0;  // largest cluster split whose clusters are all resident at once
+        for (int c = (int)std::min<int64_t>(kMaxClusterParts, max_parts); c >= 2; --c)
+            if (units <= tile_max_clusters(s, c)) {
+                best_c = c;
+                break;
+            }
+        const bool cluster = parts >= 2 && best_c >= 2 && (int64_t)best_c * 4 >= parts * 3;
+        if (cluster) parts = std::min<int64_t>(best_c, parts);
         pp = (int)((pages + parts - 1) / parts);
+        Plan p = plan_with(s, pages, pp, cluster);
+        p.tile = true;
+        return p;
     }
-    Plan p = plan_with(s, pages, pp, false);
+    Plan p = plan_with(s, pages, pp, true);
     p.tile = true;
     return p;
 }
@@ -324,10 +363,13 @@ Plan tile_plan(const pa_shape* s, int32_t max_context_len, int32_t partition_tok
 // one CTA: it needs q_len * group <= 16, and batch <= kMaxBalancedBatch.
 Plan make_plan(const pa_shape* s, int32_t max_context_len, int32_t partition_tokens, int num_sms,
                int32_t q_len = 1) {
-    if (use_tile(s, q_len))
-        return tile_plan(s, max_context_len,
-                         partition_tokens == PA_PARTITION_BALANCED ? 0 : partition_tokens, num_sms,
-                         q_len);
+    if (use_tile(s, q_len)) {
+        Plan tp = tile_plan(s, max_context_len,
+                            partition_tokens == PA_PARTITION_BALANCED ? 0 : partition_tokens,
+                            num_sms, q_len);
+        if (!clusters_enabled()) tp.cluster = false;
+        return tp;
+    }
     Plan plan;
     const int q_chunks = q_chunks_for(s, q_len);
     if (partition_tokens == PA_PARTITION_BALANCED && s->batch <= kMaxBalancedBatch &&
@@ -500,12 +542,15 @@ pa_status launch_tile(void* out, const void* q, const void* k, const void* v, co
     p.num_parts = plan.num_parts;
     p.out_dtype = s->out_dtype;
     p.final_out = plan.num_parts <= 1 ? 1 : 0;
+    p.cluster_reduce = plan.cluster ? 1 : 0;
     p.timeout_ns = kDefaultTimeoutNs;
     L.head_dim = s->head_dim;
     L.block_size = s->block_size;
     L.kv_dtype = s->kv_dtype;
     L.pdl = use_pdl();
-    L.cluster = 1;
+    L.cluster = plan.cluster ? plan.num_parts : 1;
+    const TileSmem tl = tile_smem_layout(s->head_dim, s->block_size);
+    if (plan.cluster && tile_cluster_bytes(s->head_dim) > tl.bar_off) return PA_ERR_UNSUPPORTED;
     L.grid = dim3((unsigned)plan.num_parts, (unsigned)grid_y, (unsigned)s->batch);
     L.threads = kTileThreads;
     L.smem_bytes = tile_smem_layout(s->head_dim, s->block_size).total + kSmemAlignSlack;
@@ -587,7 +632,7 @@ pa_status pa_decode_multi(void* out, const void* q, const void* k_cache, const v
     if (st != PA_OK) return st;
     const Plan plan = make_plan(shape, max_context_len, partition_tokens, sms, q_len);
     cudaStream_t cs = static_cast<cudaStream_t>(stream);
-    if (plan.tile && plan.num_parts <= 1)
+    if (plan.tile && (plan.num_parts <= 1 || plan.cluster))
         return launch_tile(out, q, k_cache, v_cache, block_tables, context_lens, shape, scale, plan,
                            nullptr, nullptr, err, cs, q_len);
     if (!plan.tile && !plan.balanced && (plan.num_parts <= 1 || plan.cluster))

@@ -187,6 +187,15 @@ __device__ __forceinline__ float ld_cluster_f32(uint32_t addr) {
     return v;
 }
 
+__device__ __forceinline__ float4 ld_cluster_v4f32(uint32_t addr) {
+    float4 v;
+    asm volatile("ld.shared::cluster.v4.f32 {%0, %1, %2, %3}, [%4];"
+                 : "=f"(v.x), "=f"(v.y), "=f"(v.z), "=f"(v.w)
+                 : "r"(addr)
+                 : "memory");
+    return v;
+}
+
 template <typename KV>
 struct Mma;
 

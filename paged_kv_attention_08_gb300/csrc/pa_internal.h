@@ -170,6 +170,14 @@ __host__ __device__ inline TileSmem tile_smem_layout(int D, int BS) {
     return L;
 }
 
+// Cluster reduction of the tile kernel: after its pages, a CTA leaves its
+// partial in its own (then idle) operand buffers at offset 0 -- O rows
+// [128][head_dim + 4] fp32, m [128], l [128] -- and the merge weights of its
+// share of the rows [128][8] follow.
+__host__ __device__ constexpr uint32_t tile_cluster_bytes(int D) {
+    return 4u * (kTileRows * (D + 4) + 2 * kTileRows + kTileRows * 8);
+}
+
 // Tensor-memory columns of the tile kernel: O [head_dim], then kTileSBufs S
 // buffers of BN fp32 columns (P, as 16-bit high and low parts, overwrites S).
 __host__ __device__ constexpr uint32_t tile_tmem_cols(int D) {
@@ -201,6 +209,10 @@ cudaError_t launch_attn_d256_multi(const AttnLaunch& L, cudaStream_t stream);
 cudaError_t launch_tile_d64(const AttnLaunch& L, cudaStream_t stream);
 cudaError_t launch_tile_d128(const AttnLaunch& L, cudaStream_t stream);
 cudaError_t launch_tile_d256(const AttnLaunch& L, cudaStream_t stream);
+// Clusters of `cluster` tile-kernel CTAs resident at once on the current device.
+int tile_max_clusters_d64(int block_size, int kv_dtype, int cluster, uint32_t smem_bytes);
+int tile_max_clusters_d128(int block_size, int kv_dtype, int cluster, uint32_t smem_bytes);
+int tile_max_clusters_d256(int block_size, int kv_dtype, int cluster, uint32_t smem_bytes);
 
 cudaError_t launch_combine(const CombineParams& p, int head_dim, dim3 grid, bool pdl,
                            cudaStream_t stream);

@@ -103,6 +103,84 @@ __global__ void __launch_bounds__(kTileThreads, 1)
         return (((size_t)b * Q + (u >> gshift)) * p.num_heads + kvh * G + (u & (G - 1))) * D;
     };
 
+    // ---- cluster reduction (at most 8 partitions of a unit form one cluster
+    // along grid x): every CTA has left its partial at offset 0 of its shared
+    // memory; CTA `rank` merges rows [rank*rpc, (rank+1)*rpc) of all of them
+    // through distributed shared memory and writes the output ----
+    constexpr int CL = D + 4;  // row stride of the parked O rows (floats)
+    float* cl_o = reinterpret_cast<float*>(smem);
+    float* cl_m = cl_o + kTileRows * CL;
+    float* cl_l = cl_m + kTileRows;
+    float* cl_w = cl_l + kTileRows;  // [rpc][8] merge weights of this CTA's rows
+    auto cluster_merge = [&]() {
+        cluster_sync_release_acquire();  // every CTA's partial is in place
+        const int P = p.num_parts;
+        const int rank = (int)blockIdx.x;
+        const int rpc = (kTileRows + P - 1) / P;
+        const int r0 = rank * rpc, r1 = min(r0 + rpc, kTileRows);
+        uint32_t rb_m[kMaxClusterParts], rb_l[kMaxClusterParts], rb_o[kMaxClusterParts];
+#pragma unroll
+        for (int q = 0; q < kMaxClusterParts; ++q) {
+            const uint32_t qq = (uint32_t)(q < P ? q : 0);
+            rb_m[q] = map_cluster_rank(smem_u32(cl_m), qq);
+            rb_l[q] = map_cluster_rank(smem_u32(cl_l), qq);
+            rb_o[q] = map_cluster_rank(smem_u32(cl_o), qq);
+        }
+        for (int t = tid; t < r1 - r0; t += kTileThreads) {
+            const int r = r0 + t;
+            float mq[kMaxClusterParts];
+            float M = NEG_INF;
+#pragma unroll
+            for (int q = 0; q < kMaxClusterParts; ++q) {
+                mq[q] = q < P ? ld_cluster_f32(rb_m[q] + 4u * r) : NEG_INF;
+                M = fmaxf(M, mq[q]);
+            }
+            float w[kMaxClusterParts], Ls = 0.f;
+#pragma unroll
+            for (int q = 0; q < kMaxClusterParts; ++q) {
+                w[q] = mq[q] == NEG_INF ? 0.f : fast_exp2(mq[q] - M);
+                if (w[q] != 0.f) Ls = fmaf(w[q], ld_cluster_f32(rb_l[q] + 4u * r), Ls);
+            }
+            const float inv = Ls > 0.f ? 1.f / Ls : 0.f;
+#pragma unroll
+            for (int q = 0; q < kMaxClusterParts; ++q) cl_w[t * 8 + q] = w[q] * inv;
+        }
+        __syncthreads();
+        for (int idx = tid; idx < (r1 - r0) * (D / 4); idx += kTileThreads) {
+            const int t = idx / (D / 4), c4 = idx % (D / 4);
+            const int r = r0 + t, u = tile * kTileRows + r;
+            if (u >= U) continue;
+            float4 a = make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll
+            for (int q = 0; q < kMaxClusterParts; ++q) {
+                const float w = cl_w[t * 8 + q];
+                if (w == 0.f) continue;  // an empty partial: nothing parked there
+                const float4 v = ld_cluster_v4f32(rb_o[q] + 4u * (r * CL + 4 * c4));
+                a.x = fmaf(w, v.x, a.x);
+                a.y = fmaf(w, v.y, a.y);
+                a.z = fmaf(w, v.z, a.z);
+                a.w = fmaf(w, v.w, a.w);
+            }
+            const size_t o = row_off(u) + 4 * c4;
+            if (p.out_dtype == PA_F32) {
+                *reinterpret_cast<float4*>(static_cast<float*>(p.out) + o) = a;
+            } else {
+                *reinterpret_cast<uint2*>(static_cast<KV*>(p.out) + o) =
+                    make_uint2(Mma<KV>::pack(a.x, a.y), Mma<KV>::pack(a.z, a.w));
+            }
+        }
+        cluster_sync_relaxed();  // no CTA leaves while others still read its partial
+    };
+
+    if (n <= 0 && p.cluster_reduce) {
+        // no pages here, but the cluster's merge needs this CTA: an empty partial
+        for (int r = tid; r < kTileRows; r += kTileThreads) {
+            cl_m[r] = NEG_INF;
+            cl_l[r] = 0.f;
+        }
+        cluster_merge();
+        return;
+    }
     if (n <= 0) {
         // Nothing of this sequence in the partition: the single pass writes the
         // empty-context result; the combine never reads such partitions.
@@ -440,8 +518,30 @@ __global__ void __launch_bounds__(kTileThreads, 1)
         float lo_half = 0.f;
         if (have_o) have_o = exchange(xl, l, lo_half);
         tc::fence_after_sync();
-        if (have_o && !dead) {
-            l += lo_half;
+        if (have_o) l += lo_half;
+        if (p.cluster_reduce) {
+            // park this CTA's partial in its own shared memory (the operand
+            // buffers are idle: every copy and MMA has completed)
+            const bool rows_ok = have_o && !dead;
+            if (wg == 0) {
+                cl_m[r] = rows_ok && l > 0.f ? m : NEG_INF;
+                cl_l[r] = rows_ok ? l : 0.f;
+            }
+            if (rows_ok) {
+                uint32_t x[16];
+#pragma unroll 1
+                for (int c0 = wg * (D / 2); c0 < (wg + 1) * (D / 2); c0 += 16) {
+                    tc::ld_32x32b_x16(lane_base + O_COL + c0, x);
+                    tc::wait_ld();
+#pragma unroll
+                    for (int c = 0; c < 16; c += 4)
+                        *reinterpret_cast<float4*>(cl_o + r * CL + c0 + c) =
+                            l > 0.f ? make_float4(__uint_as_float(x[c]), __uint_as_float(x[c + 1]),
+                                                  __uint_as_float(x[c + 2]), __uint_as_float(x[c + 3]))
+                                    : make_float4(0.f, 0.f, 0.f, 0.f);
+                }
+            }
+        } else if (have_o && !dead) {
             const bool live = u < U;
             const float inv = l > 0.f ? 1.f / l : 0.f;
             size_t orow = 0;
@@ -488,6 +588,7 @@ __global__ void __launch_bounds__(kTileThreads, 1)
         tc::fence_after_sync();
         tc::tmem_dealloc(tmem, kCols);
     }
+    if (p.cluster_reduce) cluster_merge();
 }
 
 template <int D, int BS, typename KV>
@@ -501,12 +602,60 @@ cudaError_t launch_tile_inst(const AttnLaunch& L, cudaStream_t stream) {
     cfg.blockDim = dim3(kTileThreads);
     cfg.dynamicSmemBytes = L.smem_bytes;
     cfg.stream = stream;
-    cudaLaunchAttribute attr[1];
-    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
-    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cudaLaunchAttribute attr[2];
+    int na = 0;
+    if (L.pdl) {
+        attr[na].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+        attr[na].val.programmaticStreamSerializationAllowed = 1;
+        ++na;
+    }
+    if (L.cluster > 1) {
+        attr[na].id = cudaLaunchAttributeClusterDimension;
+        attr[na].val.clusterDim.x = (unsigned)L.cluster;
+        attr[na].val.clusterDim.y = 1;
+        attr[na].val.clusterDim.z = 1;
+        ++na;
+    }
     cfg.attrs = attr;
-    cfg.numAttrs = L.pdl ? 1 : 0;
+    cfg.numAttrs = na;
     return cudaLaunchKernelEx(&cfg, kern, L.tmap_k, L.tmap_v, L.p);
+}
+
+// Clusters of `cluster` CTAs of this instantiation that can be resident at
+// once on the current device (0 if the query fails).
+template <int D, int BS, typename KV>
+int tile_max_clusters_inst(int cluster, uint32_t smem_bytes) {
+    auto kern = tile_kernel<D, BS, KV>;
+    if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem_bytes) !=
+        cudaSuccess)
+        return 0;
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3((unsigned)cluster, 1, 1);
+    cfg.blockDim = dim3(kTileThreads);
+    cfg.dynamicSmemBytes = smem_bytes;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = (unsigned)cluster;
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    int n = 0;
+    if (cudaOccupancyMaxActiveClusters(&n, kern, &cfg) != cudaSuccess) {
+        (void)cudaGetLastError();
+        return 0;
+    }
+    return n;
+}
+
+template <int D>
+int tile_max_clusters_for_d(int block_size, int kv_dtype, int cluster, uint32_t smem_bytes) {
+    const bool bf = kv_dtype == PA_BF16;
+    if (block_size == 16)
+        return bf ? tile_max_clusters_inst<D, 16, __nv_bfloat16>(cluster, smem_bytes)
+                  : tile_max_clusters_inst<D, 16, __half>(cluster, smem_bytes);
+    return bf ? tile_max_clusters_inst<D, 32, __nv_bfloat16>(cluster, smem_bytes)
+              : tile_max_clusters_inst<D, 32, __half>(cluster, smem_bytes);
 }
 
 template <int D>

@@ -134,12 +134,13 @@ def test_multi_token_workspace_size(lib):
     assert lib.pa_workspace_size_multi(ctypes.byref(s), 1, 131072, 512) == \
         lib.pa_workspace_size(ctypes.byref(s), 131072, 512)
     assert lib.pa_workspace_size_multi(ctypes.byref(s), 6, 131072, 131072) == 0   # one partition
-    # up to 16 rows (q_len 4 x group 4) run on the warp-level MMA path: <= 8
-    # partitions reduce in a cluster; more rows run on the tile kernel, whose
-    # partitions always go through the workspace
+    # up to 16 rows (q_len 4 x group 4) run on the warp-level MMA path, more on
+    # the tile kernel; on both, <= 8 partitions reduce in a cluster, more go
+    # through the workspace
     assert lib.pa_workspace_size_multi(ctypes.byref(s), 4, 8 * 512, 512) == 0
-    rows = 4 * 32 * 6 * 8
-    assert lib.pa_workspace_size_multi(ctypes.byref(s), 6, 8 * 512, 512) == \
+    assert lib.pa_workspace_size_multi(ctypes.byref(s), 6, 8 * 512, 512) == 0
+    rows = 4 * 32 * 6 * 9
+    assert lib.pa_workspace_size_multi(ctypes.byref(s), 6, 9 * 512, 512) == \
         (rows * 128 * 4 + 255) // 256 * 256 + rows * 2 * 4
 
 
