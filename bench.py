@@ -367,10 +367,22 @@ def main(argv=None):
     sms = props.multi_processor_count
     plans = {}
     for i, x in enumerate(set0):
+        G = x.q.shape[-2] // x.k_cache.shape[2]
+        rows = G * (x.q.shape[1] if x.q.dim() == 4 else 1)
+        # the library's kernel choice (see the split-KV entry points)
+        tile = rows > 16 or (rows == 16 and x.q.shape[-1] == 256)
+        if tile:
+            plans[names[i]] = {"kernel": "tcgen05 tile (128-row tiles, TMEM accumulators)",
+                               "partition_tokens": pts[i] or "auto", "rows_per_kv_head": rows,
+                               "partitions": "auto" if not pts[i] else
+                                             -(-max(x.max_context_len, 1) // pts[i]),
+                               "reduce": "workspace+combine kernel" if splits[i] else
+                                         "cluster DSMEM or none"}
+            continue
         if x.q.dim() == 4:
-            G = x.q.shape[2] // x.k_cache.shape[2]
             Q = x.q.shape[1]
-            plans[names[i]] = {"partition_tokens": pts[i] or "auto", "q_len": Q,
+            plans[names[i]] = {"kernel": "mma.sync m16n8k16", "partition_tokens": pts[i] or "auto",
+                               "q_len": Q,
                                "query_chunks": -(-Q // min(Q, 16 // G)),
                                "partitions": "auto" if not pts[i] else
                                              -(-max(x.max_context_len, 1) // pts[i]),
@@ -384,7 +396,7 @@ def main(argv=None):
                                "reduce": "balanced records + combine kernel"}
             continue
         parts = -(-max(x.max_context_len, 1) // pt)
-        plans[names[i]] = {"partition_tokens": pt, "partitions": parts,
+        plans[names[i]] = {"kernel": "mma.sync m16n8k16", "partition_tokens": pt, "partitions": parts,
                            "reduce": "none" if parts <= 1 else
                                      ("workspace+combine kernel" if splits[i] else "cluster DSMEM")}
 

@@ -148,6 +148,11 @@ int32_t pa_choose_partition_tokens(const pa_shape* shape, int32_t max_context_le
  * aligned) must hold at least pa_workspace_size(shape, max_context_len,
  * partition_tokens) bytes (may be NULL when that is 0); it is scratch owned by
  * the caller and may be reused once the stream has passed this call.
+ * Kernel choice: groups of 16 query heads at head_dim 256 run on the tcgen05
+ * tile kernel described at pa_decode_multi (its own split, from the device's
+ * resident clusters); every other shape on the warp-level kernel, whose split
+ * pa_choose_partition_tokens reports.  PA_PARTITION_BALANCED always runs the
+ * warp-level kernel.
  */
 pa_status pa_decode_splitkv(void* out, const void* q, const void* k_cache, const void* v_cache,
                             const int32_t* block_tables, const int32_t* context_lens,

@@ -277,14 +277,18 @@ bool clusters_enabled() {
 // Which kernel serves several query tokens: the tcgen05 tile kernel once
 // the rows of a (sequence, kv head) -- q_len * group -- exceed the 16 rows
 // of the warp-level MMA path (which would otherwise read the pages once per
-// 16 rows).  PA_MULTI_KERNEL=mma or =tile forces one of them for every
-// q_len > 1 (a testing and tuning switch; read on every call, results agree).
-bool use_tile(const pa_shape* s, int32_t q_len) {
-    if (q_len <= 1) return false;
+// 16 rows), and for 16 rows at head_dim 256.  PA_MULTI_KERNEL=mma forces the warp-level path for every
+// q_len > 1, =tile the tile kernel for every split-KV call, one query token
+// included (a testing and tuning switch; read on every call, results agree).
+bool use_tile(const pa_shape* s, int32_t q_len, int32_t partition_tokens) {
+    const int64_t rows = (int64_t)q_len * (s->num_heads / s->num_kv_heads);
+    if (partition_tokens == PA_PARTITION_BALANCED && rows <= 16) return false;  // honoured there
     const char* v = std::getenv("PA_MULTI_KERNEL");
-    if (v && std::strcmp(v, "mma") == 0) return false;
     if (v && std::strcmp(v, "tile") == 0) return true;
-    return (int64_t)q_len * (s->num_heads / s->num_kv_heads) > 16;
+    if (v && std::strcmp(v, "mma") == 0 && q_len > 1) return false;
+    // 16 rows at head_dim 256 too: the warp-level path needs two warps per
+    // page there and spills registers; the tile kernel was 6-23 % faster
+    return rows > 16 || (rows == 16 && s->head_dim == 256);
 }
 
 int tile_ctas_per_sm(const pa_shape* s) {
@@ -363,7 +367,7 @@ Plan tile_plan(const pa_shape* s, int32_t max_context_len, int32_t partition_tok
 // one CTA: it needs q_len * group <= 16, and batch <= kMaxBalancedBatch.
 Plan make_plan(const pa_shape* s, int32_t max_context_len, int32_t partition_tokens, int num_sms,
                int32_t q_len = 1) {
-    if (use_tile(s, q_len)) {
+    if (use_tile(s, q_len, partition_tokens)) {
         Plan tp = tile_plan(s, max_context_len,
                             partition_tokens == PA_PARTITION_BALANCED ? 0 : partition_tokens,
                             num_sms, q_len);
