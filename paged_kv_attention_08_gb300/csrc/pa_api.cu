@@ -351,14 +351,19 @@ Plan tile_plan(const pa_shape* s, int32_t max_context_len, int32_t partition_tok
                 best_c = c;
                 break;
             }
-        const bool cluster = parts >= 2 && best_c >= 2 && (int64_t)best_c * 4 >= parts * 3;
+        // the parked partial must fit in the operand buffers
+        const bool fits = tile_cluster_bytes(s->head_dim) <=
+                          tile_smem_layout(s->head_dim, s->block_size).bar_off;
+        const bool cluster =
+            fits && parts >= 2 && best_c >= 2 && (int64_t)best_c * 4 >= parts * 3;
         if (cluster) parts = std::min<int64_t>(best_c, parts);
         pp = (int)((pages + parts - 1) / parts);
         Plan p = plan_with(s, pages, pp, cluster);
         p.tile = true;
         return p;
     }
-    Plan p = plan_with(s, pages, pp, true);
+    Plan p = plan_with(s, pages, pp, tile_cluster_bytes(s->head_dim) <=
+                                         tile_smem_layout(s->head_dim, s->block_size).bar_off);
     p.tile = true;
     return p;
 }

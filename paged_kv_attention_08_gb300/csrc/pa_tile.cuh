@@ -265,11 +265,24 @@ __global__ void __launch_bounds__(kTileThreads, 1)
         const uint32_t ring = smem_u32(smem + (is_k ? L.k_off : L.v_off));
         const int32_t* table_row = p.block_tables + (size_t)b * p.max_blocks;
         const uint64_t policy = l2_policy_evict_first();
+        // the partition's table entries, 32 pages at a time (one per lane),
+        // fetched one window ahead so that no block waits for its entries
+        auto fetch = [&](int w) -> int {
+            const int jj = pb + w * 32 + lane;
+            return jj < pe ? __ldg(table_row + jj) : -1;
+        };
+        int ent_cur = fetch(0), ent_next = fetch(1), win = 0;
         int issued = 0;
         for (int k = 0; k < nblk && !*abort_flag; ++k) {
             const int st = k % NS, round = k / NS;
-            const int j = pb + k * NPB + lane;
-            const int e = (lane < NPB && j < pe) ? __ldg(table_row + j) : -1;
+            const int first = k * NPB;  // page index of the block within the partition
+            if ((first >> 5) != win) {  // NPB divides 32: a block never straddles windows
+                win = first >> 5;
+                ent_cur = ent_next;
+                ent_next = fetch(win + 1);
+            }
+            const int e0 = __shfl_sync(kFullMask, ent_cur, (first & 31) + (lane < NPB ? lane : 0));
+            const int e = lane < NPB ? e0 : -1;
             const int phys = (e >= 0 && (int64_t)e < p.num_blocks) ? e : -1;
             bool ok = true;
             if (round > 0 && lane == 0) ok = wait(empty + st, (round - 1) & 1);
