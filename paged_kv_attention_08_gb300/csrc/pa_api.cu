@@ -186,7 +186,8 @@ struct Plan {
     bool tile;       // several query tokens on the tcgen05 tile kernel (128-row tiles)
 };
 
-Plan plan_with(const pa_shape* s, int pages, int pp, bool cluster_ok) {
+Plan plan_with(const pa_shape* s, int pages, int pp, bool cluster_ok,
+               int max_cluster = kMaxClusterParts) {
     Plan p;
     p.many_ctas = false;
     p.balanced = false;
@@ -196,7 +197,7 @@ Plan plan_with(const pa_shape* s, int pages, int pp, bool cluster_ok) {
     p.num_parts = (pages + pp - 1) / pp;
     if (p.num_parts < 1) p.num_parts = 1;
     p.part_pages = p.num_parts <= 1 ? s->max_blocks_per_seq : pp;
-    p.cluster = cluster_ok && p.num_parts > 1 && p.num_parts <= kMaxClusterParts;
+    p.cluster = cluster_ok && p.num_parts > 1 && p.num_parts <= max_cluster;
     return p;
 }
 
@@ -208,7 +209,8 @@ Plan plan_with(const pa_shape* s, int pages, int pp, bool cluster_ok) {
 //    into partitions of about 64 pages, so that long and ragged sequences
 //    balance across waves; no cluster (the grid spans several waves);
 //  - a smaller grid is split to fill about 85% of one wave, either into at
-//    most 8 partitions of at least 4 pages reduced inside a cluster, or, when
+//    most 8 partitions of at least 4 pages reduced inside a cluster (up to 16
+//    where the device holds all of the call's clusters at once), or, when
 //    that gives less parallelism, into partitions of at least 16 pages
 //    combined through the workspace.
 // The longest context stands for every sequence: the host reads no lengths.
@@ -236,6 +238,37 @@ Plan balanced_plan(const pa_shape* s, int pages, int num_sms) {
     return p;
 }
 
+// Clusters of `cluster` one-token attention CTAs of tune `t` that fit on the
+// current device at once (cached per device and shape class; 0 when unknown,
+// e.g. without a device).
+int attn_max_clusters(const pa_shape* s, const Tune& t, int cluster) {
+    static std::atomic<int> cache[kMaxDevices][3][2][2][kMaxDecodeClusterParts + 1];  // n+1
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) {
+        (void)cudaGetLastError();
+        return 0;
+    }
+    const int di = s->head_dim == 64 ? 0 : (s->head_dim == 128 ? 1 : 2);
+    std::atomic<int>& slot = cache[dev][di][s->block_size == 32][s->kv_dtype == PA_BF16][cluster];
+    int v = slot.load(std::memory_order_relaxed);
+    if (v == 0) {
+        const int threads = 32 * t.nt * t.nh;
+        const uint32_t smem =
+            attn_smem_layout(s->head_dim, s->block_size, t.nt, t.ns).total + kSmemAlignSlack;
+        int n = 0;
+        switch (s->head_dim) {
+            case 64: n = attn_max_clusters_d64(s->block_size, s->kv_dtype, cluster, threads, smem); break;
+            case 128: n = attn_max_clusters_d128(s->block_size, s->kv_dtype, cluster, threads, smem); break;
+            default: n = attn_max_clusters_d256(s->block_size, s->kv_dtype, cluster, threads, smem); break;
+        }
+        v = n + 1;
+        slot.store(v, std::memory_order_relaxed);
+    }
+    return v - 1;
+}
+
+bool clusters_enabled();
+
 Plan auto_plan(const pa_shape* s, int32_t max_context_len, int num_sms, int q_chunks = 1) {
     const int pages = pages_for(s, max_context_len);
     const int64_t units = (int64_t)s->batch * s->num_kv_heads * q_chunks;
@@ -255,10 +288,27 @@ Plan auto_plan(const pa_shape* s, int32_t max_context_len, int num_sms, int q_ch
     const int64_t slots = (int64_t)num_sms * ctas_per_sm(s, pick_tune(s, false));
     int64_t fill = (int64_t)(0.85 * (double)slots / (double)units);
     if (fill < 1) fill = 1;
-    const int64_t p_cl = std::min<int64_t>(std::min<int64_t>(kMaxClusterParts, fill), ceil_div(pages, 4));
+    // clusters of up to 16 CTAs when the device holds every unit's cluster at once
+    int64_t cap = kMaxClusterParts;
+    const int64_t want = std::min<int64_t>(std::min<int64_t>(kMaxDecodeClusterParts, fill),
+                                           ceil_div(pages, 4));
+    if (want > kMaxClusterParts && clusters_enabled()) {
+        for (int64_t c = want; c > kMaxClusterParts; --c)
+            if (units <= attn_max_clusters(s, pick_tune(s, false), (int)c)) {
+                cap = c;
+                break;
+            }
+    }
+    const int64_t p_cl = std::min<int64_t>(std::min<int64_t>(cap, fill), ceil_div(pages, 4));
     const int64_t p_ws = std::min<int64_t>(fill, ceil_div(pages, 16));
-    Plan p = p_cl >= p_ws ? plan_with(s, pages, (int)ceil_div(pages, p_cl), true)
-                          : plan_with(s, pages, (int)ceil_div(pages, p_ws), false);
+    // a cluster split with fewer partitions than the workspace split still
+    // wins when partitions are short (latency-bound: the combine launch costs
+    // more than the lost parallelism), e.g. B=1, T=8K: 12 in clusters 11.6 us,
+    // 16 through the workspace 12.5 us; at T=32K/128K the workspace split wins
+    const bool short_parts = ceil_div(pages, p_cl) <= 64;
+    const bool use_cluster = p_cl >= p_ws || (short_parts && p_cl * 4 >= p_ws * 3);
+    Plan p = use_cluster ? plan_with(s, pages, (int)ceil_div(pages, p_cl), true, (int)cap)
+                         : plan_with(s, pages, (int)ceil_div(pages, p_ws), false);
     // Equal partitions of few units leave SMs idle (e.g. 32 units x 4 = 128
     // CTAs on 152 SMs); the balanced split gives every SM the same share.
     const double coverage = (double)(units * p.num_parts) / (double)slots;

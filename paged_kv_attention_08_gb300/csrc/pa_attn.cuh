@@ -608,17 +608,17 @@ __global__ void __launch_bounds__(256, 1)
         const int P = p.num_parts;
         const uint32_t rank = (uint32_t)blockIdx.x;  // the cluster spans grid x
         const uint32_t cp = smem_u32(cpart);
-        uint32_t rbase[kMaxClusterParts];
+        uint32_t rbase[kMaxDecodeClusterParts];
 #pragma unroll
-        for (int q = 0; q < kMaxClusterParts; ++q)
+        for (int q = 0; q < kMaxDecodeClusterParts; ++q)
             rbase[q] = q < P ? map_cluster_rank(cp, (uint32_t)q) : cp;
         const int chunk = (R * D + P - 1) / P;
         const int i1 = min(((int)rank + 1) * chunk, R * D);
         for (int idx = (int)rank * chunk + tid; idx < i1; idx += blockDim.x) {
             const int r = idx / D;
-            float m[kMaxClusterParts], l[kMaxClusterParts], a[kMaxClusterParts];
+            float m[kMaxDecodeClusterParts], l[kMaxDecodeClusterParts], a[kMaxDecodeClusterParts];
 #pragma unroll
-            for (int q = 0; q < kMaxClusterParts; ++q) {
+            for (int q = 0; q < kMaxDecodeClusterParts; ++q) {
                 if (q < P) {
                     m[q] = ld_cluster_f32(rbase[q] + 4u * (R * D + r));
                     l[q] = ld_cluster_f32(rbase[q] + 4u * (R * D + R + r));
@@ -627,11 +627,11 @@ __global__ void __launch_bounds__(256, 1)
             }
             float M = NEG_INF;
 #pragma unroll
-            for (int q = 0; q < kMaxClusterParts; ++q)
+            for (int q = 0; q < kMaxDecodeClusterParts; ++q)
                 if (q < P) M = fmaxf(M, m[q]);
             float A = 0.f, Ls = 0.f;
 #pragma unroll
-            for (int q = 0; q < kMaxClusterParts; ++q) {
+            for (int q = 0; q < kMaxDecodeClusterParts; ++q) {
                 if (q < P && m[q] != NEG_INF) {
                     const float f = fast_exp2(m[q] - M);
                     A = fmaf(f, a[q], A);
@@ -651,6 +651,10 @@ cudaError_t launch_attn_inst(const AttnLaunch& L, cudaStream_t stream) {
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          (int)L.smem_bytes);
     if (e != cudaSuccess) return e;
+    if (L.cluster > kMaxClusterParts) {
+        e = cudaFuncSetAttribute(kern, cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
+        if (e != cudaSuccess) return e;
+    }
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = L.grid;
     cfg.blockDim = dim3(L.threads);
@@ -673,6 +677,47 @@ cudaError_t launch_attn_inst(const AttnLaunch& L, cudaStream_t stream) {
     cfg.attrs = attr;
     cfg.numAttrs = n;
     return cudaLaunchKernelEx(&cfg, kern, L.tmap_k, L.tmap_v, L.p);
+}
+
+// Clusters of `cluster` CTAs of the one-token instantiation resident at once
+// on the current device (0 if the query fails).
+template <int D, int BS, typename KV>
+int attn_max_clusters_inst(int cluster, int threads, uint32_t smem_bytes) {
+    auto kern = attn_kernel<D, BS, KV, false>;
+    if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem_bytes) !=
+        cudaSuccess)
+        return 0;
+    if (cluster > kMaxClusterParts &&
+        cudaFuncSetAttribute(kern, cudaFuncAttributeNonPortableClusterSizeAllowed, 1) != cudaSuccess)
+        return 0;
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3((unsigned)cluster, 1, 1);
+    cfg.blockDim = dim3((unsigned)threads);
+    cfg.dynamicSmemBytes = smem_bytes;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = (unsigned)cluster;
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    int n = 0;
+    if (cudaOccupancyMaxActiveClusters(&n, kern, &cfg) != cudaSuccess) {
+        (void)cudaGetLastError();
+        return 0;
+    }
+    return n;
+}
+
+template <int D>
+int attn_max_clusters_for_d(int block_size, int kv_dtype, int cluster, int threads,
+                            uint32_t smem_bytes) {
+    const bool bf = kv_dtype == PA_BF16;
+    if (block_size == 16)
+        return bf ? attn_max_clusters_inst<D, 16, __nv_bfloat16>(cluster, threads, smem_bytes)
+                  : attn_max_clusters_inst<D, 16, __half>(cluster, threads, smem_bytes);
+    return bf ? attn_max_clusters_inst<D, 32, __nv_bfloat16>(cluster, threads, smem_bytes)
+              : attn_max_clusters_inst<D, 32, __half>(cluster, threads, smem_bytes);
 }
 
 template <int D, bool MULTI>

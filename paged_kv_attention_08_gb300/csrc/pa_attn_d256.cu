@@ -7,4 +7,8 @@ cudaError_t launch_attn_d256(const AttnLaunch& L, cudaStream_t stream) {
     if (L.p.q_len > 1) return launch_attn_d256_multi(L, stream);
     return launch_attn_for_d<256, false>(L, stream);
 }
+int attn_max_clusters_d256(int block_size, int kv_dtype, int cluster, int threads,
+                          uint32_t smem_bytes) {
+    return attn_max_clusters_for_d<256>(block_size, kv_dtype, cluster, threads, smem_bytes);
+}
 }  // namespace pa

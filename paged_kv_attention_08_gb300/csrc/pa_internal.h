@@ -108,8 +108,12 @@ __host__ __device__ inline uint32_t cluster_part_floats(int G, int D) {
     return (uint32_t)G * D + 2u * G + 3u * 8u * G;
 }
 
-// Most partitions of one (sequence, kv head) reduced inside a cluster.
+// Most partitions of one (sequence, kv head) reduced inside a cluster: 8 is
+// the portable cluster size; the one-token kernel may use clusters of up to
+// 16 (a non-portable size) where the device can hold all of a call's
+// clusters at once.
 constexpr int kMaxClusterParts = 8;
+constexpr int kMaxDecodeClusterParts = 16;
 
 // Slack added to the dynamic shared-memory request so that the kernel can
 // align its base to 1024 bytes (TMA destinations).
@@ -202,6 +206,11 @@ cudaError_t launch_attn_d64(const AttnLaunch& L, cudaStream_t stream);
 cudaError_t launch_attn_d128(const AttnLaunch& L, cudaStream_t stream);
 cudaError_t launch_attn_d256(const AttnLaunch& L, cudaStream_t stream);
 cudaError_t launch_attn_d64_multi(const AttnLaunch& L, cudaStream_t stream);
+// Clusters of `cluster` one-token attention CTAs (tune: `threads`, `smem_bytes`)
+// resident at once on the current device (0 if the query fails).
+int attn_max_clusters_d64(int block_size, int kv_dtype, int cluster, int threads, uint32_t smem_bytes);
+int attn_max_clusters_d128(int block_size, int kv_dtype, int cluster, int threads, uint32_t smem_bytes);
+int attn_max_clusters_d256(int block_size, int kv_dtype, int cluster, int threads, uint32_t smem_bytes);
 cudaError_t launch_attn_d128_multi(const AttnLaunch& L, cudaStream_t stream);
 cudaError_t launch_attn_d256_multi(const AttnLaunch& L, cudaStream_t stream);
 

@@ -90,6 +90,7 @@ def test_qdtype_output(name, mode):
     ("long_b1_t131072", "split", 512), ("long_b4_t8192", "split", 512),
     ("long_b4_t32768", "split", 512), ("long_b4_t131072", "split", 512),
     ("long_b1_t131072", "split", 0), ("long_b4_t32768", "single", 0),
+    ("long_b1_t8192", "split", 0),      # automatic: clusters of more than 8 CTAs where they fit
     ("mqa_b32_t16384", "split", 0), ("mqa_b32_t16384", "single", 0),
 ])
 def test_full_size_sampled(name, mode, pt):
