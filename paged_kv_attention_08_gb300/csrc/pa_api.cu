@@ -288,16 +288,24 @@ Plan auto_plan(const pa_shape* s, int32_t max_context_len, int num_sms, int q_ch
     const int64_t slots = (int64_t)num_sms * ctas_per_sm(s, pick_tune(s, false));
     int64_t fill = (int64_t)(0.85 * (double)slots / (double)units);
     if (fill < 1) fill = 1;
-    // clusters of up to 16 CTAs when the device holds every unit's cluster at once
-    int64_t cap = kMaxClusterParts;
+    // The largest cluster (up to 16 CTAs) of which the device holds every
+    // unit's copy at once: one cluster more than fits runs as a second wave
+    // (at ~133 KB per CTA the device holds 15 clusters of 8, so 16 units in
+    // clusters of 8 took 13.9 us at B=2, T=2048, against 8.9 us in clusters
+    // of 6).  Without a device to ask (the host-only partition query),
+    // clusters of up to 8 are assumed to fit.
+    int64_t cap = 1;
     const int64_t want = std::min<int64_t>(std::min<int64_t>(kMaxDecodeClusterParts, fill),
                                            ceil_div(pages, 4));
-    if (want > kMaxClusterParts && clusters_enabled()) {
-        for (int64_t c = want; c > kMaxClusterParts; --c)
-            if (units <= attn_max_clusters(s, pick_tune(s, false), (int)c)) {
+    if (clusters_enabled()) {
+        const Tune tall = pick_tune(s, false);
+        for (int64_t c = want; c >= 2; --c) {
+            const int n = attn_max_clusters(s, tall, (int)c);
+            if (n > 0 ? units <= n : c <= kMaxClusterParts) {
                 cap = c;
                 break;
             }
+        }
     }
     const int64_t p_cl = std::min<int64_t>(std::min<int64_t>(cap, fill), ceil_div(pages, 4));
     const int64_t p_ws = std::min<int64_t>(fill, ceil_div(pages, 16));

@@ -395,3 +395,15 @@ def test_append_then_decode_in_a_graph():
     rows = sample_rows(x, 24)
     want = oracle.decode_rows(host.q, k2, v2, host.block_tables, host.context_lens, host.scale, rows)
     assert_close_fp32(out[rows[:, 0], rows[:, 1]], want)
+
+
+@pytest.mark.parametrize("B,T,Hkv", [(2, 2048, 8), (4, 1024, 4), (16, 1500, 1)])
+def test_sixteen_unit_automatic_plan(B, T, Hkv):
+    """16 (sequence, kv head) units: the automatic plan sizes its clusters so
+    that all of them are resident at once; exact against the oracle."""
+    H = Hkv * 4
+    spec = workloads.Spec("u16", B, H, Hkv, 128, 16, torch.bfloat16, f"fixed:{T}")
+    x = workloads.make(spec, seed=9, device="cpu")
+    want = oracle.decode(x.q, x.k_cache, x.v_cache, x.block_tables, x.context_lens, x.scale)
+    xd = x.to(DEV)
+    assert_close_fp32(run(xd, "split", partition_tokens=0), want)
