@@ -137,11 +137,13 @@ int32_t pa_choose_partition_tokens(const pa_shape* shape, int32_t max_context_le
  * into one equal share per SM, and a piece that straddles two shares leaves
  * a partial record for the combine kernel);
  * one CTA per partition computes fp32 partials (m, l, acc[head_dim]) for each
- * query head of the group.  At most 8 partitions are launched as one
- * thread-block cluster and reduced through distributed shared memory inside
- * the same kernel (no workspace needed); more partitions write their partials
- * to `workspace` and a second kernel combines them with a log-sum-exp
- * reduction into out.  `max_context_len` must be >= every context_lens[b] that
+ * query head of the group.  The partitions of a (sequence, kv head) are
+ * launched as one thread-block cluster and reduced through distributed
+ * shared memory inside the same kernel (no workspace needed) when there are
+ * at most 8 of them (up to 16 for the automatic choice) and the device can
+ * hold every cluster of the call at once; otherwise they write their
+ * partials to `workspace` and a second kernel combines them with a
+ * log-sum-exp reduction into out.  pa_workspace_size reports which.  `max_context_len` must be >= every context_lens[b] that
  * should be attended in full (tokens beyond it are dropped; no device->host
  * read is made); `partition_tokens` = 0 chooses the split automatically, and a
  * choice of one partition runs the single pass.  `workspace` (device, 16-byte

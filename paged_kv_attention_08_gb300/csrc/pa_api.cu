@@ -242,17 +242,18 @@ Plan balanced_plan(const pa_shape* s, int pages, int num_sms) {
 // current device at once (cached per device and shape class; 0 when unknown,
 // e.g. without a device).
 int attn_max_clusters(const pa_shape* s, const Tune& t, int cluster) {
-    static std::atomic<int> cache[kMaxDevices][3][2][2][kMaxDecodeClusterParts + 1];  // n+1
+    static std::atomic<int> cache[kMaxDevices][3][2][2][2][kMaxDecodeClusterParts + 1];  // n+1
     int dev = 0;
     if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) {
         (void)cudaGetLastError();
         return 0;
     }
     const int di = s->head_dim == 64 ? 0 : (s->head_dim == 128 ? 1 : 2);
-    std::atomic<int>& slot = cache[dev][di][s->block_size == 32][s->kv_dtype == PA_BF16][cluster];
+    const int threads = 32 * t.nt * t.nh;  // the tune: 8-warp (one per SM) or 4-warp CTAs
+    std::atomic<int>& slot =
+        cache[dev][di][s->block_size == 32][s->kv_dtype == PA_BF16][threads >= 256][cluster];
     int v = slot.load(std::memory_order_relaxed);
     if (v == 0) {
-        const int threads = 32 * t.nt * t.nh;
         const uint32_t smem =
             attn_smem_layout(s->head_dim, s->block_size, t.nt, t.ns).total + kSmemAlignSlack;
         int n = 0;
@@ -449,6 +450,12 @@ Plan make_plan(const pa_shape* s, int32_t max_context_len, int32_t partition_tok
         plan = plan_with(s, pages_for(s, max_context_len), partition_tokens / s->block_size, true);
         plan.many_ctas =
             (int64_t)s->batch * s->num_kv_heads * q_chunks * plan.num_parts > num_sms;
+        if (plan.cluster) {
+            // the partition count is honoured; its reduction goes through the
+            // workspace when the device cannot hold every cluster at once
+            const int n = attn_max_clusters(s, pick_tune(s, plan.many_ctas), plan.num_parts);
+            if (n > 0 && (int64_t)s->batch * s->num_kv_heads * q_chunks > n) plan.cluster = false;
+        }
     }
     if (!clusters_enabled()) plan.cluster = false;
     return plan;

@@ -39,6 +39,8 @@
 //     PA_ERR_TIMEOUT in the device error word and abandons its work.
 #pragma once
 
+#include <type_traits>
+
 #include "pa_device.cuh"
 
 namespace pa {
@@ -608,39 +610,48 @@ __global__ void __launch_bounds__(256, 1)
         const int P = p.num_parts;
         const uint32_t rank = (uint32_t)blockIdx.x;  // the cluster spans grid x
         const uint32_t cp = smem_u32(cpart);
-        uint32_t rbase[kMaxDecodeClusterParts];
-#pragma unroll
-        for (int q = 0; q < kMaxDecodeClusterParts; ++q)
-            rbase[q] = q < P ? map_cluster_rank(cp, (uint32_t)q) : cp;
         const int chunk = (R * D + P - 1) / P;
         const int i1 = min(((int)rank + 1) * chunk, R * D);
-        for (int idx = (int)rank * chunk + tid; idx < i1; idx += blockDim.x) {
-            const int r = idx / D;
-            float m[kMaxDecodeClusterParts], l[kMaxDecodeClusterParts], a[kMaxDecodeClusterParts];
+        // unrolled for the cluster's size class: up to 8 ranks (portable
+        // clusters, the common case) or up to 16
+        auto merge = [&](auto maxp) {
+            constexpr int MAXP = decltype(maxp)::value;
+            uint32_t rbase[MAXP];
 #pragma unroll
-            for (int q = 0; q < kMaxDecodeClusterParts; ++q) {
-                if (q < P) {
-                    m[q] = ld_cluster_f32(rbase[q] + 4u * (R * D + r));
-                    l[q] = ld_cluster_f32(rbase[q] + 4u * (R * D + R + r));
-                    a[q] = ld_cluster_f32(rbase[q] + 4u * idx);
+            for (int q = 0; q < MAXP; ++q)
+                rbase[q] = q < P ? map_cluster_rank(cp, (uint32_t)q) : cp;
+            for (int idx = (int)rank * chunk + tid; idx < i1; idx += blockDim.x) {
+                const int r = idx / D;
+                float m[MAXP], l[MAXP], a[MAXP];
+#pragma unroll
+                for (int q = 0; q < MAXP; ++q) {
+                    if (q < P) {
+                        m[q] = ld_cluster_f32(rbase[q] + 4u * (R * D + r));
+                        l[q] = ld_cluster_f32(rbase[q] + 4u * (R * D + R + r));
+                        a[q] = ld_cluster_f32(rbase[q] + 4u * idx);
+                    }
                 }
-            }
-            float M = NEG_INF;
+                float M = NEG_INF;
 #pragma unroll
-            for (int q = 0; q < kMaxDecodeClusterParts; ++q)
-                if (q < P) M = fmaxf(M, m[q]);
-            float A = 0.f, Ls = 0.f;
+                for (int q = 0; q < MAXP; ++q)
+                    if (q < P) M = fmaxf(M, m[q]);
+                float A = 0.f, Ls = 0.f;
 #pragma unroll
-            for (int q = 0; q < kMaxDecodeClusterParts; ++q) {
-                if (q < P && m[q] != NEG_INF) {
-                    const float f = fast_exp2(m[q] - M);
-                    A = fmaf(f, a[q], A);
-                    Ls = fmaf(f, l[q], Ls);
+                for (int q = 0; q < MAXP; ++q) {
+                    if (q < P && m[q] != NEG_INF) {
+                        const float f = fast_exp2(m[q] - M);
+                        A = fmaf(f, a[q], A);
+                        Ls = fmaf(f, l[q], Ls);
+                    }
                 }
+                store_out(p.out, row_off(b, kvh, r) + idx % D, Ls > 0.f ? A / Ls : 0.f,
+                          p.out_dtype);
             }
-            store_out(p.out, row_off(b, kvh, r) + idx % D, Ls > 0.f ? A / Ls : 0.f,
-                      p.out_dtype);
-        }
+        };
+        if (P <= kMaxClusterParts)
+            merge(std::integral_constant<int, kMaxClusterParts>{});
+        else
+            merge(std::integral_constant<int, kMaxDecodeClusterParts>{});
         cluster_sync_relaxed();  // no CTA leaves while others still read its shared memory
     }
 }

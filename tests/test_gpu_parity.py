@@ -163,8 +163,12 @@ def test_cluster_split_sizes(shape, parts):
     assert -(-max(shape["lens"]) // pt) <= 8
     want = oracle.decode(x.q, x.k_cache, x.v_cache, x.block_tables, x.context_lens, x.scale)
     xd = x.to(DEV)
-    assert pa.workspace_size(xd.q, xd.k_cache, xd.block_tables, torch.float32,
-                             xd.max_context_len, pt) == 0
+    ws = pa.workspace_size(xd.q, xd.k_cache, xd.block_tables, torch.float32, xd.max_context_len, pt)
+    units = shape["B"] * shape["Hkv"]
+    if units <= 8:
+        assert ws == 0      # a handful of clusters always fits: reduced in the cluster
+    # (16 clusters of 8 CTAs do not all fit at once on a 152-SM part: the
+    # partitions then go through the workspace, which workspace_size reports)
     assert_close_fp32(run(xd, "split", partition_tokens=pt), want)
 
 
