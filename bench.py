@@ -365,40 +365,9 @@ def main(argv=None):
     splits = [ws[i].numel() > 16 for i in range(len(set0))]      # partials combined by a 2nd kernel
     launches_per_step = sum(2 if s else 1 for s in splits) + (len(set0) if args.with_append else 0)
     sms = props.multi_processor_count
-    plans = {}
-    for i, x in enumerate(set0):
-        G = x.q.shape[-2] // x.k_cache.shape[2]
-        rows = G * (x.q.shape[1] if x.q.dim() == 4 else 1)
-        # the library's kernel choice (see the split-KV entry points)
-        tile = rows > 16 or (rows == 16 and x.q.shape[-1] == 256)
-        if tile:
-            plans[names[i]] = {"kernel": "tcgen05 tile (128-row tiles, TMEM accumulators)",
-                               "partition_tokens": pts[i] or "auto", "rows_per_kv_head": rows,
-                               "partitions": "auto" if not pts[i] else
-                                             -(-max(x.max_context_len, 1) // pts[i]),
-                               "reduce": "workspace+combine kernel" if splits[i] else
-                                         "cluster DSMEM or none"}
-            continue
-        if x.q.dim() == 4:
-            Q = x.q.shape[1]
-            plans[names[i]] = {"kernel": "mma.sync m16n8k16", "partition_tokens": pts[i] or "auto",
-                               "q_len": Q,
-                               "query_chunks": -(-Q // min(Q, 16 // G)),
-                               "partitions": "auto" if not pts[i] else
-                                             -(-max(x.max_context_len, 1) // pts[i]),
-                               "reduce": "workspace+combine kernel" if splits[i] else
-                                         "cluster DSMEM or none"}
-            continue
-        pt = pts[i] or pa.choose_partition_tokens(x.q, x.k_cache, x.block_tables,
-                                                  x.max_context_len, sms)
-        if pt == pa.PARTITION_BALANCED:
-            plans[names[i]] = {"partition_tokens": "balanced", "partitions": f"{sms} equal shares",
-                               "reduce": "balanced records + combine kernel"}
-            continue
-        parts = -(-max(x.max_context_len, 1) // pt)
-        plans[names[i]] = {"kernel": "mma.sync m16n8k16", "partition_tokens": pt, "partitions": parts,
-                           "reduce": "none" if parts <= 1 else
-                                     ("workspace+combine kernel" if splits[i] else "cluster DSMEM")}
+    # the library's own description of each call's plan on this device
+    plans = {names[i]: pa.plan_info(x.q, x.k_cache, x.block_tables, x.max_context_len, pts[i])
+             for i, x in enumerate(set0)}
 
     stream = torch.cuda.Stream(device=dev)
 
@@ -656,8 +625,8 @@ def main(argv=None):
                          {"bound": "hbm", "achieved": dom_gbs, "peak": peak, "unit": "GB/s",
                           "frac": dom_gbs / peak, "peak_kind": peak_kind,
                           "step_frac": value / world / peak}) | {
-                "kernel": f"decode call on {dom_name} "
-                          f"({plans[dom_name]['partitions']} partition(s), reduce: "
+                "kernel": f"decode call on {dom_name} ({plans[dom_name]['kernel']} kernel, "
+                          f"{plans[dom_name]['partitions']} partition(s), reduce: "
                           f"{plans[dom_name]['reduce']})",
                 "bytes_per_launch": dom_bytes,
                 "traffic": ncu_traffic("pa_tile" if tensor_bound else "pa_attn", dom_name)},

@@ -192,6 +192,26 @@ pa_status pa_decode_multi(void* out, const void* q, const void* k_cache, const v
                           int32_t max_context_len, int32_t partition_tokens, void* workspace,
                           size_t workspace_bytes, void* stream);
 
+/* How a split-KV call (pa_decode_splitkv / pa_decode_multi) with these
+ * arguments runs on the current device; filled by pa_plan_info. */
+typedef struct pa_plan_desc {
+    int32_t kernel;           /* 0: warp-level m16n8k16 kernel; 1: tcgen05 tile kernel */
+    int32_t partitions;       /* partitions per (sequence, kv head[, query chunk / tile]) */
+    int32_t partition_tokens; /* tokens per partition (the longest context for one) */
+    int32_t reduce;           /* 0: none (one pass); 1: cluster (distributed shared
+                                 memory); 2: workspace + combine kernel; 3: balanced split */
+    int32_t ctas;             /* CTAs of the attention kernel */
+    int32_t threads;          /* threads per CTA */
+} pa_plan_desc;
+
+/* Describes, without launching anything, the plan a split-KV call with these
+ * arguments would use (no counterpart in the pages: a diagnostic of this
+ * library's own choices).  Needs the current device for automatic choices
+ * (partition_tokens = 0), as the calls themselves do.  Returns
+ * PA_ERR_INVALID_ARG / PA_ERR_UNSUPPORTED like the calls, else PA_OK. */
+pa_status pa_plan_info(const pa_shape* shape, int32_t q_len, int32_t max_context_len,
+                       int32_t partition_tokens, pa_plan_desc* desc);
+
 /* Workspace bytes of pa_decode_multi (0 for invalid arguments or when none is
  * needed); pa_workspace_size(shape, ...) is this with q_len = 1. */
 size_t pa_workspace_size_multi(const pa_shape* shape, int32_t q_len, int32_t max_context_len,

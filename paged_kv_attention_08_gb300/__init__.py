@@ -25,7 +25,7 @@ import threading
 import torch
 
 __all__ = ["PaError", "decode", "decode_splitkv", "decode_splitkv_noalloc", "decode_multi",
-           "append_kv", "workspace_size", "workspace_size_multi", "choose_partition_tokens",
+           "append_kv", "workspace_size", "workspace_size_multi", "plan_info", "choose_partition_tokens",
            "resolve_blocks", "device_error", "library_path", "F16", "BF16", "F32"]
 
 F16, BF16, F32 = 0, 1, 2
@@ -78,6 +78,8 @@ def _load():
             lib.pa_decode_splitkv_noalloc.restype = ctypes.c_int
             lib.pa_decode_multi.argtypes = [P, P, P, P, P, P, S, i32, f32, i32, i32, P, sz, P]
             lib.pa_decode_multi.restype = ctypes.c_int
+            lib.pa_plan_info.argtypes = [S, i32, i32, i32, P]
+            lib.pa_plan_info.restype = ctypes.c_int
             lib.pa_workspace_size_multi.argtypes = [S, i32, i32, i32]
             lib.pa_workspace_size_multi.restype = sz
             lib.pa_workspace_size.argtypes = [S, i32, i32]
@@ -216,6 +218,32 @@ def _multi_shape(q, k_cache, block_tables, out_dtype):
     if q.dim() != 4:
         raise ValueError("q must be [batch, q_len, num_heads, head_dim]")
     return make_shape(q[:, 0], k_cache, block_tables, out_dtype), int(q.shape[1])
+
+
+class _PlanDesc(ctypes.Structure):
+    _fields_ = [("kernel", ctypes.c_int32), ("partitions", ctypes.c_int32),
+                ("partition_tokens", ctypes.c_int32), ("reduce", ctypes.c_int32),
+                ("ctas", ctypes.c_int32), ("threads", ctypes.c_int32)]
+
+
+_KERNELS = {0: "mma.sync m16n8k16", 1: "tcgen05 tile"}
+_REDUCE = {0: "none", 1: "cluster DSMEM", 2: "workspace+combine kernel", 3: "balanced split"}
+
+
+def plan_info(q, k_cache, block_tables, max_context_len: int, partition_tokens: int = 0,
+              out_dtype=None) -> dict:
+    """The plan a split-KV call with these arguments uses on the current device
+    (q [B, H, D] for one query token, [B, Q, H, D] for several)."""
+    if q.dim() == 4:
+        shape, q_len = _multi_shape(q, k_cache, block_tables, out_dtype or torch.float32)
+    else:
+        shape, q_len = make_shape(q, k_cache, block_tables, out_dtype or torch.float32), 1
+    d = _PlanDesc()
+    _check(_load().pa_plan_info(ctypes.byref(shape), q_len, int(max_context_len),
+                                int(partition_tokens), ctypes.byref(d)), "pa_plan_info")
+    return {"kernel": _KERNELS[d.kernel], "partitions": d.partitions,
+            "partition_tokens": d.partition_tokens, "reduce": _REDUCE[d.reduce],
+            "ctas": d.ctas, "threads": d.threads}
 
 
 def workspace_size_multi(q, k_cache, block_tables, out_dtype, max_context_len: int,

@@ -766,6 +766,39 @@ pa_status pa_decode_splitkv(void* out, const void* q, const void* k_cache, const
                            max_context_len, partition_tokens, workspace, workspace_bytes, stream);
 }
 
+pa_status pa_plan_info(const pa_shape* shape, int32_t q_len, int32_t max_context_len,
+                       int32_t partition_tokens, pa_plan_desc* desc) {
+    pa_status st = check_shape(shape);
+    if (st != PA_OK) return st;
+    if (!desc || q_len < 1 || max_context_len < 0 || !partition_arg_ok(shape, partition_tokens))
+        return PA_ERR_INVALID_ARG;
+    int sms = 1;
+    if (partition_tokens <= 0) {
+        st = device_state(&sms, nullptr);
+        if (st != PA_OK) return st;
+    }
+    const Plan plan = make_plan(shape, max_context_len, partition_tokens, sms, q_len);
+    const int64_t G = shape->num_heads / shape->num_kv_heads;
+    desc->kernel = plan.tile ? 1 : 0;
+    desc->partitions = plan.num_parts;
+    desc->partition_tokens =
+        plan.num_parts <= 1 ? pages_for(shape, max_context_len) * shape->block_size
+                            : plan.part_pages * shape->block_size;
+    desc->reduce = plan.balanced ? 3 : (plan.num_parts <= 1 ? 0 : (plan.cluster ? 1 : 2));
+    if (plan.tile) {
+        const int64_t tiles = ((int64_t)q_len * G + kTileRows - 1) / kTileRows;
+        desc->ctas = (int32_t)((int64_t)shape->batch * shape->num_kv_heads * tiles * plan.num_parts);
+        desc->threads = kTileThreads;
+    } else {
+        const Tune t = pick_tune(shape, plan.many_ctas);
+        desc->ctas = plan.balanced ? plan.num_ctas
+                                   : (int32_t)((int64_t)shape->batch * shape->num_kv_heads *
+                                               q_chunks_for(shape, q_len) * plan.num_parts);
+        desc->threads = 32 * t.nt * t.nh;
+    }
+    return PA_OK;
+}
+
 size_t pa_workspace_size_multi(const pa_shape* shape, int32_t q_len, int32_t max_context_len,
                                int32_t partition_tokens) {
     if (check_shape(shape) != PA_OK || max_context_len < 0 || q_len < 1) return 0;

@@ -210,3 +210,26 @@ def test_binding_refuses_cpu_tensors():
         pa.decode(torch.zeros(2, 32, 128), x, torch.zeros(8, 16, 8, 128, dtype=torch.float16),
                   torch.zeros(8, 16, 8, 128, dtype=torch.float16),
                   torch.zeros(2, 4, dtype=torch.int32), torch.zeros(2, dtype=torch.int32), 0.1)
+
+
+def test_plan_info_explicit_partitions(lib):
+    """pa_plan_info describes explicit splits without a device."""
+    d = pa._PlanDesc()
+    s = shape(batch=4, max_blocks_per_seq=8192)
+    assert lib.pa_plan_info(ctypes.byref(s), 1, 131072, 512, ctypes.byref(d)) == 0
+    assert (d.kernel, d.partitions, d.partition_tokens, d.reduce) == (0, 256, 512, 2)
+    assert d.ctas == 4 * 8 * 256
+    assert lib.pa_plan_info(ctypes.byref(s), 1, 4096, 512, ctypes.byref(d)) == 0
+    assert (d.partitions, d.reduce) == (8, 1)                 # <= 8 partitions: a cluster
+    assert lib.pa_plan_info(ctypes.byref(s), 1, 4096, 4096, ctypes.byref(d)) == 0
+    assert (d.partitions, d.reduce) == (1, 0)                 # one pass
+    # 6 query tokens x group 4 = 24 rows per kv head: the tcgen05 tile kernel
+    assert lib.pa_plan_info(ctypes.byref(s), 6, 4096, 1024, ctypes.byref(d)) == 0
+    assert (d.kernel, d.partitions, d.threads) == (1, 4, 384)
+    assert d.ctas == 4 * 8 * 1 * 4
+    # up to 16 rows on the warp-level kernel: query chunks of 16 / group tokens
+    assert lib.pa_plan_info(ctypes.byref(s), 4, 4096, 4096, ctypes.byref(d)) == 0
+    assert (d.kernel, d.ctas) == (0, 4 * 8)
+    assert lib.pa_plan_info(ctypes.byref(s), 0, 4096, 512, ctypes.byref(d)) == 1
+    assert lib.pa_plan_info(ctypes.byref(s), 1, 4096, 100, ctypes.byref(d)) == 1
+    assert lib.pa_plan_info(ctypes.byref(s), 1, 4096, 512, None) == 1
