@@ -396,7 +396,7 @@ int tile_max_clusters(const pa_shape* s, int cluster) {
 // each unit's pages into as many partitions (of at least 4 pages) as fit in
 // one wave of resident CTAs.  Partitions reduce inside a cluster through
 // distributed shared memory when every unit's cluster (at most 8 CTAs) fits
-// on the device at once and the cluster split keeps at least 3/4 of those
+// on the device at once and the cluster split keeps at least 2/3 of those
 // partitions (the workspace round trip and the combine launch cost more than
 // the rest); otherwise through the workspace.
 Plan tile_plan(const pa_shape* s, int32_t max_context_len, int32_t partition_tokens, int num_sms,
@@ -422,16 +422,27 @@ Plan tile_plan(const pa_shape* s, int32_t max_context_len, int32_t partition_tok
         // the parked partial must fit in the operand buffers
         const bool fits = tile_cluster_bytes(s->head_dim) <=
                           tile_smem_layout(s->head_dim, s->block_size).bar_off;
+        // (B=2, T=4096, 64 query tokens of 16 heads: 6 partitions in clusters
+        // 32.0 us against 9 through the workspace 35.6 us)
         const bool cluster =
-            fits && parts >= 2 && best_c >= 2 && (int64_t)best_c * 4 >= parts * 3;
+            fits && parts >= 2 && best_c >= 2 && (int64_t)best_c * 3 >= parts * 2;
         if (cluster) parts = std::min<int64_t>(best_c, parts);
         pp = (int)((pages + parts - 1) / parts);
         Plan p = plan_with(s, pages, pp, cluster);
         p.tile = true;
         return p;
     }
+    // an explicit partition count: a cluster when its partial fits in shared
+    // memory and the device holds every unit's cluster at once
     Plan p = plan_with(s, pages, pp, tile_cluster_bytes(s->head_dim) <=
                                          tile_smem_layout(s->head_dim, s->block_size).bar_off);
+    if (p.cluster) {
+        const int64_t rows = (int64_t)q_len * (s->num_heads / s->num_kv_heads);
+        const int64_t units =
+            (int64_t)s->batch * s->num_kv_heads * ((rows + kTileRows - 1) / kTileRows);
+        const int n = tile_max_clusters(s, p.num_parts);
+        if (n > 0 && units > n) p.cluster = false;
+    }
     p.tile = true;
     return p;
 }
