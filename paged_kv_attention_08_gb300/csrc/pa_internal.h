@@ -145,7 +145,7 @@ struct TileSmem {
     uint32_t k_off;        // [ns] K stages
     uint32_t v_off;        // [ns] V stages
     uint32_t bar_off;      // mbarriers: k_full[ns], k_empty[ns], v_full[ns], v_empty[ns],
-                           // s_full[3], p_full[3], pv_done[3], final
+                           // s_full[3], p_full[3], pv_done[3], final, q_ready
     uint32_t phys_off;     // [ns][BN / block_size] int32 physical block of each K stage's pages
     uint32_t xchg_off;     // softmax exchange: row maxima [2][2][128], normalisers [2][128] (fp32),
                            // then mbarriers xchg[2]
@@ -164,7 +164,7 @@ __host__ __device__ inline TileSmem tile_smem_layout(int D, int BS) {
     L.v_off = L.k_off + L.tile_bytes * L.ns;
     uint32_t o = L.v_off + L.tile_bytes * L.ns;
     L.bar_off = o;
-    o += 8u * (4 * L.ns + 3 * kTileSBufs + 1);
+    o += 8u * (4 * L.ns + 3 * kTileSBufs + 2);
     L.phys_off = o;
     o += 4u * L.ns * (BN / BS);
     L.xchg_off = pa_align_up(o, 16);

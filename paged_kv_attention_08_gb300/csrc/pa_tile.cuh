@@ -74,6 +74,7 @@ __global__ void __launch_bounds__(kTileThreads, 1)
     uint64_t* p_full = s_full + NB;
     uint64_t* pv_done = s_full + 2 * NB;
     uint64_t* final_bar = s_full + 3 * NB;
+    uint64_t* q_ready = final_bar + 1;  // the Q tile is in shared memory
     int32_t* phys_of = reinterpret_cast<int32_t*>(smem + L.phys_off);  // [NS][NPB] of K stages
     float* xmax = reinterpret_cast<float*>(smem + L.xchg_off);    // [2][2][128]
     float* xl = xmax + 2 * 2 * 128;                                   // [2][128]
@@ -206,6 +207,7 @@ __global__ void __launch_bounds__(kTileThreads, 1)
             mbar_init(smem_u32(pv_done + i), 1);
         }
         mbar_init(smem_u32(final_bar), 1);
+        mbar_init(smem_u32(q_ready), kTileThreads - 64);
         mbar_init(smem_u32(xchg), 256);
         mbar_init(smem_u32(xchg + 1), 256);
         *abort_flag = 0;
@@ -218,11 +220,19 @@ __global__ void __launch_bounds__(kTileThreads, 1)
         tc::tmem_relinquish();
     }
 
+    tc::fence_before_sync();
+    __syncthreads();  // barriers initialised, tensor memory allocated
+    tc::fence_after_sync();
+    const uint32_t tmem = *tmem_slot;
+
     // ---- Q tile: rows u = tile*128 + r, zero rows past the unit's rows;
-    // written with the 128-byte swizzle the MMA descriptors expect ----
-    {
+    // written with the 128-byte swizzle the MMA descriptors expect, by every
+    // thread outside the two copy warps (which already stream K and V); the
+    // MMA issuer waits for q_ready ----
+    if (warp != 0 && warp != 3) {
+        const int qt = (warp < 3 ? (warp - 1) * 32 : 64 + (warp - 4) * 32) + lane;  // 0..319
         uint8_t* qs = smem + L.q_off;
-        for (int i = tid; i < kTileRows * (D / 8); i += kTileThreads) {
+        for (int i = qt; i < kTileRows * (D / 8); i += kTileThreads - 64) {
             const int r = i / (D / 8), c = i % (D / 8);
             const int u = tile * kTileRows + r;
             uint4 v = make_uint4(0, 0, 0, 0);
@@ -232,11 +242,8 @@ __global__ void __launch_bounds__(kTileThreads, 1)
                                       (((c & 7) ^ (r & 7)) << 4)) = v;
         }
         fence_proxy_async_smem();
+        mbar_arrive(smem_u32(q_ready));
     }
-    tc::fence_before_sync();
-    __syncthreads();
-    tc::fence_after_sync();
-    const uint32_t tmem = *tmem_slot;
 
     auto fail = [&]() {
         if (lane == 0) record_error(p.err, PA_ERR_TIMEOUT);
@@ -317,7 +324,8 @@ __global__ void __launch_bounds__(kTileThreads, 1)
             const uint32_t q_base = smem_u32(smem + L.q_off);
             bool started = false;
             bool live_prev = false;  // block i-1 holds a page (its K stage may be refilled)
-            for (int i = 0; i <= nblk && !*abort_flag; ++i) {
+            const bool q_ok = wait(q_ready, 0);
+            for (int i = 0; i <= nblk && q_ok && !*abort_flag; ++i) {
                 bool live_cur = false;
                 if (i < nblk) {
                     // S_i = Q K_i^T into buffer i % NB, once P_{i-NB} there has been consumed
