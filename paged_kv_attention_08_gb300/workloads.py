@@ -82,6 +82,9 @@ SPECS = {s.name: s for s in [
     # eight (two CTAs per kv head), and a 64-token chunk with MQA-like groups
     Spec("tiny_q3", 3, 32, 8, 128, 16, torch.float16, "list:2,37,60", pool="fixed:12",
          max_blocks=4, q_len=3),
+    # 8 query tokens x 4 heads = 32 rows per kv head: the tcgen05 tile kernel
+    Spec("tiny_q8", 2, 32, 8, 128, 16, torch.bfloat16, "list:40,70", pool="fixed:9",
+         max_blocks=5, q_len=8),
     Spec("spec_b16_t2048_q4", 16, 32, 8, 128, 16, torch.float16, "fixed:2048", q_len=4),
     Spec("spec_b4_t8192_q8", 4, 32, 8, 128, 16, torch.bfloat16, "fixed:8192", q_len=8),
     Spec("chunk_b2_t4096_q64", 2, 16, 1, 256, 32, torch.bfloat16, "fixed:4096", pool="factor:1.1",

@@ -155,8 +155,9 @@ def test_multi_token_masking_and_qdtype_output(kernel):
     assert (np.abs(got - want_r) <= TOL + ulp).all()
 
 
-def test_tiny_q3_workload(kernel):
-    x = workloads.make("tiny_q3", seed=0, device=DEV)
+@pytest.mark.parametrize("name", ["tiny_q3", "tiny_q8"])
+def test_tiny_multi_workloads(name, kernel):
+    x = workloads.make(name, seed=0, device=DEV)
     want = oracle_of(x.to("cpu"))
     for pt in [0, 16, 64]:
         check(run(x, pt), want)
