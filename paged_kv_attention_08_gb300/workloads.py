@@ -89,6 +89,8 @@ SPECS = {s.name: s for s in [
     Spec("spec_b4_t8192_q8", 4, 32, 8, 128, 16, torch.bfloat16, "fixed:8192", q_len=8),
     Spec("chunk_b2_t4096_q64", 2, 16, 1, 256, 32, torch.bfloat16, "fixed:4096", pool="factor:1.1",
          kv_std=0.5, q_len=64),
+    # a 256-token chunk on the GQA shape: 1024 rows per kv head, eight 128-row tiles
+    Spec("prefill_b16_t2048_q256", 16, 32, 8, 128, 16, torch.float16, "fixed:2048", q_len=256),
 ]}
 
 # Named groups of workloads; a group is run as a sequence of decode calls.

@@ -163,7 +163,8 @@ def test_tiny_multi_workloads(name, kernel):
         check(run(x, pt), want)
 
 
-@pytest.mark.parametrize("name", ["spec_b16_t2048_q4", "spec_b4_t8192_q8", "chunk_b2_t4096_q64"])
+@pytest.mark.parametrize("name", ["spec_b16_t2048_q4", "spec_b4_t8192_q8", "chunk_b2_t4096_q64",
+                                  "prefill_b16_t2048_q256"])
 def test_multi_token_full_size_sampled(name, kernel):
     """Full-size multi-token workloads, automatic split; sampled (b, token, head)
     rows through the oracle's one-token decode of each token's causal prefix."""
