@@ -109,8 +109,8 @@ pa_status pa_decode(void* out, const void* q, const void* k_cache, const void* v
  * context `max_context_len` and partition size `partition_tokens` (tokens per
  * split, a multiple of block_size; 0 = choose automatically for the current
  * device; PA_PARTITION_BALANCED = the balanced split).  Returns 0 for invalid
- * arguments and when no workspace is needed (one partition, or at most 8
- * reduced inside a cluster).
+ * arguments and when no workspace is needed (one partition, or partitions
+ * reduced inside a thread-block cluster: see pa_decode_splitkv).
  */
 size_t pa_workspace_size(const pa_shape* shape, int32_t max_context_len,
                          int32_t partition_tokens);
@@ -177,14 +177,22 @@ pa_status pa_decode_splitkv(void* out, const void* q, const void* k_cache, const
  * pa_decode; a query token with no such token gets zeros.  With q_len = 1
  * this is pa_decode_splitkv.
  *
- * The MMA tile's 16 rows hold (query token, head) pairs, so one CTA serves
- * floor(16 / group) query tokens of a kv head; larger q_len launches
- * ceil(q_len / that) CTAs per (sequence, kv head, partition), each reading
- * the pages again (num_kv_heads * that count must be <= 65535, else
- * PA_ERR_UNSUPPORTED).  Partitions, workspace and max_context_len as in
+ * Rows.  A (sequence, kv head) has q_len * group rows, one per (query token,
+ * head) pair.  Up to 16 rows (except exactly 16 at head_dim 256) the
+ * warp-level kernel serves them: its MMA tile's 16 rows hold the pairs, one
+ * CTA per floor(16 / group) query tokens of a kv head and partition.  Beyond
+ * that the tcgen05 tile kernel serves them: 384-thread CTAs of 128 rows (one
+ * per ceil(q_len * group / 128) tiles of a kv head and partition) with
+ * Q K^T and P V on the tensor cores (operands staged by TMA in shared memory,
+ * S and O accumulated in tensor memory), the online softmax on two
+ * warpgroups, and its partitions sized from the device's resident clusters.
+ * Either way every CTA of a (sequence, kv head) reads that sequence's pages
+ * again, and num_kv_heads times the CTA count per kv head must be <= 65535
+ * (else PA_ERR_UNSUPPORTED).  Partitions, workspace and max_context_len as in
  * pa_decode_splitkv; PA_PARTITION_BALANCED is honoured only when
  * q_len * group <= 16 (otherwise the automatic choice is used).  The
  * workspace must hold pa_workspace_size_multi(shape, q_len, ...) bytes.
+ * pa_plan_info reports the kernel and split a call will use.
  */
 pa_status pa_decode_multi(void* out, const void* q, const void* k_cache, const void* v_cache,
                           const int32_t* block_tables, const int32_t* context_lens,

@@ -9,12 +9,20 @@ or a call is rejected, an exception is raised.
     decode(out, q, k_cache, v_cache, block_tables, context_lens, scale)
     decode_splitkv(out, q, k_cache, v_cache, block_tables, context_lens, scale,
                    max_context_len, partition_tokens=0, workspace=None)
+    decode_splitkv_noalloc(out, q, k_cache, v_cache, block_tables, context_lens, scale,
+                           max_context_len, partition_tokens=0)
     decode_multi(out, q, k_cache, v_cache, block_tables, context_lens, scale,
                  max_context_len, partition_tokens=0, workspace=None)
+    append_kv(k_cache, v_cache, k_new, v_new, block_tables, positions)
     workspace_size(q, k_cache, block_tables, out_dtype, max_context_len, partition_tokens=0)
+    workspace_size_multi(q, k_cache, block_tables, out_dtype, max_context_len, partition_tokens=0)
+    plan_info(q, k_cache, block_tables, max_context_len, partition_tokens=0)
     choose_partition_tokens(q, k_cache, block_tables, max_context_len, num_sms)
     resolve_blocks(out_phys, block_tables, context_lens, block_size, num_blocks)
+    selftest_wait_timeout(timeout_ns)
     device_error()
+
+Every launching call also takes ``stream=`` (default: the current torch stream).
 """
 from __future__ import annotations
 
@@ -26,7 +34,8 @@ import torch
 
 __all__ = ["PaError", "decode", "decode_splitkv", "decode_splitkv_noalloc", "decode_multi",
            "append_kv", "workspace_size", "workspace_size_multi", "plan_info", "choose_partition_tokens",
-           "resolve_blocks", "device_error", "library_path", "F16", "BF16", "F32"]
+           "resolve_blocks", "selftest_wait_timeout", "device_error", "library_path", "F16",
+           "BF16", "F32", "PARTITION_BALANCED"]
 
 F16, BF16, F32 = 0, 1, 2
 PARTITION_BALANCED = -1   # partition_tokens value requesting the balanced split
