@@ -110,7 +110,11 @@ pa_status pa_decode(void* out, const void* q, const void* k_cache, const void* v
  * split, a multiple of block_size; 0 = choose automatically for the current
  * device; PA_PARTITION_BALANCED = the balanced split).  Returns 0 for invalid
  * arguments and when no workspace is needed (one partition, or partitions
- * reduced inside a thread-block cluster: see pa_decode_splitkv).
+ * reduced inside a thread-block cluster: see pa_decode_splitkv).  The answer
+ * is for the current device, as the call plans with its SM count (which picks
+ * the CTA shape and with it whether a cluster split fits); an explicit
+ * partition size may be queried without a device, and is then sized as for
+ * one SM.
  */
 size_t pa_workspace_size(const pa_shape* shape, int32_t max_context_len,
                          int32_t partition_tokens);
@@ -213,10 +217,11 @@ typedef struct pa_plan_desc {
 } pa_plan_desc;
 
 /* Describes, without launching anything, the plan a split-KV call with these
- * arguments would use (no counterpart in the pages: a diagnostic of this
- * library's own choices).  Needs the current device for automatic choices
- * (partition_tokens = 0), as the calls themselves do.  Returns
- * PA_ERR_INVALID_ARG / PA_ERR_UNSUPPORTED like the calls, else PA_OK. */
+ * arguments would use on the current device (no counterpart in the pages: a
+ * diagnostic of this library's own choices).  Automatic and balanced choices
+ * need the device, as the calls do; an explicit partition size may be
+ * queried without one (planned as for one SM).  Returns PA_ERR_INVALID_ARG /
+ * PA_ERR_UNSUPPORTED like the calls, else PA_OK. */
 pa_status pa_plan_info(const pa_shape* shape, int32_t q_len, int32_t max_context_len,
                        int32_t partition_tokens, pa_plan_desc* desc);
 

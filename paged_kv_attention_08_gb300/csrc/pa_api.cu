@@ -82,10 +82,13 @@ pa_status check_ptrs(const void* out, const void* q, const void* k, const void* 
     return PA_OK;
 }
 
-// SM count and error-word address of the current device (cached).
-pa_status device_state(int* sms, int32_t** err) {
+// SM count of the current device (cached).
+pa_status device_sms(int* sms, int* device) {
     int dev = 0;
-    if (cudaGetDevice(&dev) != cudaSuccess) return PA_ERR_CUDA;
+    if (cudaGetDevice(&dev) != cudaSuccess) {
+        (void)cudaGetLastError();
+        return PA_ERR_CUDA;
+    }
     if (dev < 0 || dev >= kMaxDevices) return PA_ERR_UNSUPPORTED;
     int n = g_sm_count[dev].load(std::memory_order_relaxed);
     if (n == 0) {
@@ -93,6 +96,29 @@ pa_status device_state(int* sms, int32_t** err) {
             return PA_ERR_CUDA;
         g_sm_count[dev].store(n, std::memory_order_relaxed);
     }
+    *sms = n;
+    if (device) *device = dev;
+    return PA_OK;
+}
+
+// SM count for the size and plan queries: the current device's, as the calls
+// themselves plan with it (it picks the CTA shape, and with it whether a
+// cluster split fits on the device, explicit partition sizes included).  An
+// explicit partition size may also be queried without a device: the plan is
+// then made for one SM (the split itself does not depend on the count).
+pa_status query_sms(int32_t partition_tokens, int* sms) {
+    *sms = 1;
+    const pa_status st = device_sms(sms, nullptr);
+    if (st == PA_OK) return PA_OK;
+    *sms = 1;
+    return partition_tokens > 0 ? PA_OK : st;
+}
+
+// SM count and error-word address of the current device (cached).
+pa_status device_state(int* sms, int32_t** err) {
+    int dev = 0, n = 0;
+    const pa_status st = device_sms(&n, &dev);
+    if (st != PA_OK) return st;
     int32_t* e = g_err_word[dev].load(std::memory_order_acquire);
     if (!e) {
         void* ptr = nullptr;
@@ -784,10 +810,8 @@ pa_status pa_plan_info(const pa_shape* shape, int32_t q_len, int32_t max_context
     if (!desc || q_len < 1 || max_context_len < 0 || !partition_arg_ok(shape, partition_tokens))
         return PA_ERR_INVALID_ARG;
     int sms = 1;
-    if (partition_tokens <= 0) {
-        st = device_state(&sms, nullptr);
-        if (st != PA_OK) return st;
-    }
+    st = query_sms(partition_tokens, &sms);
+    if (st != PA_OK) return st;
     const Plan plan = make_plan(shape, max_context_len, partition_tokens, sms, q_len);
     const int64_t G = shape->num_heads / shape->num_kv_heads;
     desc->kernel = plan.tile ? 1 : 0;
@@ -815,7 +839,7 @@ size_t pa_workspace_size_multi(const pa_shape* shape, int32_t q_len, int32_t max
     if (check_shape(shape) != PA_OK || max_context_len < 0 || q_len < 1) return 0;
     if (!partition_arg_ok(shape, partition_tokens)) return 0;
     int sms = 1;
-    if (partition_tokens <= 0 && device_state(&sms, nullptr) != PA_OK) return 0;
+    if (query_sms(partition_tokens, &sms) != PA_OK) return 0;
     const Plan plan = make_plan(shape, max_context_len, partition_tokens, sms, q_len);
     return workspace_bytes_for(shape, plan, nullptr, q_len);
 }

@@ -411,3 +411,37 @@ def test_sixteen_unit_automatic_plan(B, T, Hkv):
     want = oracle.decode(x.q, x.k_cache, x.v_cache, x.block_tables, x.context_lens, x.scale)
     xd = x.to(DEV)
     assert_close_fp32(run(xd, "split", partition_tokens=0), want)
+
+
+# units (sequences x kv heads) around the number of clusters of 8 / 4 / 2 CTAs
+# the device holds at once, and around 152 CTAs (the change of CTA shape)
+EXACT_WS = [(8, u) for u in (8, 15, 16, 19, 20)] + [(4, u) for u in (32, 36, 37, 38, 40)] + \
+           [(2, u) for u in (64, 76, 77, 80)]
+
+
+@pytest.mark.parametrize("parts,units", EXACT_WS, ids=lambda v: str(v))
+@pytest.mark.parametrize("kernel", ["auto", "tile"])
+def test_workspace_size_is_exact_for_explicit_splits(parts, units, kernel, monkeypatch):
+    """An explicit partition count: a workspace of exactly the reported size
+    (none when it is 0) serves the call, whose reduction is the one plan_info
+    reports; exact against the oracle."""
+    if kernel == "tile":
+        monkeypatch.setenv("PA_MULTI_KERNEL", "tile")
+    else:
+        monkeypatch.delenv("PA_MULTI_KERNEL", raising=False)
+    T = parts * 4 * 16
+    x = random_case(31, B=units, H=4, Hkv=1, D=128, bs=16, lens=[T] * units,
+                    dtype=torch.float16, spare=0, mb_extra=0)
+    want = oracle.decode(x.q, x.k_cache, x.v_cache, x.block_tables, x.context_lens, x.scale)
+    xd = x.to(DEV)
+    pt = 4 * 16
+    need = pa.workspace_size(xd.q, xd.k_cache, xd.block_tables, torch.float32, T, pt)
+    info = pa.plan_info(xd.q, xd.k_cache, xd.block_tables, T, pt)
+    assert info["partitions"] == parts
+    assert (need > 0) == (info["reduce"] == "workspace+combine kernel"), (need, info)
+    ws = torch.full((need,), 0xFF, dtype=torch.uint8, device=DEV)
+    out = torch.full(xd.q.shape, float("nan"), dtype=torch.float32, device=DEV)
+    pa.decode_splitkv(out, xd.q, xd.k_cache, xd.v_cache, xd.block_tables, xd.context_lens,
+                      xd.scale, T, pt, workspace=ws)
+    torch.cuda.synchronize()
+    assert_close_fp32(out, want)
