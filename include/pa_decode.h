@@ -123,8 +123,11 @@ size_t pa_workspace_size(const pa_shape* shape, int32_t max_context_len,
  * Partition size (tokens) the automatic choice picks for `num_sms`
  * multiprocessors: a multiple of block_size (a result >= max_context_len
  * means "no split"), or PA_PARTITION_BALANCED when it picks the balanced
- * split; 0 for invalid arguments.  Host-only, no device access (a pure
- * function, exported so that its choice can be checked without a GPU).
+ * split; 0 for invalid arguments.  A function of its arguments, exported so
+ * that the choice can be checked without a GPU, with one exception: which
+ * cluster sizes fit on the device at once is asked of the current device
+ * when there is one (cached per device); without a device, clusters of up to
+ * 8 CTAs are assumed to fit.  Launches nothing.
  * The rules are this library's own, fitted to GB300 timings: the
  * flash-decoding-bench design notes only say that the chunk size is picked
  * from the KV length.
