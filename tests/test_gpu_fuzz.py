@@ -10,8 +10,10 @@ batch with empty, one-token and block-aligned sequences, spare table columns
 and pool blocks, sometimes a masked table entry (-1 or an id past the pool),
 the entry point (single pass, split-KV, multi-token) with a partition mode
 (automatic, one pass, an explicit size, balanced), and the kernel choice
-(library's own, or either multi-token kernel forced).  Output and workspace
-start as NaN, so a row or partial that nothing wrote shows.
+(library's own, or either multi-token kernel forced), and sometimes a
+max_context_len above every length, up to past the table's reach.  Output
+and workspace start as NaN, so a row or partial that nothing wrote shows; the
+workspace has exactly the size the library reports.
 
 Bar: max |gpu - oracle| <= 2e-3 on fp32 output; q-dtype output within 2e-3
 plus one ulp of the oracle rounded to that dtype; no device error.
@@ -63,6 +65,9 @@ def draw(seed):
     c["scale_mul"] = float(g.uniform(0.5, 2.0))
     c["kernel"] = ["auto", "mma", "tile"][int(g.choice(3, p=[0.6, 0.2, 0.2]))]
     c["mask_seed"] = int(g.integers(1 << 30))
+    # sometimes a max_context_len above every length (a serving loop passing
+    # the model's limit), up to past the table's reach
+    c["ctx_extra"] = int(g.integers(1, 3 * 32 * 12)) if g.random() < 0.2 else 0
     return c
 
 
@@ -90,7 +95,7 @@ def make_inputs(seed, c):
     kc = torch.randn(pool, bs, Hkv, D, generator=gen).to(dt)
     vc = torch.randn(pool, bs, Hkv, D, generator=gen).to(dt)
     lens = torch.tensor(c["lens"], dtype=torch.int32)
-    return q, kc, vc, bt, lens, c["scale_mul"] / math.sqrt(D), max(c["lens"])
+    return q, kc, vc, bt, lens, c["scale_mul"] / math.sqrt(D), max(c["lens"]) + c["ctx_extra"]
 
 
 def partition_tokens(c, max_ctx):
@@ -105,7 +110,8 @@ def partition_tokens(c, max_ctx):
 
 
 def nan_workspace(nbytes):
-    return torch.full((max(nbytes, 16) // 4 + 1,), float("nan"), dtype=torch.float32, device=DEV)
+    """Exactly the reported size; 0xFF bytes read as NaN in every fp32 partial."""
+    return torch.full((nbytes,), 0xFF, dtype=torch.uint8, device=DEV)
 
 
 def check(got, want, out_q, dtype):
