@@ -529,8 +529,55 @@ size_t workspace_bytes_for(const pa_shape* s, const Plan& plan, size_t* ml_offse
     return off + rows * 2 * sizeof(float);
 }
 
+// The last few tensor-map pairs this host thread encoded, by everything a map
+// encodes (addresses and dimensions; no contents), so a hit is exact.  A call
+// on the same cache buffers as a recent one skips the two driver encodes.
+struct MapCacheEntry {
+    const void* k;
+    const void* v;
+    int64_t num_blocks;
+    int32_t head_dim, num_kv_heads, block_size, kv_dtype;
+    bool valid;
+    CUtensorMap mk, mv;
+};
+constexpr int kMapCacheEntries = 4;
+thread_local MapCacheEntry tl_maps[kMapCacheEntries];
+thread_local int tl_maps_next = 0;
+
+pa_status encode_maps_uncached(const pa_shape* s, const void* k, const void* v, CUtensorMap* mk,
+                               CUtensorMap* mv);
+
 pa_status encode_maps(const pa_shape* s, const void* k, const void* v, CUtensorMap* mk,
                       CUtensorMap* mv) {
+    for (int i = 0; i < kMapCacheEntries; ++i) {
+        const MapCacheEntry& c = tl_maps[i];
+        if (c.valid && c.k == k && c.v == v && c.num_blocks == s->num_blocks &&
+            c.head_dim == s->head_dim && c.num_kv_heads == s->num_kv_heads &&
+            c.block_size == s->block_size && c.kv_dtype == s->kv_dtype) {
+            *mk = c.mk;
+            *mv = c.mv;
+            return PA_OK;
+        }
+    }
+    const pa_status st = encode_maps_uncached(s, k, v, mk, mv);
+    if (st != PA_OK) return st;
+    MapCacheEntry& c = tl_maps[tl_maps_next];
+    tl_maps_next = (tl_maps_next + 1) % kMapCacheEntries;
+    c.k = k;
+    c.v = v;
+    c.num_blocks = s->num_blocks;
+    c.head_dim = s->head_dim;
+    c.num_kv_heads = s->num_kv_heads;
+    c.block_size = s->block_size;
+    c.kv_dtype = s->kv_dtype;
+    c.mk = *mk;
+    c.mv = *mv;
+    c.valid = true;
+    return PA_OK;
+}
+
+pa_status encode_maps_uncached(const pa_shape* s, const void* k, const void* v, CUtensorMap* mk,
+                               CUtensorMap* mv) {
     std::call_once(g_encode_once, [] {
         void* fn = nullptr;
         cudaDriverEntryPointQueryResult q;

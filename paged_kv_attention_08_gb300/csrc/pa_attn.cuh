@@ -656,14 +656,21 @@ __global__ void __launch_bounds__(256, 1)
     }
 }
 
+// Per-instantiation flags of the attributes set once per device.
+template <int D, int BS, typename KV, bool MULTI>
+struct AttnAttrs {
+    static inline AttrFlags smem;
+    static inline AttrFlags nonportable;
+};
+
 template <int D, int BS, typename KV, bool MULTI>
 cudaError_t launch_attn_inst(const AttnLaunch& L, cudaStream_t stream) {
     auto kern = attn_kernel<D, BS, KV, MULTI>;
-    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                         (int)L.smem_bytes);
+    using Attrs = AttnAttrs<D, BS, KV, MULTI>;
+    cudaError_t e = raise_smem_limit_once(kern, Attrs::smem);
     if (e != cudaSuccess) return e;
     if (L.cluster > kMaxClusterParts) {
-        e = cudaFuncSetAttribute(kern, cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
+        e = allow_nonportable_clusters_once(kern, Attrs::nonportable);
         if (e != cudaSuccess) return e;
     }
     cudaLaunchConfig_t cfg = {};
@@ -695,12 +702,16 @@ cudaError_t launch_attn_inst(const AttnLaunch& L, cudaStream_t stream) {
 template <int D, int BS, typename KV>
 int attn_max_clusters_inst(int cluster, int threads, uint32_t smem_bytes) {
     auto kern = attn_kernel<D, BS, KV, false>;
-    if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem_bytes) !=
-        cudaSuccess)
+    using Attrs = AttnAttrs<D, BS, KV, false>;
+    if (raise_smem_limit_once(kern, Attrs::smem) != cudaSuccess) {
+        (void)cudaGetLastError();
         return 0;
+    }
     if (cluster > kMaxClusterParts &&
-        cudaFuncSetAttribute(kern, cudaFuncAttributeNonPortableClusterSizeAllowed, 1) != cudaSuccess)
+        allow_nonportable_clusters_once(kern, Attrs::nonportable) != cudaSuccess) {
+        (void)cudaGetLastError();
         return 0;
+    }
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3((unsigned)cluster, 1, 1);
     cfg.blockDim = dim3((unsigned)threads);

@@ -7,6 +7,8 @@
 #include <cuda_runtime.h>
 #include <stdint.h>
 
+#include <atomic>
+
 #include "../../include/pa_decode.h"
 
 namespace pa {
@@ -186,6 +188,49 @@ __host__ __device__ constexpr uint32_t tile_cluster_bytes(int D) {
 // buffers of BN fp32 columns (P, as 16-bit high and low parts, overwrites S).
 __host__ __device__ constexpr uint32_t tile_tmem_cols(int D) {
     return (uint32_t)D + kTileSBufs * tile_block_tokens(D) <= 256u ? 256u : 512u;
+}
+
+// ---------------------------------------------------------------------------
+// Host: kernel attributes set once per device.  A kernel's dynamic
+// shared-memory limit only caps what a launch may request (occupancy follows
+// the bytes a launch actually asks for), so it is raised once per device to
+// all the device offers a block -- by the launch and the occupancy paths
+// alike, so that neither ever lowers it under the other -- and the
+// non-portable cluster permission is granted once where a launch needs it;
+// later calls skip the runtime calls.  `done` is the kernel's own flag array.
+// ---------------------------------------------------------------------------
+constexpr int kMaxAttrDevices = 64;
+using AttrFlags = std::atomic<int>[kMaxAttrDevices];
+
+template <typename Kern>
+cudaError_t raise_smem_limit_once(Kern kern, AttrFlags& done) {
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return e;
+    if (dev < 0 || dev >= kMaxAttrDevices) return cudaErrorInvalidDevice;
+    if (done[dev].load(std::memory_order_acquire)) return cudaSuccess;
+    int optin = 0;
+    e = cudaDeviceGetAttribute(&optin, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev);
+    if (e != cudaSuccess) return e;
+    cudaFuncAttributes fa;
+    e = cudaFuncGetAttributes(&fa, kern);
+    if (e != cudaSuccess) return e;
+    e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             optin - (int)fa.sharedSizeBytes);
+    if (e == cudaSuccess) done[dev].store(1, std::memory_order_release);
+    return e;
+}
+
+template <typename Kern>
+cudaError_t allow_nonportable_clusters_once(Kern kern, AttrFlags& done) {
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return e;
+    if (dev < 0 || dev >= kMaxAttrDevices) return cudaErrorInvalidDevice;
+    if (done[dev].load(std::memory_order_acquire)) return cudaSuccess;
+    e = cudaFuncSetAttribute(kern, cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
+    if (e == cudaSuccess) done[dev].store(1, std::memory_order_release);
+    return e;
 }
 
 struct AttnLaunch {

@@ -612,11 +612,16 @@ __global__ void __launch_bounds__(kTileThreads, 1)
     if (p.cluster_reduce) cluster_merge();
 }
 
+// Per-instantiation flag of the shared-memory limit set once per device.
+template <int D, int BS, typename KV>
+struct TileAttrs {
+    static inline AttrFlags smem;
+};
+
 template <int D, int BS, typename KV>
 cudaError_t launch_tile_inst(const AttnLaunch& L, cudaStream_t stream) {
     auto kern = tile_kernel<D, BS, KV>;
-    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                         (int)L.smem_bytes);
+    cudaError_t e = raise_smem_limit_once(kern, TileAttrs<D, BS, KV>::smem);
     if (e != cudaSuccess) return e;
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = L.grid;
@@ -647,9 +652,10 @@ cudaError_t launch_tile_inst(const AttnLaunch& L, cudaStream_t stream) {
 template <int D, int BS, typename KV>
 int tile_max_clusters_inst(int cluster, uint32_t smem_bytes) {
     auto kern = tile_kernel<D, BS, KV>;
-    if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem_bytes) !=
-        cudaSuccess)
+    if (raise_smem_limit_once(kern, TileAttrs<D, BS, KV>::smem) != cudaSuccess) {
+        (void)cudaGetLastError();
         return 0;
+    }
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3((unsigned)cluster, 1, 1);
     cfg.blockDim = dim3(kTileThreads);
