@@ -240,22 +240,31 @@ def ncu_traffic(kernel: str, workload: str):
 # ---------------------------------------------------------------------------
 # CPU oracle arm
 # ---------------------------------------------------------------------------
-def oracle_step(sets_host):
+def oracle_step(sets_host, threads=1):
+    """One whole step through the oracle; with threads > 1 its independent
+    (sequence, head) rows -- sequences for several query tokens -- run on that
+    many host threads.  Returns the most threads a call used."""
     import oracle
+    used = 1
     for x in sets_host:
-        fn = oracle.decode_multi if x.q.dim() == 4 else oracle.decode
-        fn(x.q, x.k_cache, x.v_cache, x.block_tables, x.context_lens, x.scale)
+        args = (x.q, x.k_cache, x.v_cache, x.block_tables, x.context_lens, x.scale)
+        if threads <= 1:
+            (oracle.decode_multi if x.q.dim() == 4 else oracle.decode)(*args)
+        else:
+            fn = oracle.decode_multi_mt if x.q.dim() == 4 else oracle.decode_mt
+            used = max(used, fn(*args, threads=threads)[1])
+    return used
 
 
-def time_oracle(sets_host, min_s=10.0, max_steps=None):
-    """Whole oracle steps on one host thread until ``min_s`` elapse; seconds/step."""
-    n, t0 = 0, time.perf_counter()
+def time_oracle(sets_host, min_s=10.0, max_steps=None, threads=1):
+    """Whole oracle steps until ``min_s`` elapse; (seconds/step, steps, threads used)."""
+    n, used, t0 = 0, 1, time.perf_counter()
     while True:
-        oracle_step(sets_host)
+        used = max(used, oracle_step(sets_host, threads))
         n += 1
         el = time.perf_counter() - t0
         if el >= min_s or (max_steps and n >= max_steps):
-            return el / n, n
+            return el / n, n, used
 
 
 # ---------------------------------------------------------------------------
@@ -287,21 +296,24 @@ def run_reference(args):
     names = workloads.GROUPS[args.workload]
     sets = [workloads.make(n, seed=0, device="cpu") for n in names]
     step_bytes = sum(algorithmic_bytes(x) for x in sets)
+    threads = oracle.host_threads()
+    used = 1
     for _ in range(args.warmup):
-        oracle_step(sets)
+        used = max(used, oracle_step(sets, threads))
     t0 = time.perf_counter()
     for _ in range(args.steps):
-        oracle_step(sets)
+        used = max(used, oracle_step(sets, threads))
     sec = (time.perf_counter() - t0) / max(1, args.steps)
     gbs = step_bytes / sec / 1e9
-    sample = f"{args.steps} whole steps of the {args.workload} group (every sequence, every head)"
+    sample = (f"{args.steps} whole steps of the {args.workload} group (every sequence, every "
+              f"head), fp64 oracle on {used} host threads of {oracle.cpu_model()}")
     line = {"impl": "reference", "metric": METRIC, "value": gbs, "unit": "GB/s", "n_gpus": 1,
             "steps": args.steps, "warmup": args.warmup, "ms_per_step": sec * 1e3,
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
             "data": "synthetic", "config": {"workload": describe(args.workload),
-                                            "kind": "fp64 CPU oracle, single thread"},
-            "cpu_baseline": {"value": gbs, "unit": "GB/s", "cores": 1, "kind": "oracle",
-                             "sample": sample},
+                                            "kind": f"fp64 CPU oracle, {used} host threads"},
+            "cpu_baseline": {"value": gbs, "unit": "GB/s", "cores": used, "kind": "oracle",
+                             "sample": sample, "cpu_model": oracle.cpu_model()},
             "e2e": {"value": gbs, "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
     print(json.dumps(line), flush=True)
     return 0
@@ -588,11 +600,16 @@ def main(argv=None):
 
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        import oracle
         host = [x.to("cpu") for x in set0]
-        sec, n = time_oracle(host, min_s=10.0)
-        cpu = {"value": step_bytes / sec / 1e9, "unit": "GB/s", "cores": 1, "kind": "oracle",
+        sec, n, used = time_oracle(host, min_s=10.0, threads=oracle.host_threads())
+        sec1, n1, _ = time_oracle(host, min_s=5.0, threads=1)
+        cpu = {"value": step_bytes / sec / 1e9, "unit": "GB/s", "cores": used, "kind": "oracle",
                "sample": f"{n} whole steps of the {args.workload} group (input set 0), "
-                         f"fp64 oracle on one host thread, {sec * 1e3:.1f} ms/step"}
+                         f"fp64 oracle on {used} host threads, {sec * 1e3:.1f} ms/step",
+               "cpu_model": oracle.cpu_model(),
+               "single_thread": {"value": step_bytes / sec1 / 1e9, "unit": "GB/s",
+                                 "ms_per_step": sec1 * 1e3, "steps": n1}}
 
     if rank == 0:
         line = {

@@ -152,6 +152,53 @@ def decode_rows(q, k_cache, v_cache, block_tables, context_lens, scale: float, r
     return out
 
 
+def host_threads() -> int:
+    """Host cores this process may run on (its CPU affinity)."""
+    try:
+        return max(1, len(os.sched_getaffinity(0)))
+    except (AttributeError, OSError):
+        return max(1, os.cpu_count() or 1)
+
+
+def decode_mt(q, k_cache, v_cache, block_tables, context_lens, scale: float,
+              threads: int | None = None) -> tuple[np.ndarray, int]:
+    """``decode``'s result computed on several host threads: the (sequence,
+    head) rows are cut into one contiguous chunk per thread and each chunk goes
+    through ``pao_decode_rows`` -- the same per-row arithmetic as ``decode``,
+    run side by side (the foreign calls release the interpreter lock).  For
+    timing the oracle on all the host's cores.  Returns (out, threads used)."""
+    (B, H, Hkv, D, bs, mb, NB), bt, lens = _common(q, k_cache, v_cache, block_tables, context_lens)
+    qa, ka, va = _u16(q), _u16(k_cache), _u16(v_cache)
+    n = B * H
+    threads = max(1, min(threads or host_threads(), n)) if n else 1
+    rows = np.stack(np.meshgrid(np.arange(B, dtype=np.int32), np.arange(H, dtype=np.int32),
+                                indexing="ij"), axis=-1).reshape(-1, 2).copy()
+    out = np.zeros((n, D), dtype=np.float64)
+    bounds = [n * i // threads for i in range(threads + 1)]
+    lib = _load()
+    dt, sc = _dtype_code(q), float(np.float32(scale))
+    rcs = [0] * threads
+
+    def run(i):
+        lo, hi = bounds[i], bounds[i + 1]
+        if hi > lo:
+            r = np.ascontiguousarray(rows[lo:hi])
+            o = np.zeros((hi - lo, D), dtype=np.float64)
+            rcs[i] = lib.pao_decode_rows(_ptr(o), _ptr(qa), _ptr(ka), _ptr(va), _ptr(bt),
+                                         _ptr(lens), B, H, Hkv, D, bs, mb, NB, dt, sc, _ptr(r),
+                                         hi - lo)
+            out[lo:hi] = o
+
+    workers = [threading.Thread(target=run, args=(i,)) for i in range(threads)]
+    for w in workers:
+        w.start()
+    for w in workers:
+        w.join()
+    if any(rcs):
+        raise RuntimeError("oracle decode_rows rejected its arguments")
+    return out.reshape(B, H, D), threads
+
+
 def resolve_blocks(block_tables, context_lens, block_size: int, num_blocks: int) -> np.ndarray:
     """[batch, max_blocks] int32: the physical block read for each logical page,
     -1 where the page holds no attended token."""
@@ -202,3 +249,63 @@ def decode_multi(q, k_cache, v_cache, block_tables, context_lens, scale: float) 
     if rc != 0:
         raise RuntimeError("oracle decode_multi rejected its arguments")
     return out
+
+
+def decode_multi_mt(q, k_cache, v_cache, block_tables, context_lens, scale: float,
+                    threads: int | None = None) -> tuple[np.ndarray, int]:
+    """``decode_multi``'s result computed on several host threads: the batch
+    is cut into one contiguous run of sequences per thread, each run going
+    through ``pao_decode_multi`` on its slice of q, the table and the lengths
+    (the cache is shared, read only).  For timing the oracle on all the
+    host's cores.  Returns (out, threads used)."""
+    if q.dim() != 4:
+        raise ValueError("q must be [batch, q_len, num_heads, head_dim]")
+    B, Q, H, D = q.shape
+    (_, _, Hkv, _, bs, mb, NB), bt, lens = _common(q[:, 0], k_cache, v_cache, block_tables,
+                                                  context_lens)
+    qa, ka, va = _u16(q), _u16(k_cache), _u16(v_cache)
+    out = np.zeros((B, Q, H, D), dtype=np.float64)
+    threads = max(1, min(threads or host_threads(), B)) if B else 1
+    bounds = [B * i // threads for i in range(threads + 1)]
+    lib = _load()
+    dt, sc = _dtype_code(q), float(np.float32(scale))
+    rcs = [0] * threads
+
+    def run(i):
+        lo, hi = bounds[i], bounds[i + 1]
+        if hi > lo:
+            qs = np.ascontiguousarray(qa[lo:hi])
+            bts = np.ascontiguousarray(bt[lo:hi])
+            ls = np.ascontiguousarray(lens[lo:hi])
+            o = np.zeros((hi - lo, Q, H, D), dtype=np.float64)
+            rcs[i] = lib.pao_decode_multi(_ptr(o), _ptr(qs), _ptr(ka), _ptr(va), _ptr(bts),
+                                          _ptr(ls), hi - lo, Q, H, Hkv, D, bs, mb, NB, dt, sc)
+            out[lo:hi] = o
+
+    workers = [threading.Thread(target=run, args=(i,)) for i in range(threads)]
+    for w in workers:
+        w.start()
+    for w in workers:
+        w.join()
+    if any(rcs):
+        raise RuntimeError("oracle decode_multi rejected its arguments")
+    return out, threads
+
+
+def cpu_model() -> str:
+    """The host CPU's name as /proc/cpuinfo gives it (model name, or the Arm
+    implementer and part numbers), else the machine type."""
+    import platform
+    try:
+        info = open("/proc/cpuinfo").read().splitlines()
+    except OSError:
+        info = []
+    for ln in info:
+        if ln.lower().startswith("model name"):
+            return ln.split(":", 1)[1].strip()
+    impl = next((ln.split(":", 1)[1].strip() for ln in info if ln.startswith("CPU implementer")), None)
+    part = next((ln.split(":", 1)[1].strip() for ln in info if ln.startswith("CPU part")), None)
+    if impl and part:
+        return f"{platform.machine()} (CPU implementer {impl}, part {part})"
+    return platform.machine() or "unknown"
+

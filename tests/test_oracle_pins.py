@@ -356,3 +356,27 @@ def test_multi_token_matches_causal_bruteforce():
                 s = np.where(mask, s, -np.inf)
                 np.testing.assert_allclose(got[b, i, h], scipy.special.softmax(s) @ Vb[:, h // (H // Hkv)],
                                            rtol=0, atol=1e-12)
+
+
+@pytest.mark.parametrize("threads", [1, 3, 7])
+def test_threaded_driver_equals_decode(threads):
+    """The multi-core baseline driver runs the same per-row arithmetic: its
+    output is bit-identical to the single-threaded decode, whatever the split."""
+    q, kc, vc, bt, lens, scale = small_case(41, B=3, H=8, Hkv=2, D=64, bs=16, lens=[0, 45, 130])
+    want = oracle.decode(q, kc, vc, bt, lens, scale)
+    got, used = oracle.decode_mt(q, kc, vc, bt, lens, scale, threads=threads)
+    assert used == threads
+    assert np.array_equal(got, want)
+
+
+@pytest.mark.parametrize("threads", [1, 2, 5])
+def test_threaded_multi_driver_equals_decode_multi(threads):
+    """Sub-batches through the multi-token oracle give its whole-batch result."""
+    g = torch.Generator().manual_seed(43)
+    q1, kc, vc, bt, lens, scale = small_case(43, B=5, H=8, Hkv=2, D=64, bs=16,
+                                             lens=[3, 0, 45, 130, 17])
+    q = torch.randn(5, 4, 8, 64, generator=g).to(torch.float16)
+    want = oracle.decode_multi(q, kc, vc, bt, lens, scale)
+    got, used = oracle.decode_multi_mt(q, kc, vc, bt, lens, scale, threads=threads)
+    assert used == threads
+    assert np.array_equal(got, want)
