@@ -10,8 +10,9 @@ batch with empty, one-token and block-aligned sequences, spare table columns
 and pool blocks, sometimes a masked table entry (-1 or an id past the pool),
 the entry point (single pass, split-KV, multi-token) with a partition mode
 (automatic, one pass, an explicit size, balanced), and the kernel choice
-(library's own, or either multi-token kernel forced), and sometimes a
-max_context_len above every length, up to past the table's reach.  Output
+(library's own, or either multi-token kernel forced), sometimes a
+max_context_len above every length, up to past the table's reach, and for
+some split-KV cases the allocation-free entry point.  Output
 and workspace start as NaN, so a row or partial that nothing wrote shows; the
 workspace has exactly the size the library reports.
 
@@ -68,6 +69,8 @@ def draw(seed):
     # sometimes a max_context_len above every length (a serving loop passing
     # the model's limit), up to past the table's reach
     c["ctx_extra"] = int(g.integers(1, 3 * 32 * 12)) if g.random() < 0.2 else 0
+    # split-KV calls: sometimes through the allocation-free entry point
+    c["noalloc"] = bool(g.random() < 0.3)
     return c
 
 
@@ -151,8 +154,11 @@ def test_random_case_vs_oracle(seed, monkeypatch):
     else:
         q1 = qd[:, 0].contiguous()
         out = torch.full(q1.shape, float("nan"), dtype=out_dtype, device=DEV)
+        need = pa.workspace_size(q1, kd, btd, out_dtype, max_ctx, pt)
         if c["entry"] == "single":
             pa.decode(out, q1, kd, vd, btd, ld, scale)
+        elif c["noalloc"] and need <= 8 << 20:
+            pa.decode_splitkv_noalloc(out, q1, kd, vd, btd, ld, scale, max_ctx, pt)
         else:
             ws = nan_workspace(pa.workspace_size(q1, kd, btd, out_dtype, max_ctx, pt))
             pa.decode_splitkv(out, q1, kd, vd, btd, ld, scale, max_ctx, pt, workspace=ws)
