@@ -21,7 +21,7 @@ LIB = os.path.join(HERE, "libpa_decode.so")
 
 SOURCES = ["pa_api.cu", "pa_combine.cu", "pa_attn_d64.cu", "pa_attn_d128.cu", "pa_attn_d256.cu",
            "pa_attn_d64_multi.cu", "pa_attn_d128_multi.cu", "pa_attn_d256_multi.cu",
-           "pa_tile_d64.cu", "pa_tile_d128.cu", "pa_tile_d256.cu"]
+           "pa_tile_d64.cu", "pa_tile_d128.cu", "pa_tile_d256.cu", "pa_tile_d256_compact.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 FLAGS = ["-std=c++17", "-O3", "-lineinfo", "-Xcompiler", "-fPIC", "-Xcompiler", "-O2",
          f"-I{INCLUDE}"] + ARCH

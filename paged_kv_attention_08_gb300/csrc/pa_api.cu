@@ -210,6 +210,7 @@ struct Plan {
     bool balanced;   // one CTA per SM, equal shares of the flattened page order
     int num_ctas;    // balanced: grid size
     bool tile;       // several query tokens on the tcgen05 tile kernel (128-row tiles)
+    int tile_qr;     // tile kernel: Q rows staged in shared memory (128, or 16: compact)
 };
 
 Plan plan_with(const pa_shape* s, int pages, int pp, bool cluster_ok,
@@ -219,6 +220,7 @@ Plan plan_with(const pa_shape* s, int pages, int pp, bool cluster_ok,
     p.balanced = false;
     p.num_ctas = 0;
     p.tile = false;
+    p.tile_qr = kTileRows;
     if (pp < 1) pp = 1;
     p.num_parts = (pages + pp - 1) / pp;
     if (p.num_parts < 1) p.num_parts = 1;
@@ -385,8 +387,24 @@ bool use_tile(const pa_shape* s, int32_t q_len, int32_t partition_tokens) {
     return rows > 16 || (rows == 16 && s->head_dim == 256);
 }
 
-int tile_ctas_per_sm(const pa_shape* s) {
-    const TileSmem L = tile_smem_layout(s->head_dim, s->block_size);
+// Q rows the tile kernel stages: 16 at head_dim 256 when a unit has at most 16
+// rows (its other 112 would be zeros), which buys a third stage per K / V
+// ring; otherwise a whole tile.  PA_TILE_COMPACT_Q=0 stages whole tiles
+// always (a tuning switch, read on every call; results agree).
+int tile_q_rows(const pa_shape* s, int32_t q_len) {
+    const char* v = std::getenv("PA_TILE_COMPACT_Q");
+    if (v && std::atoi(v) == 0) return kTileRows;
+    const int64_t rows = (int64_t)q_len * (s->num_heads / s->num_kv_heads);
+    return s->head_dim == 256 && rows <= kTileCompactQRows ? kTileCompactQRows : kTileRows;
+}
+
+bool tile_cluster_fits(const pa_shape* s, int qr) {
+    return tile_cluster_bytes(s->head_dim) <=
+           tile_smem_layout(s->head_dim, s->block_size, qr).bar_off;
+}
+
+int tile_ctas_per_sm(const pa_shape* s, int qr) {
+    const TileSmem L = tile_smem_layout(s->head_dim, s->block_size, qr);
     int n = (int)((227u * 1024u) / (L.total + kSmemAlignSlack));
     const int by_tmem = (int)(512u / tile_tmem_cols(s->head_dim));
     n = n < by_tmem ? n : by_tmem;
@@ -396,21 +414,28 @@ int tile_ctas_per_sm(const pa_shape* s) {
 
 // Clusters of `cluster` tile-kernel CTAs that fit on the current device at
 // once (cached per device and instantiation; 0 when unknown).
-int tile_max_clusters(const pa_shape* s, int cluster) {
-    static std::atomic<int> cache[kMaxDevices][3][2][2][kMaxClusterParts + 1];  // n + 1; 0 = unset
+int tile_max_clusters(const pa_shape* s, int cluster, int qr) {
+    // n + 1; 0 = unset
+    static std::atomic<int> cache[kMaxDevices][3][2][2][2][kMaxClusterParts + 1];
     int dev = 0;
     if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return 0;
     const int di = s->head_dim == 64 ? 0 : (s->head_dim == 128 ? 1 : 2);
+    const bool compact = qr == kTileCompactQRows && s->head_dim == 256;
     std::atomic<int>& slot =
-        cache[dev][di][s->block_size == 32][s->kv_dtype == PA_BF16][cluster];
+        cache[dev][di][s->block_size == 32][s->kv_dtype == PA_BF16][compact][cluster];
     int v = slot.load(std::memory_order_relaxed);
     if (v == 0) {
-        const uint32_t smem = tile_smem_layout(s->head_dim, s->block_size).total + kSmemAlignSlack;
+        const uint32_t smem =
+            tile_smem_layout(s->head_dim, s->block_size, compact ? qr : kTileRows).total +
+            kSmemAlignSlack;
         int n = 0;
         switch (s->head_dim) {
             case 64: n = tile_max_clusters_d64(s->block_size, s->kv_dtype, cluster, smem); break;
             case 128: n = tile_max_clusters_d128(s->block_size, s->kv_dtype, cluster, smem); break;
-            default: n = tile_max_clusters_d256(s->block_size, s->kv_dtype, cluster, smem); break;
+            default:
+                n = compact ? tile_max_clusters_d256_compact(s->block_size, s->kv_dtype, cluster, smem)
+                            : tile_max_clusters_d256(s->block_size, s->kv_dtype, cluster, smem);
+                break;
         }
         v = n + 1;
         slot.store(v, std::memory_order_relaxed);
@@ -428,26 +453,26 @@ int tile_max_clusters(const pa_shape* s, int cluster) {
 Plan tile_plan(const pa_shape* s, int32_t max_context_len, int32_t partition_tokens, int num_sms,
                int32_t q_len) {
     const int pages = pages_for(s, max_context_len);
+    const int qr = tile_q_rows(s, q_len);
     int pp;
     if (partition_tokens > 0) {
         pp = partition_tokens / s->block_size;
     } else {
         const int64_t rows = (int64_t)q_len * (s->num_heads / s->num_kv_heads);
         const int64_t units = (int64_t)s->batch * s->num_kv_heads * ((rows + kTileRows - 1) / kTileRows);
-        const int64_t slots = (int64_t)num_sms * tile_ctas_per_sm(s);
+        const int64_t slots = (int64_t)num_sms * tile_ctas_per_sm(s, qr);
         int64_t parts = slots / units;  // whole waves: one partition more would add a wave
         const int64_t max_parts = (pages + 3) / 4;
         if (parts > max_parts) parts = max_parts;
         if (parts < 1) parts = 1;
         int best_c = 0;  // largest cluster split whose clusters are all resident at once
         for (int c = (int)std::min<int64_t>(kMaxClusterParts, max_parts); c >= 2; --c)
-            if (units <= tile_max_clusters(s, c)) {
+            if (units <= tile_max_clusters(s, c, qr)) {
                 best_c = c;
                 break;
             }
         // the parked partial must fit in the operand buffers
-        const bool fits = tile_cluster_bytes(s->head_dim) <=
-                          tile_smem_layout(s->head_dim, s->block_size).bar_off;
+        const bool fits = tile_cluster_fits(s, qr);
         // (B=2, T=4096, 64 query tokens of 16 heads: 6 partitions in clusters
         // 32.0 us against 9 through the workspace 35.6 us)
         const bool cluster =
@@ -456,20 +481,21 @@ Plan tile_plan(const pa_shape* s, int32_t max_context_len, int32_t partition_tok
         pp = (int)((pages + parts - 1) / parts);
         Plan p = plan_with(s, pages, pp, cluster);
         p.tile = true;
+        p.tile_qr = qr;
         return p;
     }
     // an explicit partition count: a cluster when its partial fits in shared
     // memory and the device holds every unit's cluster at once
-    Plan p = plan_with(s, pages, pp, tile_cluster_bytes(s->head_dim) <=
-                                         tile_smem_layout(s->head_dim, s->block_size).bar_off);
+    Plan p = plan_with(s, pages, pp, tile_cluster_fits(s, qr));
     if (p.cluster) {
         const int64_t rows = (int64_t)q_len * (s->num_heads / s->num_kv_heads);
         const int64_t units =
             (int64_t)s->batch * s->num_kv_heads * ((rows + kTileRows - 1) / kTileRows);
-        const int n = tile_max_clusters(s, p.num_parts);
+        const int n = tile_max_clusters(s, p.num_parts, qr);
         if (n > 0 && units > n) p.cluster = false;
     }
     p.tile = true;
+    p.tile_qr = qr;
     return p;
 }
 
@@ -716,16 +742,17 @@ pa_status launch_tile(void* out, const void* q, const void* k, const void* v, co
     L.kv_dtype = s->kv_dtype;
     L.pdl = use_pdl();
     L.cluster = plan.cluster ? plan.num_parts : 1;
-    const TileSmem tl = tile_smem_layout(s->head_dim, s->block_size);
-    if (plan.cluster && tile_cluster_bytes(s->head_dim) > tl.bar_off) return PA_ERR_UNSUPPORTED;
+    const bool compact = plan.tile_qr == kTileCompactQRows;
+    if (compact && (s->head_dim != 256 || rows > kTileCompactQRows)) return PA_ERR_UNSUPPORTED;
+    if (plan.cluster && !tile_cluster_fits(s, plan.tile_qr)) return PA_ERR_UNSUPPORTED;
     L.grid = dim3((unsigned)plan.num_parts, (unsigned)grid_y, (unsigned)s->batch);
     L.threads = kTileThreads;
-    L.smem_bytes = tile_smem_layout(s->head_dim, s->block_size).total + kSmemAlignSlack;
+    L.smem_bytes = tile_smem_layout(s->head_dim, s->block_size, plan.tile_qr).total + kSmemAlignSlack;
     cudaError_t e;
     switch (s->head_dim) {
         case 64: e = launch_tile_d64(L, stream); break;
         case 128: e = launch_tile_d128(L, stream); break;
-        default: e = launch_tile_d256(L, stream); break;
+        default: e = compact ? launch_tile_d256_compact(L, stream) : launch_tile_d256(L, stream); break;
     }
     return e == cudaSuccess ? PA_OK : PA_ERR_CUDA;
 }

@@ -139,11 +139,19 @@ __host__ __device__ constexpr int tile_block_tokens(int D) { return D == 256 ? 6
 // S / P buffers in tensor memory: S of block j + 2 may be computed while P of
 // block j still waits for its P V MMA.
 constexpr int kTileSBufs = 3;
-__host__ __device__ constexpr int tile_stages(int D) { return D == 64 ? 4 : 2; }
+// Q rows staged in shared memory: a tile's 128, or -- at head_dim 256, for
+// units of at most 16 rows (one-token MQA: a group of 16 heads) -- only 16:
+// the MMA still runs M = 128, its rows past 16 read whatever follows the
+// compact Q tile (their results are never used), and the 56 KB saved buy a
+// third stage for each of the K and V rings.
+constexpr int kTileCompactQRows = 16;
+__host__ __device__ constexpr int tile_stages(int D, int qr = kTileRows) {
+    return D == 64 ? 4 : (D == 256 && qr == kTileCompactQRows ? 3 : 2);
+}
 
 struct TileSmem {
     uint32_t tile_bytes;   // one K (or V) block tile: BN * head_dim * 2
-    uint32_t q_off;        // Q tile
+    uint32_t q_off;        // Q tile: [head_dim / 64] column blocks of qr rows x 128 bytes
     uint32_t k_off;        // [ns] K stages
     uint32_t v_off;        // [ns] V stages
     uint32_t bar_off;      // mbarriers: k_full[ns], k_empty[ns], v_full[ns], v_empty[ns],
@@ -156,13 +164,13 @@ struct TileSmem {
     int ns;
 };
 
-__host__ __device__ inline TileSmem tile_smem_layout(int D, int BS) {
+__host__ __device__ inline TileSmem tile_smem_layout(int D, int BS, int qr = kTileRows) {
     TileSmem L;
     const int BN = tile_block_tokens(D);
-    L.ns = tile_stages(D);
+    L.ns = tile_stages(D, qr);
     L.tile_bytes = (uint32_t)BN * D * 2u;
     L.q_off = 0;
-    L.k_off = 256u * D;
+    L.k_off = 2u * qr * D;  // a multiple of 1024 (qr and D multiples of 16 and 64)
     L.v_off = L.k_off + L.tile_bytes * L.ns;
     uint32_t o = L.v_off + L.tile_bytes * L.ns;
     L.bar_off = o;
@@ -263,10 +271,12 @@ cudaError_t launch_attn_d256_multi(const AttnLaunch& L, cudaStream_t stream);
 cudaError_t launch_tile_d64(const AttnLaunch& L, cudaStream_t stream);
 cudaError_t launch_tile_d128(const AttnLaunch& L, cudaStream_t stream);
 cudaError_t launch_tile_d256(const AttnLaunch& L, cudaStream_t stream);
+cudaError_t launch_tile_d256_compact(const AttnLaunch& L, cudaStream_t stream);
 // Clusters of `cluster` tile-kernel CTAs resident at once on the current device.
 int tile_max_clusters_d64(int block_size, int kv_dtype, int cluster, uint32_t smem_bytes);
 int tile_max_clusters_d128(int block_size, int kv_dtype, int cluster, uint32_t smem_bytes);
 int tile_max_clusters_d256(int block_size, int kv_dtype, int cluster, uint32_t smem_bytes);
+int tile_max_clusters_d256_compact(int block_size, int kv_dtype, int cluster, uint32_t smem_bytes);
 
 cudaError_t launch_combine(const CombineParams& p, int head_dim, dim3 grid, bool pdl,
                            cudaStream_t stream);

@@ -44,13 +44,16 @@ namespace pa {
 
 constexpr float kTileRescaleSlack = 8.0f;  // log2 units: P may reach 2^8 before a rescale
 
-template <int D, int BS, typename KV>
+// QR: Q rows staged in shared memory (kTileRows, or kTileCompactQRows for
+// units of at most 16 rows at head_dim 256, which buys a third ring stage).
+template <int D, int BS, typename KV, int QR>
 __global__ void __launch_bounds__(kTileThreads, 1)
     tile_kernel(const __grid_constant__ CUtensorMap tmap_k,
                 const __grid_constant__ CUtensorMap tmap_v, const AttnParams p) {
     constexpr int BN = tile_block_tokens(D);  // tokens per KV block
     constexpr int NPB = BN / BS;              // pages per KV block
-    constexpr int NS = tile_stages(D);
+    constexpr int NS = tile_stages(D, QR);
+    static_assert(QR == kTileRows || (QR == kTileCompactQRows && D == 256), "staged Q rows");
     constexpr int DBLK = D / 64;
     constexpr int KSTEPS = D / 16;
     constexpr float NEG_INF = -INFINITY;
@@ -64,7 +67,7 @@ __global__ void __launch_bounds__(kTileThreads, 1)
     uint8_t* smem = reinterpret_cast<uint8_t*>(
         (reinterpret_cast<uintptr_t>(smem_raw) + (kSmemAlignSlack - 1)) &
         ~uintptr_t(kSmemAlignSlack - 1));
-    const TileSmem L = tile_smem_layout(D, BS);
+    const TileSmem L = tile_smem_layout(D, BS, QR);
     uint64_t* bars = reinterpret_cast<uint64_t*>(smem + L.bar_off);
     uint64_t* k_full = bars;
     uint64_t* k_empty = bars + NS;
@@ -225,20 +228,23 @@ __global__ void __launch_bounds__(kTileThreads, 1)
     tc::fence_after_sync();
     const uint32_t tmem = *tmem_slot;
 
-    // ---- Q tile: rows u = tile*128 + r, zero rows past the unit's rows;
-    // written with the 128-byte swizzle the MMA descriptors expect, by every
-    // thread outside the two copy warps (which already stream K and V); the
-    // MMA issuer waits for q_ready ----
+    // ---- Q tile: rows u = tile*128 + r for r < QR, zero rows past the
+    // unit's rows; written with the 128-byte swizzle the MMA descriptors
+    // expect, by every thread outside the two copy warps (which already stream
+    // K and V); the MMA issuer waits for q_ready.  With a compact Q tile the
+    // S MMA's rows past QR read whatever follows it: those rows lie past the
+    // unit's rows, their scores are masked or never read, and their P and O
+    // rows are never used ----
     if (warp != 0 && warp != 3) {
         const int qt = (warp < 3 ? (warp - 1) * 32 : 64 + (warp - 4) * 32) + lane;  // 0..319
         uint8_t* qs = smem + L.q_off;
-        for (int i = qt; i < kTileRows * (D / 8); i += kTileThreads - 64) {
+        for (int i = qt; i < QR * (D / 8); i += kTileThreads - 64) {
             const int r = i / (D / 8), c = i % (D / 8);
             const int u = tile * kTileRows + r;
             uint4 v = make_uint4(0, 0, 0, 0);
             if (u < U)
                 v = __ldg(reinterpret_cast<const uint4*>(static_cast<const KV*>(p.q) + row_off(u)) + c);
-            *reinterpret_cast<uint4*>(qs + (c >> 3) * (kTileRows * 128) + r * 128 +
+            *reinterpret_cast<uint4*>(qs + (c >> 3) * (QR * 128) + r * 128 +
                                       (((c & 7) ^ (r & 7)) << 4)) = v;
         }
         fence_proxy_async_smem();
@@ -339,7 +345,7 @@ __global__ void __launch_bounds__(kTileThreads, 1)
 #pragma unroll
                         for (int s = 0; s < KSTEPS; ++s) {
                             const uint64_t a = tc::smem_desc(
-                                q_base + (s >> 2) * (kTileRows * 128) + (s & 3) * 32, 16, 1024,
+                                q_base + (s >> 2) * (QR * 128) + (s & 3) * 32, 16, 1024,
                                 tc::kSwizzle128B);
                             const uint64_t bd = tc::smem_desc(
                                 k_base + (s >> 2) * (BN * 128) + (s & 3) * 32, 16, 1024,
@@ -613,15 +619,15 @@ __global__ void __launch_bounds__(kTileThreads, 1)
 }
 
 // Per-instantiation flag of the shared-memory limit set once per device.
-template <int D, int BS, typename KV>
+template <int D, int BS, typename KV, int QR>
 struct TileAttrs {
     static inline AttrFlags smem;
 };
 
-template <int D, int BS, typename KV>
+template <int D, int BS, typename KV, int QR>
 cudaError_t launch_tile_inst(const AttnLaunch& L, cudaStream_t stream) {
-    auto kern = tile_kernel<D, BS, KV>;
-    cudaError_t e = raise_smem_limit_once(kern, TileAttrs<D, BS, KV>::smem);
+    auto kern = tile_kernel<D, BS, KV, QR>;
+    cudaError_t e = raise_smem_limit_once(kern, TileAttrs<D, BS, KV, QR>::smem);
     if (e != cudaSuccess) return e;
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = L.grid;
@@ -649,10 +655,10 @@ cudaError_t launch_tile_inst(const AttnLaunch& L, cudaStream_t stream) {
 
 // Clusters of `cluster` CTAs of this instantiation that can be resident at
 // once on the current device (0 if the query fails).
-template <int D, int BS, typename KV>
+template <int D, int BS, typename KV, int QR>
 int tile_max_clusters_inst(int cluster, uint32_t smem_bytes) {
-    auto kern = tile_kernel<D, BS, KV>;
-    if (raise_smem_limit_once(kern, TileAttrs<D, BS, KV>::smem) != cudaSuccess) {
+    auto kern = tile_kernel<D, BS, KV, QR>;
+    if (raise_smem_limit_once(kern, TileAttrs<D, BS, KV, QR>::smem) != cudaSuccess) {
         (void)cudaGetLastError();
         return 0;
     }
@@ -675,25 +681,25 @@ int tile_max_clusters_inst(int cluster, uint32_t smem_bytes) {
     return n;
 }
 
-template <int D>
+template <int D, int QR>
 int tile_max_clusters_for_d(int block_size, int kv_dtype, int cluster, uint32_t smem_bytes) {
     const bool bf = kv_dtype == PA_BF16;
     if (block_size == 16)
-        return bf ? tile_max_clusters_inst<D, 16, __nv_bfloat16>(cluster, smem_bytes)
-                  : tile_max_clusters_inst<D, 16, __half>(cluster, smem_bytes);
-    return bf ? tile_max_clusters_inst<D, 32, __nv_bfloat16>(cluster, smem_bytes)
-              : tile_max_clusters_inst<D, 32, __half>(cluster, smem_bytes);
+        return bf ? tile_max_clusters_inst<D, 16, __nv_bfloat16, QR>(cluster, smem_bytes)
+                  : tile_max_clusters_inst<D, 16, __half, QR>(cluster, smem_bytes);
+    return bf ? tile_max_clusters_inst<D, 32, __nv_bfloat16, QR>(cluster, smem_bytes)
+              : tile_max_clusters_inst<D, 32, __half, QR>(cluster, smem_bytes);
 }
 
-template <int D>
+template <int D, int QR>
 cudaError_t launch_tile_for_d(const AttnLaunch& L, cudaStream_t stream) {
     const bool bf = L.kv_dtype == PA_BF16;
     if (L.block_size == 16)
-        return bf ? launch_tile_inst<D, 16, __nv_bfloat16>(L, stream)
-                  : launch_tile_inst<D, 16, __half>(L, stream);
+        return bf ? launch_tile_inst<D, 16, __nv_bfloat16, QR>(L, stream)
+                  : launch_tile_inst<D, 16, __half, QR>(L, stream);
     if (L.block_size == 32)
-        return bf ? launch_tile_inst<D, 32, __nv_bfloat16>(L, stream)
-                  : launch_tile_inst<D, 32, __half>(L, stream);
+        return bf ? launch_tile_inst<D, 32, __nv_bfloat16, QR>(L, stream)
+                  : launch_tile_inst<D, 32, __half, QR>(L, stream);
     return cudaErrorInvalidValue;
 }
 
