@@ -216,3 +216,32 @@ def test_tile_kernel_poison_and_permutation(monkeypatch):
                           x.scale, x.max_context_len, x.lens_host)
     assert torch.equal(run(xq, 0), base)
     assert pa.device_error() == 0
+
+
+@pytest.mark.parametrize("Q,H,Hkv", [(1, 16, 1), (2, 16, 2)], ids=["mqa_q1", "g8_q2"])
+def test_tile_compact_q_tile(monkeypatch, Q, H, Hkv):
+    """Units of at most 16 rows at head_dim 256 stage a compact Q tile (the
+    MMA's other rows read what follows it): exact against the oracle, bit-
+    identical to whole 128-row Q tiles, and unchanged by NaN in every
+    unreferenced block, in one pass and in cluster / workspace splits."""
+    monkeypatch.delenv("PA_MULTI_KERNEL", raising=False)
+    x = multi_case(29, 3, Q, H, Hkv, 256, 32, [70, 1000, 5], spare=6)
+    want = oracle_of(x)
+    xd = x.to(DEV)
+    NB = x.k_cache.shape[0]
+    used = set(x.block_tables[x.block_tables >= 0].tolist())
+    k, v = xd.k_cache.clone(), xd.v_cache.clone()
+    for blk in range(NB):
+        if blk not in used:
+            k[blk] = float("nan")
+            v[blk] = float("nan")
+    xp = workloads.Inputs(x.spec, xd.q, k, v, xd.block_tables, xd.context_lens, x.scale,
+                          x.max_context_len, x.lens_host)
+    for pt in [0, 32 * 32, 4 * 32]:
+        monkeypatch.setenv("PA_TILE_COMPACT_Q", "1")
+        compact = run(xd, pt)
+        check(compact, want)
+        assert torch.equal(run(xp, pt), compact)
+        monkeypatch.setenv("PA_TILE_COMPACT_Q", "0")
+        assert torch.equal(run(xd, pt), compact)
+    assert pa.device_error() == 0
