@@ -114,7 +114,8 @@ pa_status pa_decode(void* out, const void* q, const void* k_cache, const void* v
  * is for the current device, as the call plans with its SM count (which picks
  * the CTA shape and with it whether a cluster split fits); an explicit
  * partition size may be queried without a device, and is then sized as for
- * one SM.
+ * one SM.  A size that does not fit in a size_t is reported as SIZE_MAX, which
+ * no workspace satisfies (the call is then refused with PA_ERR_WORKSPACE).
  */
 size_t pa_workspace_size(const pa_shape* shape, int32_t max_context_len,
                          int32_t partition_tokens);

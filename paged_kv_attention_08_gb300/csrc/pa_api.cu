@@ -540,19 +540,29 @@ bool partition_arg_ok(const pa_shape* s, int32_t partition_tokens) {
 
 // Workspace: part_acc [B, Hkv, P, Q*G, D] fp32, then part_ml [B, Hkv, P, Q*G, 2]
 // fp32 (rows of a (sequence, kv head, partition): query token, then head).
+// Workspace bytes of a plan; SIZE_MAX (which no buffer satisfies, so the call
+// is refused with PA_ERR_WORKSPACE) when the size does not fit in a size_t.
 size_t workspace_bytes_for(const pa_shape* s, const Plan& plan, size_t* ml_offset,
                            int32_t q_len = 1) {
-    size_t rows;  // (m, l, acc) rows
-    if (plan.balanced) {
-        rows = (size_t)plan.num_ctas * 2 * (s->num_heads / s->num_kv_heads) * q_len;  // [C][2][QG]
+    const size_t kTooBig = SIZE_MAX;
+    size_t rows = 1;  // (m, l, acc) rows
+    auto mul = [&](size_t f) { return !__builtin_mul_overflow(rows, f, &rows); };
+    bool ok;
+    if (plan.balanced) {  // [C][2][Q*G]
+        ok = mul((size_t)plan.num_ctas) && mul(2) &&
+             mul((size_t)(s->num_heads / s->num_kv_heads)) && mul((size_t)q_len);
     } else {
         if (plan.num_parts <= 1 || plan.cluster) return 0;  // one pass, or reduced in a cluster
-        rows = (size_t)s->batch * s->num_heads * q_len * plan.num_parts;  // [B][Hkv][P][Q*G]
+        ok = mul((size_t)s->batch) && mul((size_t)s->num_heads) && mul((size_t)q_len) &&
+             mul((size_t)plan.num_parts);  // [B][Hkv][P][Q*G]
     }
-    const size_t acc = rows * s->head_dim * sizeof(float);
+    size_t acc = 0, ml = 0;
+    if (!ok || __builtin_mul_overflow(rows, (size_t)s->head_dim * sizeof(float), &acc) ||
+        __builtin_mul_overflow(rows, 2 * sizeof(float), &ml) || acc > kTooBig - 255 - ml)
+        return kTooBig;
     const size_t off = (acc + 255) / 256 * 256;
     if (ml_offset) *ml_offset = off;
-    return off + rows * 2 * sizeof(float);
+    return off + ml;
 }
 
 // The last few tensor-map pairs this host thread encoded, by everything a map

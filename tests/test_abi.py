@@ -233,3 +233,14 @@ def test_plan_info_explicit_partitions(lib):
     assert lib.pa_plan_info(ctypes.byref(s), 0, 4096, 512, ctypes.byref(d)) == 1
     assert lib.pa_plan_info(ctypes.byref(s), 1, 4096, 100, ctypes.byref(d)) == 1
     assert lib.pa_plan_info(ctypes.byref(s), 1, 4096, 512, None) == 1
+
+
+def test_workspace_size_saturates_instead_of_wrapping(lib):
+    """A shape whose partials would need more than a size_t holds reports
+    SIZE_MAX (no buffer satisfies it, so the call is refused), never a wrapped
+    small size."""
+    s = shape(batch=65535, num_heads=65535 * 16, num_kv_heads=65535, head_dim=256,
+              max_blocks_per_seq=1 << 26, num_blocks=1000)
+    max_ctx = (1 << 30) - 16
+    assert lib.pa_workspace_size_multi(ctypes.byref(s), 2000, max_ctx, 16) == 2**64 - 1
+    assert lib.pa_workspace_size_multi(ctypes.byref(s), 1, max_ctx, 16) == 2**64 - 1
