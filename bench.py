@@ -332,6 +332,8 @@ def main(argv=None):
     ap.add_argument("--partition-tokens", type=int, default=-1,
                     help="split-KV partition size; -1 = each workload's own (0/auto unless stated)")
     ap.add_argument("--no-graph", action="store_true", help="launch eagerly instead of graph replay")
+    ap.add_argument("--graph-per-step", action="store_true",
+                    help="replay one graph per step instead of one per loop over the input sets")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--with-append", action="store_true",
@@ -428,8 +430,12 @@ def main(argv=None):
             print(json.dumps({"metric": METRIC, "error": f"parity failed: max_err {max_err}"}))
             return 1
 
-    # ---- graphs: one per input set ----
+    # ---- graphs: one step per input set, and a loop graph that runs every
+    # set's step in turn (nsets steps per replay: programmatic dependent launch
+    # then links every call, step boundaries included, instead of one graph
+    # launch per step) ----
     graphs = []
+    loop_graph = None
     if not args.no_graph:
         with torch.cuda.stream(stream):
             for si in range(nsets):               # warm every set once before capture
@@ -442,6 +448,12 @@ def main(argv=None):
                 for i in range(len(set0)):
                     call(si, i, torch.cuda.current_stream())
             graphs.append(g)
+        if nsets > 1 and not args.graph_per_step:
+            loop_graph = torch.cuda.CUDAGraph()
+            with torch.cuda.graph(loop_graph, stream=stream):
+                for si in range(nsets):
+                    for i in range(len(set0)):
+                        call(si, i, torch.cuda.current_stream())
     torch.cuda.synchronize()
 
     def step(k, st):
@@ -462,14 +474,23 @@ def main(argv=None):
                 k += 1
                 if k % 256 == 0:
                     stream.synchronize()
+            if loop_graph is not None:
+                for _ in range(3):
+                    loop_graph.replay()
             stream.synchronize()
             barrier()
             torch.cuda.synchronize()
             e0 = torch.cuda.Event(enable_timing=True)
             e1 = torch.cuda.Event(enable_timing=True)
             e0.record(stream)
-            for k in range(args.steps):
+            k = 0
+            if loop_graph is not None:      # whole loops of the nsets steps
+                while k + nsets <= args.steps:
+                    loop_graph.replay()
+                    k += nsets
+            while k < args.steps:           # the rest, one step graph each
                 step(k, stream)
+                k += 1
             e1.record(stream)
             e1.synchronize()
             torch.cuda.synchronize()
@@ -643,7 +664,10 @@ def main(argv=None):
                 "plan": plans,
                 "l2": f"rotating {nsets} input sets of {set_bytes / 1e6:.1f} MB "
                       f"({nsets * set_bytes / 1e6:.0f} MB > 3x L2 {l2 / 1e6:.0f} MB)",
-                "launch": "CUDA graph replay per step" if graphs else "eager",
+                "launch": (f"CUDA graph of {nsets} steps (one per input set) per replay, "
+                           "programmatic dependent launch between all calls"
+                           if loop_graph is not None else
+                           "CUDA graph replay per step" if graphs else "eager"),
                 "append": ("each call appends the new token first (pa_append_kv); bytes "
                            "counted are the decode's only") if args.with_append else None,
                 "parallelism": f"replicas x{world}",
