@@ -93,6 +93,17 @@ def test_hand_worked_golden(case):
     np.testing.assert_allclose(out, np.array(case["expected"]), rtol=0, atol=1e-15)
 
 
+def test_hand_worked_file_is_what_its_script_writes():
+    """The stored closed-form cases are exactly what the committed script
+    builds from the logistic function (no oracle, no GPU involved)."""
+    import importlib.util
+    spec = importlib.util.spec_from_file_location(
+        "make_hand_worked_cases", os.path.join(os.path.dirname(GOLDEN), "make_hand_worked_cases.py"))
+    mod = importlib.util.module_from_spec(spec)
+    spec.loader.exec_module(mod)
+    assert json.load(open(GOLDEN)) == mod.build()
+
+
 @pytest.mark.parametrize("dtype", [torch.float16, torch.bfloat16])
 def test_single_token_returns_its_v_row(dtype):
     q, k, v, bt, _, scale = small_case(1, B=3, H=8, Hkv=2, D=16, bs=4, lens=[5, 9, 2], dtype=dtype)
