@@ -31,6 +31,8 @@
 //     memory when the max moves by more than 2^8, and write P over S as a
 //     high and a low 16-bit part (two MMAs, ~16 significant bits), then the
 //     final O / l or the partial (m, l, O) for the combine kernel.
+// Units of at most 16 rows at head_dim 256 (one-token MQA) stage only those
+// rows of Q (QR = 16): the 56 KB saved give each K / V ring a third stage.
 // Every mbarrier wait is bounded: on timeout the kernel records
 // PA_ERR_TIMEOUT, the roles stop, and tensor memory is released.
 #pragma once
