@@ -8,6 +8,7 @@ import glob
 import os
 import re
 
+import numpy as np
 import pytest
 import torch
 
@@ -244,3 +245,36 @@ def test_workspace_size_saturates_instead_of_wrapping(lib):
     max_ctx = (1 << 30) - 16
     assert lib.pa_workspace_size_multi(ctypes.byref(s), 2000, max_ctx, 16) == 2**64 - 1
     assert lib.pa_workspace_size_multi(ctypes.byref(s), 1, max_ctx, 16) == 2**64 - 1
+
+
+def test_explicit_plans_and_workspace_sizes_agree(lib):
+    """Seeded random shapes and explicit partition sizes, without a device: the
+    plan has the requested split, its reduction is a workspace one exactly when
+    pa_workspace_size asks for memory, and that size is the layout's
+    [B][Hkv][P][Q*G] rows of (D + 2) fp32 (the (m, l) block 256-byte aligned)."""
+    rng = np.random.default_rng(7)
+    for _ in range(300):
+        D = int(rng.choice([64, 128, 256]))
+        bs = int(rng.choice([16, 32]))
+        G = int(rng.choice([1, 2, 4, 8, 16]))
+        Hkv = int(rng.choice([1, 2, 4, 8]))
+        B = int(rng.integers(1, 65))
+        q_len = int(rng.choice([1, 1, 2, 4, 9, 33]))
+        mb = int(rng.integers(1, 2049))
+        s = shape(batch=B, num_heads=G * Hkv, num_kv_heads=Hkv, head_dim=D, block_size=bs,
+                  max_blocks_per_seq=mb, num_blocks=10_000)
+        max_ctx = int(rng.integers(0, mb * bs + 1))
+        pages = min(-(-max_ctx // bs), mb)
+        pp = int(rng.integers(1, 65))
+        d = pa._PlanDesc()
+        assert lib.pa_plan_info(ctypes.byref(s), q_len, max_ctx, pp * bs, ctypes.byref(d)) == 0
+        parts = max(1, -(-pages // pp))
+        assert d.partitions == parts
+        if parts > 1:
+            assert d.partition_tokens == pp * bs
+        ws = lib.pa_workspace_size_multi(ctypes.byref(s), q_len, max_ctx, pp * bs)
+        assert (ws > 0) == (d.reduce == 2), (d.reduce, ws)
+        assert d.reduce in ((0,) if parts == 1 else (1, 2))
+        if ws:
+            rows = B * G * Hkv * q_len * parts
+            assert ws == (rows * D * 4 + 255) // 256 * 256 + rows * 2 * 4
