@@ -77,6 +77,9 @@ SPECS = {s.name: s for s in [
     _long(4, 8192), _long(4, 32768), _long(4, 131072),
     Spec("mqa_b32_t16384", 32, 16, 1, 256, 32, torch.bfloat16, "fixed:16384", pool="factor:1.1",
          q_std=1.0, kv_std=0.5),
+    # the MQA shape at smoke-test size: 3 + 5 pages of 32 tokens, one spare block
+    Spec("tiny_mqa", 2, 16, 1, 256, 32, torch.bfloat16, "list:70,130", pool="fixed:9",
+         max_blocks=5, kv_std=0.5),
     # multi-token steps: a small case with a sequence shorter than q_len, four
     # drafted tokens per sequence (4 tokens x 4 heads fill the 16 MMA rows),
     # eight (two CTAs per kv head), and a 64-token chunk with MQA-like groups

@@ -59,11 +59,14 @@ def sample_rows(x, n, seed=0):
 # ---------------------------------------------------------------------------
 # workloads small enough for the whole oracle
 # ---------------------------------------------------------------------------
-@pytest.mark.parametrize("name", ["tiny", "sweep_b1_t512", "sweep_b16_t256", "sweep_b4_t2048"])
-@pytest.mark.parametrize("mode,pt", [("single", 0), ("split", 0), ("split", 16), ("split", 64)])
-def test_small_workloads_vs_oracle(name, mode, pt):
+@pytest.mark.parametrize("name", ["tiny", "sweep_b1_t512", "sweep_b16_t256", "sweep_b4_t2048",
+                                  "tiny_mqa"])
+@pytest.mark.parametrize("mode,pages", [("single", 0), ("split", 0), ("split", 1), ("split", 4)])
+def test_small_workloads_vs_oracle(name, mode, pages):
+    """Whole oracle; explicit partitions of one and of four pages."""
     x = workloads.make(name, seed=0, device=DEV)
     want = oracle.decode(x.q, x.k_cache, x.v_cache, x.block_tables, x.context_lens, x.scale)
+    pt = pages * x.k_cache.shape[1]
     assert_close_fp32(run(x, mode, partition_tokens=pt), want)
 
 
