@@ -330,6 +330,15 @@ __global__ void __launch_bounds__(kTileThreads, 1)
             constexpr uint32_t id_s = tc::idesc_f16(kType, false, kTileRows, BN);
             constexpr uint32_t id_o = tc::idesc_f16(kType, true, kTileRows, D);
             const uint32_t q_base = smem_u32(smem + L.q_off);
+            // Operand descriptors: a shared-memory descriptor holds (address >> 4)
+            // in its low 14 bits, and every address here is below 2^18, so the
+            // descriptor of base + offset is base's plus offset >> 4.  Q's are
+            // fixed for the CTA; K's and V's are one add from their stage's.
+            uint64_t qd[KSTEPS];
+#pragma unroll
+            for (int s = 0; s < KSTEPS; ++s)
+                qd[s] = tc::smem_desc(q_base + (s >> 2) * (QR * 128) + (s & 3) * 32, 16, 1024,
+                                      tc::kSwizzle128B);
             bool started = false;
             bool live_prev = false;  // block i-1 holds a page (its K stage may be refilled)
             const bool q_ok = wait(q_ready, 0);
@@ -344,16 +353,12 @@ __global__ void __launch_bounds__(kTileThreads, 1)
                     live_cur = block_live(st);
                     if (live_cur) {
                         const uint32_t k_base = smem_u32(smem + L.k_off) + (uint32_t)st * L.tile_bytes;
+                        const uint64_t kd = tc::smem_desc(k_base, 16, 1024, tc::kSwizzle128B);
 #pragma unroll
-                        for (int s = 0; s < KSTEPS; ++s) {
-                            const uint64_t a = tc::smem_desc(
-                                q_base + (s >> 2) * (QR * 128) + (s & 3) * 32, 16, 1024,
-                                tc::kSwizzle128B);
-                            const uint64_t bd = tc::smem_desc(
-                                k_base + (s >> 2) * (BN * 128) + (s & 3) * 32, 16, 1024,
-                                tc::kSwizzle128B);
-                            tc::mma_ss(tmem + S_COL + (i % NB) * BN, a, bd, id_s, s > 0);
-                        }
+                        for (int s = 0; s < KSTEPS; ++s)
+                            tc::mma_ss(tmem + S_COL + (i % NB) * BN, qd[s],
+                                       kd + (uint64_t)(((s >> 2) * (BN * 128) + (s & 3) * 32) >> 4),
+                                       id_s, s > 0);
                     }
                     tc::commit(smem_u32(s_full + i % NB));
                     tc::commit(smem_u32(k_empty + st));
@@ -368,12 +373,12 @@ __global__ void __launch_bounds__(kTileThreads, 1)
                         const uint32_t v_base = smem_u32(smem + L.v_off) + (uint32_t)st * L.tile_bytes;
                         const uint32_t p_hi = tmem + S_COL + (j % NB) * BN;
                         const uint32_t p_lo = p_hi + BN / 2;
+                        // V: MN-major, 64-column blocks BN*128 bytes apart, 8-row
+                        // groups 1024 bytes apart; rows ks*16 .. +15 per step
+                        const uint64_t vd0 = tc::smem_desc(v_base, BN * 128, 1024, tc::kSwizzle128B);
 #pragma unroll
                         for (int ks = 0; ks < BN / 16; ++ks) {
-                            // V rows ks*16 .. +15: MN-major, 64-column blocks BN*128 bytes
-                            // apart, 8-row groups 1024 bytes apart
-                            const uint64_t vd = tc::smem_desc(v_base + ks * 16 * 128, BN * 128,
-                                                              1024, tc::kSwizzle128B);
+                            const uint64_t vd = vd0 + (uint64_t)((ks * 16 * 128) >> 4);
                             tc::mma_ts(tmem + O_COL, p_hi + ks * 8, vd, id_o,
                                        (started || ks > 0) ? 1u : 0u);
                             tc::mma_ts(tmem + O_COL, p_lo + ks * 8, vd, id_o, 1u);
