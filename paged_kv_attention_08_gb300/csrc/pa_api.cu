@@ -1,5 +1,10 @@
-// Host side of the C ABI in include/pa_decode.h: validation, the split-KV
-// plan, TMA descriptors, and the launches.
+// Host side of the C ABI in include/pa_decode.h, in this order: shape and
+// argument validation; the device state (SM count, error word); the launch
+// shape of the warp-level kernel (pick_tune) and the occupancy of its
+// clusters; the split plans -- auto_plan (warp-level kernel), balanced_plan,
+// tile_plan (tcgen05 tile kernel) and make_plan, which picks among them;
+// workspace sizing; TMA descriptors (cached per host thread); the launches;
+// and the exported entry points.
 #include <cudaTypedefs.h>
 
 #include <algorithm>
