@@ -309,6 +309,29 @@ pa_status pa_decode_splitkv_noalloc(void* out, const void* q, const void* k_cach
  */
 pa_status pa_selftest_wait_timeout(uint64_t timeout_ns, void* stream);
 
+/*
+ * Test and tuning switches (no counterpart in the pages: they choose between
+ * this library's own kernels, whose results agree up to rounding order).
+ *   PA_SWITCH_MULTI_KERNEL    PA_KERNEL_AUTO (default): the library's choice;
+ *                             PA_KERNEL_MMA: the warp-level kernel for every
+ *                             q_len > 1 call; PA_KERNEL_TILE: the tcgen05 tile
+ *                             kernel for every split-KV / multi-token call
+ *   PA_SWITCH_TILE_COMPACT_Q  1 (default): the tile kernel stages only 16 Q rows
+ *                             for units of at most 16 rows at head_dim 256;
+ *                             0: it stages whole 128-row tiles
+ * The initial values come from the environment variables PA_MULTI_KERNEL
+ * (mma | tile) and PA_TILE_COMPACT_Q (0), read once when the library is
+ * loaded; no call reads the environment.  pa_set_switch changes a switch for
+ * every later call of the process (a relaxed atomic store: set it while no
+ * other host thread is between a pa_workspace_size query and the call it
+ * sizes).  Returns PA_ERR_INVALID_ARG for an unknown switch or value.
+ * pa_get_switch returns the current value, -1 for an unknown switch.
+ */
+enum { PA_SWITCH_MULTI_KERNEL = 0, PA_SWITCH_TILE_COMPACT_Q = 1 };
+enum { PA_KERNEL_AUTO = 0, PA_KERNEL_MMA = 1, PA_KERNEL_TILE = 2 };
+pa_status pa_set_switch(int32_t which, int32_t value);
+int32_t pa_get_switch(int32_t which);
+
 /* Static, human-readable name of a status. */
 const char* pa_status_string(pa_status status);
 

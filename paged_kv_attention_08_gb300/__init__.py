@@ -21,6 +21,7 @@ or a call is rejected, an exception is raised.
     resolve_blocks(out_phys, block_tables, context_lens, block_size, num_blocks)
     selftest_wait_timeout(timeout_ns)
     device_error()
+    set_switch(which, value) / get_switch(which)     (test and tuning switches)
 
 Every launching call also takes ``stream=`` (default: the current torch stream).
 """
@@ -35,10 +36,13 @@ import torch
 __all__ = ["PaError", "decode", "decode_splitkv", "decode_splitkv_noalloc", "decode_multi",
            "append_kv", "workspace_size", "workspace_size_multi", "plan_info", "choose_partition_tokens",
            "resolve_blocks", "selftest_wait_timeout", "device_error", "library_path", "F16",
-           "BF16", "F32", "PARTITION_BALANCED"]
+           "BF16", "F32", "PARTITION_BALANCED", "set_switch", "get_switch", "SWITCH_MULTI_KERNEL",
+           "SWITCH_TILE_COMPACT_Q", "KERNEL_AUTO", "KERNEL_MMA", "KERNEL_TILE"]
 
 F16, BF16, F32 = 0, 1, 2
 PARTITION_BALANCED = -1   # partition_tokens value requesting the balanced split
+SWITCH_MULTI_KERNEL, SWITCH_TILE_COMPACT_Q = 0, 1      # pa_set_switch switches
+KERNEL_AUTO, KERNEL_MMA, KERNEL_TILE = 0, 1, 2         # values of SWITCH_MULTI_KERNEL
 _STATUS = {0: "PA_OK", 1: "PA_ERR_INVALID_ARG", 2: "PA_ERR_UNSUPPORTED", 3: "PA_ERR_WORKSPACE",
            4: "PA_ERR_CUDA", 5: "PA_ERR_TIMEOUT"}
 
@@ -103,6 +107,10 @@ def _load():
             lib.pa_selftest_wait_timeout.restype = ctypes.c_int
             lib.pa_device_error.argtypes = [ctypes.POINTER(i32), P]
             lib.pa_device_error.restype = ctypes.c_int
+            lib.pa_set_switch.argtypes = [i32, i32]
+            lib.pa_set_switch.restype = ctypes.c_int
+            lib.pa_get_switch.argtypes = [i32]
+            lib.pa_get_switch.restype = i32
             lib.pa_status_string.argtypes = [ctypes.c_int]
             lib.pa_status_string.restype = ctypes.c_char_p
             _lib = lib
@@ -158,10 +166,40 @@ def _ints(block_tables, context_lens):
         raise TypeError("block_tables and context_lens must be int32")
 
 
+def _check_args(out, q, k_cache, v_cache, block_tables, context_lens, multi=False):
+    """Shapes and dtypes that the library takes on trust: it reads the problem
+    shape from q, k_cache and block_tables alone, so a v_cache, out, table or
+    length tensor of another shape or dtype would be read or written past its
+    memory.  Raises ValueError / TypeError before anything reaches the device."""
+    if q.dim() != (4 if multi else 3):
+        raise ValueError("q must be [batch, q_len, num_heads, head_dim]" if multi
+                         else "q must be [batch, num_heads, head_dim]")
+    if k_cache.dim() != 4:
+        raise ValueError("k_cache must be [num_blocks, block_size, num_kv_heads, head_dim]")
+    if tuple(v_cache.shape) != tuple(k_cache.shape):
+        raise ValueError(f"v_cache {tuple(v_cache.shape)} must be shaped like k_cache "
+                         f"{tuple(k_cache.shape)}")
+    if v_cache.dtype != k_cache.dtype:
+        raise TypeError("v_cache must have k_cache's dtype")
+    if q.dtype != k_cache.dtype:
+        raise TypeError("q must have the cache's dtype")
+    if q.shape[-1] != k_cache.shape[3]:
+        raise ValueError(f"q's head_dim {q.shape[-1]} differs from the cache's {k_cache.shape[3]}")
+    if tuple(out.shape) != tuple(q.shape):
+        raise ValueError(f"out {tuple(out.shape)} must be shaped like q {tuple(q.shape)}")
+    if out.dtype not in (torch.float32, q.dtype):
+        raise TypeError("out must be float32 or q's dtype")
+    if block_tables.dim() != 2 or block_tables.shape[0] != q.shape[0]:
+        raise ValueError("block_tables must be [batch, max_blocks_per_seq]")
+    if context_lens.dim() != 1 or context_lens.numel() != q.shape[0]:
+        raise ValueError("context_lens must be [batch]")
+    _ints(block_tables, context_lens)
+
+
 def decode(out, q, k_cache, v_cache, block_tables, context_lens, scale: float, stream=None):
     """Single-pass paged decode into ``out`` ([B,H,D], fp32 or q's dtype)."""
+    _check_args(out, q, k_cache, v_cache, block_tables, context_lens)
     _dev_tensors(out, q, k_cache, v_cache, block_tables, context_lens)
-    _ints(block_tables, context_lens)
     shape = make_shape(q, k_cache, block_tables, out.dtype)
     _check(_load().pa_decode(out.data_ptr(), q.data_ptr(), k_cache.data_ptr(), v_cache.data_ptr(),
                              block_tables.data_ptr(), context_lens.data_ptr(),
@@ -187,8 +225,8 @@ def decode_splitkv(out, q, k_cache, v_cache, block_tables, context_lens, scale: 
     """Flash-Decoding split-KV decode.  ``workspace`` is a CUDA byte tensor of at
     least ``workspace_size(...)`` bytes; when omitted one is taken from torch's
     allocator for this call."""
+    _check_args(out, q, k_cache, v_cache, block_tables, context_lens)
     _dev_tensors(out, q, k_cache, v_cache, block_tables, context_lens)
-    _ints(block_tables, context_lens)
     shape = make_shape(q, k_cache, block_tables, out.dtype)
     lib = _load()
     if workspace is None:
@@ -212,8 +250,8 @@ def decode_splitkv_noalloc(out, q, k_cache, v_cache, block_tables, context_lens,
     device memory.  Calls that may overlap on the GPU race on that scratch;
     the first call on a device should come before any stream capture.
     Raises PaError (PA_ERR_WORKSPACE) when the partials would not fit."""
+    _check_args(out, q, k_cache, v_cache, block_tables, context_lens)
     _dev_tensors(out, q, k_cache, v_cache, block_tables, context_lens)
-    _ints(block_tables, context_lens)
     shape = make_shape(q, k_cache, block_tables, out.dtype)
     _check(_load().pa_decode_splitkv_noalloc(
         out.data_ptr(), q.data_ptr(), k_cache.data_ptr(), v_cache.data_ptr(),
@@ -266,10 +304,8 @@ def decode_multi(out, q, k_cache, v_cache, block_tables, context_lens, scale: fl
                  max_context_len: int, partition_tokens: int = 0, workspace=None, stream=None):
     """Several query tokens per sequence (q, out: [B, Q, H, D]); query token i
     of sequence b attends causally to the cached tokens t <= context_lens[b] - Q + i."""
+    _check_args(out, q, k_cache, v_cache, block_tables, context_lens, multi=True)
     _dev_tensors(out, q, k_cache, v_cache, block_tables, context_lens)
-    _ints(block_tables, context_lens)
-    if out.shape != q.shape:
-        raise ValueError("out must be shaped like q")
     shape, q_len = _multi_shape(q, k_cache, block_tables, out.dtype)
     lib = _load()
     if workspace is None:
@@ -291,14 +327,19 @@ def append_kv(k_cache, v_cache, k_new, v_new, block_tables, positions, stream=No
     """Write each sequence's new token ([B, Hkv, D] k_new / v_new) into its
     cache slot at ``positions[b]``; negative positions and masked entries
     write nothing."""
-    _dev_tensors(k_cache, v_cache, k_new, v_new, block_tables, positions)
+    if k_cache.dim() != 4 or tuple(v_cache.shape) != tuple(k_cache.shape):
+        raise ValueError("k_cache and v_cache must both be [num_blocks, block_size, "
+                         "num_kv_heads, head_dim]")
+    if v_cache.dtype != k_cache.dtype or k_new.dtype != k_cache.dtype or v_new.dtype != k_cache.dtype:
+        raise TypeError("new keys/values and both caches must have one dtype")
+    if block_tables.dim() != 2 or positions.dim() != 1 or positions.numel() != block_tables.shape[0]:
+        raise ValueError("block_tables must be [batch, max_blocks_per_seq], positions [batch]")
     _ints(block_tables, positions)
-    if k_new.dtype != k_cache.dtype or v_new.dtype != v_cache.dtype:
-        raise TypeError("new keys/values must have the cache's dtype")
     B = block_tables.shape[0]
     NB, bs, Hkv, D = k_cache.shape
     if tuple(k_new.shape) != (B, Hkv, D) or tuple(v_new.shape) != (B, Hkv, D):
         raise ValueError("k_new/v_new must be [batch, num_kv_heads, head_dim]")
+    _dev_tensors(k_cache, v_cache, k_new, v_new, block_tables, positions)
     shape = _Shape(B, Hkv, Hkv, D, bs, block_tables.shape[1], NB, _dtype_code(k_cache.dtype), F32)
     _check(_load().pa_append_kv(k_cache.data_ptr(), v_cache.data_ptr(), k_new.data_ptr(),
                                 v_new.data_ptr(), block_tables.data_ptr(), positions.data_ptr(),
@@ -308,10 +349,13 @@ def append_kv(k_cache, v_cache, k_new, v_new, block_tables, positions, stream=No
 def resolve_blocks(out_phys, block_tables, context_lens, block_size: int, num_blocks: int,
                    stream=None):
     """Physical block the kernels read for each (sequence, logical page); -1 if none."""
-    _dev_tensors(out_phys, block_tables, context_lens)
-    _ints(block_tables, context_lens)
     if out_phys.dtype != torch.int32 or out_phys.shape != block_tables.shape:
         raise ValueError("out_phys must be int32 shaped like block_tables")
+    if block_tables.dim() != 2 or context_lens.dim() != 1 or \
+            context_lens.numel() != block_tables.shape[0]:
+        raise ValueError("block_tables must be [batch, max_blocks_per_seq], context_lens [batch]")
+    _ints(block_tables, context_lens)
+    _dev_tensors(out_phys, block_tables, context_lens)
     B, mb = block_tables.shape
     shape = _Shape(B, 1, 1, 64, int(block_size), mb, int(num_blocks), F16, F32)
     _check(_load().pa_resolve_blocks(out_phys.data_ptr(), block_tables.data_ptr(),
@@ -331,3 +375,13 @@ def device_error(stream=None) -> int:
     code = ctypes.c_int32(0)
     _check(_load().pa_device_error(ctypes.byref(code), _stream_ptr(stream)), "pa_device_error")
     return int(code.value)
+
+
+def set_switch(which: int, value: int):
+    """Set a test / tuning switch (SWITCH_MULTI_KERNEL: KERNEL_AUTO, KERNEL_MMA or
+    KERNEL_TILE; SWITCH_TILE_COMPACT_Q: 1 or 0) for every later call."""
+    _check(_load().pa_set_switch(int(which), int(value)), "pa_set_switch")
+
+
+def get_switch(which: int) -> int:
+    return int(_load().pa_get_switch(int(which)))

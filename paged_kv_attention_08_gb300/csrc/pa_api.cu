@@ -39,6 +39,48 @@ std::atomic<void*> g_noalloc_scratch[kMaxDevices];
 std::once_flag g_encode_once;
 PFN_cuTensorMapEncodeTiled_v12000 g_encode = nullptr;
 
+// Tuning and test switches.  The environment is read once, when the library
+// is loaded (static initialisation), never by a call:
+//   PA_TUNE_STREAMS, PA_TUNE_STAGES  warp-level kernel's streams per CTA and
+//                                    stages per stream
+//   PA_NO_PDL=1                      launch without programmatic dependent launch
+//   PA_NO_CLUSTER=1                  never reduce partitions inside a cluster
+//   PA_BALANCED=1|2                  let the automatic plan pick the balanced split
+//   PA_MULTI_KERNEL=mma|tile         initial value of PA_SWITCH_MULTI_KERNEL
+//   PA_TILE_COMPACT_Q=0              initial value of PA_SWITCH_TILE_COMPACT_Q
+// The last two can also be changed at run time through pa_set_switch.  None
+// changes a result beyond rounding order.
+int env_value(const char* name, int fallback, int (*parse)(const char*)) {
+    const char* v = std::getenv(name);
+    return (v && *v) ? parse(v) : fallback;
+}
+int parse_positive(const char* v) {
+    const int x = std::atoi(v);
+    return x > 0 ? x : 0;
+}
+int parse_flag(const char* v) { return std::atoi(v) > 0 ? 1 : 0; }
+int parse_balanced(const char* v) {
+    const int x = std::atoi(v);
+    return x < 0 ? 0 : (x > 2 ? 2 : x);
+}
+int parse_kernel(const char* v) {
+    if (std::strcmp(v, "tile") == 0) return PA_KERNEL_TILE;
+    if (std::strcmp(v, "mma") == 0) return PA_KERNEL_MMA;
+    return PA_KERNEL_AUTO;
+}
+int parse_compact(const char* v) { return std::atoi(v) == 0 ? 0 : 1; }
+
+struct LoadTimeEnv {
+    int tune_streams, tune_stages, no_pdl, no_cluster, balanced;
+};
+const LoadTimeEnv g_env = {env_value("PA_TUNE_STREAMS", 0, parse_positive),
+                           env_value("PA_TUNE_STAGES", 0, parse_positive),
+                           env_value("PA_NO_PDL", 0, parse_flag),
+                           env_value("PA_NO_CLUSTER", 0, parse_flag),
+                           env_value("PA_BALANCED", 0, parse_balanced)};
+std::atomic<int> g_switch_multi_kernel{env_value("PA_MULTI_KERNEL", PA_KERNEL_AUTO, parse_kernel)};
+std::atomic<int> g_switch_compact_q{env_value("PA_TILE_COMPACT_Q", 1, parse_compact)};
+
 int elem_size(int dtype) { return dtype == PA_F32 ? 4 : 2; }
 
 bool aligned(const void* ptr, size_t a) { return reinterpret_cast<uintptr_t>(ptr) % a == 0; }
@@ -144,13 +186,6 @@ struct Tune {
     int nh, nt, ns;
 };
 
-int env_int(const char* name, int fallback) {
-    const char* s = std::getenv(name);
-    if (!s || !*s) return fallback;
-    const int v = std::atoi(s);
-    return v > 0 ? v : fallback;
-}
-
 Tune pick_tune(const pa_shape* s, bool many_ctas) {
     Tune t;
     t.nh = s->head_dim == 256 ? 2 : 1;
@@ -167,10 +202,8 @@ Tune pick_tune(const pa_shape* s, bool many_ctas) {
         t.ns = 2;
         while (t.nt > 1 && (uint32_t)t.nt * t.ns * stage > 200u * 1024u) --t.nt;
     }
-    static const int env_nt = env_int("PA_TUNE_STREAMS", 0);
-    static const int env_ns = env_int("PA_TUNE_STAGES", 0);
-    if (env_nt > 0 && env_nt * t.nh <= 8) t.nt = env_nt;
-    if (env_ns > 0 && env_ns <= 16) t.ns = env_ns;
+    if (g_env.tune_streams > 0 && g_env.tune_streams * t.nh <= 8) t.nt = g_env.tune_streams;
+    if (g_env.tune_stages > 0 && g_env.tune_stages <= 16) t.ns = g_env.tune_stages;
     // never ask for more shared memory than a CTA may have
     while (t.ns > 1 && attn_smem_layout(s->head_dim, s->block_size, t.nt, t.ns).total +
                                kSmemAlignSlack > 227u * 1024u)
@@ -191,10 +224,7 @@ int ctas_per_sm(const pa_shape* s, const Tune& t) {
 
 // Programmatic dependent launch lets each kernel's launch overlap the tail
 // of the previous one in the stream; PA_NO_PDL=1 launches plainly instead.
-bool use_pdl() {
-    static const bool off = std::getenv("PA_NO_PDL") && std::atoi(std::getenv("PA_NO_PDL")) > 0;
-    return !off;
-}
+bool use_pdl() { return !g_env.no_pdl; }
 
 
 int pages_for(const pa_shape* s, int32_t max_context_len) {
@@ -254,15 +284,7 @@ Plan plan_with(const pa_shape* s, int pages, int pp, bool cluster_ok,
 // the idle SMs); PA_BALANCED=1 lets it pick the balanced split where equal
 // partitions leave SMs idle, PA_BALANCED=2 wherever the batch allows.  A
 // tuning switch; results agree.
-int balanced_mode() {
-    static const int m = [] {
-        const char* v = std::getenv("PA_BALANCED");
-        if (!v || !*v) return 0;
-        const int x = std::atoi(v);
-        return x < 0 ? 0 : (x > 2 ? 2 : x);
-    }();
-    return m;
-}
+int balanced_mode() { return g_env.balanced; }
 
 Plan balanced_plan(const pa_shape* s, int pages, int num_sms) {
     Plan p = plan_with(s, pages, pages, false);
@@ -370,23 +392,21 @@ Plan auto_plan(const pa_shape* s, int32_t max_context_len, int num_sms, int q_ch
 
 // PA_NO_CLUSTER=1 turns the in-cluster reduction off (partitions then always
 // go through the workspace); a tuning switch, results are the same.
-bool clusters_enabled() {
-    static const bool off = std::getenv("PA_NO_CLUSTER") && std::atoi(std::getenv("PA_NO_CLUSTER")) > 0;
-    return !off;
-}
+bool clusters_enabled() { return !g_env.no_cluster; }
 
 // Which kernel serves several query tokens: the tcgen05 tile kernel once
 // the rows of a (sequence, kv head) -- q_len * group -- exceed the 16 rows
 // of the warp-level MMA path (which would otherwise read the pages once per
-// 16 rows), and for 16 rows at head_dim 256.  PA_MULTI_KERNEL=mma forces the warp-level path for every
-// q_len > 1, =tile the tile kernel for every split-KV call, one query token
-// included (a testing and tuning switch; read on every call, results agree).
+// 16 rows), and for 16 rows at head_dim 256.  The PA_SWITCH_MULTI_KERNEL
+// switch forces the warp-level path for every q_len > 1 (PA_KERNEL_MMA) or
+// the tile kernel for every split-KV call, one query token included
+// (PA_KERNEL_TILE); results agree.
 bool use_tile(const pa_shape* s, int32_t q_len, int32_t partition_tokens) {
     const int64_t rows = (int64_t)q_len * (s->num_heads / s->num_kv_heads);
     if (partition_tokens == PA_PARTITION_BALANCED && rows <= 16) return false;  // honoured there
-    const char* v = std::getenv("PA_MULTI_KERNEL");
-    if (v && std::strcmp(v, "tile") == 0) return true;
-    if (v && std::strcmp(v, "mma") == 0 && q_len > 1) return false;
+    const int force = g_switch_multi_kernel.load(std::memory_order_relaxed);
+    if (force == PA_KERNEL_TILE) return true;
+    if (force == PA_KERNEL_MMA && q_len > 1) return false;
     // 16 rows at head_dim 256 too: the warp-level path needs two warps per
     // page there and spills registers; the tile kernel was 6-23 % faster
     return rows > 16 || (rows == 16 && s->head_dim == 256);
@@ -394,11 +414,10 @@ bool use_tile(const pa_shape* s, int32_t q_len, int32_t partition_tokens) {
 
 // Q rows the tile kernel stages: 16 at head_dim 256 when a unit has at most 16
 // rows (its other 112 would be zeros), which buys a third stage per K / V
-// ring; otherwise a whole tile.  PA_TILE_COMPACT_Q=0 stages whole tiles
-// always (a tuning switch, read on every call; results agree).
+// ring; otherwise a whole tile.  PA_SWITCH_TILE_COMPACT_Q = 0 stages whole
+// tiles always (results agree).
 int tile_q_rows(const pa_shape* s, int32_t q_len) {
-    const char* v = std::getenv("PA_TILE_COMPACT_Q");
-    if (v && std::atoi(v) == 0) return kTileRows;
+    if (g_switch_compact_q.load(std::memory_order_relaxed) == 0) return kTileRows;
     const int64_t rows = (int64_t)q_len * (s->num_heads / s->num_kv_heads);
     return s->head_dim == 256 && rows <= kTileCompactQRows ? kTileCompactQRows : kTileRows;
 }
@@ -778,6 +797,29 @@ pa_status launch_tile(void* out, const void* q, const void* k, const void* v, co
 using namespace pa;
 
 extern "C" {
+
+pa_status pa_set_switch(int32_t which, int32_t value) {
+    switch (which) {
+        case PA_SWITCH_MULTI_KERNEL:
+            if (value != PA_KERNEL_AUTO && value != PA_KERNEL_MMA && value != PA_KERNEL_TILE)
+                return PA_ERR_INVALID_ARG;
+            g_switch_multi_kernel.store(value, std::memory_order_relaxed);
+            return PA_OK;
+        case PA_SWITCH_TILE_COMPACT_Q:
+            if (value != 0 && value != 1) return PA_ERR_INVALID_ARG;
+            g_switch_compact_q.store(value, std::memory_order_relaxed);
+            return PA_OK;
+    }
+    return PA_ERR_INVALID_ARG;
+}
+
+int32_t pa_get_switch(int32_t which) {
+    switch (which) {
+        case PA_SWITCH_MULTI_KERNEL: return g_switch_multi_kernel.load(std::memory_order_relaxed);
+        case PA_SWITCH_TILE_COMPACT_Q: return g_switch_compact_q.load(std::memory_order_relaxed);
+    }
+    return -1;
+}
 
 const char* pa_status_string(pa_status status) {
     switch (status) {

@@ -278,3 +278,125 @@ def test_explicit_plans_and_workspace_sizes_agree(lib):
         if ws:
             rows = B * G * Hkv * q_len * parts
             assert ws == (rows * D * 4 + 255) // 256 * 256 + rows * 2 * 4
+
+
+def _binding_args(**over):
+    """A consistent set of (CPU) tensors for one decode call, with some replaced."""
+    a = dict(out=torch.zeros(2, 32, 128), q=torch.zeros(2, 32, 128, dtype=torch.float16),
+             k_cache=torch.zeros(8, 16, 8, 128, dtype=torch.float16),
+             v_cache=torch.zeros(8, 16, 8, 128, dtype=torch.float16),
+             block_tables=torch.zeros(2, 4, dtype=torch.int32),
+             context_lens=torch.zeros(2, dtype=torch.int32))
+    a.update(over)
+    return a
+
+
+MISMATCHES = {
+    "v_cache_shape": dict(v_cache=torch.zeros(8, 16, 8, 64, dtype=torch.float16)),
+    "v_cache_blocks": dict(v_cache=torch.zeros(4, 16, 8, 128, dtype=torch.float16)),
+    "v_cache_dtype": dict(v_cache=torch.zeros(8, 16, 8, 128, dtype=torch.bfloat16)),
+    "q_dtype": dict(q=torch.zeros(2, 32, 128, dtype=torch.bfloat16)),
+    "q_float32": dict(q=torch.zeros(2, 32, 128)),
+    "q_head_dim": dict(q=torch.zeros(2, 32, 64, dtype=torch.float16),
+                       out=torch.zeros(2, 32, 64)),
+    "out_shape": dict(out=torch.zeros(2, 16, 128)),
+    "out_dtype": dict(out=torch.zeros(2, 32, 128, dtype=torch.bfloat16)),
+    "tables_rows": dict(block_tables=torch.zeros(3, 4, dtype=torch.int32)),
+    "lens_rows": dict(context_lens=torch.zeros(3, dtype=torch.int32)),
+    "lens_dtype": dict(context_lens=torch.zeros(2, dtype=torch.int64)),
+    "tables_dim": dict(block_tables=torch.zeros(8, dtype=torch.int32)),
+}
+
+
+@pytest.mark.parametrize("name", sorted(MISMATCHES))
+@pytest.mark.parametrize("entry", ["decode", "decode_splitkv", "decode_splitkv_noalloc"])
+def test_binding_refuses_mismatched_tensors(name, entry):
+    """Every shape or dtype the library takes on trust is checked by the
+    binding before anything reaches the device: the error is the mismatch,
+    not the CPU placement of these tensors."""
+    a = _binding_args(**MISMATCHES[name])
+    fn = getattr(pa, entry)
+    extra = () if entry == "decode" else (64,)
+    with pytest.raises((ValueError, TypeError)) as e:
+        fn(a["out"], a["q"], a["k_cache"], a["v_cache"], a["block_tables"], a["context_lens"],
+           0.1, *extra)
+    assert "CUDA" not in str(e.value)
+
+
+def test_binding_refuses_mismatched_multi_token_tensors():
+    a = _binding_args(q=torch.zeros(2, 3, 32, 128, dtype=torch.float16), out=torch.zeros(2, 3, 32, 128))
+    for over in (dict(out=torch.zeros(2, 2, 32, 128)),
+                 dict(v_cache=torch.zeros(8, 16, 8, 128, dtype=torch.bfloat16)),
+                 dict(q=torch.zeros(2, 32, 128, dtype=torch.float16))):
+        b = dict(a, **over)
+        with pytest.raises((ValueError, TypeError)) as e:
+            pa.decode_multi(b["out"], b["q"], b["k_cache"], b["v_cache"], b["block_tables"],
+                            b["context_lens"], 0.1, 64)
+        assert "CUDA" not in str(e.value)
+
+
+def test_binding_refuses_mismatched_append_and_resolve():
+    kc = torch.zeros(8, 16, 8, 128, dtype=torch.float16)
+    new = torch.zeros(2, 8, 128, dtype=torch.float16)
+    bt = torch.zeros(2, 4, dtype=torch.int32)
+    pos = torch.zeros(2, dtype=torch.int32)
+    for args in ((kc, torch.zeros(8, 16, 8, 64, dtype=torch.float16), new, new, bt, pos),
+                 (kc, kc.clone(), new, new.to(torch.bfloat16), bt, pos),
+                 (kc, kc.clone(), new, new, bt, torch.zeros(3, dtype=torch.int32)),
+                 (kc, kc.clone(), new[:, :4], new, bt, pos)):
+        with pytest.raises((ValueError, TypeError)) as e:
+            pa.append_kv(*args)
+        assert "CUDA" not in str(e.value)
+    with pytest.raises(ValueError) as e:
+        pa.resolve_blocks(torch.zeros(2, 4, dtype=torch.int32), bt,
+                          torch.zeros(3, dtype=torch.int32), 16, 8)
+    assert "CUDA" not in str(e.value)
+
+
+def test_consistent_cpu_tensors_reach_the_device_check():
+    """The validator accepts a consistent set: what stops these CPU tensors is
+    the placement check."""
+    a = _binding_args()
+    with pytest.raises(ValueError, match="CUDA"):
+        pa.decode(a["out"], a["q"], a["k_cache"], a["v_cache"], a["block_tables"],
+                  a["context_lens"], 0.1)
+
+
+def test_switches_set_and_restore(lib):
+    """The test switches are set through the library (no environment read per
+    call); unknown switches and values are refused."""
+    k0 = pa.get_switch(pa.SWITCH_MULTI_KERNEL)
+    c0 = pa.get_switch(pa.SWITCH_TILE_COMPACT_Q)
+    try:
+        pa.set_switch(pa.SWITCH_MULTI_KERNEL, pa.KERNEL_TILE)
+        assert pa.get_switch(pa.SWITCH_MULTI_KERNEL) == pa.KERNEL_TILE
+        pa.set_switch(pa.SWITCH_TILE_COMPACT_Q, 0)
+        assert pa.get_switch(pa.SWITCH_TILE_COMPACT_Q) == 0
+        with pytest.raises(pa.PaError):
+            pa.set_switch(pa.SWITCH_MULTI_KERNEL, 7)
+        with pytest.raises(pa.PaError):
+            pa.set_switch(pa.SWITCH_TILE_COMPACT_Q, 2)
+        with pytest.raises(pa.PaError):
+            pa.set_switch(9, 0)
+        assert lib.pa_get_switch(9) == -1
+        # the kernel switch reaches the plan: 4 rows per kv head on the tile kernel
+        s = shape(batch=4, max_blocks_per_seq=256)
+        d = pa._PlanDesc()
+        assert lib.pa_plan_info(ctypes.byref(s), 1, 4096, 512, ctypes.byref(d)) == 0
+        assert d.kernel == 1
+        pa.set_switch(pa.SWITCH_MULTI_KERNEL, pa.KERNEL_AUTO)
+        assert lib.pa_plan_info(ctypes.byref(s), 1, 4096, 512, ctypes.byref(d)) == 0
+        assert d.kernel == 0
+    finally:
+        pa.set_switch(pa.SWITCH_MULTI_KERNEL, k0)
+        pa.set_switch(pa.SWITCH_TILE_COMPACT_Q, c0)
+
+
+def test_library_reads_no_environment_per_call():
+    """The library's source reads the environment only in its load-time
+    initialisers."""
+    src = open(os.path.join(ROOT, "paged_kv_attention_08_gb300", "csrc", "pa_api.cu")).read()
+    assert src.count("getenv") == 1          # inside env_value, used by namespace-scope initialisers
+    for f in glob.glob(os.path.join(ROOT, "paged_kv_attention_08_gb300", "csrc", "*")):
+        if not f.endswith("pa_api.cu"):
+            assert "getenv" not in open(f).read(), f

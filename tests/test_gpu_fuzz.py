@@ -133,12 +133,9 @@ def check(got, want, out_q, dtype):
 
 
 @pytest.mark.parametrize("seed", range(N_CASES), ids=lambda s: f"case{s}")
-def test_random_case_vs_oracle(seed, monkeypatch):
+def test_random_case_vs_oracle(seed, switches):
     c = draw(seed)
-    if c["kernel"] == "auto":
-        monkeypatch.delenv("PA_MULTI_KERNEL", raising=False)
-    else:
-        monkeypatch.setenv("PA_MULTI_KERNEL", c["kernel"])
+    switches(kernel=c["kernel"])
     q, kc, vc, bt, lens, scale, max_ctx = make_inputs(seed, c)
     if c["q_len"] == 1 and c["entry"] != "multi":
         want = oracle.decode(q[:, 0].contiguous(), kc, vc, bt, lens, scale)

@@ -4,7 +4,7 @@ through the C ABI, against the fp64 oracle.
 Bar: max |gpu - oracle| <= 2e-3 on fp32 output, as for the one-token decode.
 Covered, on both kernels that serve several query tokens (the warp-level MMA
 path with up to 16 rows per CTA, and the tcgen05 tile kernel with 128-row
-tiles; PA_MULTI_KERNEL forces one of them): every group size with q_len up to
+tiles; the kernel switch forces one of them): every group size with q_len up to
 and past 16 and 128 rows, sequences shorter than q_len (query tokens that see
 nothing), masked table entries, every split mode (one pass, cluster,
 workspace, balanced), the q-dtype output, and the full-size multi-token
@@ -27,12 +27,9 @@ DEV = "cuda:0"
 
 
 @pytest.fixture(params=["auto", "mma", "tile"])
-def kernel(request, monkeypatch):
+def kernel(request, switches):
     """Which kernel serves the calls: the library's choice, or one forced."""
-    if request.param == "auto":
-        monkeypatch.delenv("PA_MULTI_KERNEL", raising=False)
-    else:
-        monkeypatch.setenv("PA_MULTI_KERNEL", request.param)
+    switches(kernel=request.param)
     return request.param
 
 
@@ -184,11 +181,11 @@ def test_multi_token_full_size_sampled(name, kernel):
         check(got[rows[:, 0], i, rows[:, 1]], want)
 
 
-def test_tile_kernel_poison_and_permutation(monkeypatch):
+def test_tile_kernel_poison_and_permutation(switches):
     """Tile kernel: NaN in every unreferenced block and in the slots past each
     context leaves the output bit-identical; so does a permutation of the pool
     with the table remapped."""
-    monkeypatch.setenv("PA_MULTI_KERNEL", "tile")
+    switches(kernel="tile")
     x = multi_case(23, 3, 20, 16, 2, 128, 16, [30, 250, 77], spare=6)
     xd = x.to(DEV)
     base = run(xd, 0)
@@ -219,12 +216,12 @@ def test_tile_kernel_poison_and_permutation(monkeypatch):
 
 
 @pytest.mark.parametrize("Q,H,Hkv", [(1, 16, 1), (2, 16, 2)], ids=["mqa_q1", "g8_q2"])
-def test_tile_compact_q_tile(monkeypatch, Q, H, Hkv):
+def test_tile_compact_q_tile(switches, Q, H, Hkv):
     """Units of at most 16 rows at head_dim 256 stage a compact Q tile (the
     MMA's other rows read what follows it): exact against the oracle, bit-
     identical to whole 128-row Q tiles, and unchanged by NaN in every
     unreferenced block, in one pass and in cluster / workspace splits."""
-    monkeypatch.delenv("PA_MULTI_KERNEL", raising=False)
+    switches(kernel="auto")
     x = multi_case(29, 3, Q, H, Hkv, 256, 32, [70, 1000, 5], spare=6)
     want = oracle_of(x)
     xd = x.to(DEV)
@@ -238,10 +235,10 @@ def test_tile_compact_q_tile(monkeypatch, Q, H, Hkv):
     xp = workloads.Inputs(x.spec, xd.q, k, v, xd.block_tables, xd.context_lens, x.scale,
                           x.max_context_len, x.lens_host)
     for pt in [0, 32 * 32, 4 * 32]:
-        monkeypatch.setenv("PA_TILE_COMPACT_Q", "1")
+        switches(compact_q=1)
         compact = run(xd, pt)
         check(compact, want)
         assert torch.equal(run(xp, pt), compact)
-        monkeypatch.setenv("PA_TILE_COMPACT_Q", "0")
+        switches(compact_q=0)
         assert torch.equal(run(xd, pt), compact)
     assert pa.device_error() == 0

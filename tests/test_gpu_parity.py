@@ -424,14 +424,11 @@ EXACT_WS = [(8, u) for u in (8, 15, 16, 19, 20)] + [(4, u) for u in (32, 36, 37,
 
 @pytest.mark.parametrize("parts,units", EXACT_WS, ids=lambda v: str(v))
 @pytest.mark.parametrize("kernel", ["auto", "tile"])
-def test_workspace_size_is_exact_for_explicit_splits(parts, units, kernel, monkeypatch):
+def test_workspace_size_is_exact_for_explicit_splits(parts, units, kernel, switches):
     """An explicit partition count: a workspace of exactly the reported size
     (none when it is 0) serves the call, whose reduction is the one plan_info
     reports; exact against the oracle."""
-    if kernel == "tile":
-        monkeypatch.setenv("PA_MULTI_KERNEL", "tile")
-    else:
-        monkeypatch.delenv("PA_MULTI_KERNEL", raising=False)
+    switches(kernel=kernel)
     T = parts * 4 * 16
     x = random_case(31, B=units, H=4, Hkv=1, D=128, bs=16, lens=[T] * units,
                     dtype=torch.float16, spare=0, mb_extra=0)
