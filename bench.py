@@ -1,10 +1,10 @@
 """Benchmark of paged-attention decode on GB300.
 
 One step = one decode call for each workload of the chosen group (default:
-the pages' sweep, (batch, ctx) in {(1,512), (16,256), (4,2048)}, 32 query /
-8 kv heads, head_dim 128, block_size 16, fp16), each through
-``pa_decode_splitkv`` with the automatic partition choice (which runs the
-single pass when one partition suffices).  Inputs rotate among enough
+the long-context split-KV group, batch in {1, 4} x context in {8192, 32768,
+131072}, 32 query / 8 kv heads, head_dim 128, block_size 16, bf16), each
+through ``pa_decode_splitkv`` with the automatic partition choice (which runs
+the single pass when one partition suffices).  Inputs rotate among enough
 independent seeded sets that every step reads from HBM, not L2.  The step is
 captured once per input set as a CUDA graph and replayed, so host launch
 overhead does not pace the GPU.  Multi-token workloads (``--workload multi``:
@@ -123,6 +123,16 @@ def reduce_max(value: float, device) -> float:
     t = torch.tensor([value], dtype=torch.float64, device=device)
     dist.all_reduce(t, op=dist.ReduceOp.MAX)
     return float(t.item())
+
+
+def reduce_max_list(values, device):
+    """Element-wise max over ranks of a list of floats (identity for one process)."""
+    import torch.distributed as dist
+    if not (dist.is_available() and dist.is_initialized()):
+        return list(values)
+    t = torch.tensor(values, dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return t.tolist()
 
 
 def reduce_sum(value: float, device) -> float:
@@ -290,6 +300,17 @@ def describe(group):
     return f"{group}: {head}: " + "; ".join(f"{case(s)} {shape(s)}" for s in specs) + "; fp32 out"
 
 
+def bench_config(args):
+    """The ``config`` object of the JSON line, identical for both arms: what
+    workload is measured, with which split, and how L2 is kept out."""
+    pt = args.partition_tokens
+    return {"workload": describe(args.workload),
+            "partition_tokens": ("automatic" if pt == 0 else
+                                 "each workload's own" if pt < 0 else pt),
+            "l2": "inputs rotate over independent seeded sets totalling more than 3x L2, "
+                  "so every step reads HBM"}
+
+
 def run_reference(args):
     world, rank, _ = dist_env()
     if rank != 0:
@@ -313,8 +334,7 @@ def run_reference(args):
     line = {"impl": "reference", "metric": METRIC, "value": gbs, "unit": "GB/s", "n_gpus": 1,
             "steps": args.steps, "warmup": args.warmup, "ms_per_step": sec * 1e3,
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
-            "data": "synthetic", "config": {"workload": describe(args.workload),
-                                            "kind": f"fp64 CPU oracle, {used} host threads"},
+            "data": "synthetic", "config": bench_config(args),
             "cpu_baseline": {"value": gbs, "unit": "GB/s", "cores": used, "kind": "oracle",
                              "sample": sample, "cpu_model": oracle.cpu_model()},
             "e2e": {"value": gbs, "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
@@ -328,9 +348,12 @@ def main(argv=None):
     ap.add_argument("--steps", type=int, default=2000)
     ap.add_argument("--warmup", type=int, default=50)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
-    ap.add_argument("--workload", choices=sorted(workloads.GROUPS), default="sweep")
-    ap.add_argument("--partition-tokens", type=int, default=-1,
-                    help="split-KV partition size; -1 = each workload's own (0/auto unless stated)")
+    ap.add_argument("--workload", choices=sorted(workloads.GROUPS), default="long")
+    ap.add_argument("--partition-tokens", type=int, default=0,
+                    help="split-KV partition size in tokens; 0 = the library's automatic choice; "
+                         "-1 = each workload's own (512 tokens for the long group)")
+    ap.add_argument("--regions", type=int, default=7,
+                    help="timed regions of --steps steps each; the line reports their median")
     ap.add_argument("--no-graph", action="store_true", help="launch eagerly instead of graph replay")
     ap.add_argument("--graph-per-step", action="store_true",
                     help="replay one graph per step instead of one per loop over the input sets")
@@ -379,12 +402,14 @@ def main(argv=None):
         # every rotated set has its own longest context, hence its own plan
         need = max(workspace_bytes(pa, st[i], pts[i]) for st in sets)
         ws.append(torch.empty(max(need, 16), dtype=torch.uint8, device=dev))
-    splits = [ws[i].numel() > 16 for i in range(len(set0))]      # partials combined by a 2nd kernel
-    launches_per_step = sum(2 if s else 1 for s in splits) + (len(set0) if args.with_append else 0)
     sms = props.multi_processor_count
     # the library's own description of each call's plan on this device
     plans = {names[i]: pa.plan_info(x.q, x.k_cache, x.block_tables, x.max_context_len, pts[i])
              for i, x in enumerate(set0)}
+    # kernels per call: the attention kernel, plus the combine kernel when the
+    # partials go through the workspace
+    launches_per_step = sum(2 if p["reduce"] in ("workspace+combine kernel", "balanced split")
+                            else 1 for p in plans.values()) + (len(set0) if args.with_append else 0)
 
     stream = torch.cuda.Stream(device=dev)
 
@@ -478,24 +503,29 @@ def main(argv=None):
                 for _ in range(3):
                     loop_graph.replay()
             stream.synchronize()
-            barrier()
-            torch.cuda.synchronize()
-            e0 = torch.cuda.Event(enable_timing=True)
-            e1 = torch.cuda.Event(enable_timing=True)
-            e0.record(stream)
-            k = 0
-            if loop_graph is not None:      # whole loops of the nsets steps
-                while k + nsets <= args.steps:
-                    loop_graph.replay()
-                    k += nsets
-            while k < args.steps:           # the rest, one step graph each
-                step(k, stream)
-                k += 1
-            e1.record(stream)
-            e1.synchronize()
-            torch.cuda.synchronize()
-            barrier()
-            ms_total = e0.elapsed_time(e1)
+            # --regions timed regions of exactly --steps steps each, every one
+            # bracketed by a barrier and a device synchronize; the line reports
+            # the median region (max over ranks per region)
+            region_ms = []
+            for _ in range(max(1, args.regions)):
+                barrier()
+                torch.cuda.synchronize()
+                e0 = torch.cuda.Event(enable_timing=True)
+                e1 = torch.cuda.Event(enable_timing=True)
+                e0.record(stream)
+                k = 0
+                if loop_graph is not None:      # whole loops of the nsets steps
+                    while k + nsets <= args.steps:
+                        loop_graph.replay()
+                        k += nsets
+                while k < args.steps:           # the rest, one step graph each
+                    step(k, stream)
+                    k += 1
+                e1.record(stream)
+                e1.synchronize()
+                torch.cuda.synchronize()
+                barrier()
+                region_ms.append(e0.elapsed_time(e1))
 
             # per-call durations: one graph per workload that runs its call on the
             # input sets in turn, at least 8 calls back to back (the sets together
@@ -533,7 +563,8 @@ def main(argv=None):
                         acc[i].append(a.elapsed_time(b) / calls_per_graph)
     clk = clocks.summary() if rank == 0 else None
 
-    ms_step = reduce_max(ms_total, dev) / args.steps
+    region_ms = reduce_max_list(region_ms, dev)
+    ms_step = statistics.median(region_ms) / args.steps
     total_bytes = reduce_sum(float(step_bytes), dev)
     value = total_bytes / (ms_step * 1e-3) / 1e9
     peak, peak_kind = hbm_peak()
@@ -552,6 +583,8 @@ def main(argv=None):
     dom_tflops = dom_flops / (call_us[dom] * 1e-6) / 1e12
     tensor_bound = dom_flops / dom_bytes > tpeak * 1e12 / (peak * 1e9)
     per_call_rates = {n: {"GB/s": round(algorithmic_bytes(x) / (u * 1e-6) / 1e9, 1),
+                          "frac_of_measured_hbm": round(algorithmic_bytes(x) / (u * 1e-6) / 1e9
+                                                        / peak, 4),
                           "TFLOP/s": round(algorithmic_flops(x) / (u * 1e-6) / 1e12, 2)}
                       for n, x, u in zip(names, set0, call_us)}
 
@@ -635,16 +668,20 @@ def main(argv=None):
 
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        # whole steps of the group on all host threads for >= 10 s; one thread
+        # on a bounded sample: the group's smallest call, repeated for >= 5 s
         import oracle
         host = [x.to("cpu") for x in set0]
         sec, n, used = time_oracle(host, min_s=10.0, threads=oracle.host_threads())
-        sec1, n1, _ = time_oracle(host, min_s=5.0, threads=1)
+        small = min(range(len(host)), key=lambda i: algorithmic_bytes(host[i]))
+        sec1, n1, _ = time_oracle([host[small]], min_s=5.0, threads=1)
         cpu = {"value": step_bytes / sec / 1e9, "unit": "GB/s", "cores": used, "kind": "oracle",
                "sample": f"{n} whole steps of the {args.workload} group (input set 0), "
                          f"fp64 oracle on {used} host threads, {sec * 1e3:.1f} ms/step",
                "cpu_model": oracle.cpu_model(),
-               "single_thread": {"value": step_bytes / sec1 / 1e9, "unit": "GB/s",
-                                 "ms_per_step": sec1 * 1e3, "steps": n1}}
+               "single_thread": {"value": algorithmic_bytes(host[small]) / sec1 / 1e9,
+                                 "unit": "GB/s", "ms_per_call": sec1 * 1e3, "calls": n1,
+                                 "sample": f"the {names[small]} call, whole"}}
 
     if rank == 0:
         line = {
@@ -652,9 +689,11 @@ def main(argv=None):
             "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms_step,
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f32",
             "data": "synthetic",
-            "config": {
-                "workload": describe(args.workload),
+            "config": bench_config(args),
+            "detail": {
                 "us_per_step": ms_step * 1e3,
+                "region_us_per_step": [round(r / args.steps * 1e3, 3) for r in region_ms],
+                "gpu_launches_per_step": launches_per_step,
                 "per_call_us": {n: round(u, 3) for n, u in zip(names, call_us)},
                 "per_call_us_hot": {n: round(statistics.median(v) * 1e3, 3)
                                     for n, v in zip(names, per_call_hot)},
@@ -674,7 +713,7 @@ def main(argv=None):
                 "parity_max_abs_err": max_err,
             },
             "e2e": e2e,
-            "gpu_launches": launches_per_step * args.steps,
+            "gpu_launches": launches_per_step * args.steps * len(region_ms),
             "roofline": ({"bound": "tensor", "achieved": dom_tflops, "peak": tpeak,
                           "unit": "TFLOP/s", "frac": dom_tflops / tpeak, "peak_kind": tpeak_kind,
                           "flops_per_launch": dom_flops}

@@ -253,11 +253,14 @@ def decode_multi(q, k_cache, v_cache, block_tables, context_lens, scale: float) 
 
 def decode_multi_mt(q, k_cache, v_cache, block_tables, context_lens, scale: float,
                     threads: int | None = None) -> tuple[np.ndarray, int]:
-    """``decode_multi``'s result computed on several host threads: the batch
-    is cut into one contiguous run of sequences per thread, each run going
-    through ``pao_decode_multi`` on its slice of q, the table and the lengths
-    (the cache is shared, read only).  For timing the oracle on all the
-    host's cores.  Returns (out, threads used)."""
+    """``decode_multi``'s result computed on several host threads, for timing
+    and for checking whole outputs quickly.  The work is cut into pieces of
+    (one sequence, a run of its query tokens): the run [i0, i1) of sequence b
+    is a multi-token decode of its own -- q_len = i1 - i0 query tokens whose
+    last sits at position T - Q + i1 - 1, i.e. a context length of
+    T - Q + i1 -- so each piece goes through ``pao_decode_multi`` unchanged
+    (same per-row arithmetic, the cache shared and read only).  Returns
+    (out, threads used)."""
     if q.dim() != 4:
         raise ValueError("q must be [batch, q_len, num_heads, head_dim]")
     B, Q, H, D = q.shape
@@ -265,24 +268,36 @@ def decode_multi_mt(q, k_cache, v_cache, block_tables, context_lens, scale: floa
                                                   context_lens)
     qa, ka, va = _u16(q), _u16(k_cache), _u16(v_cache)
     out = np.zeros((B, Q, H, D), dtype=np.float64)
-    threads = max(1, min(threads or host_threads(), B)) if B else 1
-    bounds = [B * i // threads for i in range(threads + 1)]
+    want = max(1, threads or host_threads())
+    # enough pieces that every thread gets some: split each sequence's query
+    # tokens into ceil(want / B) runs
+    runs = max(1, min(Q, -(-want // B))) if B else 1
+    pieces = [(b, Q * r // runs, Q * (r + 1) // runs) for b in range(B) for r in range(runs)]
+    pieces = [p for p in pieces if p[2] > p[1]]
+    threads = max(1, min(want, len(pieces))) if pieces else 1
     lib = _load()
     dt, sc = _dtype_code(q), float(np.float32(scale))
-    rcs = [0] * threads
+    rcs = [0] * len(pieces)
+    nxt = [0]
+    lock = threading.Lock()
 
-    def run(i):
-        lo, hi = bounds[i], bounds[i + 1]
-        if hi > lo:
-            qs = np.ascontiguousarray(qa[lo:hi])
-            bts = np.ascontiguousarray(bt[lo:hi])
-            ls = np.ascontiguousarray(lens[lo:hi])
-            o = np.zeros((hi - lo, Q, H, D), dtype=np.float64)
-            rcs[i] = lib.pao_decode_multi(_ptr(o), _ptr(qs), _ptr(ka), _ptr(va), _ptr(bts),
-                                          _ptr(ls), hi - lo, Q, H, Hkv, D, bs, mb, NB, dt, sc)
-            out[lo:hi] = o
+    def run():
+        while True:
+            with lock:
+                k = nxt[0]
+                nxt[0] += 1
+            if k >= len(pieces):
+                return
+            b, i0, i1 = pieces[k]
+            qs = np.ascontiguousarray(qa[b:b + 1, i0:i1])
+            bts = np.ascontiguousarray(bt[b:b + 1])
+            ls = np.array([int(lens[b]) - Q + i1], dtype=np.int32)
+            o = np.zeros((1, i1 - i0, H, D), dtype=np.float64)
+            rcs[k] = lib.pao_decode_multi(_ptr(o), _ptr(qs), _ptr(ka), _ptr(va), _ptr(bts),
+                                          _ptr(ls), 1, i1 - i0, H, Hkv, D, bs, mb, NB, dt, sc)
+            out[b, i0:i1] = o[0]
 
-    workers = [threading.Thread(target=run, args=(i,)) for i in range(threads)]
+    workers = [threading.Thread(target=run) for _ in range(threads)]
     for w in workers:
         w.start()
     for w in workers:

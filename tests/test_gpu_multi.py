@@ -160,25 +160,27 @@ def test_tiny_multi_workloads(name, kernel):
         check(run(x, pt), want)
 
 
+_WHOLE = {}
+
+
+def whole_oracle(name, x):
+    """The whole fp64 oracle output of a workload, on all host threads, computed
+    once per workload (the kernel choices share it)."""
+    if name not in _WHOLE:
+        h = x.to("cpu")
+        _WHOLE[name] = oracle.decode_multi_mt(h.q, h.k_cache, h.v_cache, h.block_tables,
+                                              h.context_lens, h.scale)[0]
+    return _WHOLE[name]
+
+
 @pytest.mark.parametrize("name", ["spec_b16_t2048_q4", "spec_b4_t8192_q8", "chunk_b2_t4096_q64",
                                   "prefill_b16_t2048_q256"])
-def test_multi_token_full_size_sampled(name, kernel):
-    """Full-size multi-token workloads, automatic split; sampled (b, token, head)
-    rows through the oracle's one-token decode of each token's causal prefix."""
+def test_multi_token_full_size_whole_output(name, kernel):
+    """Full-size multi-token workloads, automatic split: every element of the
+    output within 2e-3 of the whole fp64 oracle."""
     x = workloads.make(name, seed=0, device=DEV)
     got = run(x, 0)
-    assert torch.isfinite(got).all()
-    host = x.to("cpu")
-    B, Q, H, _ = host.q.shape
-    g = np.random.default_rng(1)
-    for i in sorted({0, Q - 1, int(g.integers(Q))}):
-        rows = np.array(sorted({(0, 0), (B - 1, H - 1)} |
-                               {(int(g.integers(B)), int(g.integers(H))) for _ in range(6)}),
-                        dtype=np.int32)
-        prefix = torch.clamp(host.context_lens - Q + i + 1, min=0)
-        want = oracle.decode_rows(host.q[:, i].contiguous(), host.k_cache, host.v_cache,
-                                  host.block_tables, prefix, host.scale, rows)
-        check(got[rows[:, 0], i, rows[:, 1]], want)
+    check(got, whole_oracle(name, x))
 
 
 def test_tile_kernel_poison_and_permutation(switches):

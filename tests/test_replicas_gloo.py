@@ -1,5 +1,5 @@
 """bench.py's replica aggregation across ranks, on CPU with gloo (world size 2):
-the timed region is the max over ranks and the bytes are summed."""
+each timed region is the max over ranks and the bytes are summed."""
 import os
 import socket
 import sys
@@ -28,8 +28,10 @@ def _worker(rank, world, port, q):
     cpu = torch.device("cpu")
     t = bench.reduce_max(10.0 + rank * 5.0, cpu)
     b = bench.reduce_sum(1000.0 * (rank + 1), cpu)
+    # per-region times: the max over ranks of each region, then the median
+    regions = bench.reduce_max_list([1.0 + rank, 5.0 - rank, 3.0], cpu)
     bench.barrier()
-    q.put((rank, t, b))
+    q.put((rank, t, b, tuple(regions)))
     dist.destroy_process_group()
 
 
@@ -44,10 +46,11 @@ def test_max_time_and_summed_bytes_over_two_ranks():
         p.join(120)
         assert p.exitcode == 0
     got = sorted(q.get(timeout=10) for _ in range(2))
-    assert got == [(0, 15.0, 3000.0), (1, 15.0, 3000.0)]
+    assert got == [(0, 15.0, 3000.0, (2.0, 5.0, 3.0)), (1, 15.0, 3000.0, (2.0, 5.0, 3.0))]
 
 
 def test_single_process_is_identity():
     import bench
     assert bench.reduce_max(3.5, torch.device("cpu")) == 3.5
     assert bench.reduce_sum(7.0, torch.device("cpu")) == 7.0
+    assert bench.reduce_max_list([1.0, 2.0], torch.device("cpu")) == [1.0, 2.0]

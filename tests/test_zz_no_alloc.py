@@ -5,15 +5,18 @@ plug-in only fixed input/output buffers, or a latency-critical loop may not
 afford cudaMalloc's synchronisation -- so this entry point keeps its partials
 in a fixed scratch array inside the library.  These tests call it through the
 C ABI twice in a row, on different inputs, and compare each result with the
-workspace entry point (pa_decode_splitkv) within the parity tolerance, and
-check that a call needing more scratch than the array holds is refused.
+fp64 CPU oracle and with the workspace entry point (pa_decode_splitkv), both
+within the parity tolerance, and check that a call needing more scratch than
+the array holds is refused.
 
 The file name sorts last so that a run stopping at the first failure has
 already run every other test.
 """
+import numpy as np
 import pytest
 import torch
 
+import oracle
 import paged_kv_attention_08_gb300 as pa
 from paged_kv_attention_08_gb300 import workloads
 
@@ -40,6 +43,11 @@ def test_noalloc_matches_workspace_entry_point_twice():
     for (x, _), ref, got in zip(cases, refs, gots):
         assert torch.isfinite(got).all()
         assert (got - ref).abs().max().item() <= TOL, x.spec.name
+        h = x.to("cpu")
+        want = oracle.decode_mt(h.q, h.k_cache, h.v_cache, h.block_tables, h.context_lens,
+                                h.scale)[0]
+        err = np.abs(got.double().cpu().numpy() - want).max()
+        assert err <= TOL, f"{x.spec.name}: max abs err {err:.3e} against the oracle"
     assert pa.device_error() == 0
 
 
