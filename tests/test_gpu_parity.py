@@ -273,6 +273,58 @@ def test_pool_permutation_bit_identical(mode, pt):
     assert torch.equal(run(x, mode, partition_tokens=pt), base)
 
 
+def test_workspace_takes_any_contents_and_serves_shapes_in_turn():
+    """Workspace splits need no clearing of the workspace: one workspace serves
+    calls of different shapes in turn (each call's partials land where another
+    call's were), workspaces of zeros, 0xFF bytes or random bytes, and graph
+    replays of one captured call with the output poisoned in between all give
+    the oracle's result."""
+    cases = [("long_b1_t32768", 1728), ("ragged_b64", 256), ("long_b1_t8192", 432),
+             ("sweep_b4_t2048", 128)]
+    xs = [(workloads.make(n, seed=6, device=DEV), pt) for n, pt in cases]
+    wants = []
+    for x, pt in xs:
+        info = pa.plan_info(x.q, x.k_cache, x.block_tables, x.max_context_len, pt)
+        assert info["reduce"] == "workspace+combine kernel", info
+        h = x.to("cpu")
+        wants.append(oracle.decode_mt(h.q, h.k_cache, h.v_cache, h.block_tables,
+                                      h.context_lens, h.scale)[0])
+    need = max(pa.workspace_size(x.q, x.k_cache, x.block_tables, torch.float32,
+                                 x.max_context_len, pt) for x, pt in xs)
+    g = torch.Generator(device=DEV).manual_seed(3)
+    fills = [torch.zeros(need, dtype=torch.uint8, device=DEV),
+             torch.full((need,), 0xFF, dtype=torch.uint8, device=DEV),
+             torch.randint(0, 256, (need,), generator=g, device=DEV).to(torch.uint8)]
+    for ws in fills:
+        for _ in range(2):                       # shapes in turn on one workspace
+            for (x, pt), want in zip(xs, wants):
+                out = torch.full(x.q.shape, float("nan"), dtype=torch.float32, device=DEV)
+                pa.decode_splitkv(out, x.q, x.k_cache, x.v_cache, x.block_tables,
+                                  x.context_lens, x.scale, x.max_context_len, pt, workspace=ws)
+                torch.cuda.synchronize()
+                assert_close_fp32(out, want)
+    # graph replays of one captured call, the partials poisoned in between
+    x, pt = xs[0]
+    ws = fills[2]
+    out = torch.full(x.q.shape, float("nan"), dtype=torch.float32, device=DEV)
+    st = torch.cuda.Stream()
+    with torch.cuda.stream(st):
+        pa.decode_splitkv(out, x.q, x.k_cache, x.v_cache, x.block_tables, x.context_lens,
+                          x.scale, x.max_context_len, pt, workspace=ws, stream=st)
+        st.synchronize()
+        graph = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(graph, stream=st):
+            pa.decode_splitkv(out, x.q, x.k_cache, x.v_cache, x.block_tables, x.context_lens,
+                              x.scale, x.max_context_len, pt, workspace=ws,
+                              stream=torch.cuda.current_stream())
+    for _ in range(3):
+        out.fill_(float("nan"))
+        graph.replay()
+        torch.cuda.synchronize()
+        assert_close_fp32(out, wants[0])
+    assert pa.device_error() == 0
+
+
 def test_split_count_invariance():
     x = workloads.make("long_b1_t32768", seed=5, device=DEV)
     host = x.to("cpu")
