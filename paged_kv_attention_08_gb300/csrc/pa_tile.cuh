@@ -28,11 +28,13 @@
 //     them (table reach and the row's causal limit), exchange the halves'
 //     maxima, keep the running max m and normaliser l in base-2 units,
 //     rescale O in tensor
-//     memory when the max moves by more than 2^8, and write P over S as a
-//     high and a low 16-bit part (two MMAs, ~16 significant bits), then the
-//     final O / l or the partial (m, l, O) for the combine kernel.
+//     memory when the max moves by more than 2^8, and write P over S (bf16:
+//     a high and a low 16-bit part, two MMAs, ~16 significant bits; fp16:
+//     one part, 11 bits), then the final O / l or the partial (m, l, O) for
+//     the combine kernel.
 // Units of at most 16 rows at head_dim 256 (one-token MQA) stage only those
-// rows of Q (QR = 16): the 56 KB saved give each K / V ring a third stage.
+// rows of Q (QR = 16): the 56 KB saved give each K / V ring a third stage,
+// and the MMAs run at M = 64 instead of 128.
 // Every mbarrier wait is bounded: on timeout the kernel records
 // PA_ERR_TIMEOUT, the roles stop, and tensor memory is released.
 #pragma once
@@ -60,6 +62,12 @@ __global__ void __launch_bounds__(kTileThreads, 1)
     constexpr int KSTEPS = D / 16;
     constexpr float NEG_INF = -INFINITY;
     constexpr bool kBF = std::is_same<KV, __nv_bfloat16>::value;
+    // P enters the P V MMA as 16-bit values.  bf16 keeps 8 significant bits,
+    // so P is split into a high and a low part (two MMAs, ~16 bits); fp16
+    // keeps 11, a relative rounding of at most 2^-11 per weight, and is used
+    // alone, with the normaliser summed from the rounded weights so that the
+    // result stays a weighted mean of the V rows.
+    constexpr bool kSplitP = kBF;
     constexpr uint32_t kCols = tile_tmem_cols(D);
     constexpr int NB = kTileSBufs;
     constexpr uint32_t O_COL = 0, S_COL = D;  // S buffer b at S_COL + b*BN; P (hi, lo) over it
@@ -327,8 +335,13 @@ __global__ void __launch_bounds__(kTileThreads, 1)
         // ================= MMA issuer (one lane) =================
         if (lane == 0) {
             constexpr int kType = kBF ? 1 : 0;
-            constexpr uint32_t id_s = tc::idesc_f16(kType, false, kTileRows, BN);
-            constexpr uint32_t id_o = tc::idesc_f16(kType, true, kTileRows, D);
+            // a compact Q tile (at most 16 live rows) runs the MMAs at M = 64,
+            // half the padded work of M = 128: rows 0..15 of an M = 64 result
+            // (and of an M = 64 operand in tensor memory) sit in lanes 0..15,
+            // as they do at M = 128
+            constexpr int kM = QR == kTileCompactQRows ? 64 : kTileRows;
+            constexpr uint32_t id_s = tc::idesc_f16(kType, false, kM, BN);
+            constexpr uint32_t id_o = tc::idesc_f16(kType, true, kM, D);
             const uint32_t q_base = smem_u32(smem + L.q_off);
             // Operand descriptors: a shared-memory descriptor holds (address >> 4)
             // in its low 14 bits, and every address here is below 2^18, so the
@@ -381,7 +394,7 @@ __global__ void __launch_bounds__(kTileThreads, 1)
                             const uint64_t vd = vd0 + (uint64_t)((ks * 16 * 128) >> 4);
                             tc::mma_ts(tmem + O_COL, p_hi + ks * 8, vd, id_o,
                                        (started || ks > 0) ? 1u : 0u);
-                            tc::mma_ts(tmem + O_COL, p_lo + ks * 8, vd, id_o, 1u);
+                            if (kSplitP) tc::mma_ts(tmem + O_COL, p_lo + ks * 8, vd, id_o, 1u);
                         }
                         started = true;
                     }
@@ -510,16 +523,20 @@ __global__ void __launch_bounds__(kTileThreads, 1)
                         for (int c = 0; c < 16; c += 2) {
                             const float x0 = fast_exp2(fmaf(s[c0 + c], qscale, -me));
                             const float x1 = fast_exp2(fmaf(s[c0 + c + 1], qscale, -me));
-                            l += x0 + x1;
                             const uint32_t h = Mma<KV>::pack(x0, x1);
                             float h0, h1;
                             Mma<KV>::unpack(h, h0, h1);
                             ph[c / 2] = h;
-                            pl[c / 2] = Mma<KV>::pack(x0 - h0, x1 - h1);
+                            if (kSplitP) {
+                                l += x0 + x1;
+                                pl[c / 2] = Mma<KV>::pack(x0 - h0, x1 - h1);
+                            } else {
+                                l += h0 + h1;  // the weights the MMA uses
+                            }
                         }
                         const uint32_t col = (uint32_t)(wg * BH + c0) / 2;
                         tc::st_32x32b_x8(sb + col, ph);
-                        tc::st_32x32b_x8(sb + BN / 2 + col, pl);
+                        if (kSplitP) tc::st_32x32b_x8(sb + BN / 2 + col, pl);
                     }
                 }
                 tc::wait_st();
