@@ -34,7 +34,7 @@
 //     the combine kernel.
 // Units of at most 16 rows at head_dim 256 (one-token MQA) stage only those
 // rows of Q (QR = 16): the 56 KB saved give each K / V ring a third stage,
-// and the MMAs run at M = 64 instead of 128.
+// and the MMAs run at M = 64.
 // Every mbarrier wait is bounded: on timeout the kernel records
 // PA_ERR_TIMEOUT, the roles stop, and tensor memory is released.
 #pragma once
@@ -335,10 +335,11 @@ __global__ void __launch_bounds__(kTileThreads, 1)
         // ================= MMA issuer (one lane) =================
         if (lane == 0) {
             constexpr int kType = kBF ? 1 : 0;
-            // a compact Q tile (at most 16 live rows) runs the MMAs at M = 64,
-            // half the padded work of M = 128: rows 0..15 of an M = 64 result
-            // (and of an M = 64 operand in tensor memory) sit in lanes 0..15,
-            // as they do at M = 128
+            // a compact Q tile (at most 16 live rows) runs the MMAs at M = 64:
+            // rows 0..15 of an M = 64 result (and of an M = 64 operand in
+            // tensor memory) sit in lanes 0..15, as they do at M = 128 (on
+            // GB300 the tensor pipe takes as long for M = 64 as for 128: the
+            // MMAs of a block cost the same either way)
             constexpr int kM = QR == kTileCompactQRows ? 64 : kTileRows;
             constexpr uint32_t id_s = tc::idesc_f16(kType, false, kM, BN);
             constexpr uint32_t id_o = tc::idesc_f16(kType, true, kM, D);
