@@ -44,8 +44,10 @@
  * PA_OK immediately, or return an error status and launch nothing.  A
  * PA_ERR_CUDA status means the launch itself failed.  The library allocates no
  * device memory.  Entry points may be called from several host threads; the
- * only shared state is a per-device cache of the SM count and of the device
- * error word's address.
+ * shared state is a per-device cache of the SM count, of the device error
+ * word's address and of which cluster sizes fit, per-thread caches of tensor
+ * maps, and the two test switches of pa_set_switch.  No call reads the
+ * environment (the tuning variables are read once, when the library loads).
  *
  * Supported shapes: head_dim in {64, 128, 256}; block_size in {16, 32};
  * num_heads / num_kv_heads in {1, 2, 4, 8, 16}; kv_dtype fp16 or bf16; out_dtype
