@@ -305,7 +305,8 @@ def bench_config(args):
     workload is measured, with which split, and how L2 is kept out."""
     pt = args.partition_tokens
     return {"workload": describe(args.workload),
-            "partition_tokens": ("automatic" if pt == 0 else
+            "partition_tokens": ("balanced split" if getattr(args, "balanced", False) else
+                                 "automatic" if pt == 0 else
                                  "each workload's own" if pt < 0 else pt),
             "l2": "inputs rotate over independent seeded sets totalling more than 3x L2, "
                   "so every step reads HBM"}
@@ -349,9 +350,10 @@ def main(argv=None):
     ap.add_argument("--warmup", type=int, default=50)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--workload", choices=sorted(workloads.GROUPS), default="long")
-    ap.add_argument("--partition-tokens", type=int, default=0,
+    ap.add_argument("--partition-tokens", default="0",
                     help="split-KV partition size in tokens; 0 = the library's automatic choice; "
-                         "-1 = each workload's own (512 tokens for the long group)")
+                         "-1 = each workload's own (512 tokens for the long group); "
+                         "'balanced' = the balanced split")
     ap.add_argument("--regions", type=int, default=7,
                     help="timed regions of --steps steps each; the line reports their median")
     ap.add_argument("--no-graph", action="store_true", help="launch eagerly instead of graph replay")
@@ -367,6 +369,8 @@ def main(argv=None):
                     help="keep warming up (graph replays) at least this long")
     args = ap.parse_args(argv)
     args.warmup = max(args.warmup, 3)
+    args.balanced = args.partition_tokens == "balanced"
+    args.partition_tokens = 0 if args.balanced else int(args.partition_tokens)
 
     if args.impl == "reference":
         return run_reference(args)
@@ -391,7 +395,8 @@ def main(argv=None):
     nsets = max(1, min(64, math.ceil(3 * l2 / set_bytes) + 1))
     sets = [set0] + [[workloads.make(n, seed=100 * r + rank, device=dev) for n in names]
                      for r in range(1, nsets)]
-    pts = [s.partition_tokens if args.partition_tokens < 0 else args.partition_tokens for s in specs]
+    pts = [pa.PARTITION_BALANCED if args.balanced else
+           s.partition_tokens if args.partition_tokens < 0 else args.partition_tokens for s in specs]
     if args.with_append and any(s.q_len > 1 for s in specs):
         print(json.dumps({"metric": METRIC, "error": "--with-append needs one-token workloads"}))
         return 1
@@ -719,7 +724,8 @@ def main(argv=None):
                                     for n, v in zip(names, per_call_hot)},
                 "per_call_rate": per_call_rates,
                 "algorithmic_bytes_per_step": step_bytes,
-                "partition_tokens": {n: (p if p else "auto") for n, p in zip(names, pts)},
+                "partition_tokens": {n: ("balanced" if p == pa.PARTITION_BALANCED else p if p else "auto")
+                                     for n, p in zip(names, pts)},
                 "plan": plans,
                 "l2": f"rotating {nsets} input sets of {set_bytes / 1e6:.1f} MB "
                       f"({nsets * set_bytes / 1e6:.0f} MB > 3x L2 {l2 / 1e6:.0f} MB)",

@@ -403,7 +403,10 @@ bool clusters_enabled() { return !g_env.no_cluster; }
 // (PA_KERNEL_TILE); results agree.
 bool use_tile(const pa_shape* s, int32_t q_len, int32_t partition_tokens) {
     const int64_t rows = (int64_t)q_len * (s->num_heads / s->num_kv_heads);
-    if (partition_tokens == PA_PARTITION_BALANCED && rows <= 16) return false;  // honoured there
+    // the balanced split is honoured by the warp-level kernel up to 16 rows,
+    // and by the tile kernel for units of at most 16 rows at head_dim 256
+    if (partition_tokens == PA_PARTITION_BALANCED && rows <= 16)
+        return s->head_dim == 256 && s->batch <= kMaxBalancedBatch;
     const int force = g_switch_multi_kernel.load(std::memory_order_relaxed);
     if (force == PA_KERNEL_TILE) return true;
     if (force == PA_KERNEL_MMA && q_len > 1) return false;
@@ -527,6 +530,17 @@ Plan tile_plan(const pa_shape* s, int32_t max_context_len, int32_t partition_tok
 // one CTA: it needs q_len * group <= 16, and batch <= kMaxBalancedBatch.
 Plan make_plan(const pa_shape* s, int32_t max_context_len, int32_t partition_tokens, int num_sms,
                int32_t q_len = 1) {
+    if (use_tile(s, q_len, partition_tokens) && partition_tokens == PA_PARTITION_BALANCED &&
+        tile_q_rows(s, q_len) == kTileCompactQRows && s->batch <= kMaxBalancedBatch) {
+        // the balanced split of compact units on the tile kernel: one CTA per
+        // SM, each an equal share of the flattened (sequence, kv head, page)
+        // order, pieces that straddle shares combined afterwards
+        Plan p = balanced_plan(s, pages_for(s, max_context_len),
+                               num_sms * tile_ctas_per_sm(s, kTileCompactQRows));
+        p.tile = true;
+        p.tile_qr = kTileCompactQRows;
+        return p;
+    }
     if (use_tile(s, q_len, partition_tokens)) {
         Plan tp = tile_plan(s, max_context_len,
                             partition_tokens == PA_PARTITION_BALANCED ? 0 : partition_tokens,
@@ -779,7 +793,14 @@ pa_status launch_tile(void* out, const void* q, const void* k, const void* v, co
     const bool compact = plan.tile_qr == kTileCompactQRows;
     if (compact && (s->head_dim != 256 || rows > kTileCompactQRows)) return PA_ERR_UNSUPPORTED;
     if (plan.cluster && !tile_cluster_fits(s, plan.tile_qr)) return PA_ERR_UNSUPPORTED;
-    L.grid = dim3((unsigned)plan.num_parts, (unsigned)grid_y, (unsigned)s->batch);
+    p.balanced = plan.balanced ? 1 : 0;
+    if (plan.balanced) {
+        if (!compact || plan.cluster) return PA_ERR_UNSUPPORTED;
+        p.final_out = 0;
+        L.grid = dim3((unsigned)plan.num_ctas);
+    } else {
+        L.grid = dim3((unsigned)plan.num_parts, (unsigned)grid_y, (unsigned)s->batch);
+    }
     L.threads = kTileThreads;
     L.smem_bytes = tile_smem_layout(s->head_dim, s->block_size, plan.tile_qr).total + kSmemAlignSlack;
     cudaError_t e;
@@ -883,7 +904,7 @@ pa_status pa_decode_multi(void* out, const void* q, const void* k_cache, const v
     if (st != PA_OK) return st;
     const Plan plan = make_plan(shape, max_context_len, partition_tokens, sms, q_len);
     cudaStream_t cs = static_cast<cudaStream_t>(stream);
-    if (plan.tile && (plan.num_parts <= 1 || plan.cluster))
+    if (plan.tile && !plan.balanced && (plan.num_parts <= 1 || plan.cluster))
         return launch_tile(out, q, k_cache, v_cache, block_tables, context_lens, shape, scale, plan,
                            nullptr, nullptr, err, cs, q_len);
     if (!plan.tile && !plan.balanced && (plan.num_parts <= 1 || plan.cluster))
@@ -953,7 +974,9 @@ pa_status pa_plan_info(const pa_shape* shape, int32_t q_len, int32_t max_context
     desc->reduce = plan.balanced ? 3 : (plan.num_parts <= 1 ? 0 : (plan.cluster ? 1 : 2));
     if (plan.tile) {
         const int64_t tiles = ((int64_t)q_len * G + kTileRows - 1) / kTileRows;
-        desc->ctas = (int32_t)((int64_t)shape->batch * shape->num_kv_heads * tiles * plan.num_parts);
+        desc->ctas = plan.balanced ? plan.num_ctas
+                                   : (int32_t)((int64_t)shape->batch * shape->num_kv_heads * tiles *
+                                               plan.num_parts);
         desc->threads = kTileThreads;
     } else {
         const Tune t = pick_tune(shape, plan.many_ctas);

@@ -151,15 +151,19 @@ __host__ __device__ constexpr int tile_stages(int D, int qr = kTileRows) {
 
 struct TileSmem {
     uint32_t tile_bytes;   // one K (or V) block tile: BN * head_dim * 2
-    uint32_t q_off;        // Q tile: [head_dim / 64] column blocks of qr rows x 128 bytes
+    uint32_t q_off;        // Q tiles: [head_dim / 64] column blocks of qr rows x 128 bytes each;
+                           // two of them for compact units (the balanced split's segments)
     uint32_t k_off;        // [ns] K stages
     uint32_t v_off;        // [ns] V stages
     uint32_t bar_off;      // mbarriers: k_full[ns], k_empty[ns], v_full[ns], v_empty[ns],
-                           // s_full[3], p_full[3], pv_done[3], final, q_ready
+                           // s_full[3], p_full[3], pv_done[3], final, q_ready, q_full[2],
+                           // q_free[2], o_free
     uint32_t phys_off;     // [ns][BN / block_size] int32 physical block of each K stage's pages
     uint32_t xchg_off;     // softmax exchange: row maxima [2][2][128], normalisers [2][128] (fp32),
                            // then mbarriers xchg[2]
     uint32_t misc_off;     // tensor-memory base address, abort flag
+    uint32_t seq_off;      // compact units, balanced split: pages of each sequence [512]
+    uint32_t walk_off;     // compact units, balanced split: the CTA's share (4 x int64)
     uint32_t total;
     int ns;
 };
@@ -169,18 +173,25 @@ __host__ __device__ inline TileSmem tile_smem_layout(int D, int BS, int qr = kTi
     const int BN = tile_block_tokens(D);
     L.ns = tile_stages(D, qr);
     L.tile_bytes = (uint32_t)BN * D * 2u;
+    const bool compact = qr == kTileCompactQRows;
     L.q_off = 0;
-    L.k_off = 2u * qr * D;  // a multiple of 1024 (qr and D multiples of 16 and 64)
+    // a multiple of 1024 (qr and D multiples of 16 and 64)
+    L.k_off = (compact ? 2u : 1u) * 2u * qr * D;
     L.v_off = L.k_off + L.tile_bytes * L.ns;
     uint32_t o = L.v_off + L.tile_bytes * L.ns;
     L.bar_off = o;
-    o += 8u * (4 * L.ns + 3 * kTileSBufs + 2);
+    o += 8u * (4 * L.ns + 3 * kTileSBufs + 2 + 5);
     L.phys_off = o;
     o += 4u * L.ns * (BN / BS);
     L.xchg_off = pa_align_up(o, 16);
     o = L.xchg_off + 4u * (2 * 2 * 128 + 2 * 128) + 16;
     L.misc_off = pa_align_up(o, 16);
-    L.total = L.misc_off + 16;
+    o = L.misc_off + 16;
+    L.seq_off = o;
+    if (compact) o += 4u * kMaxBalancedBatch;
+    L.walk_off = pa_align_up(o, 16);
+    o = L.walk_off + (compact ? 32u : 0u);
+    L.total = pa_align_up(o, 16);
     return L;
 }
 

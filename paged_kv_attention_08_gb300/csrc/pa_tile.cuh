@@ -50,6 +50,19 @@ constexpr float kTileRescaleSlack = 8.0f;  // log2 units: P may reach 2^8 before
 
 // QR: Q rows staged in shared memory (kTileRows, or kTileCompactQRows for
 // units of at most 16 rows at head_dim 256, which buys a third ring stage).
+//
+// Work of a CTA: one segment -- (sequence, kv head, 128-row tile) and a range
+// of its pages -- from the grid position; or, for the balanced split of
+// compact units, the CTA's equal share [c W / C, (c + 1) W / C) of the
+// flattened (sequence, kv head, page) order, W pages in all, walked as a list
+// of segments (a whole unit is written out; a piece at either end of the
+// share becomes a record [C][2][unit rows] for the balanced combine kernel).
+// Every role walks the same segments and numbers the KV blocks of all of them
+// in one sequence, so that the rings, the S / P buffers and their barrier
+// phases run on across segment boundaries; Q is double-buffered (warp 2
+// stages the Q of segment s >= 1 once the last S MMA of segment s - 2 is
+// done), and the first P V MMA of a segment waits until the previous
+// segment's O has been read out.
 template <int D, int BS, typename KV, int QR>
 __global__ void __launch_bounds__(kTileThreads, 1)
     tile_kernel(const __grid_constant__ CUtensorMap tmap_k,
@@ -68,6 +81,7 @@ __global__ void __launch_bounds__(kTileThreads, 1)
     // alone, with the normaliser summed from the rounded weights so that the
     // result stays a weighted mean of the V rows.
     constexpr bool kSplitP = kBF;
+    constexpr bool kCanBalance = QR == kTileCompactQRows;  // the balanced split: compact units
     constexpr uint32_t kCols = tile_tmem_cols(D);
     constexpr int NB = kTileSBufs;
     constexpr uint32_t O_COL = 0, S_COL = D;  // S buffer b at S_COL + b*BN; P (hi, lo) over it
@@ -87,35 +101,144 @@ __global__ void __launch_bounds__(kTileThreads, 1)
     uint64_t* p_full = s_full + NB;
     uint64_t* pv_done = s_full + 2 * NB;
     uint64_t* final_bar = s_full + 3 * NB;
-    uint64_t* q_ready = final_bar + 1;  // the Q tile is in shared memory
+    uint64_t* q_ready = final_bar + 1;  // the first segment's Q tile is in shared memory
+    uint64_t* q_full = q_ready + 1;     // [2] Q buffer b holds a later segment's Q
+    uint64_t* q_free = q_full + 2;      // [2] the S MMAs of buffer b's segment have completed
+    uint64_t* o_free = q_free + 2;      // a segment's O has been read out
     int32_t* phys_of = reinterpret_cast<int32_t*>(smem + L.phys_off);  // [NS][NPB] of K stages
     float* xmax = reinterpret_cast<float*>(smem + L.xchg_off);    // [2][2][128]
     float* xl = xmax + 2 * 2 * 128;                                   // [2][128]
     uint64_t* xchg = reinterpret_cast<uint64_t*>(xl + 2 * 128);     // [2]
     uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + L.misc_off);
     volatile uint32_t* abort_flag = tmem_slot + 1;
+    int32_t* seq_pages = reinterpret_cast<int32_t*>(smem + L.seq_off);  // balanced: [B] pages
+    long long* walk0 = reinterpret_cast<long long*>(smem + L.walk_off);  // share start, end, base, b
 
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const int G = p.group, Q = p.q_len, Hkv = p.num_kv_heads, U = p.unit_rows;
     const int gshift = __ffs(G) - 1;
-    const int part = blockIdx.x, b = blockIdx.z;
-    const int kvh = (int)blockIdx.y % Hkv, tile = (int)blockIdx.y / Hkv;
+    const bool bal = kCanBalance && p.balanced;
+    const int part = blockIdx.x;
+    const int tile = bal ? 0 : (int)blockIdx.y / Hkv;
 
     grid_dependency_wait();
     grid_launch_dependents();
 
-    const int T = reachable_tokens(p.context_lens, b, p.max_blocks, BS);
-    const int npages = (T + BS - 1) / BS;
-    const int pb = part * p.part_pages;
-    const int pe = min(pb + p.part_pages, npages);
-    const int n = pe - pb;                      // pages of this partition (masked ones included)
-    const int nblk = (n + NPB - 1) / NPB;       // KV blocks
-    const int tend = min(T, pe * BS);           // tokens of this partition end here
-
     // Element offset of unit row u's query / output vector ([B, Q, H, D]).
-    auto row_off = [&](int u) -> size_t {
+    auto row_off = [&](int b, int kvh, int u) -> size_t {
         return (((size_t)b * Q + (u >> gshift)) * p.num_heads + kvh * G + (u & (G - 1))) * D;
     };
+
+    // ---- the CTA's segments ----
+    struct Seg {
+        int b, kvh, pb, pe, T, np;  // pages [pb, pe) of the np of (b, kvh); T tokens reach the table
+        bool whole;                 // the segment is the whole unit
+    };
+    struct Walk {
+        long long cur, end, base;  // flat position, end of the share, flat start of sequence b
+        int b;
+    };
+    if (bal) {
+        // pages of every sequence, their total W (times the kv heads), and the
+        // sequence holding the first page of this CTA's share
+        if (warp == 0) {
+            long long w = 0;
+            for (int b0 = lane; b0 < p.batch; b0 += 32) {
+                const int T = reachable_tokens(p.context_lens, b0, p.max_blocks, BS);
+                const int np = (T + BS - 1) / BS;
+                seq_pages[b0] = np;
+                w += np;
+            }
+#pragma unroll
+            for (int m = 16; m >= 1; m >>= 1) w += __shfl_xor_sync(kFullMask, w, m);
+            const long long W = w * Hkv, Cn = gridDim.x, c = blockIdx.x;
+            const long long start = c * W / Cn, end = (c + 1) * W / Cn;
+            __syncwarp();
+            // scan the sequences 32 at a time for the one that holds `start`
+            int b = 0;
+            long long base = 0;
+            if (start < end) {
+                for (;;) {
+                    const int bb = b + lane;
+                    const long long v = bb < p.batch ? (long long)seq_pages[bb] * Hkv : 0;
+                    long long incl = v;
+#pragma unroll
+                    for (int m = 1; m < 32; m <<= 1) {
+                        const long long o = __shfl_up_sync(kFullMask, incl, m);
+                        if (lane >= m) incl += o;
+                    }
+                    const unsigned hit = __ballot_sync(kFullMask, bb < p.batch && base + incl > start);
+                    if (hit) {
+                        const int k = __ffs(hit) - 1;
+                        base += __shfl_sync(kFullMask, incl - v, k);
+                        b += k;
+                        break;
+                    }
+                    base += __shfl_sync(kFullMask, incl, 31);
+                    b += 32;
+                }
+            }
+            if (lane == 0) {
+                walk0[0] = start;
+                walk0[1] = end;
+                walk0[2] = base;
+                walk0[3] = b;
+            }
+        }
+        __syncthreads();
+        if (walk0[0] >= walk0[1]) return;  // an empty share (fewer pages than CTAs)
+    }
+    auto walk_init = [&](Walk& w) {
+        w.cur = walk0[0];
+        w.end = walk0[1];
+        w.base = walk0[2];
+        w.b = (int)walk0[3];
+    };
+    auto walk_next = [&](Walk& w, Seg& g) -> bool {
+        if (w.cur >= w.end) return false;
+        const int np = seq_pages[w.b];
+        const long long off = w.cur - w.base;
+        const int j = (int)(off % np);
+        const int len = (int)min(w.end - w.cur, (long long)(np - j));
+        g.b = w.b;
+        g.kvh = (int)(off / np);
+        g.pb = j;
+        g.pe = j + len;
+        g.np = np;
+        g.whole = j == 0 && len == np;
+        g.T = reachable_tokens(p.context_lens, w.b, p.max_blocks, BS);
+        w.cur += len;
+        if (w.cur - w.base >= (long long)np * Hkv) {  // past this sequence's pages
+            w.base += (long long)np * Hkv;
+            ++w.b;
+            while (w.b < p.batch && seq_pages[w.b] == 0) ++w.b;
+        }
+        return true;
+    };
+    // the segment of a grid-position CTA
+    Seg seg0;
+    if (!bal) {
+        seg0.b = blockIdx.z;
+        seg0.kvh = (int)blockIdx.y % Hkv;
+        seg0.T = reachable_tokens(p.context_lens, seg0.b, p.max_blocks, BS);
+        seg0.np = (seg0.T + BS - 1) / BS;
+        seg0.pb = part * p.part_pages;
+        seg0.pe = min(seg0.pb + p.part_pages, seg0.np);
+        seg0.whole = false;
+    }
+    // calls fn(segment, index) for each of the CTA's segments until fn returns false
+    auto for_segments = [&](auto&& fn) {
+        if (!bal) {
+            (void)fn(seg0, 0);
+            return;
+        }
+        Walk w;
+        walk_init(w);
+        Seg g;
+        for (int s = 0; walk_next(w, g); ++s)
+            if (!fn(g, s)) return;
+    };
+    auto nblk_of = [&](const Seg& g) { return (g.pe - g.pb + NPB - 1) / NPB; };
 
     // ---- cluster reduction (at most 8 partitions of a unit form one cluster
     // along grid x): every CTA has left its partial at offset 0 of its shared
@@ -175,7 +298,7 @@ __global__ void __launch_bounds__(kTileThreads, 1)
                 a.z = fmaf(w, v.z, a.z);
                 a.w = fmaf(w, v.w, a.w);
             }
-            const size_t o = row_off(u) + 4 * c4;
+            const size_t o = row_off(seg0.b, seg0.kvh, u) + 4 * c4;
             if (p.out_dtype == PA_F32) {
                 *reinterpret_cast<float4*>(static_cast<float*>(p.out) + o) = a;
             } else {
@@ -186,22 +309,22 @@ __global__ void __launch_bounds__(kTileThreads, 1)
         cluster_sync_relaxed();  // no CTA leaves while others still read its partial
     };
 
-    if (n <= 0 && p.cluster_reduce) {
-        // no pages here, but the cluster's merge needs this CTA: an empty partial
-        for (int r = tid; r < kTileRows; r += kTileThreads) {
-            cl_m[r] = NEG_INF;
-            cl_l[r] = 0.f;
+    if (!bal && seg0.pe <= seg0.pb) {
+        if (p.cluster_reduce) {
+            // no pages here, but the cluster's merge needs this CTA: an empty partial
+            for (int r = tid; r < kTileRows; r += kTileThreads) {
+                cl_m[r] = NEG_INF;
+                cl_l[r] = 0.f;
+            }
+            cluster_merge();
+            return;
         }
-        cluster_merge();
-        return;
-    }
-    if (n <= 0) {
         // Nothing of this sequence in the partition: the single pass writes the
         // empty-context result; the combine never reads such partitions.
         if (p.final_out) {
             for (int idx = tid; idx < kTileRows * D; idx += kTileThreads) {
                 const int u = tile * kTileRows + idx / D;
-                if (u < U) store_out(p.out, row_off(u) + idx % D, 0.f, p.out_dtype);
+                if (u < U) store_out(p.out, row_off(seg0.b, seg0.kvh, u) + idx % D, 0.f, p.out_dtype);
             }
         }
         return;
@@ -221,6 +344,11 @@ __global__ void __launch_bounds__(kTileThreads, 1)
         }
         mbar_init(smem_u32(final_bar), 1);
         mbar_init(smem_u32(q_ready), kTileThreads - 64);
+        for (int i = 0; i < 2; ++i) {
+            mbar_init(smem_u32(q_full + i), 1);
+            mbar_init(smem_u32(q_free + i), 1);
+        }
+        mbar_init(smem_u32(o_free), 8);
         mbar_init(smem_u32(xchg), 256);
         mbar_init(smem_u32(xchg + 1), 256);
         *abort_flag = 0;
@@ -238,25 +366,33 @@ __global__ void __launch_bounds__(kTileThreads, 1)
     tc::fence_after_sync();
     const uint32_t tmem = *tmem_slot;
 
-    // ---- Q tile: rows u = tile*128 + r for r < QR, zero rows past the
-    // unit's rows; written with the 128-byte swizzle the MMA descriptors
-    // expect, by every thread outside the two copy warps (which already stream
-    // K and V); the MMA issuer waits for q_ready.  With a compact Q tile the
-    // S MMA's rows past QR read whatever follows it: those rows lie past the
-    // unit's rows, their scores are masked or never read, and their P and O
-    // rows are never used ----
-    if (warp != 0 && warp != 3) {
-        const int qt = (warp < 3 ? (warp - 1) * 32 : 64 + (warp - 4) * 32) + lane;  // 0..319
-        uint8_t* qs = smem + L.q_off;
-        for (int i = qt; i < QR * (D / 8); i += kTileThreads - 64) {
+    // ---- Q tile of a segment into Q buffer `qb`: rows u = tile*128 + r for
+    // r < QR, zero rows past the unit's rows; written with the 128-byte
+    // swizzle the MMA descriptors expect, threads `t0, t0 + step, ...`.  With a
+    // compact Q tile the S MMA's rows past QR read whatever follows it: those
+    // rows lie past the unit's rows, their scores are masked or never read,
+    // and their P and O rows are never used ----
+    auto stage_q = [&](const Seg& g, int qb, int t0, int step) {
+        uint8_t* qs = smem + L.q_off + (size_t)qb * (2u * QR * D);
+        for (int i = t0; i < QR * (D / 8); i += step) {
             const int r = i / (D / 8), c = i % (D / 8);
             const int u = tile * kTileRows + r;
             uint4 v = make_uint4(0, 0, 0, 0);
             if (u < U)
-                v = __ldg(reinterpret_cast<const uint4*>(static_cast<const KV*>(p.q) + row_off(u)) + c);
+                v = __ldg(reinterpret_cast<const uint4*>(static_cast<const KV*>(p.q) +
+                                                         row_off(g.b, g.kvh, u)) + c);
             *reinterpret_cast<uint4*>(qs + (c >> 3) * (QR * 128) + r * 128 +
                                       (((c & 7) ^ (r & 7)) << 4)) = v;
         }
+    };
+    // the first segment's Q: every thread outside the two copy warps (which
+    // already stream K and V); the MMA issuer waits for q_ready
+    if (warp != 0 && warp != 3) {
+        const int qt = (warp < 3 ? (warp - 1) * 32 : 64 + (warp - 4) * 32) + lane;  // 0..319
+        for_segments([&](const Seg& g, int s) {
+            stage_q(g, 0, qt, kTileThreads - 64);
+            return false;  // the first segment only
+        });
         fence_proxy_async_smem();
         mbar_arrive(smem_u32(q_ready));
     }
@@ -286,50 +422,69 @@ __global__ void __launch_bounds__(kTileThreads, 1)
         uint64_t* empty = is_k ? k_empty : v_empty;
         const CUtensorMap* map = is_k ? &tmap_k : &tmap_v;
         const uint32_t ring = smem_u32(smem + (is_k ? L.k_off : L.v_off));
-        const int32_t* table_row = p.block_tables + (size_t)b * p.max_blocks;
         const uint64_t policy = l2_policy_evict_first();
-        // the partition's table entries, 32 pages at a time (one per lane),
-        // fetched one window ahead so that no block waits for its entries
-        auto fetch = [&](int w) -> int {
-            const int jj = pb + w * 32 + lane;
-            return jj < pe ? __ldg(table_row + jj) : -1;
-        };
-        int ent_cur = fetch(0), ent_next = fetch(1), win = 0;
-        int issued = 0;
-        for (int k = 0; k < nblk && !*abort_flag; ++k) {
-            const int st = k % NS, round = k / NS;
-            const int first = k * NPB;  // page index of the block within the partition
-            if ((first >> 5) != win) {  // NPB divides 32: a block never straddles windows
-                win = first >> 5;
-                ent_cur = ent_next;
-                ent_next = fetch(win + 1);
-            }
-            const int e0 = __shfl_sync(kFullMask, ent_cur, (first & 31) + (lane < NPB ? lane : 0));
-            const int e = lane < NPB ? e0 : -1;
-            const int phys = (e >= 0 && (int64_t)e < p.num_blocks) ? e : -1;
-            bool ok = true;
-            if (round > 0 && lane == 0) ok = wait(empty + st, (round - 1) & 1);
-            if (!__shfl_sync(kFullMask, ok ? 1 : 0, 0)) break;
-            if (is_k && lane < NPB) phys_of[st * NPB + lane] = phys;
-            const unsigned live = __ballot_sync(kFullMask, lane < NPB && phys >= 0);
-            const uint32_t bar = smem_u32(full + st);
-            if (lane == 0) {
-                if (live) mbar_arrive_expect_tx(bar, (uint32_t)__popc(live) * 2u * BS * D);
-                else mbar_arrive(bar);
-            }
-            __syncwarp();
-            if (lane < NPB && phys >= 0) {
-                const uint32_t dst = ring + (uint32_t)st * L.tile_bytes + (uint32_t)lane * BS * 128;
+        int issued = 0;  // blocks issued, over all segments (the ring's position)
+        for_segments([&](const Seg& g, int s) {
+            const int32_t* table_row = p.block_tables + (size_t)g.b * p.max_blocks;
+            const int nblk = nblk_of(g);
+            // the segment's table entries, 32 pages at a time (one per lane),
+            // fetched one window ahead so that no block waits for its entries
+            auto fetch = [&](int w) -> int {
+                const int jj = g.pb + w * 32 + lane;
+                return jj < g.pe ? __ldg(table_row + jj) : -1;
+            };
+            int ent_cur = fetch(0), ent_next = fetch(1), win = 0;
+            for (int k = 0; k < nblk && !*abort_flag; ++k) {
+                const int st = issued % NS, round = issued / NS;
+                const int first = k * NPB;  // page index of the block within the segment
+                if ((first >> 5) != win) {  // NPB divides 32: a block never straddles windows
+                    win = first >> 5;
+                    ent_cur = ent_next;
+                    ent_next = fetch(win + 1);
+                }
+                const int e0 = __shfl_sync(kFullMask, ent_cur, (first & 31) + (lane < NPB ? lane : 0));
+                const int e = lane < NPB ? e0 : -1;
+                const int phys = (e >= 0 && (int64_t)e < p.num_blocks) ? e : -1;
+                bool ok = true;
+                if (round > 0 && lane == 0) ok = wait(empty + st, (round - 1) & 1);
+                if (!__shfl_sync(kFullMask, ok ? 1 : 0, 0)) return false;
+                if (is_k && lane < NPB) phys_of[st * NPB + lane] = phys;
+                const unsigned live = __ballot_sync(kFullMask, lane < NPB && phys >= 0);
+                const uint32_t bar = smem_u32(full + st);
+                if (lane == 0) {
+                    if (live) mbar_arrive_expect_tx(bar, (uint32_t)__popc(live) * 2u * BS * D);
+                    else mbar_arrive(bar);
+                }
+                __syncwarp();
+                if (lane < NPB && phys >= 0) {
+                    const uint32_t dst = ring + (uint32_t)st * L.tile_bytes + (uint32_t)lane * BS * 128;
 #pragma unroll
-                for (int blk = 0; blk < DBLK; ++blk)
-                    tma_load_4d(dst + blk * BN * 128, map, blk * 64, kvh, 0, phys, bar, policy);
+                    for (int blk = 0; blk < DBLK; ++blk)
+                        tma_load_4d(dst + blk * BN * 128, map, blk * 64, g.kvh, 0, phys, bar, policy);
+                }
+                ++issued;
             }
-            ++issued;
-        }
+            return !*abort_flag;
+        });
         if (*abort_flag && lane == 0) {
             // let copies still in flight land before the CTA may exit
             for (int k = issued > NS ? issued - NS : 0; k < issued; ++k)
                 (void)mbar_wait_bounded(smem_u32(full + k % NS), (k / NS) & 1, p.timeout_ns);
+        }
+    } else if (warp == 2) {
+        // ====== Q of later segments (balanced split): buffer s & 1, once the
+        // S MMAs of segment s - 2 (the buffer's previous user) are done ======
+        if (bal) {
+            for_segments([&](const Seg& g, int s) {
+                if (s == 0) return true;  // staged with the others at the start
+                if (s >= 2 && !__all_sync(kFullMask, wait(q_free + (s & 1), ((s - 2) >> 1) & 1)))
+                    return false;
+                stage_q(g, s & 1, lane, 32);
+                fence_proxy_async_smem();
+                __syncwarp();
+                if (lane == 0) mbar_arrive(smem_u32(q_full + (s & 1)));
+                return !*abort_flag;
+            });
         }
     } else if (warp == 1) {
         // ================= MMA issuer (one lane) =================
@@ -343,67 +498,89 @@ __global__ void __launch_bounds__(kTileThreads, 1)
             constexpr int kM = QR == kTileCompactQRows ? 64 : kTileRows;
             constexpr uint32_t id_s = tc::idesc_f16(kType, false, kM, BN);
             constexpr uint32_t id_o = tc::idesc_f16(kType, true, kM, D);
-            const uint32_t q_base = smem_u32(smem + L.q_off);
-            // Operand descriptors: a shared-memory descriptor holds (address >> 4)
-            // in its low 14 bits, and every address here is below 2^18, so the
-            // descriptor of base + offset is base's plus offset >> 4.  Q's are
-            // fixed for the CTA; K's and V's are one add from their stage's.
-            uint64_t qd[KSTEPS];
-#pragma unroll
-            for (int s = 0; s < KSTEPS; ++s)
-                qd[s] = tc::smem_desc(q_base + (s >> 2) * (QR * 128) + (s & 3) * 32, 16, 1024,
-                                      tc::kSwizzle128B);
-            bool started = false;
+            bool started = false;    // O holds the current segment's sum
             bool live_prev = false;  // block i-1 holds a page (its K stage may be refilled)
-            const bool q_ok = wait(q_ready, 0);
-            for (int i = 0; i <= nblk && q_ok && !*abort_flag; ++i) {
-                bool live_cur = false;
-                if (i < nblk) {
+            int seg_prev = -1;       // segment of block i-1
+            bool first_prev = false; // block i-1 is its segment's first
+            int i = 0;               // blocks over all segments
+            // O += P_j V_j (P's high and low parts) for block j = i - 1
+            auto issue_pv = [&]() -> bool {
+                const int j = i - 1, st = j % NS;
+                if (first_prev && seg_prev >= 1) {
+                    // the previous segment's O must have been read out
+                    if (!wait(o_free, (seg_prev - 1) & 1)) return false;
+                    tc::fence_after_sync();
+                    started = false;
+                }
+                if (!wait(p_full + j % NB, (j / NB) & 1)) return false;
+                if (!wait(v_full + st, (j / NS) & 1)) return false;
+                tc::fence_after_sync();
+                if (live_prev) {
+                    const uint32_t v_base = smem_u32(smem + L.v_off) + (uint32_t)st * L.tile_bytes;
+                    const uint32_t p_hi = tmem + S_COL + (j % NB) * BN;
+                    const uint32_t p_lo = p_hi + BN / 2;
+                    // V: MN-major, 64-column blocks BN*128 bytes apart, 8-row
+                    // groups 1024 bytes apart; rows ks*16 .. +15 per step
+                    const uint64_t vd0 = tc::smem_desc(v_base, BN * 128, 1024, tc::kSwizzle128B);
+#pragma unroll
+                    for (int ks = 0; ks < BN / 16; ++ks) {
+                        const uint64_t vd = vd0 + (uint64_t)((ks * 16 * 128) >> 4);
+                        tc::mma_ts(tmem + O_COL, p_hi + ks * 8, vd, id_o,
+                                   (started || ks > 0) ? 1u : 0u);
+                        if (kSplitP) tc::mma_ts(tmem + O_COL, p_lo + ks * 8, vd, id_o, 1u);
+                    }
+                    started = true;
+                }
+                tc::commit(smem_u32(pv_done + j % NB));
+                tc::commit(smem_u32(v_empty + st));
+                return true;
+            };
+            bool ok = true;
+            for_segments([&](const Seg& g, int s) {
+                // this segment's Q: buffer s & 1
+                if (s == 0) ok = wait(q_ready, 0);
+                else ok = wait(q_full + (s & 1), ((s - 1) >> 1) & 1);
+                if (!ok) return false;
+                const uint32_t q_base = smem_u32(smem + L.q_off) + (uint32_t)(s & 1) * (2u * QR * D);
+                // Operand descriptors: a shared-memory descriptor holds (address >> 4)
+                // in its low 14 bits, and every address here is below 2^18, so the
+                // descriptor of base + offset is base's plus offset >> 4.  Q's are
+                // fixed for the segment; K's and V's are one add from their stage's.
+                uint64_t qd[KSTEPS];
+#pragma unroll
+                for (int ks = 0; ks < KSTEPS; ++ks)
+                    qd[ks] = tc::smem_desc(q_base + (ks >> 2) * (QR * 128) + (ks & 3) * 32, 16, 1024,
+                                           tc::kSwizzle128B);
+                const int nblk = nblk_of(g);
+                for (int k = 0; k < nblk && !*abort_flag; ++k, ++i) {
                     // S_i = Q K_i^T into buffer i % NB, once P_{i-NB} there has been consumed
                     const int st = i % NS;
-                    if (!wait(k_full + st, (i / NS) & 1)) break;
-                    if (i >= NB && !wait(pv_done + i % NB, ((i - NB) / NB) & 1)) break;
+                    if (!wait(k_full + st, (i / NS) & 1)) return ok = false;
+                    if (i >= NB && !wait(pv_done + i % NB, ((i - NB) / NB) & 1)) return ok = false;
                     tc::fence_after_sync();
-                    live_cur = block_live(st);
+                    const bool live_cur = block_live(st);
                     if (live_cur) {
                         const uint32_t k_base = smem_u32(smem + L.k_off) + (uint32_t)st * L.tile_bytes;
                         const uint64_t kd = tc::smem_desc(k_base, 16, 1024, tc::kSwizzle128B);
 #pragma unroll
-                        for (int s = 0; s < KSTEPS; ++s)
-                            tc::mma_ss(tmem + S_COL + (i % NB) * BN, qd[s],
-                                       kd + (uint64_t)(((s >> 2) * (BN * 128) + (s & 3) * 32) >> 4),
-                                       id_s, s > 0);
+                        for (int ks = 0; ks < KSTEPS; ++ks)
+                            tc::mma_ss(tmem + S_COL + (i % NB) * BN, qd[ks],
+                                       kd + (uint64_t)(((ks >> 2) * (BN * 128) + (ks & 3) * 32) >> 4),
+                                       id_s, ks > 0);
                     }
                     tc::commit(smem_u32(s_full + i % NB));
                     tc::commit(smem_u32(k_empty + st));
+                    // the segment's last S: its Q buffer is free once these complete
+                    if (bal && k == nblk - 1) tc::commit(smem_u32(q_free + (s & 1)));
+                    if (i >= 1 && !issue_pv()) return ok = false;
+                    live_prev = live_cur;
+                    seg_prev = s;
+                    first_prev = k == 0;
                 }
-                if (i >= 1) {
-                    // O += P_j V_j with P's high and low parts
-                    const int j = i - 1, st = j % NS;
-                    if (!wait(p_full + j % NB, (j / NB) & 1)) break;
-                    if (!wait(v_full + st, (j / NS) & 1)) break;
-                    tc::fence_after_sync();
-                    if (live_prev) {
-                        const uint32_t v_base = smem_u32(smem + L.v_off) + (uint32_t)st * L.tile_bytes;
-                        const uint32_t p_hi = tmem + S_COL + (j % NB) * BN;
-                        const uint32_t p_lo = p_hi + BN / 2;
-                        // V: MN-major, 64-column blocks BN*128 bytes apart, 8-row
-                        // groups 1024 bytes apart; rows ks*16 .. +15 per step
-                        const uint64_t vd0 = tc::smem_desc(v_base, BN * 128, 1024, tc::kSwizzle128B);
-#pragma unroll
-                        for (int ks = 0; ks < BN / 16; ++ks) {
-                            const uint64_t vd = vd0 + (uint64_t)((ks * 16 * 128) >> 4);
-                            tc::mma_ts(tmem + O_COL, p_hi + ks * 8, vd, id_o,
-                                       (started || ks > 0) ? 1u : 0u);
-                            if (kSplitP) tc::mma_ts(tmem + O_COL, p_lo + ks * 8, vd, id_o, 1u);
-                        }
-                        started = true;
-                    }
-                    tc::commit(smem_u32(pv_done + j % NB));
-                    tc::commit(smem_u32(v_empty + st));
-                }
-                live_prev = live_cur;
-            }
+                return ok && !*abort_flag;
+            });
+            // the last block's P V
+            if (ok && !*abort_flag && i >= 1) (void)issue_pv();
             // every MMA issued has completed before tensor memory is released
             tc::commit(smem_u32(final_bar));
             (void)mbar_wait_bounded(smem_u32(final_bar), 0, p.timeout_ns);
@@ -420,18 +597,7 @@ __global__ void __launch_bounds__(kTileThreads, 1)
         const int sr = wg * 128 + r;  // 0 .. 255 among the softmax threads
         const uint32_t lane_base = tmem + ((uint32_t)(w4 * 32) << 16);
         const int u = tile * kTileRows + r;
-        const int ctx = max(__ldg(p.context_lens + b), 0);
-        // tokens t < lim: the row's causal limit, the table's reach, the partition's end
-        const int lim = u < U ? min(tend, ctx - Q + (u >> gshift) + 1) : 0;
         const float qscale = p.qscale;
-        const int32_t* table_row = p.block_tables + (size_t)b * p.max_blocks;
-        // which pages of block k hold data: bit q for page q (read from the
-        // table here; the K stage's record may already describe a later block)
-        auto page_bits = [&](int k) -> unsigned {
-            const int jj = pb + k * NPB + lane;
-            const int e = (lane < NPB && jj < pe && k < nblk) ? __ldg(table_row + jj) : -1;
-            return __ballot_sync(kFullMask, e >= 0 && (int64_t)e < p.num_blocks);
-        };
         // exchange round nx: publish v, return the other warpgroup's value
         int nx = 0;
         auto exchange = [&](float* buf, float v, float& other) -> bool {
@@ -445,192 +611,226 @@ __global__ void __launch_bounds__(kTileThreads, 1)
         // a warp whose 32 rows all lie past the unit's rows (a partial tile)
         // only keeps the barriers going: its P and O rows are never used
         const bool dead = tile * kTileRows + w4 * 32 >= U;
-        float m = NEG_INF, l = 0.f;  // l: this half's share of the normaliser
-        unsigned bits_next = page_bits(0);
-        int j = 0;
-        for (; j < nblk && !*abort_flag; ++j) {
-            const int st = j % NS;
-            const unsigned bits = bits_next;
-            bits_next = page_bits(j + 1);
-            // (waits are decided warp-wide: the tensor-memory accesses below
-            // are warp-collective)
-            if (!__all_sync(kFullMask, wait(s_full + j % NB, (j / NB) & 1))) break;
-            tc::fence_after_sync();
-            if (bits) {
-                const int t0 = (pb + j * NPB) * BS + wg * BH;  // first token of this half
-                const uint32_t sb = lane_base + S_COL + (j % NB) * BN;
-                float s[BH];
-                float mx = NEG_INF;
-                if (!dead) {
-                    uint32_t x[32];
+        int j = 0;  // blocks over all segments
+        for_segments([&](const Seg& g, int s) {
+            const int nblk = nblk_of(g);
+            const int jb = j;  // the segment's first block
+            const int tend = min(g.T, g.pe * BS);  // tokens of this segment end here
+            const int ctx = max(__ldg(p.context_lens + g.b), 0);
+            // tokens t < lim: the row's causal limit, the table's reach, the segment's end
+            const int lim = u < U ? min(tend, ctx - Q + (u >> gshift) + 1) : 0;
+            const int32_t* table_row = p.block_tables + (size_t)g.b * p.max_blocks;
+            // which pages of the segment's block k hold data: bit q for page q
+            // (read from the table here; the K stage's record may already
+            // describe a later block)
+            auto page_bits = [&](int k) -> unsigned {
+                const int jj = g.pb + k * NPB + lane;
+                const int e = (lane < NPB && jj < g.pe && k < nblk) ? __ldg(table_row + jj) : -1;
+                return __ballot_sync(kFullMask, e >= 0 && (int64_t)e < p.num_blocks);
+            };
+            float m = NEG_INF, l = 0.f;  // l: this half's share of the normaliser
+            unsigned bits_next = page_bits(0);
+            int k = 0;
+            for (; k < nblk && !*abort_flag; ++k, ++j) {
+                const int st = j % NS;
+                const unsigned bits = bits_next;
+                bits_next = page_bits(k + 1);
+                // (waits are decided warp-wide: the tensor-memory accesses below
+                // are warp-collective)
+                if (!__all_sync(kFullMask, wait(s_full + j % NB, (j / NB) & 1))) break;
+                tc::fence_after_sync();
+                if (bits) {
+                    const int t0 = (g.pb + k * NPB) * BS + wg * BH;  // first token of this half
+                    const uint32_t sb = lane_base + S_COL + (j % NB) * BN;
+                    float sc[BH];
+                    float mx = NEG_INF;
+                    if (!dead) {
+                        uint32_t x[32];
 #pragma unroll
-                    for (int c0 = 0; c0 < BH; c0 += 32) {
-                        tc::ld_32x32b_x32(sb + wg * BH + c0, x);
-                        tc::wait_ld();
+                        for (int c0 = 0; c0 < BH; c0 += 32) {
+                            tc::ld_32x32b_x32(sb + wg * BH + c0, x);
+                            tc::wait_ld();
 #pragma unroll
-                        for (int c = 0; c < 32; ++c) s[c0 + c] = __uint_as_float(x[c]);
-                    }
-                    // every page live and the whole half inside every row's limit:
-                    // nothing to mask
-                    if (__all_sync(kFullMask, bits == (1u << NPB) - 1u && t0 + BH <= lim)) {
+                            for (int c = 0; c < 32; ++c) sc[c0 + c] = __uint_as_float(x[c]);
+                        }
+                        // every page live and the whole half inside every row's limit:
+                        // nothing to mask
+                        if (__all_sync(kFullMask, bits == (1u << NPB) - 1u && t0 + BH <= lim)) {
 #pragma unroll
-                        for (int c = 0; c < BH; ++c) mx = fmaxf(mx, s[c]);
-                    } else {
+                            for (int c = 0; c < BH; ++c) mx = fmaxf(mx, sc[c]);
+                        } else {
 #pragma unroll
-                        for (int c = 0; c < BH; ++c) {
-                            const bool pl = (bits >> ((wg * BH + c) / BS)) & 1u;
-                            s[c] = (pl && t0 + c < lim) ? s[c] : NEG_INF;
-                            mx = fmaxf(mx, s[c]);
+                            for (int c = 0; c < BH; ++c) {
+                                const bool pl = (bits >> ((wg * BH + c) / BS)) & 1u;
+                                sc[c] = (pl && t0 + c < lim) ? sc[c] : NEG_INF;
+                                mx = fmaxf(mx, sc[c]);
+                            }
                         }
                     }
+                    float mo;
+                    if (!exchange(xmax + (nx & 1) * 256, mx, mo)) break;
+                    const float ms = fmaxf(mx, mo) * qscale;
+                    const bool need = ms > m + kTileRescaleSlack;
+                    float alpha = 1.f;
+                    if (need) {
+                        alpha = (m == NEG_INF) ? 1.f : fast_exp2(m - ms);
+                        l *= alpha;
+                        m = ms;
+                    }
+                    // O holds earlier blocks' sums only if this row had attended a token;
+                    // each warpgroup rescales its half of O's columns
+                    if (__any_sync(kFullMask, need && alpha != 1.f)) {
+                        if (j > jb && !__all_sync(kFullMask, wait(pv_done + (j - 1) % NB,
+                                                                   ((j - 1) / NB) & 1)))
+                            break;
+                        tc::fence_after_sync();
+                        uint32_t x[16];
+#pragma unroll 1
+                        for (int c0 = wg * (D / 2); c0 < (wg + 1) * (D / 2); c0 += 16) {
+                            tc::ld_32x32b_x16(lane_base + O_COL + c0, x);
+                            tc::wait_ld();
+#pragma unroll
+                            for (int c = 0; c < 16; ++c)
+                                x[c] = __float_as_uint(__uint_as_float(x[c]) * alpha);
+                            tc::st_32x32b_x16(lane_base + O_COL + c0, x);
+                        }
+                        tc::wait_st();
+                    }
+                    // P = 2^(s*scale*log2e - m) over S, as 16-bit values: for bf16 a
+                    // high and a low part, hi in columns [0, BN/2) and lo in [BN/2, BN)
+                    // of the buffer; for fp16 the high part alone
+                    const float me = (m == NEG_INF) ? 0.f : m;
+                    if (!dead) {
+#pragma unroll
+                        for (int c0 = 0; c0 < BH; c0 += 16) {
+                            uint32_t ph[8], pl[8];
+#pragma unroll
+                            for (int c = 0; c < 16; c += 2) {
+                                const float x0 = fast_exp2(fmaf(sc[c0 + c], qscale, -me));
+                                const float x1 = fast_exp2(fmaf(sc[c0 + c + 1], qscale, -me));
+                                const uint32_t h = Mma<KV>::pack(x0, x1);
+                                float h0, h1;
+                                Mma<KV>::unpack(h, h0, h1);
+                                ph[c / 2] = h;
+                                if (kSplitP) {
+                                    l += x0 + x1;
+                                    pl[c / 2] = Mma<KV>::pack(x0 - h0, x1 - h1);
+                                } else {
+                                    l += h0 + h1;  // the weights the MMA uses
+                                }
+                            }
+                            const uint32_t col = (uint32_t)(wg * BH + c0) / 2;
+                            tc::st_32x32b_x8(sb + col, ph);
+                            if (kSplitP) tc::st_32x32b_x8(sb + BN / 2 + col, pl);
+                        }
+                    }
+                    tc::wait_st();
+                    // zero the V rows of masked pages and past the segment's last
+                    // token (0 * NaN would otherwise reach O), once the stage's
+                    // copies have landed
+                    const int tb = (g.pb + k * NPB) * BS;
+                    const bool holes = tb + BN > tend || bits != (1u << NPB) - 1u;
+                    if (holes) {
+                        if (!__all_sync(kFullMask, wait(v_full + st, (j / NS) & 1))) break;
+                        uint8_t* vt = smem + L.v_off + (size_t)st * L.tile_bytes;
+                        for (int idx = sr; idx < BN * DBLK * 8; idx += 256) {
+                            const int row = idx / (DBLK * 8), rem = idx % (DBLK * 8);
+                            if (!((bits >> (row / BS)) & 1u) || tb + row >= tend)
+                                *reinterpret_cast<uint4*>(vt + (rem >> 3) * BN * 128 + row * 128 +
+                                                          (rem & 7) * 16) = make_uint4(0, 0, 0, 0);
+                        }
+                        fence_proxy_async_smem();
+                    }
                 }
-                float mo;
-                if (!exchange(xmax + (nx & 1) * 256, mx, mo)) break;
-                const float ms = fmaxf(mx, mo) * qscale;
-                const bool need = ms > m + kTileRescaleSlack;
-                float alpha = 1.f;
-                if (need) {
-                    alpha = (m == NEG_INF) ? 1.f : fast_exp2(m - ms);
-                    l *= alpha;
-                    m = ms;
+                tc::fence_before_sync();
+                mbar_arrive(smem_u32(p_full + j % NB));
+            }
+            // ---- epilogue of the segment: O / l, or the partial (m, l, O);
+            // each warpgroup its half of the columns ----
+            bool have_o = __all_sync(kFullMask, k == nblk && !*abort_flag);
+            if (have_o)
+                have_o = __all_sync(kFullMask, wait(pv_done + (j - 1) % NB, ((j - 1) / NB) & 1));
+            float lo_half = 0.f;
+            if (have_o) have_o = exchange(xl, l, lo_half);
+            tc::fence_after_sync();
+            if (have_o) l += lo_half;
+            if (p.cluster_reduce) {
+                // park this CTA's partial in its own shared memory (the operand
+                // buffers are idle: every copy and MMA has completed)
+                const bool rows_ok = have_o && !dead;
+                if (wg == 0) {
+                    cl_m[r] = rows_ok && l > 0.f ? m : NEG_INF;
+                    cl_l[r] = rows_ok ? l : 0.f;
                 }
-                // O holds earlier blocks' sums only if this row had attended a token;
-                // each warpgroup rescales its half of O's columns
-                if (__any_sync(kFullMask, need && alpha != 1.f)) {
-                    if (j >= 1 && !__all_sync(kFullMask, wait(pv_done + (j - 1) % NB,
-                                                              ((j - 1) / NB) & 1)))
-                        break;
-                    tc::fence_after_sync();
+                if (rows_ok) {
                     uint32_t x[16];
 #pragma unroll 1
                     for (int c0 = wg * (D / 2); c0 < (wg + 1) * (D / 2); c0 += 16) {
                         tc::ld_32x32b_x16(lane_base + O_COL + c0, x);
                         tc::wait_ld();
 #pragma unroll
-                        for (int c = 0; c < 16; ++c)
-                            x[c] = __float_as_uint(__uint_as_float(x[c]) * alpha);
-                        tc::st_32x32b_x16(lane_base + O_COL + c0, x);
-                    }
-                    tc::wait_st();
-                }
-                // P = 2^(s*scale*log2e - m) as high and low 16-bit parts over S:
-                // hi in columns [0, BN/2), lo in [BN/2, BN) of the buffer
-                const float me = (m == NEG_INF) ? 0.f : m;
-                if (!dead) {
-#pragma unroll
-                    for (int c0 = 0; c0 < BH; c0 += 16) {
-                        uint32_t ph[8], pl[8];
-#pragma unroll
-                        for (int c = 0; c < 16; c += 2) {
-                            const float x0 = fast_exp2(fmaf(s[c0 + c], qscale, -me));
-                            const float x1 = fast_exp2(fmaf(s[c0 + c + 1], qscale, -me));
-                            const uint32_t h = Mma<KV>::pack(x0, x1);
-                            float h0, h1;
-                            Mma<KV>::unpack(h, h0, h1);
-                            ph[c / 2] = h;
-                            if (kSplitP) {
-                                l += x0 + x1;
-                                pl[c / 2] = Mma<KV>::pack(x0 - h0, x1 - h1);
-                            } else {
-                                l += h0 + h1;  // the weights the MMA uses
-                            }
-                        }
-                        const uint32_t col = (uint32_t)(wg * BH + c0) / 2;
-                        tc::st_32x32b_x8(sb + col, ph);
-                        if (kSplitP) tc::st_32x32b_x8(sb + BN / 2 + col, pl);
+                        for (int c = 0; c < 16; c += 4)
+                            *reinterpret_cast<float4*>(cl_o + r * CL + c0 + c) =
+                                l > 0.f ? make_float4(__uint_as_float(x[c]), __uint_as_float(x[c + 1]),
+                                                      __uint_as_float(x[c + 2]), __uint_as_float(x[c + 3]))
+                                        : make_float4(0.f, 0.f, 0.f, 0.f);
                     }
                 }
-                tc::wait_st();
-                // zero the V rows of masked pages and past the partition's last
-                // token (0 * NaN would otherwise reach O), once the stage's
-                // copies have landed
-                const int tb = (pb + j * NPB) * BS;
-                const bool holes = tb + BN > tend || bits != (1u << NPB) - 1u;
-                if (holes) {
-                    if (!__all_sync(kFullMask, wait(v_full + st, (j / NS) & 1))) break;
-                    uint8_t* vt = smem + L.v_off + (size_t)st * L.tile_bytes;
-                    for (int idx = sr; idx < BN * DBLK * 8; idx += 256) {
-                        const int row = idx / (DBLK * 8), rem = idx % (DBLK * 8);
-                        if (!((bits >> (row / BS)) & 1u) || tb + row >= tend)
-                            *reinterpret_cast<uint4*>(vt + (rem >> 3) * BN * 128 + row * 128 +
-                                                      (rem & 7) * 16) = make_uint4(0, 0, 0, 0);
+            } else if (have_o && !dead) {
+                // a grid-position CTA: out (one partition) or its partition's
+                // workspace rows; the balanced split: out for a whole unit, else
+                // the CTA's record slot -- 0 for its first segment, 1 for a later one
+                const bool fin = bal ? g.whole : (bool)p.final_out;
+                const bool live = u < U;
+                const float inv = l > 0.f ? 1.f / l : 0.f;
+                size_t orow = 0;
+                if (live) {
+                    if (fin)
+                        orow = row_off(g.b, g.kvh, u);
+                    else if (bal)
+                        orow = (((size_t)blockIdx.x * 2 + (s == 0 ? 0 : 1)) * U + u) * D;
+                    else
+                        orow = ((((size_t)g.b * Hkv + g.kvh) * p.num_parts + part) * U + u) * D;
+                    if (!fin && wg == 0) {
+                        p.part_ml[(orow / D) * 2] = l > 0.f ? m : NEG_INF;
+                        p.part_ml[(orow / D) * 2 + 1] = l;
                     }
-                    fence_proxy_async_smem();
                 }
-            }
-            tc::fence_before_sync();
-            mbar_arrive(smem_u32(p_full + j % NB));
-        }
-        // ---- epilogue: O / l, or the partial (m, l, O); each warpgroup its
-        // half of the columns ----
-        bool have_o = __all_sync(kFullMask, j == nblk && !*abort_flag);
-        if (have_o)
-            have_o = __all_sync(kFullMask,
-                                wait(pv_done + (nblk - 1) % NB, ((nblk - 1) / NB) & 1));
-        float lo_half = 0.f;
-        if (have_o) have_o = exchange(xl, l, lo_half);
-        tc::fence_after_sync();
-        if (have_o) l += lo_half;
-        if (p.cluster_reduce) {
-            // park this CTA's partial in its own shared memory (the operand
-            // buffers are idle: every copy and MMA has completed)
-            const bool rows_ok = have_o && !dead;
-            if (wg == 0) {
-                cl_m[r] = rows_ok && l > 0.f ? m : NEG_INF;
-                cl_l[r] = rows_ok ? l : 0.f;
-            }
-            if (rows_ok) {
                 uint32_t x[16];
 #pragma unroll 1
                 for (int c0 = wg * (D / 2); c0 < (wg + 1) * (D / 2); c0 += 16) {
                     tc::ld_32x32b_x16(lane_base + O_COL + c0, x);
                     tc::wait_ld();
+                    if (!live) continue;
+                    float v[16];
 #pragma unroll
-                    for (int c = 0; c < 16; c += 4)
-                        *reinterpret_cast<float4*>(cl_o + r * CL + c0 + c) =
-                            l > 0.f ? make_float4(__uint_as_float(x[c]), __uint_as_float(x[c + 1]),
-                                                  __uint_as_float(x[c + 2]), __uint_as_float(x[c + 3]))
-                                    : make_float4(0.f, 0.f, 0.f, 0.f);
+                    for (int c = 0; c < 16; ++c)
+                        v[c] = l > 0.f ? __uint_as_float(x[c]) * (fin ? inv : 1.f) : 0.f;
+                    if (!fin || p.out_dtype == PA_F32) {
+                        float* dst = (fin ? static_cast<float*>(p.out) : p.part_acc) + orow + c0;
+#pragma unroll
+                        for (int c = 0; c < 16; c += 4)
+                            *reinterpret_cast<float4*>(dst + c) =
+                                make_float4(v[c], v[c + 1], v[c + 2], v[c + 3]);
+                    } else {
+                        uint32_t w[8];
+#pragma unroll
+                        for (int c = 0; c < 16; c += 2) w[c / 2] = Mma<KV>::pack(v[c], v[c + 1]);
+                        uint4* dst = reinterpret_cast<uint4*>(static_cast<KV*>(p.out) + orow + c0);
+                        dst[0] = make_uint4(w[0], w[1], w[2], w[3]);
+                        dst[1] = make_uint4(w[4], w[5], w[6], w[7]);
+                    }
                 }
             }
-        } else if (have_o && !dead) {
-            const bool live = u < U;
-            const float inv = l > 0.f ? 1.f / l : 0.f;
-            size_t orow = 0;
-            if (live) {
-                orow = p.final_out ? row_off(u)
-                                   : ((((size_t)b * Hkv + kvh) * p.num_parts + part) * U + u) * D;
-                if (!p.final_out && wg == 0) {
-                    p.part_ml[(orow / D) * 2] = l > 0.f ? m : NEG_INF;
-                    p.part_ml[(orow / D) * 2 + 1] = l;
-                }
+            if (bal) {
+                // O of this segment has been read out: the next segment's first
+                // P V may overwrite it
+                tc::fence_before_sync();
+                __syncwarp();
+                if (lane == 0) mbar_arrive(smem_u32(o_free));
             }
-            uint32_t x[16];
-#pragma unroll 1
-            for (int c0 = wg * (D / 2); c0 < (wg + 1) * (D / 2); c0 += 16) {
-                tc::ld_32x32b_x16(lane_base + O_COL + c0, x);
-                tc::wait_ld();
-                if (!live) continue;
-                float v[16];
-#pragma unroll
-                for (int c = 0; c < 16; ++c)
-                    v[c] = l > 0.f ? __uint_as_float(x[c]) * (p.final_out ? inv : 1.f) : 0.f;
-                if (!p.final_out || p.out_dtype == PA_F32) {
-                    float* dst = (p.final_out ? static_cast<float*>(p.out) : p.part_acc) + orow + c0;
-#pragma unroll
-                    for (int c = 0; c < 16; c += 4)
-                        *reinterpret_cast<float4*>(dst + c) =
-                            make_float4(v[c], v[c + 1], v[c + 2], v[c + 3]);
-                } else {
-                    uint32_t w[8];
-#pragma unroll
-                    for (int c = 0; c < 16; c += 2) w[c / 2] = Mma<KV>::pack(v[c], v[c + 1]);
-                    uint4* dst = reinterpret_cast<uint4*>(static_cast<KV*>(p.out) + orow + c0);
-                    dst[0] = make_uint4(w[0], w[1], w[2], w[3]);
-                    dst[1] = make_uint4(w[4], w[5], w[6], w[7]);
-                }
-            }
-        }
+            return have_o && !*abort_flag;
+        });
     }
 
     // ---- release tensor memory once every role is done with it ----
