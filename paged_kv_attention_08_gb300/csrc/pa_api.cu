@@ -46,6 +46,7 @@ PFN_cuTensorMapEncodeTiled_v12000 g_encode = nullptr;
 //   PA_NO_PDL=1                      launch without programmatic dependent launch
 //   PA_NO_CLUSTER=1                  never reduce partitions inside a cluster
 //   PA_BALANCED=1|2                  let the automatic plan pick the balanced split
+//   PA_NO_PERSIST=1                  tile kernel: one CTA per unit instead of persistent CTAs
 //   PA_MULTI_KERNEL=mma|tile         initial value of PA_SWITCH_MULTI_KERNEL
 //   PA_TILE_COMPACT_Q=0              initial value of PA_SWITCH_TILE_COMPACT_Q
 // The last two can also be changed at run time through pa_set_switch.  None
@@ -71,13 +72,14 @@ int parse_kernel(const char* v) {
 int parse_compact(const char* v) { return std::atoi(v) == 0 ? 0 : 1; }
 
 struct LoadTimeEnv {
-    int tune_streams, tune_stages, no_pdl, no_cluster, balanced;
+    int tune_streams, tune_stages, no_pdl, no_cluster, balanced, no_persist;
 };
 const LoadTimeEnv g_env = {env_value("PA_TUNE_STREAMS", 0, parse_positive),
                            env_value("PA_TUNE_STAGES", 0, parse_positive),
                            env_value("PA_NO_PDL", 0, parse_flag),
                            env_value("PA_NO_CLUSTER", 0, parse_flag),
-                           env_value("PA_BALANCED", 0, parse_balanced)};
+                           env_value("PA_BALANCED", 0, parse_balanced),
+                           env_value("PA_NO_PERSIST", 0, parse_flag)};
 std::atomic<int> g_switch_multi_kernel{env_value("PA_MULTI_KERNEL", PA_KERNEL_AUTO, parse_kernel)};
 std::atomic<int> g_switch_compact_q{env_value("PA_TILE_COMPACT_Q", 1, parse_compact)};
 
@@ -246,6 +248,7 @@ struct Plan {
     int num_ctas;    // balanced: grid size
     bool tile;       // several query tokens on the tcgen05 tile kernel (128-row tiles)
     int tile_qr;     // tile kernel: Q rows staged in shared memory (128, or 16: compact)
+    bool persistent; // tile kernel, one pass: num_ctas CTAs take the units in turn, whole
 };
 
 Plan plan_with(const pa_shape* s, int pages, int pp, bool cluster_ok,
@@ -256,6 +259,7 @@ Plan plan_with(const pa_shape* s, int pages, int pp, bool cluster_ok,
     p.num_ctas = 0;
     p.tile = false;
     p.tile_qr = kTileRows;
+    p.persistent = false;
     if (pp < 1) pp = 1;
     p.num_parts = (pages + pp - 1) / pp;
     if (p.num_parts < 1) p.num_parts = 1;
@@ -509,6 +513,14 @@ Plan tile_plan(const pa_shape* s, int32_t max_context_len, int32_t partition_tok
         Plan p = plan_with(s, pages, pp, cluster);
         p.tile = true;
         p.tile_qr = qr;
+        // one pass over more units than fit at once: persistent CTAs, one
+        // per resident slot, take the units in turn, so that a unit's start
+        // (its Q, the first K / V blocks) overlaps the previous unit's end
+        if (p.num_parts <= 1 && units > slots && tile_q_bufs(s->head_dim, qr) == 2 &&
+            !g_env.no_persist) {
+            p.persistent = true;
+            p.num_ctas = (int)slots;
+        }
         return p;
     }
     // an explicit partition count: a cluster when its partial fits in shared
@@ -794,9 +806,15 @@ pa_status launch_tile(void* out, const void* q, const void* k, const void* v, co
     if (compact && (s->head_dim != 256 || rows > kTileCompactQRows)) return PA_ERR_UNSUPPORTED;
     if (plan.cluster && !tile_cluster_fits(s, plan.tile_qr)) return PA_ERR_UNSUPPORTED;
     p.balanced = plan.balanced ? 1 : 0;
+    p.persistent = plan.persistent ? 1 : 0;
     if (plan.balanced) {
         if (!compact || plan.cluster) return PA_ERR_UNSUPPORTED;
         p.final_out = 0;
+        L.grid = dim3((unsigned)plan.num_ctas);
+    } else if (plan.persistent) {
+        if (plan.cluster || plan.num_parts > 1 || tile_q_bufs(s->head_dim, plan.tile_qr) != 2)
+            return PA_ERR_UNSUPPORTED;
+        p.final_out = 1;
         L.grid = dim3((unsigned)plan.num_ctas);
     } else {
         L.grid = dim3((unsigned)plan.num_parts, (unsigned)grid_y, (unsigned)s->batch);
@@ -881,7 +899,7 @@ pa_status pa_decode(void* out, const void* q, const void* k_cache, const void* v
     st = device_state(&sms, &err);
     if (st != PA_OK) return st;
     Plan plan{shape->max_blocks_per_seq, 1, false,
-              (int64_t)shape->batch * shape->num_kv_heads > sms, false, 0, false};
+              (int64_t)shape->batch * shape->num_kv_heads > sms, false, 0, false, kTileRows, false};
     return launch_attention(out, q, k_cache, v_cache, block_tables, context_lens, shape, scale,
                             plan, nullptr, nullptr, err, static_cast<cudaStream_t>(stream));
 }
@@ -974,13 +992,13 @@ pa_status pa_plan_info(const pa_shape* shape, int32_t q_len, int32_t max_context
     desc->reduce = plan.balanced ? 3 : (plan.num_parts <= 1 ? 0 : (plan.cluster ? 1 : 2));
     if (plan.tile) {
         const int64_t tiles = ((int64_t)q_len * G + kTileRows - 1) / kTileRows;
-        desc->ctas = plan.balanced ? plan.num_ctas
+        desc->ctas = (plan.balanced || plan.persistent) ? plan.num_ctas
                                    : (int32_t)((int64_t)shape->batch * shape->num_kv_heads * tiles *
                                                plan.num_parts);
         desc->threads = kTileThreads;
     } else {
         const Tune t = pick_tune(shape, plan.many_ctas);
-        desc->ctas = plan.balanced ? plan.num_ctas
+        desc->ctas = (plan.balanced || plan.persistent) ? plan.num_ctas
                                    : (int32_t)((int64_t)shape->batch * shape->num_kv_heads *
                                                q_chunks_for(shape, q_len) * plan.num_parts);
         desc->threads = 32 * t.nt * t.nh;

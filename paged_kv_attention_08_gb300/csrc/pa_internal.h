@@ -39,6 +39,8 @@ struct AttnParams {
     int32_t balanced;         // 1: CTA c takes pages [c*W/C, (c+1)*W/C) of the flattened
                               //    (sequence, kv head, page) order; units it covers whole are
                               //    written out, pieces become records [C][2][G] in part_acc/ml
+    int32_t persistent;       // tile kernel: 1: CTA c takes the units c, c + C, c + 2C, ... whole
+                              //    (C = gridDim.x; units = (sequence, kv head, 128-row tile))
     int32_t cluster_reduce;   // 1: the num_parts partitions of a (sequence, kv head) form one
                               //    thread-block cluster and reduce through distributed shared
                               //    memory; 0: partials go to the workspace for the combine kernel
@@ -149,10 +151,17 @@ __host__ __device__ constexpr int tile_stages(int D, int qr = kTileRows) {
     return D == 64 ? 4 : (D == 256 && qr == kTileCompactQRows ? 3 : 2);
 }
 
+// Q tiles in shared memory: two (a unit's Q while the next one's is staged)
+// where they fit beside the rings -- compact tiles, and whole tiles up to
+// head_dim 128 -- else one.
+__host__ __device__ constexpr int tile_q_bufs(int D, int qr = kTileRows) {
+    return (qr == kTileCompactQRows || D <= 128) ? 2 : 1;
+}
+
 struct TileSmem {
     uint32_t tile_bytes;   // one K (or V) block tile: BN * head_dim * 2
     uint32_t q_off;        // Q tiles: [head_dim / 64] column blocks of qr rows x 128 bytes each;
-                           // two of them for compact units (the balanced split's segments)
+                           // tile_q_bufs of them
     uint32_t k_off;        // [ns] K stages
     uint32_t v_off;        // [ns] V stages
     uint32_t bar_off;      // mbarriers: k_full[ns], k_empty[ns], v_full[ns], v_empty[ns],
@@ -176,7 +185,7 @@ __host__ __device__ inline TileSmem tile_smem_layout(int D, int BS, int qr = kTi
     const bool compact = qr == kTileCompactQRows;
     L.q_off = 0;
     // a multiple of 1024 (qr and D multiples of 16 and 64)
-    L.k_off = (compact ? 2u : 1u) * 2u * qr * D;
+    L.k_off = (uint32_t)tile_q_bufs(D, qr) * 2u * qr * D;
     L.v_off = L.k_off + L.tile_bytes * L.ns;
     uint32_t o = L.v_off + L.tile_bytes * L.ns;
     L.bar_off = o;

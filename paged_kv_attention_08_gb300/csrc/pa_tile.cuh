@@ -82,6 +82,7 @@ __global__ void __launch_bounds__(kTileThreads, 1)
     // result stays a weighted mean of the V rows.
     constexpr bool kSplitP = kBF;
     constexpr bool kCanBalance = QR == kTileCompactQRows;  // the balanced split: compact units
+    constexpr bool kTwoQ = tile_q_bufs(D, QR) == 2;         // several segments per CTA possible
     constexpr uint32_t kCols = tile_tmem_cols(D);
     constexpr int NB = kTileSBufs;
     constexpr uint32_t O_COL = 0, S_COL = D;  // S buffer b at S_COL + b*BN; P (hi, lo) over it
@@ -118,8 +119,10 @@ __global__ void __launch_bounds__(kTileThreads, 1)
     const int G = p.group, Q = p.q_len, Hkv = p.num_kv_heads, U = p.unit_rows;
     const int gshift = __ffs(G) - 1;
     const bool bal = kCanBalance && p.balanced;
+    const bool pers = kTwoQ && !bal && p.persistent;
+    const bool multi = bal || pers;  // the CTA may take several segments
     const int part = blockIdx.x;
-    const int tile = bal ? 0 : (int)blockIdx.y / Hkv;
+    const int tiles = (U + kTileRows - 1) / kTileRows;  // 128-row tiles of a unit
 
     grid_dependency_wait();
     grid_launch_dependents();
@@ -131,12 +134,14 @@ __global__ void __launch_bounds__(kTileThreads, 1)
 
     // ---- the CTA's segments ----
     struct Seg {
-        int b, kvh, pb, pe, T, np;  // pages [pb, pe) of the np of (b, kvh); T tokens reach the table
-        bool whole;                 // the segment is the whole unit
+        int b, kvh, tile, pb, pe, T, np;  // pages [pb, pe) of the np of (b, kvh); T tokens
+                                          // reach the table; rows of `tile`
+        bool whole;                       // the segment is the whole unit
     };
     struct Walk {
-        long long cur, end, base;  // flat position, end of the share, flat start of sequence b
+        long long cur, end, base;  // balanced: flat position, end of the share, flat start of b
         int b;
+        long long x;               // persistent: the next unit index
     };
     if (bal) {
         // pages of every sequence, their total W (times the kv heads), and the
@@ -189,12 +194,38 @@ __global__ void __launch_bounds__(kTileThreads, 1)
         if (walk0[0] >= walk0[1]) return;  // an empty share (fewer pages than CTAs)
     }
     auto walk_init = [&](Walk& w) {
+        if (pers) {
+            w.x = blockIdx.x;
+            return;
+        }
         w.cur = walk0[0];
         w.end = walk0[1];
         w.base = walk0[2];
         w.b = (int)walk0[3];
     };
+    // unit x of the persistent order: tiles of a (sequence, kv head) in turn,
+    // so that the CTAs working at once share each page through L2
+    auto unit_of = [&](long long x, Seg& g) {
+        g.tile = (int)(x % tiles);
+        const long long bk = x / tiles;
+        g.kvh = (int)(bk % Hkv);
+        g.b = (int)(bk / Hkv);
+        g.T = reachable_tokens(p.context_lens, g.b, p.max_blocks, BS);
+        g.np = (g.T + BS - 1) / BS;
+        g.pb = 0;
+        g.pe = g.np;
+        g.whole = true;
+    };
+    const long long nunits = (long long)p.batch * Hkv * tiles;
     auto walk_next = [&](Walk& w, Seg& g) -> bool {
+        if (pers) {  // the CTA's units with pages (empty ones are written out apart)
+            while (w.x < nunits) {
+                unit_of(w.x, g);
+                w.x += gridDim.x;
+                if (g.np > 0) return true;
+            }
+            return false;
+        }
         if (w.cur >= w.end) return false;
         const int np = seq_pages[w.b];
         const long long off = w.cur - w.base;
@@ -202,6 +233,7 @@ __global__ void __launch_bounds__(kTileThreads, 1)
         const int len = (int)min(w.end - w.cur, (long long)(np - j));
         g.b = w.b;
         g.kvh = (int)(off / np);
+        g.tile = 0;
         g.pb = j;
         g.pe = j + len;
         g.np = np;
@@ -217,9 +249,10 @@ __global__ void __launch_bounds__(kTileThreads, 1)
     };
     // the segment of a grid-position CTA
     Seg seg0;
-    if (!bal) {
+    if (!multi) {
         seg0.b = blockIdx.z;
         seg0.kvh = (int)blockIdx.y % Hkv;
+        seg0.tile = (int)blockIdx.y / Hkv;
         seg0.T = reachable_tokens(p.context_lens, seg0.b, p.max_blocks, BS);
         seg0.np = (seg0.T + BS - 1) / BS;
         seg0.pb = part * p.part_pages;
@@ -228,7 +261,7 @@ __global__ void __launch_bounds__(kTileThreads, 1)
     }
     // calls fn(segment, index) for each of the CTA's segments until fn returns false
     auto for_segments = [&](auto&& fn) {
-        if (!bal) {
+        if (!multi) {
             (void)fn(seg0, 0);
             return;
         }
@@ -285,7 +318,7 @@ __global__ void __launch_bounds__(kTileThreads, 1)
         __syncthreads();
         for (int idx = tid; idx < (r1 - r0) * (D / 4); idx += kTileThreads) {
             const int t = idx / (D / 4), c4 = idx % (D / 4);
-            const int r = r0 + t, u = tile * kTileRows + r;
+            const int r = r0 + t, u = seg0.tile * kTileRows + r;
             if (u >= U) continue;
             float4 a = make_float4(0.f, 0.f, 0.f, 0.f);
 #pragma unroll
@@ -309,7 +342,7 @@ __global__ void __launch_bounds__(kTileThreads, 1)
         cluster_sync_relaxed();  // no CTA leaves while others still read its partial
     };
 
-    if (!bal && seg0.pe <= seg0.pb) {
+    if (!multi && seg0.pe <= seg0.pb) {
         if (p.cluster_reduce) {
             // no pages here, but the cluster's merge needs this CTA: an empty partial
             for (int r = tid; r < kTileRows; r += kTileThreads) {
@@ -323,7 +356,7 @@ __global__ void __launch_bounds__(kTileThreads, 1)
         // empty-context result; the combine never reads such partitions.
         if (p.final_out) {
             for (int idx = tid; idx < kTileRows * D; idx += kTileThreads) {
-                const int u = tile * kTileRows + idx / D;
+                const int u = seg0.tile * kTileRows + idx / D;
                 if (u < U) store_out(p.out, row_off(seg0.b, seg0.kvh, u) + idx % D, 0.f, p.out_dtype);
             }
         }
@@ -374,9 +407,10 @@ __global__ void __launch_bounds__(kTileThreads, 1)
     // and their P and O rows are never used ----
     auto stage_q = [&](const Seg& g, int qb, int t0, int step) {
         uint8_t* qs = smem + L.q_off + (size_t)qb * (2u * QR * D);
+#pragma unroll 4
         for (int i = t0; i < QR * (D / 8); i += step) {
             const int r = i / (D / 8), c = i % (D / 8);
-            const int u = tile * kTileRows + r;
+            const int u = g.tile * kTileRows + r;
             uint4 v = make_uint4(0, 0, 0, 0);
             if (u < U)
                 v = __ldg(reinterpret_cast<const uint4*>(static_cast<const KV*>(p.q) +
@@ -472,9 +506,9 @@ __global__ void __launch_bounds__(kTileThreads, 1)
                 (void)mbar_wait_bounded(smem_u32(full + k % NS), (k / NS) & 1, p.timeout_ns);
         }
     } else if (warp == 2) {
-        // ====== Q of later segments (balanced split): buffer s & 1, once the
-        // S MMAs of segment s - 2 (the buffer's previous user) are done ======
-        if (bal) {
+        // ====== Q of later segments: buffer s & 1, once the S MMAs of
+        // segment s - 2 (the buffer's previous user) are done ======
+        if (multi) {
             for_segments([&](const Seg& g, int s) {
                 if (s == 0) return true;  // staged with the others at the start
                 if (s >= 2 && !__all_sync(kFullMask, wait(q_free + (s & 1), ((s - 2) >> 1) & 1)))
@@ -571,7 +605,7 @@ __global__ void __launch_bounds__(kTileThreads, 1)
                     tc::commit(smem_u32(s_full + i % NB));
                     tc::commit(smem_u32(k_empty + st));
                     // the segment's last S: its Q buffer is free once these complete
-                    if (bal && k == nblk - 1) tc::commit(smem_u32(q_free + (s & 1)));
+                    if (multi && k == nblk - 1) tc::commit(smem_u32(q_free + (s & 1)));
                     if (i >= 1 && !issue_pv()) return ok = false;
                     live_prev = live_cur;
                     seg_prev = s;
@@ -596,7 +630,6 @@ __global__ void __launch_bounds__(kTileThreads, 1)
         const int r = w4 * 32 + lane;
         const int sr = wg * 128 + r;  // 0 .. 255 among the softmax threads
         const uint32_t lane_base = tmem + ((uint32_t)(w4 * 32) << 16);
-        const int u = tile * kTileRows + r;
         const float qscale = p.qscale;
         // exchange round nx: publish v, return the other warpgroup's value
         int nx = 0;
@@ -608,11 +641,24 @@ __global__ void __launch_bounds__(kTileThreads, 1)
             ++nx;
             return ok;
         };
-        // a warp whose 32 rows all lie past the unit's rows (a partial tile)
-        // only keeps the barriers going: its P and O rows are never used
-        const bool dead = tile * kTileRows + w4 * 32 >= U;
+        if (pers) {
+            // the CTA's units without a page: an all-zero output
+            for (long long x = blockIdx.x; x < nunits; x += gridDim.x) {
+                Seg g;
+                unit_of(x, g);
+                if (g.np > 0) continue;
+                for (int idx = sr; idx < kTileRows * D; idx += 256) {
+                    const int uu = g.tile * kTileRows + idx / D;
+                    if (uu < U) store_out(p.out, row_off(g.b, g.kvh, uu) + idx % D, 0.f, p.out_dtype);
+                }
+            }
+        }
         int j = 0;  // blocks over all segments
         for_segments([&](const Seg& g, int s) {
+            const int u = g.tile * kTileRows + r;
+            // a warp whose 32 rows all lie past the unit's rows (a partial tile)
+            // only keeps the barriers going: its P and O rows are never used
+            const bool dead = g.tile * kTileRows + w4 * 32 >= U;
             const int nblk = nblk_of(g);
             const int jb = j;  // the segment's first block
             const int tend = min(g.T, g.pe * BS);  // tokens of this segment end here
@@ -780,7 +826,7 @@ __global__ void __launch_bounds__(kTileThreads, 1)
                 // a grid-position CTA: out (one partition) or its partition's
                 // workspace rows; the balanced split: out for a whole unit, else
                 // the CTA's record slot -- 0 for its first segment, 1 for a later one
-                const bool fin = bal ? g.whole : (bool)p.final_out;
+                const bool fin = bal ? g.whole : (pers || p.final_out);
                 const bool live = u < U;
                 const float inv = l > 0.f ? 1.f / l : 0.f;
                 size_t orow = 0;
@@ -822,7 +868,7 @@ __global__ void __launch_bounds__(kTileThreads, 1)
                     }
                 }
             }
-            if (bal) {
+            if (multi) {
                 // O of this segment has been read out: the next segment's first
                 // P V may overwrite it
                 tc::fence_before_sync();
