@@ -165,7 +165,7 @@ struct TileSmem {
     uint32_t k_off;        // [ns] K stages
     uint32_t v_off;        // [ns] V stages
     uint32_t bar_off;      // mbarriers: k_full[ns], k_empty[ns], v_full[ns], v_empty[ns],
-                           // s_full[3], p_full[3], pv_done[3], final, q_ready, q_full[2],
+                           // s_full[3], p_full[2][3], pv_done[3], final, q_ready, q_full[2],
                            // q_free[2], o_free
     uint32_t phys_off;     // [ns][BN / block_size] int32 physical block of each K stage's pages
     uint32_t xchg_off;     // softmax exchange: row maxima [2][2][128], normalisers [2][128] (fp32),
@@ -189,7 +189,7 @@ __host__ __device__ inline TileSmem tile_smem_layout(int D, int BS, int qr = kTi
     L.v_off = L.k_off + L.tile_bytes * L.ns;
     uint32_t o = L.v_off + L.tile_bytes * L.ns;
     L.bar_off = o;
-    o += 8u * (4 * L.ns + 3 * kTileSBufs + 2 + 5);
+    o += 8u * (4 * L.ns + 4 * kTileSBufs + 2 + 5);  // p_full: one set per softmax warpgroup
     L.phys_off = o;
     o += 4u * L.ns * (BN / BS);
     L.xchg_off = pa_align_up(o, 16);
@@ -212,8 +212,9 @@ __host__ __device__ constexpr uint32_t tile_cluster_bytes(int D) {
     return 4u * (kTileRows * (D + 4) + 2 * kTileRows + kTileRows * 8);
 }
 
-// Tensor-memory columns of the tile kernel: O [head_dim], then kTileSBufs S
-// buffers of BN fp32 columns (P, as 16-bit high and low parts, overwrites S).
+// Tensor-memory columns of the tile kernel: O [head_dim] (two of them, one per
+// softmax warpgroup, at head_dim <= 128), then the S buffers of BN fp32
+// columns (P, as 16-bit high and low parts, overwrites S) in what is left.
 __host__ __device__ constexpr uint32_t tile_tmem_cols(int D) {
     return (uint32_t)D + kTileSBufs * tile_block_tokens(D) <= 256u ? 256u : 512u;
 }

@@ -84,9 +84,17 @@ __global__ void __launch_bounds__(kTileThreads, 1)
     constexpr bool kCanBalance = QR == kTileCompactQRows;  // the balanced split: compact units
     constexpr bool kTwoQ = tile_q_bufs(D, QR) == 2;         // several segments per CTA possible
     constexpr uint32_t kCols = tile_tmem_cols(D);
-    constexpr int NB = kTileSBufs;
-    constexpr uint32_t O_COL = 0, S_COL = D;  // S buffer b at S_COL + b*BN; P (hi, lo) over it
-    static_assert(D + NB * BN <= 512, "tensor memory");
+    // Whole tiles up to head_dim 128 give each softmax warpgroup an O of its
+    // own: warpgroup h keeps the running max, the normaliser and O of its half
+    // of every block's keys, so the two never wait on each other inside the
+    // block loop; the halves are merged once, in the epilogue.  Otherwise the
+    // warpgroups share one O and exchange their row maxima every block.
+    constexpr bool kHalfO = QR == kTileRows && D <= 128;
+    constexpr int NB = kHalfO ? (512 - 2 * D) / BN : kTileSBufs;  // S / P buffers
+    // O (h) at O_COL + h * D; S buffer b at S_COL + b*BN; P (hi, lo) over it
+    constexpr uint32_t O_COL = 0, S_COL = kHalfO ? 2 * D : D;
+    static_assert(NB >= 2 && NB <= kTileSBufs, "S / P buffers");
+    static_assert(S_COL + NB * BN <= 512, "tensor memory");
 
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = reinterpret_cast<uint8_t*>(
@@ -99,9 +107,9 @@ __global__ void __launch_bounds__(kTileThreads, 1)
     uint64_t* v_full = bars + 2 * NS;
     uint64_t* v_empty = bars + 3 * NS;
     uint64_t* s_full = bars + 4 * NS;
-    uint64_t* p_full = s_full + NB;
-    uint64_t* pv_done = s_full + 2 * NB;
-    uint64_t* final_bar = s_full + 3 * NB;
+    uint64_t* p_full = s_full + kTileSBufs;  // [2][3]: per softmax warpgroup with kHalfO
+    uint64_t* pv_done = p_full + 2 * kTileSBufs;
+    uint64_t* final_bar = pv_done + kTileSBufs;
     uint64_t* q_ready = final_bar + 1;  // the first segment's Q tile is in shared memory
     uint64_t* q_full = q_ready + 1;     // [2] Q buffer b holds a later segment's Q
     uint64_t* q_free = q_full + 2;      // [2] the S MMAs of buffer b's segment have completed
@@ -372,7 +380,8 @@ __global__ void __launch_bounds__(kTileThreads, 1)
         }
         for (int i = 0; i < NB; ++i) {
             mbar_init(smem_u32(s_full + i), 1);
-            mbar_init(smem_u32(p_full + i), 256);
+            mbar_init(smem_u32(p_full + i), kHalfO ? 128 : 256);
+            mbar_init(smem_u32(p_full + kTileSBufs + i), 128);
             mbar_init(smem_u32(pv_done + i), 1);
         }
         mbar_init(smem_u32(final_bar), 1);
@@ -546,24 +555,49 @@ __global__ void __launch_bounds__(kTileThreads, 1)
                     tc::fence_after_sync();
                     started = false;
                 }
-                if (!wait(p_full + j % NB, (j / NB) & 1)) return false;
                 if (!wait(v_full + st, (j / NS) & 1)) return false;
-                tc::fence_after_sync();
-                if (live_prev) {
-                    const uint32_t v_base = smem_u32(smem + L.v_off) + (uint32_t)st * L.tile_bytes;
-                    const uint32_t p_hi = tmem + S_COL + (j % NB) * BN;
-                    const uint32_t p_lo = p_hi + BN / 2;
-                    // V: MN-major, 64-column blocks BN*128 bytes apart, 8-row
-                    // groups 1024 bytes apart; rows ks*16 .. +15 per step
-                    const uint64_t vd0 = tc::smem_desc(v_base, BN * 128, 1024, tc::kSwizzle128B);
+                const uint32_t v_base = smem_u32(smem + L.v_off) + (uint32_t)st * L.tile_bytes;
+                // V: MN-major, 64-column blocks BN*128 bytes apart, 8-row
+                // groups 1024 bytes apart; rows ks*16 .. +15 per step
+                const uint64_t vd0 = tc::smem_desc(v_base, BN * 128, 1024, tc::kSwizzle128B);
+                if constexpr (kHalfO) {
+                    // each warpgroup's half of the keys into its own O, as soon as
+                    // that half's P is in tensor memory
 #pragma unroll
-                    for (int ks = 0; ks < BN / 16; ++ks) {
-                        const uint64_t vd = vd0 + (uint64_t)((ks * 16 * 128) >> 4);
-                        tc::mma_ts(tmem + O_COL, p_hi + ks * 8, vd, id_o,
-                                   (started || ks > 0) ? 1u : 0u);
-                        if (kSplitP) tc::mma_ts(tmem + O_COL, p_lo + ks * 8, vd, id_o, 1u);
+                    for (int h = 0; h < 2; ++h) {
+                        if (!wait(p_full + h * kTileSBufs + j % NB, (j / NB) & 1)) return false;
+                        tc::fence_after_sync();
+                        if (live_prev) {
+                            // half h's P: hi at columns h*BN/2 .., lo BN/4 after it
+                            const uint32_t ph = tmem + S_COL + (j % NB) * BN + h * (BN / 2);
+#pragma unroll
+                            for (int kk = 0; kk < BN / 32; ++kk) {
+                                const int ks = h * (BN / 32) + kk;  // token rows of V
+                                const uint64_t vd = vd0 + (uint64_t)((ks * 16 * 128) >> 4);
+                                tc::mma_ts(tmem + O_COL + h * D, ph + kk * 8, vd, id_o,
+                                           (started || kk > 0) ? 1u : 0u);
+                                if (kSplitP)
+                                    tc::mma_ts(tmem + O_COL + h * D, ph + BN / 4 + kk * 8, vd, id_o, 1u);
+                            }
+                        }
                     }
-                    started = true;
+                    if (live_prev) started = true;
+                } else {
+                    if (!wait(p_full + j % NB, (j / NB) & 1)) return false;
+                    tc::fence_after_sync();
+                    if (live_prev) {
+                        // P of all BN keys: hi at columns 0 .., lo BN/2 after it
+                        const uint32_t p_hi = tmem + S_COL + (j % NB) * BN;
+                        const uint32_t p_lo = p_hi + BN / 2;
+#pragma unroll
+                        for (int ks = 0; ks < BN / 16; ++ks) {
+                            const uint64_t vd = vd0 + (uint64_t)((ks * 16 * 128) >> 4);
+                            tc::mma_ts(tmem + O_COL, p_hi + ks * 8, vd, id_o,
+                                       (started || ks > 0) ? 1u : 0u);
+                            if (kSplitP) tc::mma_ts(tmem + O_COL, p_lo + ks * 8, vd, id_o, 1u);
+                        }
+                        started = true;
+                    }
                 }
                 tc::commit(smem_u32(pv_done + j % NB));
                 tc::commit(smem_u32(v_empty + st));
@@ -713,9 +747,14 @@ __global__ void __launch_bounds__(kTileThreads, 1)
                             }
                         }
                     }
-                    float mo;
-                    if (!exchange(xmax + (nx & 1) * 256, mx, mo)) break;
-                    const float ms = fmaxf(mx, mo) * qscale;
+                    float ms;
+                    if constexpr (kHalfO) {
+                        ms = mx * qscale;  // this warpgroup's half of the keys alone
+                    } else {
+                        float mo;
+                        if (!exchange(xmax + (nx & 1) * 256, mx, mo)) break;
+                        ms = fmaxf(mx, mo) * qscale;
+                    }
                     const bool need = ms > m + kTileRescaleSlack;
                     float alpha = 1.f;
                     if (need) {
@@ -724,21 +763,24 @@ __global__ void __launch_bounds__(kTileThreads, 1)
                         m = ms;
                     }
                     // O holds earlier blocks' sums only if this row had attended a token;
-                    // each warpgroup rescales its half of O's columns
+                    // each warpgroup rescales its own O (kHalfO) or its half of the
+                    // shared O's columns
                     if (__any_sync(kFullMask, need && alpha != 1.f)) {
                         if (j > jb && !__all_sync(kFullMask, wait(pv_done + (j - 1) % NB,
                                                                    ((j - 1) / NB) & 1)))
                             break;
                         tc::fence_after_sync();
+                        constexpr int kRC = kHalfO ? D : D / 2;  // columns rescaled
+                        const uint32_t ob = lane_base + O_COL + (kHalfO ? wg * D : wg * (D / 2));
                         uint32_t x[16];
 #pragma unroll 1
-                        for (int c0 = wg * (D / 2); c0 < (wg + 1) * (D / 2); c0 += 16) {
-                            tc::ld_32x32b_x16(lane_base + O_COL + c0, x);
+                        for (int c0 = 0; c0 < kRC; c0 += 16) {
+                            tc::ld_32x32b_x16(ob + c0, x);
                             tc::wait_ld();
 #pragma unroll
                             for (int c = 0; c < 16; ++c)
                                 x[c] = __float_as_uint(__uint_as_float(x[c]) * alpha);
-                            tc::st_32x32b_x16(lane_base + O_COL + c0, x);
+                            tc::st_32x32b_x16(ob + c0, x);
                         }
                         tc::wait_st();
                     }
@@ -765,9 +807,15 @@ __global__ void __launch_bounds__(kTileThreads, 1)
                                     l += h0 + h1;  // the weights the MMA uses
                                 }
                             }
-                            const uint32_t col = (uint32_t)(wg * BH + c0) / 2;
-                            tc::st_32x32b_x8(sb + col, ph);
-                            if (kSplitP) tc::st_32x32b_x8(sb + BN / 2 + col, pl);
+                            // kHalfO: the warpgroup's P inside its own S columns
+                            // (hi then lo), which it alone reads; otherwise hi in
+                            // [0, BN/2) and lo in [BN/2, BN) of the buffer (the
+                            // per-block exchange has seen both halves' S loaded)
+                            const uint32_t col_hi = kHalfO ? (uint32_t)(wg * BH + c0 / 2)
+                                                           : (uint32_t)(wg * BH + c0) / 2;
+                            const uint32_t col_lo = kHalfO ? col_hi + BH / 2 : col_hi + BN / 2;
+                            tc::st_32x32b_x8(sb + col_hi, ph);
+                            if (kSplitP) tc::st_32x32b_x8(sb + col_lo, pl);
                         }
                     }
                     tc::wait_st();
@@ -789,17 +837,51 @@ __global__ void __launch_bounds__(kTileThreads, 1)
                     }
                 }
                 tc::fence_before_sync();
-                mbar_arrive(smem_u32(p_full + j % NB));
+                mbar_arrive(smem_u32(p_full + (kHalfO ? wg * kTileSBufs : 0) + j % NB));
             }
             // ---- epilogue of the segment: O / l, or the partial (m, l, O);
             // each warpgroup its half of the columns ----
             bool have_o = __all_sync(kFullMask, k == nblk && !*abort_flag);
             if (have_o)
                 have_o = __all_sync(kFullMask, wait(pv_done + (j - 1) % NB, ((j - 1) / NB) & 1));
-            float lo_half = 0.f;
-            if (have_o) have_o = exchange(xl, l, lo_half);
+            // the rows' normaliser (and, with an O per warpgroup, their max and
+            // the weights of the two O's)
+            float w_own = 1.f, w_oth = 0.f;
+            if constexpr (kHalfO) {
+                float m_oth = NEG_INF, l_oth = 0.f;
+                if (have_o) have_o = exchange(xmax + (nx & 1) * 256, m, m_oth);
+                if (have_o) have_o = exchange(xl, l, l_oth);
+                const float M = fmaxf(m, m_oth);
+                w_own = m == NEG_INF ? 0.f : fast_exp2(m - M);
+                w_oth = m_oth == NEG_INF ? 0.f : fast_exp2(m_oth - M);
+                l = l * w_own + l_oth * w_oth;
+                m = M;
+            } else {
+                float lo_half = 0.f;
+                if (have_o) have_o = exchange(xl, l, lo_half);
+                if (have_o) l += lo_half;
+            }
             tc::fence_after_sync();
-            if (have_o) l += lo_half;
+            // the row's (unnormalised) O for columns c0 .. c0 + 15
+            auto load_o = [&](int c0, float (&v)[16]) {
+                uint32_t x[16];
+                if constexpr (kHalfO) {
+                    uint32_t y[16];
+                    tc::ld_32x32b_x16(lane_base + O_COL + wg * D + c0, x);
+                    tc::ld_32x32b_x16(lane_base + O_COL + (1 - wg) * D + c0, y);
+                    tc::wait_ld();
+                    // (an O never written holds garbage, but then its weight is 0)
+#pragma unroll
+                    for (int c = 0; c < 16; ++c)
+                        v[c] = (w_own != 0.f ? __uint_as_float(x[c]) * w_own : 0.f) +
+                               (w_oth != 0.f ? __uint_as_float(y[c]) * w_oth : 0.f);
+                } else {
+                    tc::ld_32x32b_x16(lane_base + O_COL + c0, x);
+                    tc::wait_ld();
+#pragma unroll
+                    for (int c = 0; c < 16; ++c) v[c] = __uint_as_float(x[c]);
+                }
+            };
             if (p.cluster_reduce) {
                 // park this CTA's partial in its own shared memory (the operand
                 // buffers are idle: every copy and MMA has completed)
@@ -809,16 +891,14 @@ __global__ void __launch_bounds__(kTileThreads, 1)
                     cl_l[r] = rows_ok ? l : 0.f;
                 }
                 if (rows_ok) {
-                    uint32_t x[16];
+                    float v[16];
 #pragma unroll 1
                     for (int c0 = wg * (D / 2); c0 < (wg + 1) * (D / 2); c0 += 16) {
-                        tc::ld_32x32b_x16(lane_base + O_COL + c0, x);
-                        tc::wait_ld();
+                        load_o(c0, v);
 #pragma unroll
                         for (int c = 0; c < 16; c += 4)
                             *reinterpret_cast<float4*>(cl_o + r * CL + c0 + c) =
-                                l > 0.f ? make_float4(__uint_as_float(x[c]), __uint_as_float(x[c + 1]),
-                                                      __uint_as_float(x[c + 2]), __uint_as_float(x[c + 3]))
+                                l > 0.f ? make_float4(v[c], v[c + 1], v[c + 2], v[c + 3])
                                         : make_float4(0.f, 0.f, 0.f, 0.f);
                     }
                 }
@@ -842,16 +922,13 @@ __global__ void __launch_bounds__(kTileThreads, 1)
                         p.part_ml[(orow / D) * 2 + 1] = l;
                     }
                 }
-                uint32_t x[16];
 #pragma unroll 1
                 for (int c0 = wg * (D / 2); c0 < (wg + 1) * (D / 2); c0 += 16) {
-                    tc::ld_32x32b_x16(lane_base + O_COL + c0, x);
-                    tc::wait_ld();
-                    if (!live) continue;
                     float v[16];
+                    load_o(c0, v);
+                    if (!live) continue;
 #pragma unroll
-                    for (int c = 0; c < 16; ++c)
-                        v[c] = l > 0.f ? __uint_as_float(x[c]) * (fin ? inv : 1.f) : 0.f;
+                    for (int c = 0; c < 16; ++c) v[c] = l > 0.f ? v[c] * (fin ? inv : 1.f) : 0.f;
                     if (!fin || p.out_dtype == PA_F32) {
                         float* dst = (fin ? static_cast<float*>(p.out) : p.part_acc) + orow + c0;
 #pragma unroll
