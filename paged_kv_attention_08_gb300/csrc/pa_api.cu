@@ -695,6 +695,27 @@ pa_status encode_maps_uncached(const pa_shape* s, const void* k, const void* v, 
     return PA_OK;
 }
 
+// The Q tiles of the tile kernel's later segments: q [batch * q_len, heads,
+// head_dim] read in boxes of 64 columns x (G heads x qr / G tokens), or x qr
+// heads of one token when the group has qr or more heads -- a tile's rows in
+// order -- with the 128-byte swizzle; past the last token the fill value (0).
+pa_status encode_q_map(const pa_shape* s, const void* q, int32_t q_len, int qr, CUtensorMap* mq) {
+    if (!g_encode) return PA_ERR_CUDA;  // set up by the K / V maps' first encode
+    const int G = s->num_heads / s->num_kv_heads;
+    const cuuint64_t e = elem_size(s->kv_dtype);
+    const cuuint64_t dims[3] = {(cuuint64_t)s->head_dim, (cuuint64_t)s->num_heads,
+                                (cuuint64_t)s->batch * (cuuint64_t)q_len};
+    const cuuint64_t strides[2] = {e * s->head_dim, e * s->head_dim * s->num_heads};
+    const cuuint32_t box[3] = {64u, (cuuint32_t)(G >= qr ? qr : G), (cuuint32_t)(G >= qr ? 1 : qr / G)};
+    const cuuint32_t estr[3] = {1u, 1u, 1u};
+    const CUtensorMapDataType dt =
+        s->kv_dtype == PA_BF16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16;
+    const CUresult r = g_encode(mq, dt, 3, const_cast<void*>(q), dims, strides, box, estr,
+                                CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                                CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    return r == CUDA_SUCCESS ? PA_OK : PA_ERR_CUDA;
+}
+
 pa_status launch_attention(void* out, const void* q, const void* k, const void* v,
                            const int32_t* bt, const int32_t* lens, const pa_shape* s, float scale,
                            const Plan& plan, float* part_acc, float* part_ml, int32_t* err,
@@ -818,6 +839,10 @@ pa_status launch_tile(void* out, const void* q, const void* k, const void* v, co
         L.grid = dim3((unsigned)plan.num_ctas);
     } else {
         L.grid = dim3((unsigned)plan.num_parts, (unsigned)grid_y, (unsigned)s->batch);
+    }
+    if (plan.balanced || plan.persistent) {
+        st = encode_q_map(s, q, q_len, plan.tile_qr, &L.tmap_q);
+        if (st != PA_OK) return st;
     }
     L.threads = kTileThreads;
     L.smem_bytes = tile_smem_layout(s->head_dim, s->block_size, plan.tile_qr).total + kSmemAlignSlack;

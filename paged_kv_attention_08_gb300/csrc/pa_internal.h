@@ -167,7 +167,8 @@ struct TileSmem {
     uint32_t bar_off;      // mbarriers: k_full[ns], k_empty[ns], v_full[ns], v_empty[ns],
                            // s_full[3], p_full[2][3], pv_done[3], final, q_ready, q_full[2],
                            // q_free[2], o_free
-    uint32_t phys_off;     // [ns][BN / block_size] int32 physical block of each K stage's pages
+    uint32_t phys_off;     // [ns][BN / block_size] int32 physical block of each K stage's pages,
+                           // then [ns] int32: V stage holds a page
     uint32_t xchg_off;     // softmax exchange: row maxima [2][2][128], normalisers [2][128] (fp32),
                            // then mbarriers xchg[2]
     uint32_t misc_off;     // tensor-memory base address, abort flag
@@ -191,7 +192,7 @@ __host__ __device__ inline TileSmem tile_smem_layout(int D, int BS, int qr = kTi
     L.bar_off = o;
     o += 8u * (4 * L.ns + 4 * kTileSBufs + 2 + 5);  // p_full: one set per softmax warpgroup
     L.phys_off = o;
-    o += 4u * L.ns * (BN / BS);
+    o += 4u * L.ns * (BN / BS + 1);
     L.xchg_off = pa_align_up(o, 16);
     o = L.xchg_off + 4u * (2 * 2 * 128 + 2 * 128) + 16;
     L.misc_off = pa_align_up(o, 16);
@@ -266,6 +267,7 @@ struct AttnLaunch {
     AttnParams p;
     CUtensorMap tmap_k;
     CUtensorMap tmap_v;
+    CUtensorMap tmap_q;  // tile kernel, several segments per CTA: the Q tiles of later segments
     int head_dim, block_size, kv_dtype;
     bool pdl;     // launch with programmatic stream serialization
     int cluster;  // > 1: cluster size along x (= partitions per sequence and kv head)

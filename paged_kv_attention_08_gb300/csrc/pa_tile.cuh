@@ -66,7 +66,8 @@ constexpr float kTileRescaleSlack = 8.0f;  // log2 units: P may reach 2^8 before
 template <int D, int BS, typename KV, int QR>
 __global__ void __launch_bounds__(kTileThreads, 1)
     tile_kernel(const __grid_constant__ CUtensorMap tmap_k,
-                const __grid_constant__ CUtensorMap tmap_v, const AttnParams p) {
+                const __grid_constant__ CUtensorMap tmap_v,
+                const __grid_constant__ CUtensorMap tmap_q, const AttnParams p) {
     constexpr int BN = tile_block_tokens(D);  // tokens per KV block
     constexpr int NPB = BN / BS;              // pages per KV block
     constexpr int NS = tile_stages(D, QR);
@@ -115,6 +116,7 @@ __global__ void __launch_bounds__(kTileThreads, 1)
     uint64_t* q_free = q_full + 2;      // [2] the S MMAs of buffer b's segment have completed
     uint64_t* o_free = q_free + 2;      // a segment's O has been read out
     int32_t* phys_of = reinterpret_cast<int32_t*>(smem + L.phys_off);  // [NS][NPB] of K stages
+    int32_t* v_live = phys_of + NS * NPB;  // [NS]: V stage's block holds a page
     float* xmax = reinterpret_cast<float*>(smem + L.xchg_off);    // [2][2][128]
     float* xl = xmax + 2 * 2 * 128;                                   // [2][128]
     uint64_t* xchg = reinterpret_cast<uint64_t*>(xl + 2 * 128);     // [2]
@@ -384,7 +386,7 @@ __global__ void __launch_bounds__(kTileThreads, 1)
             mbar_init(smem_u32(p_full + kTileSBufs + i), 128);
             mbar_init(smem_u32(pv_done + i), 1);
         }
-        mbar_init(smem_u32(final_bar), 1);
+        mbar_init(smem_u32(final_bar), 2);  // the S and the P V issuer
         mbar_init(smem_u32(q_ready), kTileThreads - 64);
         for (int i = 0; i < 2; ++i) {
             mbar_init(smem_u32(q_full + i), 1);
@@ -397,6 +399,7 @@ __global__ void __launch_bounds__(kTileThreads, 1)
         mbar_init_fence();
         prefetch_tensormap(&tmap_k);
         prefetch_tensormap(&tmap_v);
+        if (multi) prefetch_tensormap(&tmap_q);
     }
     if (warp == 2) {  // tensor memory for O and the S / P buffers
         tc::tmem_alloc(smem_u32(tmem_slot), kCols);
@@ -467,7 +470,35 @@ __global__ void __launch_bounds__(kTileThreads, 1)
         const uint32_t ring = smem_u32(smem + (is_k ? L.k_off : L.v_off));
         const uint64_t policy = l2_policy_evict_first();
         int issued = 0;  // blocks issued, over all segments (the ring's position)
+        int q_last = 0;  // V warp: the last segment whose Q copy was issued (0: none)
         for_segments([&](const Seg& g, int s) {
+            if (!is_k && multi && s >= 1) {
+                // Q of segment s into buffer s & 1 once the S MMAs of segment
+                // s - 2 (the buffer's previous user) are done.  The box is the
+                // tile's rows (G heads x QR / G query tokens, or QR heads of one
+                // token when the group is larger), 64 columns at a time, in the
+                // 128-byte swizzle the S MMA reads; rows past the unit's rows
+                // hold the next tokens' queries or the fill value, and are
+                // masked like the zero rows of a staged tile
+                bool qok = true;
+                if (lane == 0) {
+                    const int qb = s & 1;
+                    if (s >= 2) qok = wait(q_free + qb, ((s - 2) >> 1) & 1);
+                    if (qok) {
+                        const int r0 = g.tile * kTileRows;  // the tile's first row
+                        const int hc = G >= QR ? g.kvh * G + (r0 & (G - 1)) : g.kvh * G;
+                        const int qc = g.b * Q + (r0 >> gshift);
+                        const uint32_t qbar = smem_u32(q_full + qb);
+                        const uint32_t qdst = smem_u32(smem + L.q_off) + (uint32_t)qb * (2u * QR * D);
+                        mbar_arrive_expect_tx(qbar, 2u * QR * D);
+#pragma unroll
+                        for (int blk = 0; blk < DBLK; ++blk)
+                            tma_load_3d(qdst + blk * (QR * 128), &tmap_q, blk * 64, hc, qc, qbar);
+                        q_last = s;
+                    }
+                }
+                if (!__shfl_sync(kFullMask, qok ? 1 : 0, 0)) return false;
+            }
             const int32_t* table_row = p.block_tables + (size_t)g.b * p.max_blocks;
             const int nblk = nblk_of(g);
             // the segment's table entries, 32 pages at a time (one per lane),
@@ -493,6 +524,7 @@ __global__ void __launch_bounds__(kTileThreads, 1)
                 if (!__shfl_sync(kFullMask, ok ? 1 : 0, 0)) return false;
                 if (is_k && lane < NPB) phys_of[st * NPB + lane] = phys;
                 const unsigned live = __ballot_sync(kFullMask, lane < NPB && phys >= 0);
+                if (!is_k && lane == 0) v_live[st] = live != 0u;
                 const uint32_t bar = smem_u32(full + st);
                 if (lane == 0) {
                     if (live) mbar_arrive_expect_tx(bar, (uint32_t)__popc(live) * 2u * BS * D);
@@ -510,27 +542,92 @@ __global__ void __launch_bounds__(kTileThreads, 1)
             return !*abort_flag;
         });
         if (*abort_flag && lane == 0) {
-            // let copies still in flight land before the CTA may exit
+            // let copies still in flight land before the CTA may exit (no one
+            // else arrives on q_full, so its phase stays complete once it is)
             for (int k = issued > NS ? issued - NS : 0; k < issued; ++k)
                 (void)mbar_wait_bounded(smem_u32(full + k % NS), (k / NS) & 1, p.timeout_ns);
+            if (q_last > 0)
+                (void)mbar_wait_bounded(smem_u32(q_full + (q_last & 1)), ((q_last - 1) >> 1) & 1,
+                                        p.timeout_ns);
         }
     } else if (warp == 2) {
-        // ====== Q of later segments: buffer s & 1, once the S MMAs of
-        // segment s - 2 (the buffer's previous user) are done ======
-        if (multi) {
+        // ======= P V issuer (one lane): O += P_j V_j as soon as block j's P
+        // is in tensor memory, apart from the S issuer so that neither waits
+        // behind the other's MMAs being accepted =======
+        if (lane == 0) {
+            constexpr int kType = kBF ? 1 : 0;
+            // (compact Q tiles: M = 64, rows 0..15 in lanes 0..15 as at M = 128)
+            constexpr int kM = QR == kTileCompactQRows ? 64 : kTileRows;
+            constexpr uint32_t id_o = tc::idesc_f16(kType, true, kM, D);
+            int j = 0;  // blocks over all segments
+            bool ok = true;
             for_segments([&](const Seg& g, int s) {
-                if (s == 0) return true;  // staged with the others at the start
-                if (s >= 2 && !__all_sync(kFullMask, wait(q_free + (s & 1), ((s - 2) >> 1) & 1)))
-                    return false;
-                stage_q(g, s & 1, lane, 32);
-                fence_proxy_async_smem();
-                __syncwarp();
-                if (lane == 0) mbar_arrive(smem_u32(q_full + (s & 1)));
-                return !*abort_flag;
+                bool started = false;  // O holds this segment's sum
+                if (s >= 1) {
+                    // the previous segment's O must have been read out
+                    if (!wait(o_free, (s - 1) & 1)) return ok = false;
+                    tc::fence_after_sync();
+                }
+                const int nblk = nblk_of(g);
+                for (int k = 0; k < nblk && !*abort_flag; ++k, ++j) {
+                    const int st = j % NS;
+                    if (!wait(v_full + st, (j / NS) & 1)) return ok = false;
+                    const bool live = v_live[st] != 0;  // the block holds a page
+                    const uint32_t v_base = smem_u32(smem + L.v_off) + (uint32_t)st * L.tile_bytes;
+                    // V: MN-major, 64-column blocks BN*128 bytes apart, 8-row
+                    // groups 1024 bytes apart; rows ks*16 .. +15 per step
+                    const uint64_t vd0 = tc::smem_desc(v_base, BN * 128, 1024, tc::kSwizzle128B);
+                    if constexpr (kHalfO) {
+                        // each warpgroup's half of the keys into its own O, as soon as
+                        // that half's P is in tensor memory
+#pragma unroll
+                        for (int h = 0; h < 2; ++h) {
+                            if (!wait(p_full + h * kTileSBufs + j % NB, (j / NB) & 1)) return ok = false;
+                            tc::fence_after_sync();
+                            if (live) {
+                                // half h's P: hi at columns h*BN/2 .., lo BN/4 after it
+                                const uint32_t ph = tmem + S_COL + (j % NB) * BN + h * (BN / 2);
+#pragma unroll
+                                for (int kk = 0; kk < BN / 32; ++kk) {
+                                    const int ks = h * (BN / 32) + kk;  // token rows of V
+                                    const uint64_t vd = vd0 + (uint64_t)((ks * 16 * 128) >> 4);
+                                    tc::mma_ts(tmem + O_COL + h * D, ph + kk * 8, vd, id_o,
+                                               (started || kk > 0) ? 1u : 0u);
+                                    if (kSplitP)
+                                        tc::mma_ts(tmem + O_COL + h * D, ph + BN / 4 + kk * 8, vd, id_o, 1u);
+                                }
+                            }
+                        }
+                        if (live) started = true;
+                    } else {
+                        if (!wait(p_full + j % NB, (j / NB) & 1)) return ok = false;
+                        tc::fence_after_sync();
+                        if (live) {
+                            // P of all BN keys: hi at columns 0 .., lo BN/2 after it
+                            const uint32_t p_hi = tmem + S_COL + (j % NB) * BN;
+                            const uint32_t p_lo = p_hi + BN / 2;
+#pragma unroll
+                            for (int ks = 0; ks < BN / 16; ++ks) {
+                                const uint64_t vd = vd0 + (uint64_t)((ks * 16 * 128) >> 4);
+                                tc::mma_ts(tmem + O_COL, p_hi + ks * 8, vd, id_o,
+                                           (started || ks > 0) ? 1u : 0u);
+                                if (kSplitP) tc::mma_ts(tmem + O_COL, p_lo + ks * 8, vd, id_o, 1u);
+                            }
+                            started = true;
+                        }
+                    }
+                    tc::commit(smem_u32(pv_done + j % NB));
+                    tc::commit(smem_u32(v_empty + st));
+                }
+                return ok && !*abort_flag;
             });
+            // every MMA issued has completed before tensor memory is released
+            tc::commit(smem_u32(final_bar));
+            (void)mbar_wait_bounded(smem_u32(final_bar), 0, p.timeout_ns);
         }
+        __syncwarp();
     } else if (warp == 1) {
-        // ================= MMA issuer (one lane) =================
+        // ================= S issuer (one lane) =================
         if (lane == 0) {
             constexpr int kType = kBF ? 1 : 0;
             // a compact Q tile (at most 16 live rows) runs the MMAs at M = 64:
@@ -540,69 +637,7 @@ __global__ void __launch_bounds__(kTileThreads, 1)
             // MMAs of a block cost the same either way)
             constexpr int kM = QR == kTileCompactQRows ? 64 : kTileRows;
             constexpr uint32_t id_s = tc::idesc_f16(kType, false, kM, BN);
-            constexpr uint32_t id_o = tc::idesc_f16(kType, true, kM, D);
-            bool started = false;    // O holds the current segment's sum
-            bool live_prev = false;  // block i-1 holds a page (its K stage may be refilled)
-            int seg_prev = -1;       // segment of block i-1
-            bool first_prev = false; // block i-1 is its segment's first
-            int i = 0;               // blocks over all segments
-            // O += P_j V_j (P's high and low parts) for block j = i - 1
-            auto issue_pv = [&]() -> bool {
-                const int j = i - 1, st = j % NS;
-                if (first_prev && seg_prev >= 1) {
-                    // the previous segment's O must have been read out
-                    if (!wait(o_free, (seg_prev - 1) & 1)) return false;
-                    tc::fence_after_sync();
-                    started = false;
-                }
-                if (!wait(v_full + st, (j / NS) & 1)) return false;
-                const uint32_t v_base = smem_u32(smem + L.v_off) + (uint32_t)st * L.tile_bytes;
-                // V: MN-major, 64-column blocks BN*128 bytes apart, 8-row
-                // groups 1024 bytes apart; rows ks*16 .. +15 per step
-                const uint64_t vd0 = tc::smem_desc(v_base, BN * 128, 1024, tc::kSwizzle128B);
-                if constexpr (kHalfO) {
-                    // each warpgroup's half of the keys into its own O, as soon as
-                    // that half's P is in tensor memory
-#pragma unroll
-                    for (int h = 0; h < 2; ++h) {
-                        if (!wait(p_full + h * kTileSBufs + j % NB, (j / NB) & 1)) return false;
-                        tc::fence_after_sync();
-                        if (live_prev) {
-                            // half h's P: hi at columns h*BN/2 .., lo BN/4 after it
-                            const uint32_t ph = tmem + S_COL + (j % NB) * BN + h * (BN / 2);
-#pragma unroll
-                            for (int kk = 0; kk < BN / 32; ++kk) {
-                                const int ks = h * (BN / 32) + kk;  // token rows of V
-                                const uint64_t vd = vd0 + (uint64_t)((ks * 16 * 128) >> 4);
-                                tc::mma_ts(tmem + O_COL + h * D, ph + kk * 8, vd, id_o,
-                                           (started || kk > 0) ? 1u : 0u);
-                                if (kSplitP)
-                                    tc::mma_ts(tmem + O_COL + h * D, ph + BN / 4 + kk * 8, vd, id_o, 1u);
-                            }
-                        }
-                    }
-                    if (live_prev) started = true;
-                } else {
-                    if (!wait(p_full + j % NB, (j / NB) & 1)) return false;
-                    tc::fence_after_sync();
-                    if (live_prev) {
-                        // P of all BN keys: hi at columns 0 .., lo BN/2 after it
-                        const uint32_t p_hi = tmem + S_COL + (j % NB) * BN;
-                        const uint32_t p_lo = p_hi + BN / 2;
-#pragma unroll
-                        for (int ks = 0; ks < BN / 16; ++ks) {
-                            const uint64_t vd = vd0 + (uint64_t)((ks * 16 * 128) >> 4);
-                            tc::mma_ts(tmem + O_COL, p_hi + ks * 8, vd, id_o,
-                                       (started || ks > 0) ? 1u : 0u);
-                            if (kSplitP) tc::mma_ts(tmem + O_COL, p_lo + ks * 8, vd, id_o, 1u);
-                        }
-                        started = true;
-                    }
-                }
-                tc::commit(smem_u32(pv_done + j % NB));
-                tc::commit(smem_u32(v_empty + st));
-                return true;
-            };
+            int i = 0;  // blocks over all segments
             bool ok = true;
             for_segments([&](const Seg& g, int s) {
                 // this segment's Q: buffer s & 1
@@ -613,7 +648,7 @@ __global__ void __launch_bounds__(kTileThreads, 1)
                 // Operand descriptors: a shared-memory descriptor holds (address >> 4)
                 // in its low 14 bits, and every address here is below 2^18, so the
                 // descriptor of base + offset is base's plus offset >> 4.  Q's are
-                // fixed for the segment; K's and V's are one add from their stage's.
+                // fixed for the segment; K's are one add from their stage's.
                 uint64_t qd[KSTEPS];
 #pragma unroll
                 for (int ks = 0; ks < KSTEPS; ++ks)
@@ -626,8 +661,7 @@ __global__ void __launch_bounds__(kTileThreads, 1)
                     if (!wait(k_full + st, (i / NS) & 1)) return ok = false;
                     if (i >= NB && !wait(pv_done + i % NB, ((i - NB) / NB) & 1)) return ok = false;
                     tc::fence_after_sync();
-                    const bool live_cur = block_live(st);
-                    if (live_cur) {
+                    if (block_live(st)) {
                         const uint32_t k_base = smem_u32(smem + L.k_off) + (uint32_t)st * L.tile_bytes;
                         const uint64_t kd = tc::smem_desc(k_base, 16, 1024, tc::kSwizzle128B);
 #pragma unroll
@@ -640,15 +674,9 @@ __global__ void __launch_bounds__(kTileThreads, 1)
                     tc::commit(smem_u32(k_empty + st));
                     // the segment's last S: its Q buffer is free once these complete
                     if (multi && k == nblk - 1) tc::commit(smem_u32(q_free + (s & 1)));
-                    if (i >= 1 && !issue_pv()) return ok = false;
-                    live_prev = live_cur;
-                    seg_prev = s;
-                    first_prev = k == 0;
                 }
                 return ok && !*abort_flag;
             });
-            // the last block's P V
-            if (ok && !*abort_flag && i >= 1) (void)issue_pv();
             // every MMA issued has completed before tensor memory is released
             tc::commit(smem_u32(final_bar));
             (void)mbar_wait_bounded(smem_u32(final_bar), 0, p.timeout_ns);
@@ -998,7 +1026,7 @@ cudaError_t launch_tile_inst(const AttnLaunch& L, cudaStream_t stream) {
     }
     cfg.attrs = attr;
     cfg.numAttrs = na;
-    return cudaLaunchKernelEx(&cfg, kern, L.tmap_k, L.tmap_v, L.p);
+    return cudaLaunchKernelEx(&cfg, kern, L.tmap_k, L.tmap_v, L.tmap_q, L.p);
 }
 
 // Clusters of `cluster` CTAs of this instantiation that can be resident at
