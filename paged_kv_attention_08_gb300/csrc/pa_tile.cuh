@@ -296,8 +296,10 @@ __global__ void __launch_bounds__(kTileThreads, 1)
         cluster_sync_release_acquire();  // every CTA's partial is in place
         const int P = p.num_parts;
         const int rank = (int)blockIdx.x;
-        const int rpc = (kTileRows + P - 1) / P;
-        const int r0 = rank * rpc, r1 = min(r0 + rpc, kTileRows);
+        // the tile's rows that hold unit rows, shared out among the cluster
+        const int nr = min(U - seg0.tile * kTileRows, kTileRows);
+        const int rpc = (nr + P - 1) / P;
+        const int r0 = min(rank * rpc, nr), r1 = min(r0 + rpc, nr);
         uint32_t rb_m[kMaxClusterParts], rb_l[kMaxClusterParts], rb_o[kMaxClusterParts];
 #pragma unroll
         for (int q = 0; q < kMaxClusterParts; ++q) {
