@@ -7,8 +7,9 @@ path with up to 16 rows per CTA, and the tcgen05 tile kernel with 128-row
 tiles; the kernel switch forces one of them): every group size with q_len up to
 and past 16 and 128 rows, sequences shorter than q_len (query tokens that see
 nothing), masked table entries, every split mode (one pass, cluster,
-workspace, balanced), the q-dtype output, and the full-size multi-token
-workloads on sampled rows.
+workspace, balanced), the q-dtype output, the full-size multi-token
+workloads whole, and the padding rows of Q tiles that persistent CTAs and the
+balanced split load by TMA (another sequence's queries, poisoned with NaN).
 """
 import math
 
@@ -243,4 +244,46 @@ def test_tile_compact_q_tile(switches, Q, H, Hkv):
         assert torch.equal(run(xp, pt), compact)
         switches(compact_q=0)
         assert torch.equal(run(xd, pt), compact)
+    assert pa.device_error() == 0
+
+
+@pytest.mark.parametrize("case", ["whole_persistent", "compact_persistent", "compact_balanced"])
+def test_padding_rows_read_other_sequences_queries(switches, case):
+    """A CTA's later segments (persistent CTAs, the balanced split) load their Q
+    tile by TMA: the tile's rows past the unit's rows then hold the next query
+    tokens, i.e. another sequence's queries (or the fill value past the last
+    one), where a staged tile holds zeros.  Those rows are masked, so NaN
+    queries in one sequence leave every other sequence's output exact.
+    Cases: 40 tokens x 4 heads = 160 rows (a full and a partial 128-row tile)
+    over 320 units; 3 tokens x 4 heads = 12 rows at head_dim 256 (compact
+    tiles) over 200 units; the same rows through the balanced split."""
+    switches(kernel="auto")
+    if case == "whole_persistent":
+        x = multi_case(41, 20, 40, 32, 8, 128, 16, [40 + 7 * b for b in range(20)],
+                       dtype=torch.float16)
+        pt, units = 0, 20 * 8 * 2
+    elif case == "compact_persistent":
+        # (the automatic choice serves 12-row units with the warp-level kernel)
+        switches(kernel="tile")
+        x = multi_case(42, 200, 3, 4, 1, 256, 32, [3 + 5 * b for b in range(200)])
+        pt, units = 0, 200
+    else:
+        x = multi_case(43, 24, 3, 8, 2, 256, 32, [3 + 37 * b for b in range(24)])
+        pt, units = pa.PARTITION_BALANCED, 48
+    want = oracle_of(x)
+    poisoned = 5
+    q = x.q.clone()
+    q[poisoned] = float("nan")
+    xn = workloads.Inputs(x.spec, q, x.k_cache, x.v_cache, x.block_tables, x.context_lens,
+                          x.scale, x.max_context_len, x.lens_host)
+    xd = xn.to(DEV)
+    plan = pa.plan_info(xd.q, xd.k_cache, xd.block_tables, xd.max_context_len, pt)
+    assert plan["kernel"] == "tcgen05 tile", plan
+    if pt == pa.PARTITION_BALANCED:
+        assert plan["reduce"] == "balanced split", plan
+    else:
+        assert plan["partitions"] == 1 and plan["ctas"] < units, plan  # persistent CTAs
+    got = run(xd, pt)
+    keep = [b for b in range(x.q.shape[0]) if b != poisoned]
+    check(got[keep], want[keep])
     assert pa.device_error() == 0
