@@ -10,28 +10,30 @@
 // online softmax, flash-decoding-bench "design.md" for the split into
 // partitions with a (max, sum, weighted values) partial each).
 //
-// One CTA per (sequence, 128-row tile and kv head, partition of pages); the
-// partition's pages are taken in KV blocks of BN tokens (128; 64 at
-// head_dim 256):
-//   - warp 0 streams the blocks: one lane per page reads its block-table entry
-//     and issues a 4-D TMA copy per 64-column block of the page's K and V
-//     tiles (128-byte swizzle) into consecutive rows of a stage, so that a
-//     block's pages form one BN-row operand;
-//   - warp 1 (one lane) issues the MMAs: S = Q K^T for a block (M = 128 rows,
-//     N = BN tokens, K = head_dim; Q and K from shared memory) into one of two
-//     S buffers in tensor memory, and O += P V (M = 128, N = head_dim,
-//     K = BN; P from tensor memory, V from shared memory, MN-major) into the
-//     O accumulator in tensor memory.  S of block j + 1 is computed while the
-//     softmax works on block j;
+// One CTA per (sequence, 128-row tile and kv head, partition of pages), or a
+// CTA taking a list of such segments in turn (persistent CTAs, the balanced
+// split); pages are taken in KV blocks of BN tokens (128; 64 at head_dim 256):
+//   - warps 0 and 3 stream the blocks, K and V in rings of their own: one
+//     lane per page reads its block-table entry and issues a 4-D TMA copy per
+//     64-column block of the page's tile (128-byte swizzle) into consecutive
+//     rows of a stage, so that a block's pages form one BN-row operand; the V
+//     warp also loads later segments' Q tiles through a Q tensor map;
+//   - warp 1 (one lane) issues S = Q K^T for a block (M = 128 rows, N = BN
+//     tokens, K = head_dim; Q and K from shared memory) into an S buffer in
+//     tensor memory as soon as the buffer's previous P V is done; warp 2
+//     (one lane, after allocating tensor memory) issues O += P V (M = 128,
+//     N = head_dim, K = BN; P from tensor memory, V from shared memory,
+//     MN-major) as soon as the block's P is in tensor memory;
 //   - warps 4-11 (two warpgroups, one half of a block's columns each) own one
 //     row per thread (a tensor-memory lane): they read the row's scores, mask
-//     them (table reach and the row's causal limit), exchange the halves'
-//     maxima, keep the running max m and normaliser l in base-2 units,
-//     rescale O in tensor
-//     memory when the max moves by more than 2^8, and write P over S (bf16:
-//     a high and a low 16-bit part, two MMAs, ~16 significant bits; fp16:
-//     one part, 11 bits), then the final O / l or the partial (m, l, O) for
-//     the combine kernel.
+//     them (table reach and the row's causal limit), keep the running max m
+//     and normaliser l in base-2 units, rescale O in tensor memory when the
+//     max moves by more than 2^8, and write P over S (bf16: a high and a low
+//     16-bit part, two MMAs, ~16 significant bits; fp16: one part, 11 bits),
+//     then the final O / l or the partial (m, l, O) for the combine.  Whole
+//     tiles up to head_dim 128 give each warpgroup an O accumulator of its own
+//     (its half of the keys; the two are merged once per segment); otherwise
+//     the two share O and exchange row maxima every block.
 // Units of at most 16 rows at head_dim 256 (one-token MQA) stage only those
 // rows of Q (QR = 16): the 56 KB saved give each K / V ring a third stage,
 // and the MMAs run at M = 64.
