@@ -689,8 +689,9 @@ __global__ void __launch_bounds__(kTileThreads, 1)
     } else if (warp >= 4) {
         // ============ softmax: two warpgroups, one row per thread each ============
         // warpgroup wg takes columns [wg*BH, (wg+1)*BH) of every block and
-        // output columns [wg*D/2, (wg+1)*D/2); the two exchange row maxima (and,
-        // at the end, normalisers) through shared memory
+        // output columns [wg*D/2, (wg+1)*D/2); with a shared O the two exchange
+        // row maxima every block, with an O each (kHalfO) only at the end of a
+        // segment, with their normalisers, through shared memory
         constexpr int BH = BN / 2;
         const int wg = (warp - 4) >> 2, w4 = warp & 3;
         const int r = w4 * 32 + lane;
