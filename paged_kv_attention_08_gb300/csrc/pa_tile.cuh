@@ -857,14 +857,19 @@ __global__ void __launch_bounds__(kTileThreads, 1)
                     tc::wait_st();
                     // zero the V rows of masked pages and past the segment's last
                     // token (0 * NaN would otherwise reach O), once the stage's
-                    // copies have landed
+                    // copies have landed.  With an O per warpgroup, half h's P V
+                    // MMAs wait for warpgroup h's arrival alone, so each
+                    // warpgroup zeroes the rows of its own half of the keys;
+                    // otherwise the two share all BN rows
                     const int tb = (g.pb + k * NPB) * BS;
                     const bool holes = tb + BN > tend || bits != (1u << NPB) - 1u;
                     if (holes) {
                         if (!__all_sync(kFullMask, wait(v_full + st, (j / NS) & 1))) break;
                         uint8_t* vt = smem + L.v_off + (size_t)st * L.tile_bytes;
-                        for (int idx = sr; idx < BN * DBLK * 8; idx += 256) {
-                            const int row = idx / (DBLK * 8), rem = idx % (DBLK * 8);
+                        constexpr int kZRows = kHalfO ? BH : BN, kZThreads = kHalfO ? 128 : 256;
+                        const int zrow0 = kHalfO ? wg * BH : 0, zt = kHalfO ? r : sr;
+                        for (int idx = zt; idx < kZRows * DBLK * 8; idx += kZThreads) {
+                            const int row = zrow0 + idx / (DBLK * 8), rem = idx % (DBLK * 8);
                             if (!((bits >> (row / BS)) & 1u) || tb + row >= tend)
                                 *reinterpret_cast<uint4*>(vt + (rem >> 3) * BN * 128 + row * 128 +
                                                           (rem & 7) * 16) = make_uint4(0, 0, 0, 0);

@@ -218,6 +218,43 @@ def test_tile_kernel_poison_and_permutation(switches):
     assert pa.device_error() == 0
 
 
+@pytest.mark.parametrize("D,dt", [(64, torch.float16), (128, torch.bfloat16)],
+                         ids=["d64_fp16", "d128_bf16"])
+def test_tile_masked_v_rows_per_warpgroup(switches, D, dt):
+    """Whole tiles up to head_dim 128 keep an O per softmax warpgroup, and each
+    half of a block's keys goes to its P V MMAs once that half's warpgroup has
+    written its P and zeroed the half's masked V rows (a V row read before it
+    is zeroed puts 0 * NaN into O).  NaN in every slot past each context and in
+    every unreferenced block, over 384 persistent units whose last blocks end
+    at every 16-token offset: ten calls, each bit-identical to the unpoisoned
+    result, which is exact against the oracle."""
+    switches(kernel="auto")
+    B = 24
+    lens = [40 + 21 * b for b in range(B)]
+    x = multi_case(47, B, 40, 32, 8, D, 16, lens, dtype=dt, spare=5)
+    xd = x.to(DEV)
+    plan = pa.plan_info(xd.q, xd.k_cache, xd.block_tables, xd.max_context_len, 0)
+    assert plan["kernel"] == "tcgen05 tile" and plan["ctas"] < B * 8 * 2, plan
+    base = run(xd, 0)
+    check(base, oracle_of(x))
+    NB = x.k_cache.shape[0]
+    used = set(x.block_tables[x.block_tables >= 0].tolist())
+    k, v = xd.k_cache.clone(), xd.v_cache.clone()
+    for blk in range(NB):
+        if blk not in used:
+            k[blk] = float("nan")
+            v[blk] = float("nan")
+    for b, t in enumerate(x.lens_host):
+        last = int(x.block_tables[b, (t - 1) // 16])
+        k[last, t % 16 or 16:] = float("nan")
+        v[last, t % 16 or 16:] = float("nan")
+    xp = workloads.Inputs(x.spec, xd.q, k, v, xd.block_tables, xd.context_lens, x.scale,
+                          x.max_context_len, x.lens_host)
+    for _ in range(10):
+        assert torch.equal(run(xp, 0), base)
+    assert pa.device_error() == 0
+
+
 @pytest.mark.parametrize("Q,H,Hkv", [(1, 16, 1), (2, 16, 2)], ids=["mqa_q1", "g8_q2"])
 def test_tile_compact_q_tile(switches, Q, H, Hkv):
     """Units of at most 16 rows at head_dim 256 stage a compact Q tile (the
@@ -247,7 +284,8 @@ def test_tile_compact_q_tile(switches, Q, H, Hkv):
     assert pa.device_error() == 0
 
 
-@pytest.mark.parametrize("case", ["whole_persistent", "compact_persistent", "compact_balanced"])
+@pytest.mark.parametrize("case", ["whole_persistent", "whole_persistent_bf16", "whole_persistent_d64",
+                                  "compact_persistent", "compact_balanced"])
 def test_padding_rows_read_other_sequences_queries(switches, case):
     """A CTA's later segments (persistent CTAs, the balanced split) load their Q
     tile by TMA: the tile's rows past the unit's rows then hold the next query
@@ -255,12 +293,14 @@ def test_padding_rows_read_other_sequences_queries(switches, case):
     one), where a staged tile holds zeros.  Those rows are masked, so NaN
     queries in one sequence leave every other sequence's output exact.
     Cases: 40 tokens x 4 heads = 160 rows (a full and a partial 128-row tile)
-    over 320 units; 3 tokens x 4 heads = 12 rows at head_dim 256 (compact
-    tiles) over 200 units; the same rows through the balanced split."""
+    over 320 units, fp16 and bf16 at head_dim 128 and fp16 at 64; 3 tokens x
+    4 heads = 12 rows at head_dim 256 (compact tiles) over 200 units; the same
+    rows through the balanced split."""
     switches(kernel="auto")
-    if case == "whole_persistent":
-        x = multi_case(41, 20, 40, 32, 8, 128, 16, [40 + 7 * b for b in range(20)],
-                       dtype=torch.float16)
+    if case.startswith("whole_persistent"):
+        D = 64 if case.endswith("d64") else 128
+        dt = torch.bfloat16 if case.endswith("bf16") else torch.float16
+        x = multi_case(41, 20, 40, 32, 8, D, 16, [40 + 7 * b for b in range(20)], dtype=dt)
         pt, units = 0, 20 * 8 * 2
     elif case == "compact_persistent":
         # (the automatic choice serves 12-row units with the warp-level kernel)
