@@ -176,6 +176,13 @@ __device__ __forceinline__ void ldsm_x4_trans(uint32_t addr, uint32_t& r0, uint3
 }
 
 // 2^x on the special-function unit (relative error ~2^-22; -inf -> +0).
+// max(a, b, c) in one instruction (three-operand max, sm_100 and later)
+__device__ __forceinline__ float fmax3(float a, float b, float c) {
+    float r;
+    asm("max.f32 %0, %1, %2, %3;" : "=f"(r) : "f"(a), "f"(b), "f"(c));
+    return r;
+}
+
 __device__ __forceinline__ float fast_exp2(float x) {
     float y;
     asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
@@ -237,6 +244,15 @@ struct Mma<__half> {
         const float2 f = __half22float2(*reinterpret_cast<const __half2*>(&v));
         x0 = f.x;
         x1 = f.y;
+    }
+    // (l + x0) + x1 for the two packed values, each widened exactly inside a
+    // mixed-precision add (f16 operand, f32 sum: one instruction apiece)
+    static __device__ __forceinline__ float add2(uint32_t v, float l) {
+        asm("{\n\t.reg .f16 lo, hi;\n\tmov.b32 {lo, hi}, %1;\n\t"
+            "add.rn.f32.f16 %0, lo, %0;\n\tadd.rn.f32.f16 %0, hi, %0;\n\t}"
+            : "+f"(l)
+            : "r"(v));
+        return l;
     }
 };
 

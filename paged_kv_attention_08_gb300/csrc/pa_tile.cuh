@@ -769,19 +769,17 @@ __global__ void __launch_bounds__(kTileThreads, 1)
 #pragma unroll
                             for (int c = 0; c < 32; ++c) sc[c0 + c] = __uint_as_float(x[c]);
                         }
-                        // every page live and the whole half inside every row's limit:
-                        // nothing to mask
-                        if (__all_sync(kFullMask, bits == (1u << NPB) - 1u && t0 + BH <= lim)) {
-#pragma unroll
-                            for (int c = 0; c < BH; ++c) mx = fmaxf(mx, sc[c]);
-                        } else {
+                        // masked unless every page is live and the whole half lies
+                        // inside every row's limit; then the row maximum, three at a time
+                        if (!__all_sync(kFullMask, bits == (1u << NPB) - 1u && t0 + BH <= lim)) {
 #pragma unroll
                             for (int c = 0; c < BH; ++c) {
                                 const bool pl = (bits >> ((wg * BH + c) / BS)) & 1u;
                                 sc[c] = (pl && t0 + c < lim) ? sc[c] : NEG_INF;
-                                mx = fmaxf(mx, sc[c]);
                             }
                         }
+#pragma unroll
+                        for (int c = 0; c < BH; c += 2) mx = fmax3(mx, sc[c], sc[c + 1]);
                     }
                     float ms;
                     if constexpr (kHalfO) {
@@ -833,14 +831,14 @@ __global__ void __launch_bounds__(kTileThreads, 1)
                                 const float x0 = fast_exp2(fmaf(sc[c0 + c], qscale, -me));
                                 const float x1 = fast_exp2(fmaf(sc[c0 + c + 1], qscale, -me));
                                 const uint32_t h = Mma<KV>::pack(x0, x1);
-                                float h0, h1;
-                                Mma<KV>::unpack(h, h0, h1);
                                 ph[c / 2] = h;
-                                if (kSplitP) {
+                                if constexpr (kSplitP) {
+                                    float h0, h1;
+                                    Mma<KV>::unpack(h, h0, h1);
                                     l += x0 + x1;
                                     pl[c / 2] = Mma<KV>::pack(x0 - h0, x1 - h1);
                                 } else {
-                                    l += h0 + h1;  // the weights the MMA uses
+                                    l = Mma<KV>::add2(h, l);  // the weights the MMA uses
                                 }
                             }
                             // kHalfO: the warpgroup's P inside its own S columns
