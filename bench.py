@@ -752,7 +752,8 @@ def main(argv=None):
                           f"{plans[dom_name]['partitions']} partition(s), reduce: "
                           f"{plans[dom_name]['reduce']})",
                 "bytes_per_launch": dom_bytes,
-                "traffic": ncu_traffic("pa_tile" if tensor_bound else "pa_attn", dom_name)},
+                "traffic": ncu_traffic("pa_tile" if "tile" in plans[dom_name]["kernel"] else "pa_attn",
+                                       dom_name)},
             "cpu_baseline": cpu,
             "clocks": clk,
         }
