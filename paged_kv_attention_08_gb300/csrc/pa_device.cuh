@@ -119,6 +119,14 @@ __device__ __forceinline__ void tma_load_3d(uint32_t dst, const CUtensorMap* map
         : "memory");
 }
 
+// Eight floats in one 32-byte store (sm_100 and later): a whole L2 sector per
+// lane.  dst must be 32-byte aligned.
+__device__ __forceinline__ void st_global_v8(float* dst, const float* v) {
+    asm volatile("st.global.v8.f32 [%0], {%1, %2, %3, %4, %5, %6, %7, %8};" ::"l"(dst), "f"(v[0]),
+                 "f"(v[1]), "f"(v[2]), "f"(v[3]), "f"(v[4]), "f"(v[5]), "f"(v[6]), "f"(v[7])
+                 : "memory");
+}
+
 // L2 policy for data read exactly once per step: evict it first.
 __device__ __forceinline__ uint64_t l2_policy_evict_first() {
     uint64_t pol;

@@ -969,11 +969,19 @@ __global__ void __launch_bounds__(kTileThreads, 1)
 #pragma unroll
                     for (int c = 0; c < 16; ++c) v[c] = l > 0.f ? v[c] * (fin ? inv : 1.f) : 0.f;
                     if (!fin || p.out_dtype == PA_F32) {
-                        float* dst = (fin ? static_cast<float*>(p.out) : p.part_acc) + orow + c0;
+                        float* base = fin ? static_cast<float*>(p.out) : p.part_acc;
+                        float* dst = base + orow + c0;
+                        // rows start at multiples of head_dim floats and c0 at multiples
+                        // of 16: a 32-byte aligned base gives whole-sector stores
+                        if ((reinterpret_cast<uintptr_t>(base) & 31) == 0) {
+                            st_global_v8(dst, v);
+                            st_global_v8(dst + 8, v + 8);
+                        } else {
 #pragma unroll
-                        for (int c = 0; c < 16; c += 4)
-                            *reinterpret_cast<float4*>(dst + c) =
-                                make_float4(v[c], v[c + 1], v[c + 2], v[c + 3]);
+                            for (int c = 0; c < 16; c += 4)
+                                *reinterpret_cast<float4*>(dst + c) =
+                                    make_float4(v[c], v[c + 1], v[c + 2], v[c + 3]);
+                        }
                     } else {
                         uint32_t w[8];
 #pragma unroll

@@ -255,6 +255,42 @@ def test_tile_masked_v_rows_per_warpgroup(switches, D, dt):
     assert pa.device_error() == 0
 
 
+def test_tile_output_16_byte_aligned(switches):
+    """The tile kernel writes fp32 rows in whole 32-byte sectors when the output
+    (or the workspace's partials) starts on a 32-byte boundary, else in 16-byte
+    stores: an output and a workspace 16 bytes past a 32-byte boundary give
+    results bit-identical to the aligned call, in one pass and through the
+    workspace."""
+    switches(kernel="tile")
+    lens = [300, 77, 1000]
+    x = multi_case(53, 3, 40, 16, 2, 128, 16, lens)
+    xd = x.to(DEV)
+    pages = -(-max(lens) // 16)
+    n = xd.q.numel()
+
+    def off16(numel):
+        # a NaN-filled fp32 view of `numel` elements starting 16 bytes past a 32-byte boundary
+        buf = torch.full((numel + 16,), float("nan"), dtype=torch.float32, device=DEV)
+        k = (-(buf.data_ptr() // 4) % 8) + 4
+        v = buf[k:k + numel]
+        assert v.data_ptr() % 32 == 16
+        return v
+
+    for pt, reduce in [(pages * 16, "none"), (2 * 16, "workspace")]:
+        plan = pa.plan_info(xd.q, xd.k_cache, xd.block_tables, xd.max_context_len, pt)
+        assert plan["kernel"] == "tcgen05 tile" and reduce in plan["reduce"], plan
+        want = run(xd, pt)
+        need = pa.workspace_size_multi(xd.q, xd.k_cache, xd.block_tables, torch.float32,
+                                       xd.max_context_len, pt)
+        out = off16(n).view(xd.q.shape)
+        ws = off16(max(need, 16) // 4 + 1)
+        pa.decode_multi(out, xd.q, xd.k_cache, xd.v_cache, xd.block_tables, xd.context_lens,
+                        xd.scale, xd.max_context_len, pt, workspace=ws)
+        torch.cuda.synchronize()
+        assert torch.equal(out, want)
+    assert pa.device_error() == 0
+
+
 @pytest.mark.parametrize("Q,H,Hkv", [(1, 16, 1), (2, 16, 2)], ids=["mqa_q1", "g8_q2"])
 def test_tile_compact_q_tile(switches, Q, H, Hkv):
     """Units of at most 16 rows at head_dim 256 stage a compact Q tile (the
