@@ -255,6 +255,96 @@ def test_tile_masked_v_rows_per_warpgroup(switches, D, dt):
     assert pa.device_error() == 0
 
 
+def _slot(x, b, t):
+    """(pool block, slot) of sequence b's token t."""
+    bs = x.k_cache.shape[1]
+    return int(x.block_tables[b, t // bs]), t % bs
+
+
+def test_tile_fp16_p_edge_cases(switches):
+    """fp16 inputs on the tile kernel, where P enters the P V MMA as one fp16
+    part (11 significant bits): (a) a query token that sees one cached token
+    returns that token's V exactly; (b) a token whose score exceeds every
+    other by ~134 (natural log units) returns its V exactly (the other weights
+    round to 0, the normaliser is 1); (c) weights in [1/2, 1], each V row +-1
+    with the sign of its weight's fp16 rounding error so that the errors add
+    up: the error against the oracle stays within one fp16 rounding per weight,
+    2^-11 * max|V - O| <= 2^-10, and above 2^-14 (the case exercises the
+    rounding), and the output is within 2e-5 of the same weights rounded once
+    to fp16 with the normaliser summed from the rounded weights (unrounded
+    weights differ from that by 1.7e-4 here, a bf16 part by 3.3e-4)."""
+    switches(kernel="tile")
+    dt = torch.float16
+    G = 8
+    # (a) T = Q: query token 0 sits at position 0 and sees token 0 alone
+    x = multi_case(61, 2, 40, 16, 2, 128, 16, [40, 40], dtype=dt)
+    got = run(x.to(DEV), 0).cpu()
+    check(got, oracle_of(x))
+    for b in range(2):
+        for kvh in range(2):
+            blk, sl = _slot(x, b, 0)
+            v0 = x.v_cache[blk, sl, kvh].float()
+            assert torch.equal(got[b, 0, kvh * G:(kvh + 1) * G], v0.expand(G, -1))
+    # (b) one dominant token (token 0, seen by every query token)
+    x = multi_case(62, 2, 40, 16, 2, 128, 16, [700, 300], dtype=dt)
+    q = torch.zeros_like(x.q)
+    q[..., 0] = 40.0
+    k = x.k_cache.clone()
+    k[..., 0] = k[..., 0].clamp(-2, 2)  # other scores <= 80 * scale
+    for b in range(2):
+        blk, sl = _slot(x, b, 0)
+        k[blk, sl] = 0
+        k[blk, sl, :, 0] = 40.0  # 1600 * scale
+    xb = workloads.Inputs(x.spec, q, k, x.v_cache, x.block_tables, x.context_lens, x.scale,
+                          x.max_context_len, x.lens_host)
+    got = run(xb.to(DEV), 0).cpu()
+    check(got, oracle_of(xb))
+    for b in range(2):
+        blk, sl = _slot(x, b, 0)
+        for kvh in range(2):
+            want = x.v_cache[blk, sl, kvh].float().expand(40, G, -1)
+            assert torch.equal(got[b, :, kvh * G:(kvh + 1) * G], want)
+    # (c) adversarial rounding: scores c_t (q = e_0, k_t = c_t e_0), the maximum
+    # 8 at tokens 0 and 64 (both halves of the first block, so both softmax
+    # warpgroups subtract the same maximum); the weight is computed here as the
+    # kernel does, 2^fma(c_t, qscale, -8 qscale) in fp32, and V_t = sign of its
+    # fp16 rounding error
+    T = 1024
+    x = multi_case(63, 1, 8, 8, 1, 128, 16, [T], dtype=dt)
+    gen = torch.Generator().manual_seed(64)
+    c = (torch.rand(T, generator=gen) * 7.8 + 0.2).to(dt)
+    c[0] = 8.0
+    c[64] = 8.0
+    qscale = np.float32(np.float32(x.scale) * np.float32(1.4426950408889634))
+    ms = np.float32(np.float32(8.0) * qscale)
+    arg = (c.double().numpy() * float(qscale) - float(ms)).astype(np.float32).astype(np.float64)
+    w = np.exp2(arg)
+    sign = np.where(w.astype(np.float16).astype(np.float64) >= w, 1.0, -1.0)
+    q = torch.zeros_like(x.q)
+    q[..., 0] = 1.0
+    k = torch.zeros_like(x.k_cache)
+    v = torch.zeros_like(x.v_cache)
+    for t in range(T):
+        blk, sl = _slot(x, 0, t)
+        k[blk, sl, 0, 0] = c[t]
+        v[blk, sl, 0, :] = float(sign[t])
+    xc = workloads.Inputs(x.spec, q, k, v, x.block_tables, x.context_lens, x.scale,
+                          x.max_context_len, x.lens_host)
+    xcd = xc.to(DEV)
+    # one partition, so that both warpgroups subtract the maximum 8 qscale
+    plan = pa.plan_info(xcd.q, xcd.k_cache, xcd.block_tables, xcd.max_context_len, T)
+    assert plan["kernel"] == "tcgen05 tile" and plan["partitions"] == 1, plan
+    got = run(xcd, T).double().cpu().numpy()  # [1, 8, 8, 128]
+    err = np.abs(got - oracle_of(xc)).max()
+    assert 2.0 ** -14 < err <= 2.0 ** -10, err
+    p16 = w.astype(np.float16).astype(np.float64)
+    for i in range(8):  # query token i sees tokens 0 .. T - 8 + i
+        n = T - 8 + i + 1
+        emu = (p16[:n] * sign[:n]).sum() / p16[:n].sum()
+        assert np.abs(got[0, i] - emu).max() <= 2e-5, (i, np.abs(got[0, i] - emu).max())
+    assert pa.device_error() == 0
+
+
 def test_tile_output_16_byte_aligned(switches):
     """The tile kernel writes fp32 rows in whole 32-byte sectors when the output
     (or the workspace's partials) starts on a 32-byte boundary, else in 16-byte
