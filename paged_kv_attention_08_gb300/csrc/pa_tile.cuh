@@ -30,10 +30,12 @@
 //     and normaliser l in base-2 units, rescale O in tensor memory when the
 //     max moves by more than 2^8, and write P over S (bf16: a high and a low
 //     16-bit part, two MMAs, ~16 significant bits; fp16: one part, 11 bits),
-//     then the final O / l or the partial (m, l, O) for the combine.  Whole
-//     tiles up to head_dim 128 give each warpgroup an O accumulator of its own
-//     (its half of the keys; the two are merged once per segment); otherwise
-//     the two share O and exchange row maxima every block.
+//     zero the V rows that P weights with 0 (slots past the last token, pages
+//     the table does not reach: 0 * NaN would reach O), and write the final
+//     O / l or the partial (m, l, O) for the combine.  Whole tiles up to
+//     head_dim 128 give each warpgroup an O accumulator of its own (its half
+//     of the keys, whose V rows it zeroes itself; the two are merged once per
+//     segment); otherwise the two share O and exchange row maxima every block.
 // Units of at most 16 rows at head_dim 256 (one-token MQA) stage only those
 // rows of Q (QR = 16): the 56 KB saved give each K / V ring a third stage,
 // and the MMAs run at M = 64.
@@ -61,10 +63,10 @@ constexpr float kTileRescaleSlack = 8.0f;  // log2 units: P may reach 2^8 before
 // share becomes a record [C][2][unit rows] for the balanced combine kernel).
 // Every role walks the same segments and numbers the KV blocks of all of them
 // in one sequence, so that the rings, the S / P buffers and their barrier
-// phases run on across segment boundaries; Q is double-buffered (warp 2
-// stages the Q of segment s >= 1 once the last S MMA of segment s - 2 is
-// done), and the first P V MMA of a segment waits until the previous
-// segment's O has been read out.
+// phases run on across segment boundaries; Q is double-buffered (the V copy
+// warp loads the Q of segment s >= 1 by TMA once the last S MMA of segment
+// s - 2 has completed), and the first P V MMA of a segment waits until the
+// previous segment's O has been read out.
 template <int D, int BS, typename KV, int QR>
 __global__ void __launch_bounds__(kTileThreads, 1)
     tile_kernel(const __grid_constant__ CUtensorMap tmap_k,
