@@ -250,6 +250,13 @@ def ncu_traffic(kernel: str, workload: str):
     return None
 
 
+def dominant_traffic(plan: dict, workload: str):
+    """DRAM bytes per launch of the kernel the plan picked for `workload`: the
+    tile kernel's summaries are profiles/pa_tile_<workload>.txt, the warp-level
+    kernel's pa_attn_<workload>.txt (an HBM-bound call may run on either)."""
+    return ncu_traffic("pa_tile" if "tile" in plan["kernel"] else "pa_attn", workload)
+
+
 # ---------------------------------------------------------------------------
 # CPU oracle arm
 # ---------------------------------------------------------------------------
@@ -752,8 +759,7 @@ def main(argv=None):
                           f"{plans[dom_name]['partitions']} partition(s), reduce: "
                           f"{plans[dom_name]['reduce']})",
                 "bytes_per_launch": dom_bytes,
-                "traffic": ncu_traffic("pa_tile" if "tile" in plans[dom_name]["kernel"] else "pa_attn",
-                                       dom_name)},
+                "traffic": dominant_traffic(plans[dom_name], dom_name)},
             "cpu_baseline": cpu,
             "clocks": clk,
         }
